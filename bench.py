@@ -1,0 +1,347 @@
+"""Benchmark of the bf16 -> fp32 GEMM on one GB300 (or N independent replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+A step is one tg_gemm call over the workload (4096^3 by default: the square
+problem the headline TFLOP/s is quoted on), inputs already resident in HBM.
+L2 is flushed (a 512 MB write) between steps, outside the timed events.
+Prints one JSON line (rank 0).  With --impl reference the oracle (fp64 CPU
+triple loop) is timed instead, on a bounded sample of rows of the same
+workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+DEFAULT_WORKLOAD = "square_4096"
+METRIC = "bf16->fp32 GEMM TFLOP/s at 1 GB300 and % of dense BF16 tensor (or HBM) roofline"
+KERNEL_SOURCES = ["tiled_gemm_codegen_gb300/csrc/tg_kernel.cuh", "tiled_gemm_codegen_gb300/csrc/tg_ptx.cuh",
+                  "tiled_gemm_codegen_gb300/csrc/tg_internal.h"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ------------------------------------------------------------------ helpers
+def kernel_source_hash() -> str:
+    import hashlib
+
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    want = kernel_source_hash()
+    with open(TRAFFIC_FILE) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 3 and not line.startswith("#") and parts[0] == workload and parts[1] == want:
+                return int(parts[2])
+    return None
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                smax.append(float(p[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, p[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(n_gpus: int):
+    """(rank, world, local_rank, torch.distributed or None)."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world <= 1:
+        return 0, 1, 0, None
+    import torch
+    import torch.distributed as dist
+
+    rank = int(os.environ["RANK"])
+    local = int(os.environ.get("LOCAL_RANK", rank))
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    if backend == "nccl":
+        torch.cuda.set_device(local)
+    dist.init_process_group(backend=backend)
+    return rank, world, local, dist
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, value: float) -> float:
+    if dist is None:
+        return value
+    import torch
+
+    dev = torch.device("cuda", torch.cuda.current_device()) if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+def oracle_sample(w, seconds: float = 10.0, max_rows: int | None = None):
+    """Time the oracle (as it stands) on the first R rows of C; R is sized
+    from a short calibration run to about `seconds` of CPU work."""
+    import oracle
+
+    A, B = synth.workload_inputs(w)
+    a = synth.bits_u16(A if w.batch == 1 else A[0])
+    b = synth.bits_u16(B if w.batch == 1 else B[0])
+    threads = oracle.num_threads()
+    probe = max(1, min(w.M, 4))
+    t0 = time.perf_counter()
+    oracle.gemm_f64(a[:probe], b, probe, w.N, w.K)
+    dt = max(time.perf_counter() - t0, 1e-6)
+    rows = int(max(1, min(max_rows or w.M, w.M, probe * seconds / dt)))
+    t0 = time.perf_counter()
+    oracle.gemm_f64(a[:rows], b, rows, w.N, w.K)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows * w.N * w.K
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"rows 0..{rows - 1} of C for one problem of {w.name} "
+                      f"({rows}x{w.N}x{w.K}, {flops / 1e9:.2f} GFLOP in {dt:.2f} s)",
+            "seconds": dt}
+
+
+def run_reference(args, rank, world, dist):
+    """--impl reference: the oracle, timed on the host cores, rank 0 only."""
+    if rank != 0:
+        return
+    w = synth.WORKLOADS[args.workload]
+    step_seconds = float(os.environ.get("TG_REF_STEP_SECONDS", "8"))
+    for _ in range(args.warmup and 1):
+        oracle_sample(w, seconds=0.5)
+    vals, secs = [], []
+    last = None
+    for _ in range(args.steps):
+        last = oracle_sample(w, seconds=step_seconds)
+        vals.append(last["value"])
+        secs.append(last["seconds"])
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(secs),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.name, "batch": w.batch, "M": w.M, "N": w.N, "K": w.K,
+                                        "sample": "row subset per step (bounded CPU work)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": last["cores"], "kind": "oracle",
+                         "sample": last["sample"]},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_gpu(args, rank, world, local, dist):
+    import torch
+
+    import tiled_gemm_codegen_gb300 as tg
+
+    tg.load()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    w = synth.WORKLOADS[args.workload]
+    A_cpu, B_cpu = synth.workload_inputs(w)
+    A = A_cpu.to(device)
+    B = B_cpu.to(device)
+    C = torch.empty((w.batch, w.M, w.N) if w.batch > 1 else (w.M, w.N), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    info = tg.plan(w.M, w.N, w.K, w.batch, A=A.data_ptr(), B=B.data_ptr(), C=C.data_ptr())
+    launches_per_step = 1 + info["pack_a"] + info["pack_b"]
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+
+    def step():
+        tg.gemm(A, B, C)
+
+    # warm-up (also JIT-loads the module, allocates workspaces)
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    st = tg.device_error()
+    if st != tg.TG_OK:
+        raise RuntimeError(f"device error during warm-up: {st}")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(dist)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(float(i))  # evict A, B, C from L2 (outside the timed events)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    st = tg.device_error()
+    if st != tg.TG_OK:
+        raise RuntimeError(f"device error during timing: {st}")
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]  # ms, GEMM call only
+    ms_mean = sum(per) / len(per)
+    ms_max = max_over_ranks(dist, ms_mean)
+    flops = float(w.flops)
+    value = world * flops / (ms_max * 1e-3) / 1e12
+
+    # end to end through the host-buffer entry point (pinned memory)
+    Ah = A_cpu.pin_memory()
+    Bh = B_cpu.pin_memory()
+    Ch = torch.empty(C.shape, dtype=torch.float32).pin_memory()
+    tg.gemm_host(Ah, Bh, Ch)
+    e2e_ms = []
+    for _ in range(max(3, min(args.steps, 10))):
+        flush.fill_(2.0)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        tg.gemm_host(Ah, Bh, Ch)
+        e2e_ms.append((time.perf_counter() - t0) * 1e3)
+    e2e_ms_max = max_over_ranks(dist, statistics.median(e2e_ms))
+    e2e_value = world * flops / (e2e_ms_max * 1e-3) / 1e12
+
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    achieved = flops / (ms_mean * 1e-3) / 1e12  # this rank's kernel
+    roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": measured_traffic(w.name),
+                "peak_source": f"{peak_src} bf16_tflops (burst; kernel timed alone)",
+                "algorithmic_flops_per_launch": int(flops),
+                "hbm_frac": round(w.bytes_moved / (ms_mean * 1e-3) / 1e9 / float(peaks["hbm_gbs"]), 4)}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = oracle_sample(w, seconds=args.cpu_seconds)
+        cpu.pop("seconds", None)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.batch, "M": w.M, "N": w.N, "K": w.K,
+                       "accumulate": "fp32", "l2": "flushed (512 MB write) between steps",
+                       "parallelism": "replicas" if world > 1 else "single GPU",
+                       "plan": {k: info[k] for k in ("block_n", "stages", "split_k", "grid", "pack_a",
+                                                     "pack_b", "epilogue")}},
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": int(A_cpu.numel() * 2 + B_cpu.numel() * 2),
+                    "d2h_bytes_per_step": int(C.numel() * 4)},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk,
+            "ms_min": round(min(per), 4),
+            "wall_s": round(wall, 3),
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--impl", default="tg", choices=["tg", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "tg":
+        ap.error("--warmup must be at least 3")
+    rank, world, local, dist = dist_setup(args.gpus)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world, dist)
+        else:
+            run_gpu(args, rank, world, local, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,157 @@
+/*
+ * tg_gemm.h - C ABI of the tiled bf16 -> fp32 GEMM for GB300 (sm_103a).
+ *
+ * The operation (all entry points below compute it):
+ *
+ *     for every b < batch:   C_b[i][j] = sum_{k < K} A_b[i][k] * B_b[k][j]
+ *
+ * with A_b = A + b*strideA, B_b = B + b*strideB, C_b = C + b*strideC and
+ * row-major addressing A_b[i][k] = A_b[i*lda + k], B_b[k][j] = B_b[k*ldb + j],
+ * C_b[i][j] = C_b[i*ldc + j] (all strides in ELEMENTS).  A and B are bf16,
+ * C is fp32; products are accumulated in fp32 and C is OVERWRITTEN.
+ *
+ * Sources for the operation and its schedule:
+ *   - LuisaCompute "Pipelines and stage boundaries", section "Stage boundaries
+ *     are lexical": the k-tile pipeline "load" stage (A and B tiles read with
+ *     zero bounds) feeding the "compute" stage acc = mma(a, b, acc).
+ *   - LuisaCompute "Execution Nests and coordinates", section "Dimensions and
+ *     spaces": A(m, reduction), B(reduction, n), C(m, n).
+ *   - OCANNL "Module Ir.Schedule": Split (tile loops), Pad-to-tile (arbitrary
+ *     extents through zero-filled fringes and masks), Stage (shared-memory
+ *     tiles), pipeline_depth, Tensorize, Partition (guard-free interior tiles
+ *     plus masked fringe tiles) and the deterministic two-pass split reduction
+ *     (split-K with a fixed combine order).
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers are DEVICE pointers unless the name says _host.  The caller
+ *     owns A, B, C and the stream; the library never frees caller memory.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream)
+ *     and return once the work is enqueued.  Device-side failures (a watchdog
+ *     expiry) are reported later by tg_device_error().
+ *   - Arguments are validated before anything is enqueued:
+ *       TG_ERR_INVALID_ARG  for a NULL pointer with a nonzero extent, M, N or
+ *                           K < 0, batch < 1, lda < K, ldb < N, ldc < N, a
+ *                           negative batch stride, batch strides that make
+ *                           two problems share an element of C, C
+ *                           overlapping A or B, or an extent > 2^31 - 1.
+ *   - M == 0 or N == 0: returns TG_OK and enqueues nothing.
+ *     K == 0: C is filled with zeros (the empty sum).
+ *   - Any alignment is accepted.  Operands whose base address or row/batch
+ *     stride is not a multiple of 16 bytes are first copied by the library
+ *     into an aligned scratch copy (the "pack" pass); an fp32 C whose rows
+ *     are not 16-byte aligned is written with plain masked stores instead of
+ *     tensor-memory-accelerator stores.
+ *   - Rounding: fp32 accumulation in an order fixed by the plan (tile shape
+ *     and split-K factor).  Results are bitwise reproducible run to run for
+ *     a fixed plan; different plans may differ in the last bits.
+ *   - Thread safety: calls on different streams may run concurrently; each
+ *     stream has its own scratch workspace.
+ */
+#ifndef TG_GEMM_H
+#define TG_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st *tg_stream_t;
+
+typedef enum tg_status {
+    TG_OK = 0,
+    TG_ERR_INVALID_ARG = 1, /* rejected before any work was enqueued       */
+    TG_ERR_UNSUPPORTED = 2, /* valid request this build cannot run          */
+    TG_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed            */
+    TG_ERR_OOM = 4,         /* workspace allocation failed                  */
+    TG_ERR_TIMEOUT = 5      /* a device-side wait exceeded its limit        */
+} tg_status;
+
+/* Plan overrides for tests and tuning (zero-initialise, then set fields).
+ * A zero field means "let the planner choose". */
+typedef struct tg_options {
+    int32_t block_n;     /* output tile width: 64, 128, 192 or 256            */
+    int32_t stages;      /* shared-memory ring depth, 2 .. the tile's maximum */
+    int32_t split_k;     /* K splits per output tile (1 = none)               */
+    int32_t force_pack;  /* nonzero: copy A and B through the pack pass       */
+    int32_t epilogue;    /* 1 = tensor-memory-accelerator stores, 2 = plain   */
+                         /* masked stores (1 needs a 16-byte aligned C)       */
+    int32_t max_ctas;    /* cap on the persistent grid (0 = one CTA per SM)   */
+    uint64_t timeout_ns; /* watchdog limit of every device-side wait          */
+                         /* (0 = 2 s)                                         */
+    int32_t debug_stall; /* nonzero: the epilogue first waits on a barrier    */
+                         /* nothing completes, so the watchdog must fire and  */
+                         /* tg_device_error() must return TG_ERR_TIMEOUT      */
+    int32_t reserved[7];
+} tg_options;
+
+/* What the planner chose (tg_plan output). */
+typedef struct tg_plan_info {
+    int32_t block_m, block_n, block_k, stages;
+    int32_t tiles_m, tiles_n, k_blocks, split_k;
+    int64_t num_units;   /* batch * tiles_m * tiles_n * split_k                */
+    int32_t grid;        /* persistent CTAs launched                          */
+    int32_t pack_a;      /* 1 when A goes through the pack pass                */
+    int32_t pack_b;      /* 1 when B goes through the pack pass                */
+    int32_t epilogue;    /* 1 = tensor-memory-accelerator stores, 2 = plain    */
+    int32_t smem_bytes;  /* dynamic shared memory per CTA                     */
+    int32_t tmem_cols;   /* tensor-memory columns allocated per CTA           */
+    int64_t workspace_bytes; /* scratch this call needs (pack copies, split-K  */
+                             /* partial tiles, tile counters)                  */
+    int32_t reserved[6];
+} tg_plan_info;
+
+/* The GEMM (see the header comment for the operation and conventions). */
+tg_status tg_gemm(const void *A, const void *B, float *C,
+                  int64_t M, int64_t N, int64_t K,
+                  int64_t lda, int64_t ldb, int64_t ldc,
+                  int64_t batch, int64_t strideA, int64_t strideB, int64_t strideC,
+                  tg_stream_t stream);
+
+/* Same as tg_gemm with plan overrides (opt may be NULL).  Returns
+ * TG_ERR_INVALID_ARG for an override outside its documented range. */
+tg_status tg_gemm_ex(const void *A, const void *B, float *C,
+                     int64_t M, int64_t N, int64_t K,
+                     int64_t lda, int64_t ldb, int64_t ldc,
+                     int64_t batch, int64_t strideA, int64_t strideB, int64_t strideC,
+                     tg_stream_t stream, const tg_options *opt);
+
+/* The GEMM on HOST buffers: copies the spans of A and B that the strides
+ * reach to device scratch owned by the library, runs tg_gemm_ex there, and
+ * copies the reached span of C back.  Synchronous: returns after C is on the
+ * host (pinned host memory makes the copies faster; pageable also works).
+ * Elements of C between rows (ldc > N) or between problems are preserved. */
+tg_status tg_gemm_host(const void *A_host, const void *B_host, float *C_host,
+                       int64_t M, int64_t N, int64_t K,
+                       int64_t lda, int64_t ldb, int64_t ldc,
+                       int64_t batch, int64_t strideA, int64_t strideB, int64_t strideC,
+                       tg_stream_t stream, const tg_options *opt);
+
+/* The plan tg_gemm_ex would use for these arguments, without touching the
+ * pointers' memory.  sm_count > 0 plans for that many SMs and makes no CUDA
+ * call at all (host-only); sm_count == 0 queries the current device. */
+tg_status tg_plan(const void *A, const void *B, const float *C,
+                  int64_t M, int64_t N, int64_t K,
+                  int64_t lda, int64_t ldb, int64_t ldc,
+                  int64_t batch, int64_t strideA, int64_t strideB, int64_t strideC,
+                  int32_t sm_count, const tg_options *opt, tg_plan_info *out);
+
+/* Synchronises `stream`, then reads and clears the device error word that
+ * the kernels' watchdog writes.  TG_ERR_TIMEOUT if a wait expired since the
+ * last call (the split-K tile counters are then reset too), TG_ERR_CUDA if
+ * the stream reports a CUDA error, else TG_OK. */
+tg_status tg_device_error(tg_stream_t stream);
+
+/* Static English name of a status code. */
+const char *tg_status_string(tg_status s);
+
+/* Frees every cached workspace on every device.  Call only when no work
+ * enqueued by this library is still running. */
+void tg_shutdown(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TG_GEMM_H */

@@ -1,0 +1,165 @@
+"""The C-ABI library on a machine without a GPU: it builds, loads, exports
+every entry point the header declares, its structs match the header's
+layout, and its host logic (argument checks, planner) behaves as documented.
+No call here reaches the GPU: validation and tg_plan(sm_count > 0) run
+before (and without) any CUDA call."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import subprocess
+import tempfile
+
+import pytest
+
+import synth
+import tiled_gemm_codegen_gb300 as tg
+from tiled_gemm_codegen_gb300 import _abi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tg_gemm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return _abi.load(build_if_missing=True)
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tg_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert set(names) == set(_abi.SIGNATURES), names
+    for name in names:
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", _abi.library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    assert set(names) <= exported
+    assert {n for n in exported if not n.startswith("_")} == set(names), "unexpected exports"
+
+
+def test_struct_layout_matches_header():
+    src = r"""
+#include <stddef.h>
+#include <stdio.h>
+#include "tg_gemm.h"
+int main(void) {
+  printf("%zu %zu %zu %zu\n", sizeof(tg_options), offsetof(tg_options, timeout_ns),
+         offsetof(tg_options, debug_stall), sizeof(tg_plan_info));
+  printf("%zu %zu %zu\n", offsetof(tg_plan_info, num_units), offsetof(tg_plan_info, grid),
+         offsetof(tg_plan_info, workspace_bytes));
+  return 0;
+}
+"""
+    with tempfile.TemporaryDirectory() as d:
+        c = os.path.join(d, "layout.c")
+        exe = os.path.join(d, "layout")
+        open(c, "w").write(src)
+        subprocess.run(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), c, "-o", exe], check=True)
+        vals = [int(x) for x in subprocess.run([exe], capture_output=True, text=True,
+                                               check=True).stdout.split()]
+    O, P = _abi.tg_options, _abi.tg_plan_info
+    assert vals == [ctypes.sizeof(O), O.timeout_ns.offset, O.debug_stall.offset, ctypes.sizeof(P),
+                    P.num_units.offset, P.grid.offset, P.workspace_bytes.offset]
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        assert tg.tg_status_string(code)
+    assert tg.tg_status_string(99) == "unknown status"
+
+
+A0, B0, C0 = 0x10000, 0x20000000, 0x40000000  # placeholder addresses, never dereferenced
+
+
+@pytest.mark.parametrize("args", [
+    dict(M=-1), dict(N=-2), dict(K=-3), dict(batch=0), dict(lda=3), dict(ldb=4), dict(ldc=5),
+    dict(M=2 ** 31), dict(A=0), dict(B=0), dict(C=0), dict(strideA=-1),
+    dict(batch=2, strideC=10),                  # problems overlap in C
+    dict(C=A0 + 8),                             # C overlaps A
+    dict(C=B0),                                 # C overlaps B
+    dict(lda=2 ** 41),
+])
+def test_invalid_arguments_rejected_before_any_cuda_call(lib, args):
+    base = dict(A=A0, B=B0, C=C0, M=8, N=8, K=8, lda=8, ldb=8, ldc=8, batch=1,
+                strideA=64, strideB=64, strideC=64)
+    base.update(args)
+    st = tg.tg_gemm(base["A"], base["B"], base["C"], base["M"], base["N"], base["K"], base["lda"],
+                    base["ldb"], base["ldc"], base["batch"], base["strideA"], base["strideB"],
+                    base["strideC"], None)
+    assert st == tg.TG_ERR_INVALID_ARG
+
+
+def test_empty_output_is_ok_without_gpu(lib):
+    assert tg.tg_gemm(0, 0, 0, 0, 5, 7, 7, 5, 5, 1, 0, 0, 0, None) == tg.TG_OK
+    assert tg.tg_gemm(0, 0, 0, 5, 0, 7, 7, 0, 0, 1, 0, 0, 0, None) == tg.TG_OK
+
+
+def _plan(w, **kw):
+    return tg.plan(w.M, w.N, w.K, w.batch, sm_count=152, **kw)
+
+
+def test_plan_of_each_workload(lib):
+    for w in synth.WORKLOADS.values():
+        info = _plan(w)
+        assert info["block_m"] == 128 and info["block_k"] == 64
+        assert info["tiles_m"] == -(-w.M // 128)
+        assert info["tiles_n"] == -(-w.N // info["block_n"])
+        assert info["k_blocks"] == -(-w.K // 64)
+        assert info["num_units"] == w.batch * info["tiles_m"] * info["tiles_n"] * info["split_k"]
+        assert 1 <= info["grid"] <= 152 and info["grid"] <= info["num_units"]
+        assert info["split_k"] <= info["k_blocks"]
+        assert info["smem_bytes"] <= 232448
+        assert info["tmem_cols"] in (128, 256, 512) and info["tmem_cols"] >= 2 * info["block_n"]
+        assert info["pack_a"] == 0 and info["pack_b"] == 0 or w.name == "ragged_4097x4095x4100" \
+            or w.name == "ragged_197x131x77"
+
+
+def test_plan_ragged_workload_packs_and_uses_plain_stores(lib):
+    """4097 x 4095 x 4100: lda = 4100 bf16 (8200 B) and ldb = 4095 (8190 B)
+    are not 16-byte multiples, so both operands are packed; ldc = 4095 fp32
+    (16380 B) rules out TMA stores of C."""
+    w = synth.WORKLOADS["ragged_4097x4095x4100"]
+    info = _plan(w)
+    assert info["pack_a"] == 1 and info["pack_b"] == 1 and info["epilogue"] == 2
+    assert info["tiles_m"] == 33 and info["k_blocks"] == 65
+    assert info["workspace_bytes"] >= 2 * (4097 * 4104 + 4100 * 4096)
+
+
+def test_plan_split_k_workspace(lib):
+    info = tg.plan(64, 2048, 8192, sm_count=152, options=tg.make_options(block_n=256, split_k=4))
+    assert info["split_k"] == 4 and info["num_units"] == 8 * 4
+    assert info["workspace_bytes"] >= 8 * 4 * 128 * 256 * 4
+
+
+@pytest.mark.parametrize("opt", [dict(block_n=96), dict(block_n=256, stages=5), dict(split_k=10 ** 6),
+                                 dict(epilogue=3), dict(max_ctas=-1)])
+def test_plan_rejects_bad_overrides(lib, opt):
+    with pytest.raises(tg.TgError):
+        tg.plan(512, 512, 512, sm_count=152, options=tg.make_options(**opt))
+
+
+def test_plan_rejects_tma_store_on_misaligned_c(lib):
+    with pytest.raises(tg.TgError):
+        tg.plan(64, 63, 64, ldc=63, sm_count=152, options=tg.make_options(epilogue=1))
+
+
+def test_plan_honours_overrides(lib):
+    info = tg.plan(1000, 1000, 1000, sm_count=152,
+                   options=tg.make_options(block_n=192, stages=3, split_k=2, max_ctas=5, force_pack=1))
+    assert (info["block_n"], info["stages"], info["split_k"], info["grid"]) == (192, 3, 2, 5)
+    assert info["pack_a"] == 1 and info["pack_b"] == 1
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    """No CPU fallback: a missing library is an error, not a slower path."""
+    monkeypatch.setattr(_abi, "_LIB", None)
+    monkeypatch.setattr(_abi, "library_path", lambda: str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        _abi.load()

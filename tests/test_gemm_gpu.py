@@ -1,0 +1,305 @@
+"""GPU parity of the CUDA path against the oracle, through the C ABI.
+
+Exact-arithmetic cases use small-integer bf16 inputs (every partial sum is
+an exact fp32 integer), so the GPU must equal the fp64 oracle bit for bit
+whatever the tiling, ring depth, split or store path.  Random-float cases use
+the contract's tolerance (relative Frobenius <= 1e-5, per element
+<= 1e-5 sqrt(K) max|C|).
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import tiled_gemm_codegen_gb300 as tg
+from gpu_helpers import assert_close, dev, oracle_dense, run
+
+pytestmark = pytest.mark.gpu
+
+WIDTHS = [64, 128, 192, 256]
+EDGE_SHAPES = [
+    (1, 1, 1), (7, 5, 3), (16, 16, 16), (17, 63, 65), (64, 64, 64), (127, 129, 128),
+    (128, 128, 128), (129, 255, 257), (255, 257, 129), (200, 300, 40), (65, 513, 191),
+]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    tg.load()
+    yield
+
+
+def _seed(*xs):
+    s = 17
+    for x in xs:
+        s = (s * 1000003 + int(x)) % (2 ** 31)
+    return s
+
+
+@pytest.mark.parametrize("bn", WIDTHS)
+@pytest.mark.parametrize("shape", EDGE_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_exact_integer_edge_shapes(bn, shape):
+    M, N, K = shape
+    A, B = synth.make_int_inputs(1, M, N, K, seed=_seed(M, N, K, bn))
+    got = run(A, B, options=tg.make_options(block_n=bn))
+    assert np.array_equal(got, oracle_dense(A, B))
+
+
+@pytest.mark.parametrize("bn", WIDTHS)
+def test_exact_integer_batched(bn):
+    batch, M, N, K = 3, 131, 197, 333
+    A, B = synth.make_int_inputs(batch, M, N, K, seed=_seed(batch, bn))
+    got = run(A, B, options=tg.make_options(block_n=bn))
+    assert np.array_equal(got, oracle_dense(A, B))
+
+
+@pytest.mark.parametrize("shape", [(197, 131, 77), (300, 200, 500), (129, 513, 1000),
+                                   (1000, 64, 2048), (64, 1024, 4096)],
+                         ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("dist", ["uniform", "normal"])
+def test_float_parity_default_plan(shape, dist):
+    M, N, K = shape
+    A, B = synth.make_inputs(1, M, N, K, dist, seed=_seed(M, N, K))
+    assert_close(run(A, B), oracle_dense(A, B), K, f"{shape} {dist}")
+
+
+@pytest.mark.parametrize("bn", WIDTHS)
+def test_float_parity_each_width(bn):
+    M, N, K = 257, 389, 700
+    A, B = synth.make_inputs(2, M, N, K, "normal", seed=_seed(bn, 5))
+    assert_close(run(A, B, options=tg.make_options(block_n=bn)), oracle_dense(A, B), K, f"bn={bn}")
+
+
+@pytest.mark.parametrize("bn,depths", [(64, [2, 4, 6, 8]), (128, [2, 3, 4, 6]),
+                                       (192, [2, 3, 4]), (256, [2, 3, 4])])
+def test_ring_depth_bitwise_invariance(bn, depths):
+    """OCANNL pipeline_depth: the pipelined rendering reads the same values in
+    the same order, so the output is bitwise independent of the depth."""
+    M, N, K = 300, 520, 1100
+    A, B = synth.make_inputs(1, M, N, K, "uniform", seed=_seed(bn, 7))
+    outs = [run(A, B, options=tg.make_options(block_n=bn, stages=s)) for s in depths]
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0])
+    assert_close(outs[0], oracle_dense(A, B), K)
+
+
+def test_persistent_grid_bitwise_invariance():
+    """A CTA that walks many tiles (accumulator double buffer, ring phases
+    wrapping) gives the same bits as one tile per CTA."""
+    M, N, K = 640, 768, 512
+    A, B = synth.make_inputs(1, M, N, K, "normal", seed=3)
+    base = run(A, B, options=tg.make_options(block_n=128))
+    for ctas in (1, 3, 7):
+        got = run(A, B, options=tg.make_options(block_n=128, max_ctas=ctas))
+        assert np.array_equal(got, base), ctas
+
+
+def test_epilogue_paths_bitwise_equal():
+    M, N, K = 333, 444, 555
+    A, B = synth.make_inputs(1, M, N, K, "uniform", seed=4)
+    t = run(A, B, options=tg.make_options(block_n=192, epilogue=1))
+    d = run(A, B, options=tg.make_options(block_n=192, epilogue=2))
+    assert np.array_equal(t, d)
+    assert_close(t, oracle_dense(A, B), K)
+
+
+def test_pack_path_bitwise_equal():
+    M, N, K = 190, 250, 310
+    A, B = synth.make_inputs(1, M, N, K, "normal", seed=5)
+    plain = run(A, B, options=tg.make_options(block_n=128))
+    packed = run(A, B, options=tg.make_options(block_n=128, force_pack=1))
+    assert np.array_equal(plain, packed)
+
+
+@pytest.mark.parametrize("splits", [2, 3, 4, 7])
+def test_split_k_exact_integer(splits):
+    """Split reduction: the combined partials equal the full sum exactly
+    with integer inputs."""
+    M, N, K = 150, 300, 2048
+    A, B = synth.make_int_inputs(1, M, N, K, seed=splits)
+    got = run(A, B, options=tg.make_options(block_n=128, split_k=splits))
+    assert np.array_equal(got, oracle_dense(A, B))
+
+
+def test_split_k_deterministic_and_close():
+    """Deterministic per plan (bitwise run to run), within tolerance of the
+    oracle and of other split factors (OCANNL two-pass split reduction)."""
+    M, N, K = 64, 2048, 8192
+    A, B = synth.make_inputs(1, M, N, K, "normal002", seed=9)
+    ref = oracle_dense(A, B)
+    outs = {}
+    for s in (1, 2, 4, 8):
+        o1 = run(A, B, options=tg.make_options(block_n=256, split_k=s))
+        o2 = run(A, B, options=tg.make_options(block_n=256, split_k=s))
+        assert np.array_equal(o1, o2), s
+        assert_close(o1, ref, K, f"split {s}")
+        outs[s] = o1
+
+
+def test_split_k_batched_ragged():
+    batch, M, N, K = 3, 100, 300, 1000
+    A, B = synth.make_int_inputs(batch, M, N, K, seed=12)
+    got = run(A, B, options=tg.make_options(block_n=64, split_k=5, max_ctas=4))
+    assert np.array_equal(got, oracle_dense(A, B))
+
+
+def _guarded_c(M, N, ldc, rows_pad=3, lead=0):
+    """A NaN-filled device buffer and a view C[M, N] with row stride ldc
+    starting `lead` elements in."""
+    total = lead + (M + rows_pad) * ldc
+    buf = torch.full((total,), float("nan"), dtype=torch.float32, device=dev())
+    view = buf[lead: lead + M * ldc].view(M, ldc)[:, :N]
+    return buf, view
+
+
+@pytest.mark.parametrize("ldc_pad,lead", [(0, 0), (24, 0), (3, 0), (8, 1), (5, 3)])
+def test_guard_bands(ldc_pad, lead):
+    """Elements of C outside the M x N block (row padding, trailing rows,
+    leading elements) are never written; covers both store paths."""
+    M, N, K = 150, 200, 96
+    ldc = N + ldc_pad
+    A, B = synth.make_int_inputs(1, M, N, K, seed=ldc_pad)
+    buf, C = _guarded_c(M, N, ldc, lead=lead)
+    tg.gemm(A.to(dev()), B.to(dev()), C)
+    assert tg.device_error() == tg.TG_OK
+    host = buf.cpu().numpy()
+    mask = np.zeros(host.shape, dtype=bool)
+    for i in range(M):
+        mask[lead + i * ldc: lead + i * ldc + N] = True
+    assert np.all(np.isnan(host[~mask])), "write outside the M x N block"
+    got = np.stack([host[lead + i * ldc: lead + i * ldc + N] for i in range(M)]).astype(np.float64)
+    assert np.array_equal(got, oracle_dense(A, B))
+
+
+@pytest.mark.parametrize("a_off,b_off,lda_pad,ldb_pad", [(1, 0, 0, 0), (0, 3, 0, 0), (0, 0, 1, 0),
+                                                          (0, 0, 0, 5), (2, 1, 3, 7)])
+def test_misaligned_operands_use_pack(a_off, b_off, lda_pad, ldb_pad):
+    M, N, K = 97, 211, 150
+    lda, ldb = K + lda_pad, N + ldb_pad
+    Ai, Bi = synth.make_int_inputs(1, M, N, K, seed=a_off * 10 + b_off)
+    abuf = torch.zeros(a_off + M * lda, dtype=torch.bfloat16)
+    bbuf = torch.zeros(b_off + K * ldb, dtype=torch.bfloat16)
+    abuf[a_off:].view(M, lda)[:, :K] = Ai
+    bbuf[b_off:].view(K, ldb)[:, :N] = Bi
+    ad = abuf.to(dev())
+    bd = bbuf.to(dev())
+    A = ad[a_off:].view(M, lda)[:, :K]
+    B = bd[b_off:].view(K, ldb)[:, :N]
+    C = torch.empty(M, N, dtype=torch.float32, device=dev())
+    info = tg.plan(M, N, K, lda=lda, ldb=ldb, A=A.data_ptr(), B=B.data_ptr(), C=C.data_ptr())
+    assert info["pack_a"] == int(a_off % 8 != 0 or lda % 8 != 0)
+    assert info["pack_b"] == int(b_off % 8 != 0 or ldb % 8 != 0)
+    tg.gemm(A, B, C)
+    assert tg.device_error() == tg.TG_OK
+    assert np.array_equal(C.cpu().double().numpy(), oracle_dense(Ai, Bi))
+
+
+def test_strided_batches_with_gaps():
+    batch, M, N, K = 4, 70, 90, 110
+    Ai, Bi = synth.make_int_inputs(batch, M, N, K, seed=21)
+    sA, sB = M * K + 64, K * N + 40
+    abuf = torch.zeros(batch * sA, dtype=torch.bfloat16)
+    bbuf = torch.zeros(batch * sB, dtype=torch.bfloat16)
+    for b in range(batch):
+        abuf[b * sA: b * sA + M * K] = Ai[b].reshape(-1)
+        bbuf[b * sB: b * sB + K * N] = Bi[b].reshape(-1)
+    ad, bd = abuf.to(dev()), bbuf.to(dev())
+    A = torch.as_strided(ad, (batch, M, K), (sA, K, 1))
+    B = torch.as_strided(bd, (batch, K, N), (sB, N, 1))
+    got = tg.gemm(A, B)
+    assert tg.device_error() == tg.TG_OK
+    assert np.array_equal(got.cpu().double().numpy(), oracle_dense(Ai, Bi))
+
+
+def test_broadcast_operand():
+    """Batch stride 0: the same B for every problem."""
+    batch, M, N, K = 5, 130, 140, 150
+    Ai, _ = synth.make_int_inputs(batch, M, N, K, seed=31)
+    _, Bi = synth.make_int_inputs(1, M, N, K, seed=32)
+    got = tg.gemm(Ai.to(dev()), Bi.to(dev()))
+    assert tg.device_error() == tg.TG_OK
+    ref = oracle_dense(Ai, Bi.unsqueeze(0).expand(batch, K, N).contiguous())
+    assert np.array_equal(got.cpu().double().numpy(), ref)
+
+
+def test_k_zero_and_empty():
+    C = torch.full((5, 6), 7.0, device=dev())
+    A = torch.empty(5, 0, dtype=torch.bfloat16, device=dev())
+    B = torch.empty(0, 6, dtype=torch.bfloat16, device=dev())
+    tg.gemm(A, B, C)
+    assert tg.device_error() == tg.TG_OK
+    assert torch.all(C.cpu() == 0)
+    # M == 0: nothing enqueued, status OK
+    A0 = torch.empty(0, 4, dtype=torch.bfloat16, device=dev())
+    B0 = torch.ones(4, 3, dtype=torch.bfloat16, device=dev())
+    C0 = tg.gemm(A0, B0)
+    assert C0.shape == (0, 3)
+
+
+def test_host_entry_point_matches_device():
+    M, N, K = 210, 170, 390
+    A, B = synth.make_inputs(1, M, N, K, "uniform", seed=41)
+    ch = tg.gemm_host(A.pin_memory(), B.pin_memory())
+    cd = run(A, B)
+    assert np.array_equal(ch.double().numpy(), cd)
+    # gaps between rows of a host C are preserved
+    ldc = N + 6
+    Cbuf = torch.full((M, ldc), -3.0)
+    tg.gemm_host(A, B, Cbuf[:, :N])
+    assert torch.all(Cbuf[:, N:] == -3.0)
+    assert np.array_equal(Cbuf[:, :N].double().numpy(), cd)
+
+
+def test_watchdog_reports_timeout_and_recovers():
+    """A wait on a barrier nothing completes: the kernel gives up after the
+    limit, records the error and exits; the host reads TG_ERR_TIMEOUT, the
+    word is cleared, and the next call is exact again."""
+    M, N, K = 300, 300, 256
+    A, B = synth.make_int_inputs(1, M, N, K, seed=51)
+    ad, bd = A.to(dev()), B.to(dev())
+    for ctas in (0, 1):  # one tile per CTA, and one CTA walking all tiles
+        opts = tg.make_options(debug_stall=1, timeout_ns=20_000_000, block_n=128, max_ctas=ctas)
+        tg.gemm(ad, bd, options=opts)
+        assert tg.device_error() == tg.TG_ERR_TIMEOUT
+        assert tg.device_error() == tg.TG_OK
+    got = tg.gemm(ad, bd)
+    assert tg.device_error() == tg.TG_OK
+    assert np.array_equal(got.cpu().double().numpy(), oracle_dense(A, B))
+
+
+def test_split_k_counters_reset_after_timeout():
+    """An aborted split-K launch leaves the counters part-way; reading the
+    error resets them, so the next split-K call is exact."""
+    M, N, K = 128, 256, 1024
+    A, B = synth.make_int_inputs(1, M, N, K, seed=61)
+    ad, bd = A.to(dev()), B.to(dev())
+    tg.gemm(ad, bd, options=tg.make_options(debug_stall=1, timeout_ns=20_000_000, split_k=4))
+    assert tg.device_error() == tg.TG_ERR_TIMEOUT
+    got = tg.gemm(ad, bd, options=tg.make_options(split_k=4))
+    assert tg.device_error() == tg.TG_OK
+    assert np.array_equal(got.cpu().double().numpy(), oracle_dense(A, B))
+
+
+def test_invalid_arguments_on_device():
+    A = torch.zeros(4, 4, dtype=torch.bfloat16, device=dev())
+    B = torch.zeros(4, 4, dtype=torch.bfloat16, device=dev())
+    C = torch.zeros(4, 4, dtype=torch.float32, device=dev())
+    # C overlapping A
+    st = tg.tg_gemm(A.data_ptr(), B.data_ptr(), A.data_ptr(), 4, 4, 4, 4, 4, 4, 1, 16, 16, 16)
+    assert st == tg.TG_ERR_INVALID_ARG
+    # bad override
+    st = tg.tg_gemm_ex(A.data_ptr(), B.data_ptr(), C.data_ptr(), 4, 4, 4, 4, 4, 4, 1, 16, 16, 16,
+                       None, tg.make_options(block_n=96))
+    assert st == tg.TG_ERR_INVALID_ARG
+    st = tg.tg_gemm_ex(A.data_ptr(), B.data_ptr(), C.data_ptr(), 4, 4, 4, 4, 4, 4, 1, 16, 16, 16,
+                       None, tg.make_options(stages=5, block_n=256))
+    assert st == tg.TG_ERR_INVALID_ARG
+
+
+def test_plan_queries_device():
+    info = tg.plan(4096, 4096, 4096)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert 1 <= info["grid"] <= sms

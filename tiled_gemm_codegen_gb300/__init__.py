@@ -1,0 +1,194 @@
+"""tiled_gemm_codegen_gb300 - a tiled bf16 -> fp32 GEMM for GB300 (sm_103a).
+
+The product is the C-ABI CUDA library declared in ``include/tg_gemm.h``.
+This package is its thin Python binding: the C functions under the same
+names (``tg_gemm``, ``tg_gemm_ex``, ``tg_gemm_host``, ``tg_plan``,
+``tg_device_error``, ``tg_status_string``, ``tg_shutdown``) taking raw
+pointers and sizes, plus conveniences that read pointers, shapes and
+strides off torch tensors.  PyTorch only provides device memory and
+streams; no arithmetic happens here.
+"""
+from __future__ import annotations
+
+import ctypes
+
+from ._abi import (TG_ERR_CUDA, TG_ERR_INVALID_ARG, TG_ERR_OOM, TG_ERR_TIMEOUT,
+                   TG_ERR_UNSUPPORTED, TG_OK, STATUS_NAMES, library_path, load, tg_options,
+                   tg_plan_info)
+
+__all__ = [
+    "TG_OK", "TG_ERR_INVALID_ARG", "TG_ERR_UNSUPPORTED", "TG_ERR_CUDA", "TG_ERR_OOM",
+    "TG_ERR_TIMEOUT", "TgError", "tg_options", "tg_plan_info", "load", "library_path",
+    "tg_gemm", "tg_gemm_ex", "tg_gemm_host", "tg_plan", "tg_device_error", "tg_status_string",
+    "tg_shutdown", "make_options", "gemm", "gemm_host", "plan", "device_error",
+]
+
+
+class TgError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        name = STATUS_NAMES.get(status, str(status))
+        super().__init__(f"{what}: {name} ({tg_status_string(status)})" if what else name)
+
+
+# ---------------------------------------------------------------- raw C ABI
+def tg_gemm(A, B, C, M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC, stream=None) -> int:
+    return load().tg_gemm(A, B, C, M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC, stream)
+
+
+def tg_gemm_ex(A, B, C, M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC, stream=None,
+               opt=None) -> int:
+    return load().tg_gemm_ex(A, B, C, M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC,
+                             stream, ctypes.byref(opt) if opt is not None else None)
+
+
+def tg_gemm_host(A, B, C, M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC, stream=None,
+                 opt=None) -> int:
+    return load().tg_gemm_host(A, B, C, M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC,
+                               stream, ctypes.byref(opt) if opt is not None else None)
+
+
+def tg_plan(A, B, C, M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC, sm_count=0,
+            opt=None, out=None):
+    out = tg_plan_info() if out is None else out
+    st = load().tg_plan(A, B, C, M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC,
+                        sm_count, ctypes.byref(opt) if opt is not None else None, ctypes.byref(out))
+    return st, out
+
+
+def tg_device_error(stream=None) -> int:
+    return load().tg_device_error(stream)
+
+
+def tg_status_string(status: int) -> str:
+    return load().tg_status_string(status).decode()
+
+
+def tg_shutdown() -> None:
+    load().tg_shutdown()
+
+
+# ---------------------------------------------------------------- conveniences
+def make_options(**kw) -> tg_options:
+    o = tg_options()
+    for k, v in kw.items():
+        if not hasattr(o, k):
+            raise TypeError(f"unknown option {k!r}")
+        setattr(o, k, int(v))
+    return o
+
+
+def _stream_ptr(stream):
+    import torch
+
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _operand_geometry(t, rows_dim, what):
+    """(ptr, rows, cols, ld, batch, batch_stride) of a 2-D or 3-D tensor
+    whose last dim has unit stride."""
+    if t.dim() not in (2, 3):
+        raise ValueError(f"{what} must be 2-D or 3-D")
+    if t.stride(-1) != 1 and t.size(-1) > 1:
+        raise ValueError(f"{what} must have unit stride in its last dimension")
+    rows, cols = t.shape[-2], t.shape[-1]
+    ld = t.stride(-2) if rows > 1 else max(cols, 1)
+    if t.dim() == 3:
+        batch, sb = t.shape[0], (t.stride(0) if t.shape[0] > 1 else 0)
+    else:
+        batch, sb = 1, 0
+    return t.data_ptr(), rows, cols, max(ld, cols), batch, sb
+
+
+def gemm(A, B, C=None, *, options: tg_options | None = None, stream=None):
+    """C = A @ B (per problem) for CUDA bf16 tensors A [.., M, K], B [.., K, N];
+    C is an fp32 CUDA tensor [.., M, N] (allocated when None).  Asynchronous
+    on ``stream`` (default: torch's current stream)."""
+    import torch
+
+    if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
+        raise TypeError("A and B must be bf16")
+    if not (A.is_cuda and B.is_cuda):
+        raise ValueError("A and B must be CUDA tensors (use gemm_host for host buffers)")
+    pa, M, K, lda, ba, sA = _operand_geometry(A, -2, "A")
+    pb, K2, N, ldb, bb, sB = _operand_geometry(B, -2, "B")
+    if K2 != K:
+        raise ValueError(f"inner dimensions differ: {K} vs {K2}")
+    batch = max(ba, bb)
+    if ba not in (1, batch) or bb not in (1, batch):
+        raise ValueError("batch sizes differ")
+    if ba == 1:
+        sA = 0
+    if bb == 1:
+        sB = 0
+    if C is None:
+        shape = (batch, M, N) if (A.dim() == 3 or B.dim() == 3) else (M, N)
+        C = torch.empty(shape, dtype=torch.float32, device=A.device)
+    if C.dtype != torch.float32 or not C.is_cuda:
+        raise TypeError("C must be an fp32 CUDA tensor")
+    pc, Mc, Nc, ldc, bc, sC = _operand_geometry(C, -2, "C")
+    if (Mc, Nc) != (M, N) or bc != batch:
+        raise ValueError("C has the wrong shape")
+    st = tg_gemm_ex(pa, pb, pc, M, N, K, lda, ldb, ldc, batch, sA, sB, sC, _stream_ptr(stream),
+                    options)
+    if st != TG_OK:
+        raise TgError(st, "tg_gemm_ex")
+    return C
+
+
+def gemm_host(A, B, C=None, *, options: tg_options | None = None, stream=None):
+    """The same product on HOST (CPU) tensors, through tg_gemm_host (copies in
+    and out inside the call; synchronous)."""
+    import torch
+
+    if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
+        raise TypeError("A and B must be bf16")
+    if A.is_cuda or B.is_cuda:
+        raise ValueError("gemm_host takes host tensors")
+    pa, M, K, lda, ba, sA = _operand_geometry(A, -2, "A")
+    pb, K2, N, ldb, bb, sB = _operand_geometry(B, -2, "B")
+    if K2 != K:
+        raise ValueError(f"inner dimensions differ: {K} vs {K2}")
+    batch = max(ba, bb)
+    if ba == 1:
+        sA = 0
+    if bb == 1:
+        sB = 0
+    if C is None:
+        shape = (batch, M, N) if (A.dim() == 3 or B.dim() == 3) else (M, N)
+        C = torch.empty(shape, dtype=torch.float32)
+    pc, Mc, Nc, ldc, bc, sC = _operand_geometry(C, -2, "C")
+    if (Mc, Nc) != (M, N) or bc != batch:
+        raise ValueError("C has the wrong shape")
+    st = tg_gemm_host(pa, pb, pc, M, N, K, lda, ldb, ldc, batch, sA, sB, sC,
+                      _stream_ptr(stream), options)
+    if st != TG_OK:
+        raise TgError(st, "tg_gemm_host")
+    return C
+
+
+def plan(M, N, K, batch=1, *, lda=None, ldb=None, ldc=None, strideA=None, strideB=None,
+         strideC=None, A=0x1000, B=0x100000000, C=0x200000000, sm_count=0, options=None) -> dict:
+    """The plan tg_gemm_ex would use (host-only when sm_count > 0).  The
+    default addresses are placeholders with 16-byte alignment; pass real or
+    deliberately misaligned addresses to see the pack decisions."""
+    lda = K if lda is None else lda
+    ldb = N if ldb is None else ldb
+    ldc = N if ldc is None else ldc
+    strideA = M * lda if strideA is None else strideA
+    strideB = K * ldb if strideB is None else strideB
+    strideC = M * ldc if strideC is None else strideC
+    st, info = tg_plan(A, B, C, M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC,
+                       sm_count, options)
+    if st != TG_OK:
+        raise TgError(st, "tg_plan")
+    return info.as_dict()
+
+
+def device_error(stream=None) -> int:
+    """Synchronise the stream and return (and clear) its watchdog status."""
+    return tg_device_error(_stream_ptr(stream))

@@ -1,0 +1,645 @@
+// Host side of the C ABI declared in include/tg_gemm.h: argument checks,
+// planning, per-stream workspaces, TMA descriptors, and the two small
+// kernels of the path besides the GEMM itself (the pack pass that realigns
+// operands TMA cannot address, and the zero fill of the K == 0 case).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "tg_gemm.h"
+#include "tg_internal.h"
+#include "tg_plan.h"
+
+#define TG_API extern "C" __attribute__((visibility("default")))
+
+namespace tg {
+namespace {
+
+constexpr uint64_t DEFAULT_TIMEOUT_NS = 2000000000ull;  // 2 s
+constexpr int64_t EXTENT_LIMIT = INT32_MAX;
+
+// ------------------------------------------------------------ small kernels
+// Pack (the realign pass): copy a batch of rows x cols bf16 matrices with
+// arbitrary element strides into a dense buffer whose rows are padded to a
+// multiple of 8 elements (16 bytes) - the address form TMA can load.  The
+// pad columns are written as 0; the GEMM never reads them (its tensor map
+// extent is the true column count).
+__global__ void pack_bf16_kernel(const uint16_t *__restrict__ src, uint16_t *__restrict__ dst,
+                                 int64_t rows, int64_t cols, int64_t ld_src, int64_t s_src,
+                                 int64_t ld_dst, int64_t total_chunks)
+{
+    const int64_t chunks_per_row = ld_dst / 8;
+    for (int64_t c = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; c < total_chunks;
+         c += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t row_g = c / chunks_per_row;
+        const int64_t col0 = (c - row_g * chunks_per_row) * 8;
+        const int64_t b = row_g / rows;
+        const int64_t r = row_g - b * rows;
+        const uint16_t *s = src + b * s_src + r * ld_src + col0;
+        uint16_t v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = (col0 + e < cols) ? s[e] : static_cast<uint16_t>(0);
+        uint4 out;
+        out.x = static_cast<uint32_t>(v[0]) | (static_cast<uint32_t>(v[1]) << 16);
+        out.y = static_cast<uint32_t>(v[2]) | (static_cast<uint32_t>(v[3]) << 16);
+        out.z = static_cast<uint32_t>(v[4]) | (static_cast<uint32_t>(v[5]) << 16);
+        out.w = static_cast<uint32_t>(v[6]) | (static_cast<uint32_t>(v[7]) << 16);
+        *reinterpret_cast<uint4 *>(dst + row_g * ld_dst + col0) = out;
+    }
+}
+
+// K == 0: every entry of C is the empty sum.
+__global__ void zero_c_kernel(float *C, int64_t M, int64_t N, int64_t ldc, int64_t sC,
+                              int64_t total)
+{
+    for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
+         e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t b = e / (M * N);
+        const int64_t r = e - b * M * N;
+        const int64_t i = r / N;
+        const int64_t j = r - i * N;
+        C[b * sC + i * ldc + j] = 0.0f;
+    }
+}
+
+// ------------------------------------------------------------ argument checks
+struct Args {
+    const void *A;
+    const void *B;
+    float *C;
+    int64_t M, N, K, lda, ldb, ldc, batch, sA, sB, sC;
+};
+
+// Elements spanned by one operand over all problems (0 if empty).  Callers
+// have bounded every factor (extents < 2^31, strides <= 2^40) and checked
+// the total against SPAN_LIMIT in 128-bit arithmetic first.
+int64_t span_elems(int64_t rows, int64_t cols, int64_t ld, int64_t batch, int64_t stride)
+{
+    if (rows == 0 || cols == 0) return 0;
+    return (batch - 1) * stride + (rows - 1) * ld + cols;
+}
+
+constexpr __int128 SPAN_LIMIT = static_cast<__int128>(1) << 56;  // elements
+
+bool span_ok(int64_t rows, int64_t cols, int64_t ld, int64_t batch, int64_t stride)
+{
+    if (rows == 0 || cols == 0) return true;
+    const __int128 s = static_cast<__int128>(batch - 1) * stride +
+                       static_cast<__int128>(rows - 1) * ld + cols;
+    return s < SPAN_LIMIT;
+}
+
+bool ranges_overlap(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1)
+{
+    return a0 < b1 && b0 < a1;
+}
+
+// Checks everything the header promises, before any CUDA call.
+tg_status validate(const Args &a)
+{
+    if (a.M < 0 || a.N < 0 || a.K < 0 || a.batch < 1) return TG_ERR_INVALID_ARG;
+    if (a.M > EXTENT_LIMIT || a.N > EXTENT_LIMIT || a.K > EXTENT_LIMIT || a.batch > EXTENT_LIMIT)
+        return TG_ERR_INVALID_ARG;
+    if (a.sA < 0 || a.sB < 0 || a.sC < 0) return TG_ERR_INVALID_ARG;
+    if (a.lda < a.K || a.ldb < a.N || a.ldc < a.N) return TG_ERR_INVALID_ARG;
+    // strides beyond 2^40 elements are not addressable in any case
+    const int64_t STRIDE_LIMIT = int64_t(1) << 40;
+    if (a.lda > STRIDE_LIMIT || a.ldb > STRIDE_LIMIT || a.ldc > STRIDE_LIMIT ||
+        a.sA > STRIDE_LIMIT || a.sB > STRIDE_LIMIT || a.sC > STRIDE_LIMIT)
+        return TG_ERR_INVALID_ARG;
+    if (a.M == 0 || a.N == 0) return TG_OK;
+    if (!span_ok(a.M, a.N, a.ldc, a.batch, a.sC) || !span_ok(a.M, a.K, a.lda, a.batch, a.sA) ||
+        !span_ok(a.K, a.N, a.ldb, a.batch, a.sB))
+        return TG_ERR_INVALID_ARG;
+    if (a.C == nullptr) return TG_ERR_INVALID_ARG;
+    if (a.K > 0 && (a.A == nullptr || a.B == nullptr)) return TG_ERR_INVALID_ARG;
+    // distinct problems may not share an element of C
+    const int64_t one_c = (a.M - 1) * a.ldc + a.N;
+    if (a.batch > 1 && a.sC < one_c) return TG_ERR_INVALID_ARG;
+    if (a.K > 0) {
+        const uintptr_t c0 = reinterpret_cast<uintptr_t>(a.C);
+        const uintptr_t c1 = c0 + 4u * static_cast<uintptr_t>(span_elems(a.M, a.N, a.ldc, a.batch, a.sC));
+        const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.A);
+        const uintptr_t a1 = a0 + 2u * static_cast<uintptr_t>(span_elems(a.M, a.K, a.lda, a.batch, a.sA));
+        const uintptr_t b0 = reinterpret_cast<uintptr_t>(a.B);
+        const uintptr_t b1 = b0 + 2u * static_cast<uintptr_t>(span_elems(a.K, a.N, a.ldb, a.batch, a.sB));
+        if (ranges_overlap(c0, c1, a0, a1) || ranges_overlap(c0, c1, b0, b1))
+            return TG_ERR_INVALID_ARG;
+    }
+    return TG_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+PlanInput plan_input(const Args &a, int sms, const tg_options *opt)
+{
+    PlanInput in{};
+    in.M = a.M;
+    in.N = a.N;
+    in.K = a.K;
+    in.batch = a.batch;
+    in.a_bcast = a.batch > 1 && a.sA == 0;
+    in.b_bcast = a.batch > 1 && a.sB == 0;
+    const bool batched_a = a.batch > 1 && !in.a_bcast;
+    const bool batched_b = a.batch > 1 && !in.b_bcast;
+    in.a_tma_ok = aligned16(a.A) && (a.lda * 2) % 16 == 0 && (!batched_a || (a.sA * 2) % 16 == 0);
+    in.b_tma_ok = aligned16(a.B) && (a.ldb * 2) % 16 == 0 && (!batched_b || (a.sB * 2) % 16 == 0);
+    in.c_tma_ok = aligned16(a.C) && (a.ldc * 4) % 16 == 0 && (a.batch == 1 || (a.sC * 4) % 16 == 0);
+    in.sm_count = sms;
+    if (opt) {
+        in.block_n = opt->block_n;
+        in.stages = opt->stages;
+        in.split_k = opt->split_k;
+        in.force_pack = opt->force_pack;
+        in.epilogue = opt->epilogue;
+        in.max_ctas = opt->max_ctas;
+    }
+    return in;
+}
+
+void fill_info(const Plan &p, tg_plan_info *out)
+{
+    std::memset(out, 0, sizeof(*out));
+    out->block_m = BM;
+    out->block_n = p.bn;
+    out->block_k = BK;
+    out->stages = p.stages;
+    out->tiles_m = p.tiles_m;
+    out->tiles_n = p.tiles_n;
+    out->k_blocks = p.k_blocks;
+    out->split_k = p.splits;
+    out->num_units = p.units;
+    out->grid = p.grid;
+    out->pack_a = p.pack_a ? 1 : 0;
+    out->pack_b = p.pack_b ? 1 : 0;
+    out->epilogue = p.epilogue;
+    out->smem_bytes = p.smem;
+    out->tmem_cols = p.tmem;
+    out->workspace_bytes = p.workspace();
+}
+
+// ------------------------------------------------------------ device state
+struct DeviceInfo {
+    int sms = 0;
+};
+
+struct Workspace {
+    int device = -1;
+    void *arena = nullptr;  // pack copies + split-K partials
+    size_t arena_cap = 0;
+    int32_t *counters = nullptr;  // split-K arrival counters (kept zero between calls)
+    size_t counters_cap = 0;
+    uint32_t *err = nullptr;  // device error word of this stream
+    void *host_arena = nullptr;  // device copies of tg_gemm_host operands
+    size_t host_cap = 0;
+};
+
+std::mutex g_mutex;
+std::map<int, DeviceInfo> g_devices;
+std::map<std::pair<int, cudaStream_t>, Workspace> g_workspaces;
+
+tg_status cuda_status(cudaError_t e)
+{
+    if (e == cudaSuccess) return TG_OK;
+    if (e == cudaErrorMemoryAllocation) return TG_ERR_OOM;
+    return TG_ERR_CUDA;
+}
+
+tg_status device_sms(int dev, int *sms)
+{
+    auto it = g_devices.find(dev);
+    if (it != g_devices.end()) {
+        *sms = it->second.sms;
+        return TG_OK;
+    }
+    int v = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_status(e);
+    g_devices[dev].sms = v;
+    *sms = v;
+    return TG_OK;
+}
+
+Workspace &workspace_for(int dev, cudaStream_t stream)
+{
+    Workspace &w = g_workspaces[{dev, stream}];
+    w.device = dev;
+    return w;
+}
+
+// Grows a device buffer; waits for the stream first so that no kernel still
+// uses the old one.
+tg_status grow(void **buf, size_t *cap, size_t need, cudaStream_t stream)
+{
+    if (need <= *cap) return TG_OK;
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (*buf) cudaFree(*buf);
+    *buf = nullptr;
+    *cap = 0;
+    const size_t want = need + need / 4;
+    e = cudaMalloc(buf, want);
+    if (e != cudaSuccess) {
+        *buf = nullptr;
+        return cuda_status(e);
+    }
+    *cap = want;
+    return TG_OK;
+}
+
+tg_status ensure_err_word(Workspace &w, cudaStream_t stream)
+{
+    if (w.err) return TG_OK;
+    cudaError_t e = cudaMalloc(reinterpret_cast<void **>(&w.err), 256);
+    if (e != cudaSuccess) {
+        w.err = nullptr;
+        return cuda_status(e);
+    }
+    e = cudaMemsetAsync(w.err, 0, 256, stream);
+    return cuda_status(e);
+}
+
+tg_status ensure_counters(Workspace &w, size_t bytes, cudaStream_t stream)
+{
+    if (bytes <= w.counters_cap) return TG_OK;
+    void *p = w.counters;
+    tg_status st = grow(&p, &w.counters_cap, bytes, stream);
+    w.counters = static_cast<int32_t *>(p);
+    if (st != TG_OK) return st;
+    return cuda_status(cudaMemsetAsync(w.counters, 0, w.counters_cap, stream));
+}
+
+// ------------------------------------------------------------ TMA descriptors
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// A rank-3 tiled map: dim0 contiguous (d0 elements), dim1 rows (stride1
+// bytes), dim2 problems (stride2 bytes); box {box0, box1, 1}; 128B swizzle;
+// out-of-range elements read as zero.
+bool encode_3d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t d0, uint64_t d1,
+               uint64_t d2, uint64_t stride1, uint64_t stride2, uint32_t box0, uint32_t box1)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {stride1, stride2};
+    const cuuint32_t box[3] = {box0, box1, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Stride of the problem dimension when there is only one problem (any valid
+// value; never used to step).
+uint64_t single_problem_stride(uint64_t rows, uint64_t stride1)
+{
+    const uint64_t s = rows * stride1;
+    return (s + 15) / 16 * 16;
+}
+
+cudaError_t launch_gemm(int bn, const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
+                        const KernelParams &p, int stages, int grid, cudaStream_t s)
+{
+    switch (bn) {
+        case 64: return launch_gemm_bn64(ta, tb, tc, p, stages, grid, s);
+        case 128: return launch_gemm_bn128(ta, tb, tc, p, stages, grid, s);
+        case 192: return launch_gemm_bn192(ta, tb, tc, p, stages, grid, s);
+        case 256: return launch_gemm_bn256(ta, tb, tc, p, stages, grid, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+int grid_for(int64_t work, int sms)
+{
+    int64_t g = (work + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(sms) * 8;
+    if (g > cap) g = cap;
+    if (g < 1) g = 1;
+    return static_cast<int>(g);
+}
+
+// The whole device-side path of one call (arguments already validated).
+tg_status run_gemm(const Args &a, cudaStream_t stream, const tg_options *opt)
+{
+    if (a.M == 0 || a.N == 0) return TG_OK;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_status(e);
+    std::lock_guard<std::mutex> lock(g_mutex);
+    int sms = 0;
+    tg_status st = device_sms(dev, &sms);
+    if (st != TG_OK) return st;
+
+    if (a.K == 0) {
+        const int64_t total = a.batch * a.M * a.N;
+        zero_c_kernel<<<grid_for(total, sms), 256, 0, stream>>>(a.C, a.M, a.N, a.ldc, a.sC, total);
+        return cuda_status(cudaGetLastError());
+    }
+
+    PlanInput in = plan_input(a, sms, opt);
+    Plan plan;
+    if (!make_plan(in, plan)) return TG_ERR_INVALID_ARG;
+
+    Workspace &w = workspace_for(dev, stream);
+    st = ensure_err_word(w, stream);
+    if (st != TG_OK) return st;
+
+    const void *A = a.A;
+    const void *B = a.B;
+    int64_t lda = a.lda, ldb = a.ldb, sA = a.sA, sB = a.sB;
+
+    // Encode the operand maps; an operand TMA cannot describe is packed.
+    CUtensorMap ta{}, tb{}, tc{};
+    auto encode_a = [&]() {
+        const uint64_t z = in.a_bcast || a.batch == 1 ? 1 : static_cast<uint64_t>(a.batch);
+        const uint64_t s2 = z == 1 ? single_problem_stride(a.M, lda * 2) : static_cast<uint64_t>(sA) * 2;
+        return encode_3d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, a.K, a.M, z, lda * 2, s2, BK, BM);
+    };
+    auto encode_b = [&]() {
+        const uint64_t z = in.b_bcast || a.batch == 1 ? 1 : static_cast<uint64_t>(a.batch);
+        const uint64_t s2 = z == 1 ? single_problem_stride(a.K, ldb * 2) : static_cast<uint64_t>(sB) * 2;
+        return encode_3d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, a.N, a.K, z, ldb * 2, s2, 64, BK);
+    };
+    if (!encode_fn()) return TG_ERR_CUDA;
+    if (!plan.pack_a && !encode_a()) {
+        plan.pack_a = true;
+        plan.ws_pack_a = round_up((in.a_bcast ? 1 : a.batch) * a.M * round_up(a.K, 8) * 2, 256);
+    }
+    if (!plan.pack_b && !encode_b()) {
+        plan.pack_b = true;
+        plan.ws_pack_b = round_up((in.b_bcast ? 1 : a.batch) * a.K * round_up(a.N, 8) * 2, 256);
+    }
+
+    const size_t arena_need = static_cast<size_t>(plan.ws_pack_a + plan.ws_pack_b + plan.ws_partials);
+    if (arena_need > 0) {
+        st = grow(&w.arena, &w.arena_cap, arena_need, stream);
+        if (st != TG_OK) return st;
+    }
+    if (plan.ws_counters > 0) {
+        st = ensure_counters(w, static_cast<size_t>(plan.ws_counters), stream);
+        if (st != TG_OK) return st;
+    }
+    uint8_t *arena = static_cast<uint8_t *>(w.arena);
+    uint16_t *pack_a_buf = reinterpret_cast<uint16_t *>(arena);
+    uint16_t *pack_b_buf = reinterpret_cast<uint16_t *>(arena + plan.ws_pack_a);
+    float *partials = reinterpret_cast<float *>(arena + plan.ws_pack_a + plan.ws_pack_b);
+
+    if (plan.pack_a) {
+        const int64_t nb = in.a_bcast ? 1 : a.batch;
+        const int64_t ld2 = round_up(a.K, 8);
+        const int64_t chunks = nb * a.M * (ld2 / 8);
+        pack_bf16_kernel<<<grid_for(chunks, sms), 256, 0, stream>>>(
+            static_cast<const uint16_t *>(a.A), pack_a_buf, a.M, a.K, a.lda, a.sA, ld2, chunks);
+        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_status(e);
+        A = pack_a_buf;
+        lda = ld2;
+        sA = in.a_bcast ? 0 : a.M * ld2;
+        if (!encode_a()) return TG_ERR_CUDA;
+    }
+    if (plan.pack_b) {
+        const int64_t nb = in.b_bcast ? 1 : a.batch;
+        const int64_t ld2 = round_up(a.N, 8);
+        const int64_t chunks = nb * a.K * (ld2 / 8);
+        pack_bf16_kernel<<<grid_for(chunks, sms), 256, 0, stream>>>(
+            static_cast<const uint16_t *>(a.B), pack_b_buf, a.K, a.N, a.ldb, a.sB, ld2, chunks);
+        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_status(e);
+        B = pack_b_buf;
+        ldb = ld2;
+        sB = in.b_bcast ? 0 : a.K * ld2;
+        if (!encode_b()) return TG_ERR_CUDA;
+    }
+    if (plan.epilogue == 1) {
+        const uint64_t z = static_cast<uint64_t>(a.batch);
+        const uint64_t s2 = z == 1 ? single_problem_stride(a.M, a.ldc * 4) : static_cast<uint64_t>(a.sC) * 4;
+        if (!encode_3d(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.C, a.N, a.M, z, a.ldc * 4, s2,
+                       EPI_CHUNK, EPI_CHUNK)) {
+            if (opt && opt->epilogue == 1) return TG_ERR_UNSUPPORTED;
+            plan.epilogue = 2;
+        }
+    }
+    if (plan.epilogue != 1) tc = ta;  // unused by the kernel; any valid map
+
+    KernelParams p{};
+    p.M = static_cast<int32_t>(a.M);
+    p.N = static_cast<int32_t>(a.N);
+    p.K = static_cast<int32_t>(a.K);
+    p.batch = static_cast<int32_t>(a.batch);
+    p.tiles_m = plan.tiles_m;
+    p.tiles_n = plan.tiles_n;
+    p.splits = plan.splits;
+    p.k_blocks = plan.k_blocks;
+    p.num_units = plan.units;
+    p.group_m = plan.group_m;
+    p.a_bcast = in.a_bcast ? 1 : 0;
+    p.b_bcast = in.b_bcast ? 1 : 0;
+    p.epi_tma = plan.epilogue == 1 ? 1 : 0;
+    p.C = a.C;
+    p.ldc = a.ldc;
+    p.strideC = a.sC;
+    p.partials = plan.splits > 1 ? partials : nullptr;
+    p.counters = plan.splits > 1 ? w.counters : nullptr;
+    p.err = w.err;
+    p.timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : DEFAULT_TIMEOUT_NS;
+    p.debug_stall = (opt && opt->debug_stall) ? 1 : 0;
+
+    if (std::getenv("TG_TRACE"))
+        std::fprintf(stderr,
+                     "tg_gemm M=%lld N=%lld K=%lld batch=%lld: BN=%d stages=%d tiles=%dx%d kb=%d "
+                     "split=%d units=%lld grid=%d pack=%d/%d epi=%d\n",
+                     (long long)a.M, (long long)a.N, (long long)a.K, (long long)a.batch, plan.bn,
+                     plan.stages, plan.tiles_m, plan.tiles_n, plan.k_blocks, plan.splits,
+                     (long long)plan.units, plan.grid, plan.pack_a, plan.pack_b, plan.epilogue);
+
+    e = launch_gemm(plan.bn, ta, tb, tc, p, plan.stages, plan.grid, stream);
+    return cuda_status(e);
+}
+
+}  // namespace
+}  // namespace tg
+
+using namespace tg;
+
+TG_API const char *tg_status_string(tg_status s)
+{
+    switch (s) {
+        case TG_OK: return "ok";
+        case TG_ERR_INVALID_ARG: return "invalid argument";
+        case TG_ERR_UNSUPPORTED: return "unsupported";
+        case TG_ERR_CUDA: return "CUDA error";
+        case TG_ERR_OOM: return "out of device memory";
+        case TG_ERR_TIMEOUT: return "device wait timed out";
+        default: return "unknown status";
+    }
+}
+
+TG_API tg_status tg_gemm_ex(const void *A, const void *B, float *C, int64_t M, int64_t N, int64_t K,
+                            int64_t lda, int64_t ldb, int64_t ldc, int64_t batch, int64_t strideA,
+                            int64_t strideB, int64_t strideC, tg_stream_t stream,
+                            const tg_options *opt)
+{
+    const Args a{A, B, C, M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC};
+    tg_status st = validate(a);
+    if (st != TG_OK) return st;
+    if (opt) {
+        // option ranges are checked here too, before anything is enqueued
+        PlanInput in = plan_input(a, 148, opt);
+        Plan pl;
+        if (M > 0 && N > 0 && K > 0 && !make_plan(in, pl)) return TG_ERR_INVALID_ARG;
+    }
+    return run_gemm(a, reinterpret_cast<cudaStream_t>(stream), opt);
+}
+
+TG_API tg_status tg_gemm(const void *A, const void *B, float *C, int64_t M, int64_t N, int64_t K,
+                         int64_t lda, int64_t ldb, int64_t ldc, int64_t batch, int64_t strideA,
+                         int64_t strideB, int64_t strideC, tg_stream_t stream)
+{
+    return tg_gemm_ex(A, B, C, M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC, stream,
+                      nullptr);
+}
+
+TG_API tg_status tg_plan(const void *A, const void *B, const float *C, int64_t M, int64_t N,
+                         int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int64_t batch,
+                         int64_t strideA, int64_t strideB, int64_t strideC, int32_t sm_count,
+                         const tg_options *opt, tg_plan_info *out)
+{
+    if (!out || sm_count < 0) return TG_ERR_INVALID_ARG;
+    const Args a{A, B, const_cast<float *>(C), M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC};
+    tg_status st = validate(a);
+    if (st != TG_OK) return st;
+    int sms = sm_count;
+    if (sms == 0) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return cuda_status(e);
+        std::lock_guard<std::mutex> lock(g_mutex);
+        st = device_sms(dev, &sms);
+        if (st != TG_OK) return st;
+    }
+    std::memset(out, 0, sizeof(*out));
+    if (M == 0 || N == 0 || K == 0) return TG_OK;  // nothing (or only a zero fill) to plan
+    Plan p;
+    if (!make_plan(plan_input(a, sms, opt), p)) return TG_ERR_INVALID_ARG;
+    fill_info(p, out);
+    return TG_OK;
+}
+
+TG_API tg_status tg_gemm_host(const void *A_host, const void *B_host, float *C_host, int64_t M,
+                              int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                              int64_t batch, int64_t strideA, int64_t strideB, int64_t strideC,
+                              tg_stream_t stream_, const tg_options *opt)
+{
+    const Args a{A_host, B_host, C_host, M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC};
+    tg_status st = validate(a);
+    if (st != TG_OK) return st;
+    if (M == 0 || N == 0) return TG_OK;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_status(e);
+
+    const int64_t na = K > 0 ? span_elems(M, K, lda, batch, strideA) : 0;
+    const int64_t nb = K > 0 ? span_elems(K, N, ldb, batch, strideB) : 0;
+    const int64_t nc = span_elems(M, N, ldc, batch, strideC);
+    const size_t off_b = static_cast<size_t>(round_up(na * 2, 256));
+    const size_t off_c = off_b + static_cast<size_t>(round_up(nb * 2, 256));
+    const size_t need = off_c + static_cast<size_t>(round_up(nc * 4, 256));
+    uint8_t *dbuf = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        Workspace &w = workspace_for(dev, stream);
+        st = grow(&w.host_arena, &w.host_cap, need, stream);
+        if (st != TG_OK) return st;
+        dbuf = static_cast<uint8_t *>(w.host_arena);
+    }
+    void *dA = dbuf;
+    void *dB = dbuf + off_b;
+    float *dC = reinterpret_cast<float *>(dbuf + off_c);
+    if (na > 0 && (e = cudaMemcpyAsync(dA, A_host, na * 2, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+        return cuda_status(e);
+    if (nb > 0 && (e = cudaMemcpyAsync(dB, B_host, nb * 2, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+        return cuda_status(e);
+    st = run_gemm(Args{dA, dB, dC, M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC}, stream, opt);
+    if (st != TG_OK) return st;
+    // Copy back only the M x N block of every problem (gaps keep host data).
+    if (ldc == N && (batch == 1 || strideC == M * N)) {
+        e = cudaMemcpyAsync(C_host, dC, static_cast<size_t>(batch * M * N) * 4, cudaMemcpyDeviceToHost, stream);
+        if (e != cudaSuccess) return cuda_status(e);
+    } else {
+        for (int64_t b = 0; b < batch; ++b) {
+            e = cudaMemcpy2DAsync(C_host + b * strideC, ldc * 4, dC + b * strideC, ldc * 4, N * 4, M,
+                                  cudaMemcpyDeviceToHost, stream);
+            if (e != cudaSuccess) return cuda_status(e);
+        }
+    }
+    e = cudaStreamSynchronize(stream);
+    return cuda_status(e);
+}
+
+TG_API tg_status tg_device_error(tg_stream_t stream_)
+{
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return TG_ERR_CUDA;
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return TG_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    auto it = g_workspaces.find({dev, stream});
+    if (it == g_workspaces.end() || !it->second.err) return TG_OK;
+    Workspace &w = it->second;
+    uint32_t word = 0;
+    if ((e = cudaMemcpyAsync(&word, w.err, 4, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
+        return TG_ERR_CUDA;
+    if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return TG_ERR_CUDA;
+    if (word == ERR_NONE) return TG_OK;
+    // Clear the word, and the split-K counters an aborted kernel may have
+    // left part-way.
+    cudaMemsetAsync(w.err, 0, 4, stream);
+    if (w.counters) cudaMemsetAsync(w.counters, 0, w.counters_cap, stream);
+    cudaStreamSynchronize(stream);
+    return TG_ERR_TIMEOUT;
+}
+
+TG_API void tg_shutdown(void)
+{
+    std::lock_guard<std::mutex> lock(g_mutex);
+    int cur = 0;
+    cudaGetDevice(&cur);
+    for (auto &kv : g_workspaces) {
+        Workspace &w = kv.second;
+        cudaSetDevice(w.device);
+        if (w.arena) cudaFree(w.arena);
+        if (w.counters) cudaFree(w.counters);
+        if (w.err) cudaFree(w.err);
+        if (w.host_arena) cudaFree(w.host_arena);
+    }
+    g_workspaces.clear();
+    g_devices.clear();
+    cudaSetDevice(cur);
+}

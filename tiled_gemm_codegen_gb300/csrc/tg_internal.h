@@ -1,0 +1,81 @@
+// Internal interface between the host library (tg_host.cu) and the kernel
+// translation units (tg_kernel_bn*.cu).  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>  // CUtensorMap (type only; the driver is reached through cudart)
+#include <cuda_runtime.h>
+
+namespace tg {
+
+// Fixed tile geometry.  BM = 128 rows = the 128 tensor-memory lanes of one
+// SM; BK = 64 bf16 = 128 bytes = one 128B swizzle atom row.
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int EPI_CHUNK = 32;      // columns per tensor-memory load / store box
+constexpr int NUM_THREADS = 192;   // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int EPI_BUFS = 2;        // staging buffers per epilogue warp
+constexpr int SMEM_LIMIT = 232448; // max dynamic shared memory per CTA (227 KB)
+
+// Watchdog codes written to the device error word (first writer wins).
+enum : uint32_t {
+    ERR_NONE = 0,
+    ERR_TIMEOUT_PRODUCER = 1,
+    ERR_TIMEOUT_MMA = 2,
+    ERR_TIMEOUT_EPILOGUE = 3,
+    ERR_TIMEOUT_DRAIN = 4,
+};
+
+struct KernelParams {
+    int32_t M, N, K, batch;
+    int32_t tiles_m, tiles_n;
+    int32_t splits;       // K splits per output tile (>= 1)
+    int32_t k_blocks;     // ceil(K / BK)
+    int64_t num_units;    // batch * tiles_m * tiles_n * splits
+    int32_t group_m;      // tile-row group of the rasterisation
+    int32_t a_bcast;      // 1: A has batch stride 0 (same A for every problem)
+    int32_t b_bcast;      // 1: B has batch stride 0
+    int32_t epi_tma;      // 1: TMA store of C; 0: plain masked stores
+    float *C;             // plain-store epilogue target
+    int64_t ldc, strideC;
+    float *partials;      // split-K partial tiles
+    int32_t *counters;    // split-K arrival counters, one per output tile
+    uint32_t *err;        // device error word
+    uint64_t timeout_ns;
+    int32_t debug_stall;
+};
+
+// Shared-memory budget of one tile width (identical on host and device).
+template <int BN>
+struct Geometry {
+    static constexpr int A_STAGE = BM * BK * 2;          // 16 KB
+    static constexpr int B_STAGE = BK * BN * 2;          // BN * 128 B
+    static constexpr int STAGE = A_STAGE + B_STAGE;
+    static constexpr int EPI_BYTES = 4 * EPI_BUFS * EPI_CHUNK * EPI_CHUNK * 4;  // 32 KB
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int ALIGN_SLACK = 1024;
+    static constexpr int MAX_STAGES_RAW = (SMEM_LIMIT - EPI_BYTES - BAR_BYTES - ALIGN_SLACK) / STAGE;
+    static constexpr int MAX_STAGES = MAX_STAGES_RAW > 8 ? 8 : MAX_STAGES_RAW;
+    static constexpr int TMEM_COLS = (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
+    // At least 120 KB, so that two CTAs never share an SM: the persistent
+    // kernel assumes it owns the SM's tensor memory (up to all 512 columns).
+    static constexpr int ONE_CTA_PER_SM = 120 * 1024;
+    static constexpr int smem_bytes(int stages) {
+        return stages * STAGE + EPI_BYTES + BAR_BYTES + ALIGN_SLACK > ONE_CTA_PER_SM
+                   ? stages * STAGE + EPI_BYTES + BAR_BYTES + ALIGN_SLACK
+                   : ONE_CTA_PER_SM;
+    }
+};
+
+// Launch of the persistent GEMM kernel for one tile width (defined in the
+// per-width translation units).  Returns the launch's cudaError_t.
+cudaError_t launch_gemm_bn64(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
+                             const KernelParams &p, int stages, int grid, cudaStream_t s);
+cudaError_t launch_gemm_bn128(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
+                              const KernelParams &p, int stages, int grid, cudaStream_t s);
+cudaError_t launch_gemm_bn192(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
+                              const KernelParams &p, int stages, int grid, cudaStream_t s);
+cudaError_t launch_gemm_bn256(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
+                              const KernelParams &p, int stages, int grid, cudaStream_t s);
+
+}  // namespace tg

@@ -1,0 +1,451 @@
+// Persistent, warp-specialised bf16 -> fp32 GEMM kernel for sm_103a.
+//
+// One CTA per SM walks a static list of work units (output tile x K split).
+// Roles (the "Active subsets" of one accumulator's producers and consumers,
+// LuisaCompute "Execution Nests and coordinates", Logical anchor and
+// execution frontier):
+//   warp 0, lane 0 : TMA producer.  Loads the A tile [BM x BK] (K-major) and
+//                    the B tile [BK x BN] (N-major) of k-block kb into ring
+//                    slot kb mod STAGES with the 128-byte swizzle; boxes that
+//                    run past M, N or K are zero-filled by the TMA unit
+//                    (OCANNL "Module Ir.Schedule", Pad-to-tile and Stage:
+//                    out-of-range slots hold the additive identity 0).
+//   warp 1, lane 0 : MMA issuer.  BK/16 tcgen05.mma per slot into a tensor-
+//                    memory accumulator; the first one of a unit overwrites
+//                    (the zero-initialised accumulator of OCANNL Privatize).
+//   warps 2..5     : epilogue.  tcgen05.ld of the accumulator (warp w reads
+//                    TMEM lanes 32*(w%4) ..), then either a TMA store of
+//                    32 x 32 fp32 boxes through swizzled shared memory (the
+//                    store clips rows >= M and columns >= N), or plain masked
+//                    stores when C is not 16-byte aligned.
+// Synchronisation is the issue / completion / release protocol of
+// LuisaCompute "Pipelines and stage boundaries" (section "Issue, completion
+// and release are different events"):
+//   full[s]    : TMA completion (expect_tx bytes)         -> MMA may read s
+//   empty[s]   : tcgen05.commit after the slot's MMAs     -> TMA may refill s
+//   tfull[b]   : tcgen05.commit after a unit's last MMA   -> epilogue may read b
+//   tempty[b]  : 128 epilogue arrivals after the last ld  -> MMA may reuse b
+// The ring of STAGES slots generalises OCANNL's pipeline_depth: slot and
+// phase are (it mod STAGES, (it / STAGES) & 1), and the values the MMA reads
+// do not depend on STAGES, so the result is bitwise independent of it.
+//
+// Split-K (OCANNL "Module Ir.Schedule", Deterministic two-pass split
+// reduction): every split writes its fp32 partial tile to scratch, then the
+// last split to arrive at the tile's counter sums all partials in the fixed
+// order s = 0, 1, ..., splits-1 and stores C.  No split ever waits for
+// another, so the combine needs no grid-wide barrier.
+//
+// Every mbarrier wait is bounded (timeout_ns, %globaltimer).  On expiry the
+// waiting role records an error code in the device error word, raises a
+// CTA-wide abort flag that makes the other roles leave their loops, and the
+// CTA then waits (bounded) for its own TMA loads, MMAs and TMA stores in
+// flight, frees its tensor memory and returns.
+#pragma once
+
+#include "tg_internal.h"
+#include "tg_ptx.cuh"
+
+namespace tg {
+
+// tcgen05 shared-memory matrix descriptor, 128-byte swizzle.
+//   bits  0-13 start address >> 4     bits 16-29 leading byte offset >> 4
+//   bits 32-45 stride byte offset >> 4   bit 46 descriptor version (1)
+//   bits 49-51 base offset (0: atoms are 1024-byte aligned)
+//   bits 61-63 swizzle mode (2 = 128B)
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo)
+{
+    return static_cast<uint64_t>((addr >> 4) & 0x3FFFu) |
+           (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+           (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor of tcgen05.mma.kind::f16: D fp32 (bits 4-5 = 1),
+// A bf16 (bits 7-9 = 1), B bf16 (bits 10-12 = 1), A K-major (bit 15 = 0),
+// B MN-major (bit 16 = 1), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+template <int BN>
+__host__ __device__ constexpr uint32_t instr_desc_bf16()
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
+           (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
+}
+
+struct Unit {
+    int32_t b, tm, tn, split, kb0, kb1;
+    int64_t tile;  // linear output-tile index over (batch, tiles_m, tiles_n)
+};
+
+// Work unit u -> (problem, tile row, tile column, K split).  Splits of one
+// tile are adjacent; tiles are rasterised in groups of group_m tile rows so
+// that concurrently running CTAs share A and B panels in L2.
+__device__ __forceinline__ Unit decode_unit(const KernelParams &p, int64_t u)
+{
+    Unit w;
+    w.split = static_cast<int32_t>(u % p.splits);
+    const int64_t t = u / p.splits;
+    w.tile = t;
+    const int64_t per_batch = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
+    w.b = static_cast<int32_t>(t / per_batch);
+    const int64_t r = t % per_batch;
+    const int64_t group_tiles = static_cast<int64_t>(p.group_m) * p.tiles_n;
+    const int32_t g = static_cast<int32_t>(r / group_tiles);
+    const int32_t first_m = g * p.group_m;
+    const int32_t gsize = min(p.tiles_m - first_m, p.group_m);
+    const int32_t in = static_cast<int32_t>(r % group_tiles);
+    w.tm = first_m + in % gsize;
+    w.tn = in / gsize;
+    w.kb0 = static_cast<int32_t>((static_cast<int64_t>(w.split) * p.k_blocks) / p.splits);
+    w.kb1 = static_cast<int32_t>((static_cast<int64_t>(w.split + 1) * p.k_blocks) / p.splits);
+    return w;
+}
+
+enum WaitResult : int { WAIT_OK = 0, WAIT_TIMEOUT = 1, WAIT_ABORTED = 2 };
+
+struct Watchdog {
+    uint64_t timeout_ns;
+    volatile int32_t *abort_flag;
+    uint32_t *err;
+};
+
+// Bounded wait for the phase of parity `parity` of mbarrier `bar`.
+__device__ __forceinline__ int wait_bounded(uint32_t bar, uint32_t parity, const Watchdog &wd)
+{
+    if (ptx::mbar_try_wait(bar, parity)) return WAIT_OK;
+    const uint64_t t0 = ptx::global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (ptx::mbar_try_wait(bar, parity)) return WAIT_OK;
+        if ((it & 15u) == 0) {
+            if (*wd.abort_flag) return WAIT_ABORTED;
+            if (ptx::global_timer_ns() - t0 > wd.timeout_ns) return WAIT_TIMEOUT;
+        }
+    }
+}
+
+// Bounded wait that ignores the abort flag: used to drain this CTA's own
+// asynchronous operations before it exits.
+__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, const Watchdog &wd)
+{
+    const uint64_t t0 = ptx::global_timer_ns();
+    for (uint32_t it = 0;; ++it) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if ((it & 15u) == 15u && ptx::global_timer_ns() - t0 > wd.timeout_ns) {
+            atomicCAS(wd.err, 0u, static_cast<uint32_t>(ERR_TIMEOUT_DRAIN));
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void raise_abort(const Watchdog &wd, uint32_t code)
+{
+    atomicCAS(wd.err, 0u, code);
+    *wd.abort_flag = 1;
+    __threadfence_block();
+}
+
+// All 128 epilogue threads agree on a predicate (named barrier 1).
+__device__ __forceinline__ bool epi_all(bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred))
+        : "memory");
+    return r != 0;
+}
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmC, const KernelParams p)
+{
+    using G = Geometry<BN>;
+    static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "tile width");
+    static_assert(G::smem_bytes(STAGES) <= SMEM_LIMIT, "shared memory budget");
+    constexpr uint32_t B_BOX_BYTES = BK * 64 * 2;  // one 64-column box of B: 8 KB
+    constexpr uint32_t EPI_BOX_BYTES = EPI_CHUNK * EPI_CHUNK * 4;  // 4 KB
+
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_addr(smem_raw);
+    const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+    uint8_t *smem = smem_raw + pad;
+    const uint32_t sA = raw + pad;                  // STAGES x [BM x BK] bf16
+    const uint32_t sB = sA + STAGES * G::A_STAGE;   // STAGES x [BK x BN] bf16
+    const uint32_t sE = sB + STAGES * G::B_STAGE;   // 4 warps x EPI_BUFS x 4 KB
+    uint8_t *bar_area = smem + STAGES * G::STAGE + G::EPI_BYTES;
+    const uint32_t bar0 = ptx::smem_addr(bar_area);
+    // barrier k lives at bar0 + 8k:
+    //   [0, S) full   [S, 2S) empty   2S+{0,1} tfull   2S+{2,3} tempty
+    //   2S+4 mma-done   2S+5 stall (never completed)
+    const uint32_t done_bar = bar0 + 8u * (2 * STAGES + 4);
+    const uint32_t stall_bar = bar0 + 8u * (2 * STAGES + 5);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_area + 8 * (2 * STAGES + 6));
+    volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(tmem_slot + 1);
+    volatile int32_t *last_flag = reinterpret_cast<volatile int32_t *>(tmem_slot + 2);
+    auto full_bar = [&](uint32_t s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](uint32_t s) { return bar0 + 8u * (STAGES + s); };
+    auto tfull_bar = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + b); };
+    auto tempty_bar = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+
+    const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x >> 5), 0);
+    const int lane = static_cast<int>(threadIdx.x & 31);
+
+    if (threadIdx.x == 0) {
+        for (uint32_t s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(full_bar(s), 1);
+            ptx::mbar_init(empty_bar(s), 1);
+        }
+        for (uint32_t b = 0; b < 2; ++b) {
+            ptx::mbar_init(tfull_bar(b), 1);
+            ptx::mbar_init(tempty_bar(b), 128);
+        }
+        ptx::mbar_init(done_bar, 1);
+        ptx::mbar_init(stall_bar, 1);
+        *abort_flag = 0;
+        *last_flag = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&tmA);
+        ptx::prefetch_tensormap(&tmB);
+        if (p.epi_tma) ptx::prefetch_tensormap(&tmC);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_addr(tmem_slot), G::TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const Watchdog wd{p.timeout_ns, abort_flag, p.err};
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int64_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+                const Unit w = decode_unit(p, u);
+                const int32_t zA = p.a_bcast ? 0 : w.b;
+                const int32_t zB = p.b_bcast ? 0 : w.b;
+                for (int32_t kb = w.kb0; kb < w.kb1; ++kb, ++it) {
+                    const uint32_t s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1u;
+                    const int r = wait_bounded(empty_bar(s), ph ^ 1u, wd);
+                    if (r != WAIT_OK) {
+                        if (r == WAIT_TIMEOUT) raise_abort(wd, ERR_TIMEOUT_PRODUCER);
+                        ok = false;
+                        break;
+                    }
+                    ptx::mbar_arrive_expect_tx(full_bar(s), G::STAGE);
+                    ptx::tma_load_3d(sA + s * G::A_STAGE, &tmA, full_bar(s), kb * BK, w.tm * BM, zA);
+#pragma unroll
+                    for (int j = 0; j < BN / 64; ++j)
+                        ptx::tma_load_3d(sB + s * G::B_STAGE + j * B_BOX_BYTES, &tmB, full_bar(s),
+                                         w.tn * BN + 64 * j, kb * BK, zB);
+                }
+            }
+            // Drain: the last load issued into every slot has landed.
+            const uint32_t first = it > STAGES ? it - STAGES : 0u;
+            for (uint32_t j = first; j < it; ++j)
+                if (!wait_drain(full_bar(j % STAGES), (j / STAGES) & 1u, wd)) break;
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = instr_desc_bf16<BN>();
+            uint32_t it = 0, t = 0;
+            bool ok = true;
+            for (int64_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++t) {
+                const Unit w = decode_unit(p, u);
+                const uint32_t buf = t & 1u;
+                const uint32_t tph = (t >> 1) & 1u;
+                int r = wait_bounded(tempty_bar(buf), tph ^ 1u, wd);
+                if (r != WAIT_OK) {
+                    if (r == WAIT_TIMEOUT) raise_abort(wd, ERR_TIMEOUT_MMA);
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t d_tmem = tmem_base + buf * BN;
+                for (int32_t kb = w.kb0; kb < w.kb1; ++kb, ++it) {
+                    const uint32_t s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1u;
+                    r = wait_bounded(full_bar(s), ph, wd);
+                    if (r != WAIT_OK) {
+                        if (r == WAIT_TIMEOUT) raise_abort(wd, ERR_TIMEOUT_MMA);
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t a_addr = sA + s * G::A_STAGE;
+                    const uint32_t b_addr = sB + s * G::B_STAGE;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        // A: K-major, 8-row atoms 1024 B apart; +32 B per 16 k.
+                        const uint64_t ad = smem_desc_sw128(a_addr + kk * 32, 16, 1024);
+                        // B: N-major, 64-column atoms one box (BK x 128 B) apart
+                        // (leading offset), 8 k-rows 1024 B apart (stride
+                        // offset); +16 rows x 128 B per 16 k.
+                        const uint64_t bd = smem_desc_sw128(b_addr + kk * 2048, BK * 128, 1024);
+                        ptx::mma_bf16(d_tmem, ad, bd, idesc, (kb > w.kb0 || kk > 0) ? 1u : 0u);
+                    }
+                    ptx::mma_commit(empty_bar(s));
+                }
+                if (!ok) break;
+                ptx::mma_commit(tfull_bar(buf));
+            }
+            // Every MMA issued above completes before tensor memory is freed.
+            ptx::mma_commit(done_bar);
+            wait_drain(done_bar, 0, wd);
+        }
+    } else {
+        // ------------------------------------------------ epilogue
+        const int q = warp & 3;  // tensor-memory lane quadrant of this warp
+        const int row = q * 32 + lane;
+        const uint32_t stage_base = sE + static_cast<uint32_t>(q * EPI_BUFS) * EPI_BOX_BYTES;
+        uint32_t st_cnt = 0;
+        bool ok = true;
+        if (p.debug_stall) {
+            // Watchdog self-test: a barrier that nothing ever completes.
+            const int r = wait_bounded(stall_bar, 0, wd);
+            if (r == WAIT_TIMEOUT) raise_abort(wd, ERR_TIMEOUT_EPILOGUE);
+            ok = epi_all(r == WAIT_OK);
+        }
+
+        auto store_chunk = [&](const uint32_t (&v)[32], const Unit &w, int c) {
+            const int32_t m0 = w.tm * BM;
+            const int32_t col0 = w.tn * BN + c * EPI_CHUNK;
+            if (p.epi_tma) {
+                if (m0 + q * 32 < p.M && col0 < p.N) {  // warp-uniform
+                    const uint32_t box = stage_base + (st_cnt % EPI_BUFS) * EPI_BOX_BYTES;
+                    ++st_cnt;
+                    if (lane == 0) ptx::bulk_wait_group_read<EPI_BUFS - 1>();
+                    __syncwarp();
+                    // Row `lane` of the box, 16-byte unit jj stored at unit
+                    // jj ^ (lane mod 8): the 128B swizzle the TMA store reads.
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj)
+                        ptx::st_shared_v4(box + lane * 128 + ((jj ^ (lane & 7)) << 4), v[4 * jj],
+                                          v[4 * jj + 1], v[4 * jj + 2], v[4 * jj + 3]);
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        ptx::tma_store_3d(&tmC, box, col0, m0 + q * 32, w.b);
+                        ptx::bulk_commit_group();
+                    }
+                }
+            } else {
+                const int32_t m = m0 + row;
+                if (m < p.M && col0 < p.N) {
+                    float *dst = p.C + static_cast<int64_t>(w.b) * p.strideC +
+                                 static_cast<int64_t>(m) * p.ldc + col0;
+                    const int32_t nvalid = min(EPI_CHUNK, p.N - col0);
+#pragma unroll
+                    for (int j = 0; j < EPI_CHUNK; ++j)
+                        if (j < nvalid) dst[j] = __uint_as_float(v[j]);
+                }
+            }
+        };
+
+        uint32_t t = 0;
+        for (int64_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++t) {
+            const Unit w = decode_unit(p, u);
+            const uint32_t buf = t & 1u;
+            const uint32_t tph = (t >> 1) & 1u;
+            const int r = wait_bounded(tfull_bar(buf), tph, wd);
+            if (r == WAIT_TIMEOUT) raise_abort(wd, ERR_TIMEOUT_EPILOGUE);
+            if (!epi_all(r == WAIT_OK)) break;
+            ptx::tc_fence_after();
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
+            if (p.splits == 1) {
+#pragma unroll 1
+                for (int c = 0; c < BN / EPI_CHUNK; ++c) {
+                    uint32_t v[32];
+                    ptx::tmem_load_32cols(taddr + c * EPI_CHUNK, v);
+                    if (c == BN / EPI_CHUNK - 1) {
+                        ptx::tc_fence_before();
+                        ptx::mbar_arrive(tempty_bar(buf));
+                    }
+                    store_chunk(v, w, c);
+                }
+            } else {
+                // Partial tile -> scratch, column-major inside the tile so
+                // that a warp's 32 rows of one column are one 128-byte line.
+                const bool row_ok = (w.tm * BM + row) < p.M;
+                float *ws0 = p.partials + w.tile * static_cast<int64_t>(p.splits) * (BM * BN);
+                float *mine = ws0 + static_cast<int64_t>(w.split) * (BM * BN);
+#pragma unroll 1
+                for (int c = 0; c < BN / EPI_CHUNK; ++c) {
+                    uint32_t v[32];
+                    ptx::tmem_load_32cols(taddr + c * EPI_CHUNK, v);
+                    if (c == BN / EPI_CHUNK - 1) {
+                        ptx::tc_fence_before();
+                        ptx::mbar_arrive(tempty_bar(buf));
+                    }
+                    if (row_ok) {
+#pragma unroll
+                        for (int j = 0; j < EPI_CHUNK; ++j)
+                            __stcg(mine + (c * EPI_CHUNK + j) * BM + row, __uint_as_float(v[j]));
+                    }
+                }
+                __threadfence();
+                ptx::named_barrier_sync(1, 128);
+                if (warp == 2 && lane == 0) {
+                    const int32_t old = atomicAdd(p.counters + w.tile, 1);
+                    const int32_t last = (old == p.splits - 1) ? 1 : 0;
+                    if (last) atomicExch(p.counters + w.tile, 0);  // ready for the next call
+                    *last_flag = last;
+                }
+                ptx::named_barrier_sync(1, 128);
+                if (*last_flag) {
+                    __threadfence();
+#pragma unroll 1
+                    for (int c = 0; c < BN / EPI_CHUNK; ++c) {
+                        float acc[32];
+#pragma unroll
+                        for (int j = 0; j < EPI_CHUNK; ++j)
+                            acc[j] = row_ok ? __ldcg(ws0 + (c * EPI_CHUNK + j) * BM + row) : 0.0f;
+                        for (int s = 1; s < p.splits; ++s) {
+                            const float *ps = ws0 + static_cast<int64_t>(s) * (BM * BN);
+#pragma unroll
+                            for (int j = 0; j < EPI_CHUNK; ++j)
+                                if (row_ok) acc[j] += __ldcg(ps + (c * EPI_CHUNK + j) * BM + row);
+                        }
+                        uint32_t v[32];
+#pragma unroll
+                        for (int j = 0; j < EPI_CHUNK; ++j) v[j] = __float_as_uint(acc[j]);
+                        store_chunk(v, w, c);
+                    }
+                }
+                ptx::named_barrier_sync(1, 128);
+            }
+        }
+        // Every TMA store issued by this warp has completed its writes.
+        if (lane == 0) ptx::bulk_wait_group<0>();
+        __syncwarp();
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, G::TMEM_COLS);
+    }
+}
+
+template <int BN, int STAGES>
+cudaError_t launch_fixed(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
+                         const KernelParams &p, int grid, cudaStream_t s)
+{
+    constexpr int smem = Geometry<BN>::smem_bytes(STAGES);
+    auto kern = gemm_kernel<BN, STAGES>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, NUM_THREADS, smem, s>>>(ta, tb, tc, p);
+    return cudaGetLastError();
+}
+
+}  // namespace tg

@@ -1,0 +1,189 @@
+// Host-side planning of one GEMM call: tile width, ring depth, K splits,
+// persistent grid, pack and epilogue decisions.  Pure integer logic, no CUDA
+// calls, so tg_plan() can run (and be tested) on a machine without a GPU.
+//
+// Tiling is OCANNL "Module Ir.Schedule" Split applied to the three loops:
+// ceil(M/BM) x ceil(N/BN) output tiles per problem and ceil(K/BK) k-blocks;
+// the fringe tiles are padded to the tile (Pad-to-tile) by TMA zero fill.
+// The K split is the two-pass split reduction of the same page: k-blocks
+// [floor(s*KB/S), floor((s+1)*KB/S)) go to split s.
+#pragma once
+
+#include <algorithm>
+#include <climits>
+#include <cstdint>
+
+#include "tg_internal.h"
+
+namespace tg {
+
+// Ring depths instantiated for each tile width (kept small for build time).
+constexpr bool stage_supported(int bn, int s)
+{
+    switch (bn) {
+        case 64: return s == 2 || s == 4 || s == 6 || s == 8;
+        case 128: return s == 2 || s == 3 || s == 4 || s == 6;
+        case 192: return s == 2 || s == 3 || s == 4;
+        case 256: return s == 2 || s == 3 || s == 4;
+        default: return false;
+    }
+}
+
+constexpr int max_stages(int bn)
+{
+    return bn == 64 ? Geometry<64>::MAX_STAGES
+           : bn == 128 ? Geometry<128>::MAX_STAGES
+           : bn == 192 ? Geometry<192>::MAX_STAGES
+           : bn == 256 ? Geometry<256>::MAX_STAGES
+                       : 0;
+}
+
+static_assert(stage_supported(64, max_stages(64)), "deepest ring of BN=64 instantiated");
+static_assert(stage_supported(128, max_stages(128)), "deepest ring of BN=128 instantiated");
+static_assert(stage_supported(192, max_stages(192)), "deepest ring of BN=192 instantiated");
+static_assert(stage_supported(256, max_stages(256)), "deepest ring of BN=256 instantiated");
+
+constexpr int smem_bytes_for(int bn, int stages)
+{
+    return bn == 64 ? Geometry<64>::smem_bytes(stages)
+           : bn == 128 ? Geometry<128>::smem_bytes(stages)
+           : bn == 192 ? Geometry<192>::smem_bytes(stages)
+                       : Geometry<256>::smem_bytes(stages);
+}
+
+constexpr int tmem_cols_for(int bn)
+{
+    return bn == 64 ? Geometry<64>::TMEM_COLS
+           : bn == 128 ? Geometry<128>::TMEM_COLS
+           : bn == 192 ? Geometry<192>::TMEM_COLS
+                       : Geometry<256>::TMEM_COLS;
+}
+
+struct PlanInput {
+    int64_t M, N, K, batch;
+    bool a_tma_ok, b_tma_ok, c_tma_ok;  // 16-byte alignment of base and strides
+    bool a_bcast, b_bcast;               // batch stride 0 with batch > 1
+    int sm_count;
+    // overrides (0 = choose)
+    int block_n, stages, split_k, force_pack, epilogue, max_ctas;
+};
+
+struct Plan {
+    int bn = 0, stages = 0;
+    int tiles_m = 0, tiles_n = 0, k_blocks = 0, splits = 1;
+    int64_t units = 0;
+    int grid = 0;
+    bool pack_a = false, pack_b = false;
+    int epilogue = 1;  // 1 TMA store, 2 plain stores
+    int smem = 0, tmem = 0;
+    int group_m = 8;
+    int64_t ws_pack_a = 0, ws_pack_b = 0, ws_partials = 0, ws_counters = 0;
+    int64_t workspace() const { return ws_pack_a + ws_pack_b + ws_partials + ws_counters; }
+};
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+
+// Cost model (nanoseconds) used to rank candidate plans.  The MMA time of a
+// k-block is 2*BM*BN*BK flops at the SM's share of the dense bf16 peak,
+// divided by an efficiency that falls for narrow tiles (fixed per-k-block
+// costs: barrier round trips, descriptor setup, operand re-reads).  The memory
+// time is the unique A/B/C bytes plus split-K partial traffic at the lower of
+// HBM bandwidth and what the active CTAs can pull.
+inline double plan_cost_ns(const PlanInput &in, int bn, int splits, int k_blocks, int64_t tiles,
+                           int sms)
+{
+    const double sm_flops = 1.95e15 / 152.0;  // per-SM dense bf16, flop/s
+    const double eff = bn >= 256 ? 0.90 : bn >= 192 ? 0.86 : bn >= 128 ? 0.80 : 0.60;
+    const double kb_ns = (2.0 * BM * bn * BK) / sm_flops * 1e9 / eff;
+    const int64_t units = tiles * splits;
+    const int64_t waves = ceil_div(units, sms);
+    const int64_t kb_unit = ceil_div(k_blocks, splits);
+    const double t_mma = static_cast<double>(waves) * static_cast<double>(kb_unit) * kb_ns;
+    const double ab = 2.0 * in.batch * (in.M * in.K + in.K * in.N);
+    const double c = 4.0 * in.batch * in.M * in.N;
+    const double partial = splits > 1 ? 2.0 * 4.0 * in.batch * in.M * in.N * splits : 0.0;
+    const int64_t active = units < sms ? units : sms;
+    const double bw = std::min(6.5e12, static_cast<double>(active) * 50e9);
+    const double t_mem = (ab + c + partial) / bw * 1e9;
+    const double fixup = splits > 1 ? 2000.0 : 0.0;
+    return (t_mma > t_mem ? t_mma : t_mem) + fixup;
+}
+
+// Returns false (and leaves `out` unspecified) for an invalid override.
+inline bool make_plan(const PlanInput &in, Plan &out)
+{
+    Plan p;
+    const int sms = in.sm_count > 0 ? in.sm_count : 1;
+    const int64_t kb = ceil_div(in.K, BK);
+    if (kb > INT32_MAX) return false;
+    p.k_blocks = static_cast<int>(kb);
+    p.tiles_m = static_cast<int>(ceil_div(in.M, BM));
+
+    const int cand_bn[4] = {256, 192, 128, 64};
+    if (in.block_n != 0 && in.block_n != 64 && in.block_n != 128 && in.block_n != 192 &&
+        in.block_n != 256)
+        return false;
+    if (in.split_k < 0 || in.stages < 0 || in.max_ctas < 0) return false;
+    if (in.epilogue < 0 || in.epilogue > 2) return false;
+    if (in.split_k > 0 && in.split_k > p.k_blocks) return false;
+
+    double best = 0.0;
+    bool have = false;
+    for (int bn : cand_bn) {
+        if (in.block_n != 0 && bn != in.block_n) continue;
+        const int64_t tiles_n = ceil_div(in.N, bn);
+        const int64_t tiles = in.batch * p.tiles_m * tiles_n;
+        int split_lo = 1, split_hi = 1;
+        if (in.split_k > 0) {
+            split_lo = split_hi = in.split_k;
+        } else if (tiles < sms) {
+            // Few tiles: consider splitting K so the grid fills the SMs,
+            // keeping at least 8 k-blocks per split.
+            split_hi = static_cast<int>(std::min<int64_t>(16, std::max<int64_t>(1, p.k_blocks / 8)));
+        }
+        for (int s = split_lo; s <= split_hi; ++s) {
+            const double c = plan_cost_ns(in, bn, s, p.k_blocks, tiles, sms);
+            if (!have || c < best * 0.999) {
+                have = true;
+                best = c;
+                p.bn = bn;
+                p.splits = s;
+                p.tiles_n = static_cast<int>(tiles_n);
+            }
+        }
+    }
+    if (!have) return false;
+
+    // Ring depth: the deepest instantiated one unless overridden.
+    if (in.stages != 0) {
+        if (!stage_supported(p.bn, in.stages)) return false;
+        p.stages = in.stages;
+    } else {
+        p.stages = max_stages(p.bn);
+    }
+    p.units = in.batch * p.tiles_m * static_cast<int64_t>(p.tiles_n) * p.splits;
+    int64_t grid = p.units < sms ? p.units : sms;
+    if (in.max_ctas > 0 && grid > in.max_ctas) grid = in.max_ctas;
+    p.grid = static_cast<int>(grid);
+    p.group_m = 8;
+
+    p.pack_a = in.force_pack || !in.a_tma_ok;
+    p.pack_b = in.force_pack || !in.b_tma_ok;
+    if (in.epilogue == 1 && !in.c_tma_ok) return false;
+    p.epilogue = in.epilogue != 0 ? in.epilogue : (in.c_tma_ok ? 1 : 2);
+    p.smem = smem_bytes_for(p.bn, p.stages);
+    p.tmem = tmem_cols_for(p.bn);
+
+    const int64_t batch_a = in.a_bcast ? 1 : in.batch;
+    const int64_t batch_b = in.b_bcast ? 1 : in.batch;
+    p.ws_pack_a = p.pack_a ? round_up(batch_a * in.M * round_up(in.K, 8) * 2, 256) : 0;
+    p.ws_pack_b = p.pack_b ? round_up(batch_b * in.K * round_up(in.N, 8) * 2, 256) : 0;
+    const int64_t tiles_total = in.batch * p.tiles_m * static_cast<int64_t>(p.tiles_n);
+    p.ws_partials = p.splits > 1 ? tiles_total * p.splits * BM * p.bn * 4 : 0;
+    p.ws_counters = p.splits > 1 ? round_up(tiles_total * 4, 256) : 0;
+    out = p;
+    return true;
+}
+
+}  // namespace tg
