@@ -137,6 +137,44 @@ tg_status tg_plan(const void *A, const void *B, const float *C,
                   int64_t batch, int64_t strideA, int64_t strideB, int64_t strideC,
                   int32_t sm_count, const tg_options *opt, tg_plan_info *out);
 
+/* The split-K GEMM for callers that cannot allocate device memory.  (No page
+ * of the method has a counterpart: this is a deployment variant of the
+ * split-K path above.)
+ *
+ * Who needs it: code that runs as a plugin inside a host framework whose
+ * memory pool owns the device (a cudaMalloc there bypasses the pool's
+ * accounting or fails under its memory cap), and services that must not
+ * allocate after start-up because cudaMalloc/cudaFree may synchronise the
+ * device and have unbounded latency.  tg_gemm_ex allocates its split-K
+ * scratch (partial tiles, tile counters, error word) on first use; this
+ * entry point instead uses one static device array compiled into the
+ * library and calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * Same operation, arguments and argument checks as tg_gemm_ex, with the K
+ * dimension split into `split_k` parts (1 <= split_k <= ceil(K/64)).
+ * Limits of the static scratch (TG_ERR_UNSUPPORTED beyond them):
+ *   - split-K partial tiles: at most 16 MiB, i.e.
+ *     output tiles x split_k x 128 x block_n x 4 bytes <= 16 MiB;
+ *   - at most 4096 output tiles (batch x ceil(M/128) x ceil(N/block_n));
+ *   - A and B must be addressable by TMA: 16-byte aligned base, and row
+ *     and batch strides that are multiples of 8 elements (this path has no
+ *     pack copy).
+ * The array (16 MiB + 16 KiB + 256 B) lives on every GPU that loads the
+ * library until the process exits.  The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress) once; make that first call
+ * before any stream capture.  Every call shares the one array, which keeps
+ * the previous call's contents; each call clears the tile counters and the
+ * error word it uses before its kernel.  Calls whose kernels overlap on the
+ * GPU (different streams, or graph branches) race on the array: serialise
+ * them.  A watchdog expiry in this entry point's kernel is recorded in the
+ * array's own error word (cleared by the next call), not in the per-stream
+ * word that tg_device_error() reads. */
+tg_status tg_gemm_splitk_static(const void *A, const void *B, float *C,
+                                int64_t M, int64_t N, int64_t K,
+                                int64_t lda, int64_t ldb, int64_t ldc,
+                                int64_t batch, int64_t strideA, int64_t strideB,
+                                int64_t strideC, int32_t split_k, tg_stream_t stream);
+
 /* Synchronises `stream`, then reads and clears the device error word that
  * the kernels' watchdog writes.  TG_ERR_TIMEOUT if a wait expired since the
  * last call (the split-K tile counters are then reset too), TG_ERR_CUDA if

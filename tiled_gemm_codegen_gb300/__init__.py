@@ -2,7 +2,7 @@
 
 The product is the C-ABI CUDA library declared in ``include/tg_gemm.h``.
 This package is its thin Python binding: the C functions under the same
-names (``tg_gemm``, ``tg_gemm_ex``, ``tg_gemm_host``, ``tg_plan``,
+names (``tg_gemm``, ``tg_gemm_ex``, ``tg_gemm_host``, ``tg_gemm_splitk_static``, ``tg_plan``,
 ``tg_device_error``, ``tg_status_string``, ``tg_shutdown``) taking raw
 pointers and sizes, plus conveniences that read pointers, shapes and
 strides off torch tensors.  PyTorch only provides device memory and
@@ -19,7 +19,7 @@ from ._abi import (TG_ERR_CUDA, TG_ERR_INVALID_ARG, TG_ERR_OOM, TG_ERR_TIMEOUT,
 __all__ = [
     "TG_OK", "TG_ERR_INVALID_ARG", "TG_ERR_UNSUPPORTED", "TG_ERR_CUDA", "TG_ERR_OOM",
     "TG_ERR_TIMEOUT", "TgError", "tg_options", "tg_plan_info", "load", "library_path",
-    "tg_gemm", "tg_gemm_ex", "tg_gemm_host", "tg_plan", "tg_device_error", "tg_status_string",
+    "tg_gemm", "tg_gemm_ex", "tg_gemm_host", "tg_gemm_splitk_static", "tg_plan", "tg_device_error", "tg_status_string",
     "tg_shutdown", "make_options", "gemm", "gemm_host", "plan", "device_error",
 ]
 
@@ -46,6 +46,12 @@ def tg_gemm_host(A, B, C, M, N, K, lda, ldb, ldc, batch, strideA, strideB, strid
                  opt=None) -> int:
     return load().tg_gemm_host(A, B, C, M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC,
                                stream, ctypes.byref(opt) if opt is not None else None)
+
+
+def tg_gemm_splitk_static(A, B, C, M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC,
+                          split_k, stream=None) -> int:
+    return load().tg_gemm_splitk_static(A, B, C, M, N, K, lda, ldb, ldc, batch, strideA, strideB,
+                                        strideC, split_k, stream)
 
 
 def tg_plan(A, B, C, M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC, sm_count=0,

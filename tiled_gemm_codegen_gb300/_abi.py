@@ -78,6 +78,7 @@ SIGNATURES = {
     "tg_gemm_host": (_GEMM_ARGS + [ctypes.POINTER(tg_options)], ctypes.c_int),
     "tg_plan": ([_vp, _vp, _vp] + [_i64] * 10 + [ctypes.c_int32, ctypes.POINTER(tg_options),
                                                    ctypes.POINTER(tg_plan_info)], ctypes.c_int),
+    "tg_gemm_splitk_static": ([_vp, _vp, _vp] + [_i64] * 10 + [ctypes.c_int32, _vp], ctypes.c_int),
     "tg_device_error": ([_vp], ctypes.c_int),
     "tg_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "tg_shutdown": ([], None),

@@ -482,6 +482,53 @@ tg_status run_gemm(const Args &a, cudaStream_t stream, const tg_options *opt)
 }
 
 }  // namespace
+
+// Helpers shared with other translation units of the library (declared in
+// tg_internal.h); thin wrappers over the functions above.
+int shared_validate(const void *A, const void *B, const float *C, int64_t M, int64_t N, int64_t K,
+                    int64_t lda, int64_t ldb, int64_t ldc, int64_t batch, int64_t sA, int64_t sB,
+                    int64_t sC)
+{
+    return validate(Args{A, B, const_cast<float *>(C), M, N, K, lda, ldb, ldc, batch, sA, sB, sC});
+}
+
+bool shared_plan(const void *A, const void *B, const float *C, int64_t M, int64_t N, int64_t K,
+                 int64_t lda, int64_t ldb, int64_t ldc, int64_t batch, int64_t sA, int64_t sB,
+                 int64_t sC, int sms, const tg_options *opt, Plan *out, PlanInput *in_out)
+{
+    const PlanInput in =
+        plan_input(Args{A, B, const_cast<float *>(C), M, N, K, lda, ldb, ldc, batch, sA, sB, sC}, sms, opt);
+    if (in_out) *in_out = in;
+    return make_plan(in, *out);
+}
+
+bool shared_encode_3d(CUtensorMap *m, bool fp32, const void *base, uint64_t d0, uint64_t d1,
+                      uint64_t d2, uint64_t stride1, uint64_t stride2, uint32_t box0, uint32_t box1)
+{
+    return encode_3d(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                     base, d0, d1, d2, stride1, stride2, box0, box1);
+}
+
+uint64_t shared_single_problem_stride(uint64_t rows, uint64_t stride1)
+{
+    return single_problem_stride(rows, stride1);
+}
+
+cudaError_t shared_launch_gemm(int bn, const CUtensorMap &ta, const CUtensorMap &tb,
+                               const CUtensorMap &tc, const KernelParams &p, int stages, int grid,
+                               cudaStream_t s)
+{
+    return launch_gemm(bn, ta, tb, tc, p, stages, grid, s);
+}
+
+cudaError_t shared_zero_fill(float *C, int64_t M, int64_t N, int64_t ldc, int64_t sC, int64_t batch,
+                             int sms, cudaStream_t s)
+{
+    const int64_t total = batch * M * N;
+    zero_c_kernel<<<grid_for(total, sms), 256, 0, s>>>(C, M, N, ldc, sC, total);
+    return cudaGetLastError();
+}
+
 }  // namespace tg
 
 using namespace tg;

@@ -187,3 +187,24 @@ inline bool make_plan(const PlanInput &in, Plan &out)
 }
 
 }  // namespace tg
+
+// Host helpers shared between the library's translation units (defined in
+// tg_host.cu).
+#include "tg_gemm.h"
+
+namespace tg {
+int shared_validate(const void *A, const void *B, const float *C, int64_t M, int64_t N, int64_t K,
+                    int64_t lda, int64_t ldb, int64_t ldc, int64_t batch, int64_t sA, int64_t sB,
+                    int64_t sC);
+bool shared_plan(const void *A, const void *B, const float *C, int64_t M, int64_t N, int64_t K,
+                 int64_t lda, int64_t ldb, int64_t ldc, int64_t batch, int64_t sA, int64_t sB,
+                 int64_t sC, int sms, const tg_options *opt, Plan *out, PlanInput *in_out);
+bool shared_encode_3d(CUtensorMap *m, bool fp32, const void *base, uint64_t d0, uint64_t d1,
+                      uint64_t d2, uint64_t stride1, uint64_t stride2, uint32_t box0, uint32_t box1);
+uint64_t shared_single_problem_stride(uint64_t rows, uint64_t stride1);
+cudaError_t shared_launch_gemm(int bn, const CUtensorMap &ta, const CUtensorMap &tb,
+                               const CUtensorMap &tc, const KernelParams &p, int stages, int grid,
+                               cudaStream_t s);
+cudaError_t shared_zero_fill(float *C, int64_t M, int64_t N, int64_t ldc, int64_t sC, int64_t batch,
+                             int sms, cudaStream_t s);
+}  // namespace tg
