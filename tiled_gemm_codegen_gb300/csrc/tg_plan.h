@@ -86,15 +86,17 @@ inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 
 // Cost model (nanoseconds) used to rank candidate plans.  The MMA time of a
 // k-block is 2*BM*BN*BK flops at the SM's share of the dense bf16 peak,
-// divided by an efficiency that falls for narrow tiles (fixed per-k-block
-// costs: barrier round trips, descriptor setup, operand re-reads).  The memory
-// time is the unique A/B/C bytes plus split-K partial traffic at the lower of
-// HBM bandwidth and what the active CTAs can pull.
+// divided by an efficiency that falls for narrow tiles.  The efficiencies are
+// the measured in-wave rates on GB300 (4096^3, 1 CTA per SM): a k-block costs
+// a near-constant ~250 ns of operand ingest plus the MMA time, so narrow tiles
+// waste most of it.  The memory time is the unique A/B/C bytes plus split-K
+// partial traffic at the lower of HBM bandwidth and what the active CTAs can
+// pull.
 inline double plan_cost_ns(const PlanInput &in, int bn, int splits, int k_blocks, int64_t tiles,
                            int sms)
 {
     const double sm_flops = 1.95e15 / 152.0;  // per-SM dense bf16, flop/s
-    const double eff = bn >= 256 ? 0.90 : bn >= 192 ? 0.86 : bn >= 128 ? 0.80 : 0.60;
+    const double eff = bn >= 256 ? 0.80 : bn >= 192 ? 0.645 : bn >= 128 ? 0.54 : 0.29;
     const double kb_ns = (2.0 * BM * bn * BK) / sm_flops * 1e9 / eff;
     const int64_t units = tiles * splits;
     const int64_t waves = ceil_div(units, sms);
