@@ -83,7 +83,10 @@ typedef struct tg_options {
     int32_t debug_stall; /* nonzero: the epilogue first waits on a barrier    */
                          /* nothing completes, so the watchdog must fire and  */
                          /* tg_device_error() must return TG_ERR_TIMEOUT      */
-    int32_t reserved[7];
+    int32_t cta_pair;    /* 1 = one CTA per output tile; 2 = two-SM tiles:    */
+                         /* a cluster of two CTAs computes 256 x block_n with */
+                         /* one tcgen05 cta_group::2 MMA (block_n 128 or 256) */
+    int32_t reserved[6];
 } tg_options;
 
 /* What the planner chose (tg_plan output). */
@@ -99,7 +102,9 @@ typedef struct tg_plan_info {
     int32_t tmem_cols;   /* tensor-memory columns allocated per CTA           */
     int64_t workspace_bytes; /* scratch this call needs (pack copies, split-K  */
                              /* partial tiles, tile counters)                  */
-    int32_t reserved[6];
+    int32_t cta_pair;    /* 1 = one CTA per tile, 2 = two-SM tiles (block_m  */
+                         /* is then 256 and grid counts CTAs, 2 per cluster) */
+    int32_t reserved[5];
 } tg_plan_info;
 
 /* The GEMM (see the header comment for the operation and conventions). */

@@ -108,8 +108,11 @@ def _plan(w, **kw):
 def test_plan_of_each_workload(lib):
     for w in synth.WORKLOADS.values():
         info = _plan(w)
-        assert info["block_m"] == 128 and info["block_k"] == 64
-        assert info["tiles_m"] == -(-w.M // 128)
+        assert info["block_k"] == 64 and info["cta_pair"] in (1, 2)
+        assert info["block_m"] == 128 * info["cta_pair"]
+        assert info["tiles_m"] == -(-w.M // info["block_m"])
+        if info["cta_pair"] == 2:
+            assert info["block_n"] in (128, 256) and info["grid"] % 2 == 0
         assert info["tiles_n"] == -(-w.N // info["block_n"])
         assert info["k_blocks"] == -(-w.K // 64)
         assert info["num_units"] == w.batch * info["tiles_m"] * info["tiles_n"] * info["split_k"]
@@ -128,7 +131,7 @@ def test_plan_ragged_workload_packs_and_uses_plain_stores(lib):
     w = synth.WORKLOADS["ragged_4097x4095x4100"]
     info = _plan(w)
     assert info["pack_a"] == 1 and info["pack_b"] == 1 and info["epilogue"] == 2
-    assert info["tiles_m"] == 33 and info["k_blocks"] == 65
+    assert info["tiles_m"] == -(-4097 // info["block_m"]) and info["k_blocks"] == 65
     assert info["workspace_bytes"] >= 2 * (4097 * 4104 + 4100 * 4096)
 
 
@@ -139,7 +142,8 @@ def test_plan_split_k_workspace(lib):
 
 
 @pytest.mark.parametrize("opt", [dict(block_n=96), dict(block_n=256, stages=5), dict(split_k=10 ** 6),
-                                 dict(epilogue=3), dict(max_ctas=-1)])
+                                 dict(epilogue=3), dict(max_ctas=-1), dict(cta_pair=3),
+                                 dict(cta_pair=2, block_n=64), dict(cta_pair=2, block_n=128, stages=6)])
 def test_plan_rejects_bad_overrides(lib, opt):
     with pytest.raises(tg.TgError):
         tg.plan(512, 512, 512, sm_count=152, options=tg.make_options(**opt))
@@ -148,6 +152,20 @@ def test_plan_rejects_bad_overrides(lib, opt):
 def test_plan_rejects_tma_store_on_misaligned_c(lib):
     with pytest.raises(tg.TgError):
         tg.plan(64, 63, 64, ldc=63, sm_count=152, options=tg.make_options(epilogue=1))
+
+
+def test_plan_pair_choices(lib):
+    """Two-SM tiles for the large tensor-bound square problem; one CTA per
+    tile where 256-row tiles would waste rows or leave pairs idle."""
+    sq = _plan(synth.WORKLOADS["square_4096"])
+    assert sq["cta_pair"] == 2 and sq["block_m"] == 256 and sq["block_n"] == 256
+    assert sq["grid"] == 152 and sq["tiles_m"] == 16
+    sk = _plan(synth.WORKLOADS["skinny_64x28672x8192"])
+    assert sk["cta_pair"] == 1
+    forced = tg.plan(1000, 1000, 1000, sm_count=152, options=tg.make_options(cta_pair=2, block_n=128))
+    assert forced["cta_pair"] == 2 and forced["block_m"] == 256 and forced["tiles_m"] == 4
+    with pytest.raises(tg.TgError):
+        tg.plan(1000, 1000, 1000, sm_count=152, options=tg.make_options(cta_pair=2, block_n=192))
 
 
 def test_plan_honours_overrides(lib):

@@ -20,6 +20,9 @@ from gpu_helpers import assert_close, dev, oracle_dense, run
 pytestmark = pytest.mark.gpu
 
 WIDTHS = [64, 128, 192, 256]
+# (tile width, cta_pair): one CTA per tile for every width, two-SM tiles
+# (cluster of two CTAs, tcgen05 cta_group::2) for widths 128 and 256
+CONFIGS = [(64, 1), (128, 1), (192, 1), (256, 1), (128, 2), (256, 2)]
 EDGE_SHAPES = [
     (1, 1, 1), (7, 5, 3), (16, 16, 16), (17, 63, 65), (64, 64, 64), (127, 129, 128),
     (128, 128, 128), (129, 255, 257), (255, 257, 129), (200, 300, 40), (65, 513, 191),
@@ -39,20 +42,26 @@ def _seed(*xs):
     return s
 
 
-@pytest.mark.parametrize("bn", WIDTHS)
+def _cfg_id(c):
+    return f"bn{c[0]}{'-pair' if c[1] == 2 else ''}"
+
+
+@pytest.mark.parametrize("cfg", CONFIGS, ids=_cfg_id)
 @pytest.mark.parametrize("shape", EDGE_SHAPES, ids=lambda s: "x".join(map(str, s)))
-def test_exact_integer_edge_shapes(bn, shape):
+def test_exact_integer_edge_shapes(cfg, shape):
+    bn, pair = cfg
     M, N, K = shape
     A, B = synth.make_int_inputs(1, M, N, K, seed=_seed(M, N, K, bn))
-    got = run(A, B, options=tg.make_options(block_n=bn))
+    got = run(A, B, options=tg.make_options(block_n=bn, cta_pair=pair))
     assert np.array_equal(got, oracle_dense(A, B))
 
 
-@pytest.mark.parametrize("bn", WIDTHS)
-def test_exact_integer_batched(bn):
+@pytest.mark.parametrize("cfg", CONFIGS, ids=_cfg_id)
+def test_exact_integer_batched(cfg):
+    bn, pair = cfg
     batch, M, N, K = 3, 131, 197, 333
     A, B = synth.make_int_inputs(batch, M, N, K, seed=_seed(batch, bn))
-    got = run(A, B, options=tg.make_options(block_n=bn))
+    got = run(A, B, options=tg.make_options(block_n=bn, cta_pair=pair))
     assert np.array_equal(got, oracle_dense(A, B))
 
 
@@ -66,42 +75,57 @@ def test_float_parity_default_plan(shape, dist):
     assert_close(run(A, B), oracle_dense(A, B), K, f"{shape} {dist}")
 
 
-@pytest.mark.parametrize("bn", WIDTHS)
-def test_float_parity_each_width(bn):
+@pytest.mark.parametrize("cfg", CONFIGS, ids=_cfg_id)
+def test_float_parity_each_width(cfg):
+    bn, pair = cfg
     M, N, K = 257, 389, 700
     A, B = synth.make_inputs(2, M, N, K, "normal", seed=_seed(bn, 5))
-    assert_close(run(A, B, options=tg.make_options(block_n=bn)), oracle_dense(A, B), K, f"bn={bn}")
+    assert_close(run(A, B, options=tg.make_options(block_n=bn, cta_pair=pair)), oracle_dense(A, B),
+                 K, f"bn={bn} pair={pair}")
 
 
-@pytest.mark.parametrize("bn,depths", [(64, [2, 4, 6, 8]), (128, [2, 3, 4, 6]),
-                                       (192, [2, 3, 4]), (256, [2, 3, 4])])
-def test_ring_depth_bitwise_invariance(bn, depths):
+@pytest.mark.parametrize("bn,pair,depths", [(64, 1, [2, 4, 6, 8]), (128, 1, [2, 3, 4, 6]),
+                                            (192, 1, [2, 3, 4]), (256, 1, [2, 3, 4]),
+                                            (128, 2, [2, 4, 8]), (256, 2, [2, 4, 6])])
+def test_ring_depth_bitwise_invariance(bn, pair, depths):
     """OCANNL pipeline_depth: the pipelined rendering reads the same values in
     the same order, so the output is bitwise independent of the depth."""
     M, N, K = 300, 520, 1100
     A, B = synth.make_inputs(1, M, N, K, "uniform", seed=_seed(bn, 7))
-    outs = [run(A, B, options=tg.make_options(block_n=bn, stages=s)) for s in depths]
+    outs = [run(A, B, options=tg.make_options(block_n=bn, stages=s, cta_pair=pair)) for s in depths]
     for o in outs[1:]:
         assert np.array_equal(o, outs[0])
     assert_close(outs[0], oracle_dense(A, B), K)
 
 
-def test_persistent_grid_bitwise_invariance():
-    """A CTA that walks many tiles (accumulator double buffer, ring phases
-    wrapping) gives the same bits as one tile per CTA."""
+@pytest.mark.parametrize("pair", [1, 2])
+def test_persistent_grid_bitwise_invariance(pair):
+    """A CTA (or CTA pair) that walks many tiles (accumulator double buffer,
+    ring phases wrapping) gives the same bits as one tile per worker."""
     M, N, K = 640, 768, 512
     A, B = synth.make_inputs(1, M, N, K, "normal", seed=3)
-    base = run(A, B, options=tg.make_options(block_n=128))
-    for ctas in (1, 3, 7):
-        got = run(A, B, options=tg.make_options(block_n=128, max_ctas=ctas))
+    base = run(A, B, options=tg.make_options(block_n=128, cta_pair=pair))
+    for ctas in (2, 6, 14):
+        got = run(A, B, options=tg.make_options(block_n=128, max_ctas=ctas, cta_pair=pair))
         assert np.array_equal(got, base), ctas
 
 
-def test_epilogue_paths_bitwise_equal():
+def test_pair_tiles_equal_single_tiles_exactly():
+    """Two-SM tiles and one-CTA tiles compute the same exact sums."""
+    M, N, K = 513, 600, 700
+    A, B = synth.make_int_inputs(1, M, N, K, seed=77)
+    one = run(A, B, options=tg.make_options(block_n=256, cta_pair=1))
+    two = run(A, B, options=tg.make_options(block_n=256, cta_pair=2))
+    assert np.array_equal(one, two)
+    assert np.array_equal(two, oracle_dense(A, B))
+
+
+@pytest.mark.parametrize("bn,pair", [(192, 1), (256, 2)])
+def test_epilogue_paths_bitwise_equal(bn, pair):
     M, N, K = 333, 444, 555
     A, B = synth.make_inputs(1, M, N, K, "uniform", seed=4)
-    t = run(A, B, options=tg.make_options(block_n=192, epilogue=1))
-    d = run(A, B, options=tg.make_options(block_n=192, epilogue=2))
+    t = run(A, B, options=tg.make_options(block_n=bn, epilogue=1, cta_pair=pair))
+    d = run(A, B, options=tg.make_options(block_n=bn, epilogue=2, cta_pair=pair))
     assert np.array_equal(t, d)
     assert_close(t, oracle_dense(A, B), K)
 
@@ -114,13 +138,14 @@ def test_pack_path_bitwise_equal():
     assert np.array_equal(plain, packed)
 
 
+@pytest.mark.parametrize("pair", [1, 2])
 @pytest.mark.parametrize("splits", [2, 3, 4, 7])
-def test_split_k_exact_integer(splits):
+def test_split_k_exact_integer(splits, pair):
     """Split reduction: the combined partials equal the full sum exactly
     with integer inputs."""
     M, N, K = 150, 300, 2048
     A, B = synth.make_int_inputs(1, M, N, K, seed=splits)
-    got = run(A, B, options=tg.make_options(block_n=128, split_k=splits))
+    got = run(A, B, options=tg.make_options(block_n=128, split_k=splits, cta_pair=pair))
     assert np.array_equal(got, oracle_dense(A, B))
 
 
@@ -260,8 +285,10 @@ def test_watchdog_reports_timeout_and_recovers():
     M, N, K = 300, 300, 256
     A, B = synth.make_int_inputs(1, M, N, K, seed=51)
     ad, bd = A.to(dev()), B.to(dev())
-    for ctas in (0, 1):  # one tile per CTA, and one CTA walking all tiles
-        opts = tg.make_options(debug_stall=1, timeout_ns=20_000_000, block_n=128, max_ctas=ctas)
+    # one tile per CTA, one CTA walking all tiles, and the same for CTA pairs
+    for ctas, pair in ((0, 1), (1, 1), (0, 2), (2, 2)):
+        opts = tg.make_options(debug_stall=1, timeout_ns=20_000_000, block_n=128, max_ctas=ctas,
+                               cta_pair=pair)
         tg.gemm(ad, bd, options=opts)
         assert tg.device_error() == tg.TG_ERR_TIMEOUT
         assert tg.device_error() == tg.TG_OK

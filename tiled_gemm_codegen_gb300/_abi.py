@@ -39,7 +39,8 @@ class tg_options(ctypes.Structure):
         ("max_ctas", ctypes.c_int32),
         ("timeout_ns", ctypes.c_uint64),
         ("debug_stall", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 7),
+        ("cta_pair", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 6),
     ]
 
 
@@ -61,7 +62,8 @@ class tg_plan_info(ctypes.Structure):
         ("smem_bytes", ctypes.c_int32),
         ("tmem_cols", ctypes.c_int32),
         ("workspace_bytes", ctypes.c_int64),
-        ("reserved", ctypes.c_int32 * 6),
+        ("cta_pair", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 5),
     ]
 
     def as_dict(self) -> dict:

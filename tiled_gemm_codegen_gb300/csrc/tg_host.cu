@@ -11,6 +11,7 @@
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <tuple>
 #include <utility>
 
 #include "tg_gemm.h"
@@ -160,6 +161,7 @@ PlanInput plan_input(const Args &a, int sms, const tg_options *opt)
         in.force_pack = opt->force_pack;
         in.epilogue = opt->epilogue;
         in.max_ctas = opt->max_ctas;
+        in.cta_pair = opt->cta_pair;
     }
     return in;
 }
@@ -167,7 +169,8 @@ PlanInput plan_input(const Args &a, int sms, const tg_options *opt)
 void fill_info(const Plan &p, tg_plan_info *out)
 {
     std::memset(out, 0, sizeof(*out));
-    out->block_m = BM;
+    out->block_m = p.pair ? 2 * BM : BM;
+    out->cta_pair = p.pair ? 2 : 1;
     out->block_n = p.bn;
     out->block_k = BK;
     out->stages = p.stages;
@@ -324,16 +327,34 @@ uint64_t single_problem_stride(uint64_t rows, uint64_t stride1)
     return (s + 15) / 16 * 16;
 }
 
-cudaError_t launch_gemm(int bn, const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
-                        const KernelParams &p, int stages, int grid, cudaStream_t s)
+cudaError_t launch_gemm(int bn, bool pair, const CUtensorMap &ta, const CUtensorMap &tb,
+                        const CUtensorMap &tc, const KernelParams &p, int stages, int grid,
+                        cudaStream_t s)
 {
     switch (bn) {
-        case 64: return launch_gemm_bn64(ta, tb, tc, p, stages, grid, s);
-        case 128: return launch_gemm_bn128(ta, tb, tc, p, stages, grid, s);
-        case 192: return launch_gemm_bn192(ta, tb, tc, p, stages, grid, s);
-        case 256: return launch_gemm_bn256(ta, tb, tc, p, stages, grid, s);
+        case 64: return launch_gemm_bn64(ta, tb, tc, p, stages, pair, grid, s);
+        case 128: return launch_gemm_bn128(ta, tb, tc, p, stages, pair, grid, s);
+        case 192: return launch_gemm_bn192(ta, tb, tc, p, stages, pair, grid, s);
+        case 256: return launch_gemm_bn256(ta, tb, tc, p, stages, pair, grid, s);
         default: return cudaErrorInvalidValue;
     }
+}
+
+// Co-resident two-CTA clusters of a pair configuration, cached per device.
+int max_pairs(int dev, int bn, int stages)
+{
+    static std::map<std::tuple<int, int, int>, int> cache;
+    const auto key = std::make_tuple(dev, bn, stages);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    int n = 0;
+    switch (bn) {
+        case 128: n = max_pairs_bn128(stages); break;
+        case 256: n = max_pairs_bn256(stages); break;
+        default: n = 0;
+    }
+    cache[key] = n;
+    return n;
 }
 
 int grid_for(int64_t work, int sms)
@@ -472,12 +493,21 @@ tg_status run_gemm(const Args &a, cudaStream_t stream, const tg_options *opt)
     if (std::getenv("TG_TRACE"))
         std::fprintf(stderr,
                      "tg_gemm M=%lld N=%lld K=%lld batch=%lld: BN=%d stages=%d tiles=%dx%d kb=%d "
-                     "split=%d units=%lld grid=%d pack=%d/%d epi=%d\n",
+                     "split=%d pair=%d units=%lld grid=%d pack=%d/%d epi=%d\n",
                      (long long)a.M, (long long)a.N, (long long)a.K, (long long)a.batch, plan.bn,
-                     plan.stages, plan.tiles_m, plan.tiles_n, plan.k_blocks, plan.splits,
+                     plan.stages, plan.tiles_m, plan.tiles_n, plan.k_blocks, plan.splits, plan.pair ? 2 : 1,
                      (long long)plan.units, plan.grid, plan.pack_a, plan.pack_b, plan.epilogue);
 
-    e = launch_gemm(plan.bn, ta, tb, tc, p, plan.stages, plan.grid, stream);
+    int grid = plan.grid;
+    if (plan.pair) {
+        // never more clusters than can be resident at once (persistent)
+        const int pairs = max_pairs(dev, plan.bn, plan.stages);
+        if (pairs <= 0) return TG_ERR_UNSUPPORTED;
+        if (grid > 2 * pairs) grid = 2 * pairs;
+        if (std::getenv("TG_TRACE"))
+            std::fprintf(stderr, "tg_gemm: co-resident CTA pairs %d, launch grid %d\n", pairs, grid);
+    }
+    e = launch_gemm(plan.bn, plan.pair, ta, tb, tc, p, plan.stages, grid, stream);
     return cuda_status(e);
 }
 
@@ -518,7 +548,7 @@ cudaError_t shared_launch_gemm(int bn, const CUtensorMap &ta, const CUtensorMap 
                                const CUtensorMap &tc, const KernelParams &p, int stages, int grid,
                                cudaStream_t s)
 {
-    return launch_gemm(bn, ta, tb, tc, p, stages, grid, s);
+    return launch_gemm(bn, false, ta, tb, tc, p, stages, grid, s);
 }
 
 cudaError_t shared_zero_fill(float *C, int64_t M, int64_t N, int64_t ldc, int64_t sC, int64_t batch,

@@ -45,14 +45,17 @@ struct KernelParams {
     int32_t debug_stall;
 };
 
-// Shared-memory budget of one tile width (identical on host and device).
-template <int BN>
+// Shared-memory budget of one tile width.  PAIR: the tile is computed by a
+// cluster of two CTAs on two SMs (tcgen05 cta_group::2): each CTA holds its
+// own 128 rows of A and half of the BN columns of B.
+template <int BN, bool PAIR = false>
 struct Geometry {
-    static constexpr int A_STAGE = BM * BK * 2;          // 16 KB
-    static constexpr int B_STAGE = BK * BN * 2;          // BN * 128 B
+    static constexpr int B_COLS = PAIR ? BN / 2 : BN;     // B columns this CTA loads
+    static constexpr int A_STAGE = BM * BK * 2;           // 16 KB
+    static constexpr int B_STAGE = BK * B_COLS * 2;       // B_COLS * 128 B
     static constexpr int STAGE = A_STAGE + B_STAGE;
     static constexpr int EPI_BYTES = 4 * EPI_BUFS * EPI_CHUNK * EPI_CHUNK * 4;  // 32 KB
-    static constexpr int BAR_BYTES = 256;
+    static constexpr int BAR_BYTES = 512;
     static constexpr int ALIGN_SLACK = 1024;
     static constexpr int MAX_STAGES_RAW = (SMEM_LIMIT - EPI_BYTES - BAR_BYTES - ALIGN_SLACK) / STAGE;
     static constexpr int MAX_STAGES = MAX_STAGES_RAW > 8 ? 8 : MAX_STAGES_RAW;
@@ -68,14 +71,17 @@ struct Geometry {
 };
 
 // Launch of the persistent GEMM kernel for one tile width (defined in the
-// per-width translation units).  Returns the launch's cudaError_t.
-cudaError_t launch_gemm_bn64(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
-                             const KernelParams &p, int stages, int grid, cudaStream_t s);
-cudaError_t launch_gemm_bn128(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
-                              const KernelParams &p, int stages, int grid, cudaStream_t s);
-cudaError_t launch_gemm_bn192(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
-                              const KernelParams &p, int stages, int grid, cudaStream_t s);
-cudaError_t launch_gemm_bn256(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
-                              const KernelParams &p, int stages, int grid, cudaStream_t s);
+// per-width translation units).  pair: two-SM tiles (grid counts CTAs, a
+// multiple of 2).  Returns the launch's cudaError_t.
+#define TG_DECLARE_LAUNCH(BN_)                                                                   \
+    cudaError_t launch_gemm_bn##BN_(const CUtensorMap &ta, const CUtensorMap &tb,                \
+                                    const CUtensorMap &tc, const KernelParams &p, int stages,   \
+                                    bool pair, int grid, cudaStream_t s);                       \
+    int max_pairs_bn##BN_(int stages);
+TG_DECLARE_LAUNCH(64)
+TG_DECLARE_LAUNCH(128)
+TG_DECLARE_LAUNCH(192)
+TG_DECLARE_LAUNCH(256)
+#undef TG_DECLARE_LAUNCH
 
 }  // namespace tg

@@ -1,45 +1,58 @@
 // Persistent, warp-specialised bf16 -> fp32 GEMM kernel for sm_103a.
 //
-// One CTA per SM walks a static list of work units (output tile x K split).
-// Roles (the "Active subsets" of one accumulator's producers and consumers,
-// LuisaCompute "Execution Nests and coordinates", Logical anchor and
-// execution frontier):
-//   warp 0, lane 0 : TMA producer.  Loads the A tile [BM x BK] (K-major) and
-//                    the B tile [BK x BN] (N-major) of k-block kb into ring
-//                    slot kb mod STAGES with the 128-byte swizzle; boxes that
-//                    run past M, N or K are zero-filled by the TMA unit
-//                    (OCANNL "Module Ir.Schedule", Pad-to-tile and Stage:
-//                    out-of-range slots hold the additive identity 0).
-//   warp 1, lane 0 : MMA issuer.  BK/16 tcgen05.mma per slot into a tensor-
-//                    memory accumulator; the first one of a unit overwrites
-//                    (the zero-initialised accumulator of OCANNL Privatize).
+// One CTA per SM (or one two-CTA cluster per SM pair, PAIR) walks a static
+// list of work units (output tile x K split).  Roles (the "Active subsets"
+// of one accumulator's producers and consumers, LuisaCompute "Execution
+// Nests and coordinates", Logical anchor and execution frontier):
+//   warp 0, lane 0 : TMA producer.  Loads this CTA's A rows [128 x BK]
+//                    (K-major) and its B columns [BK x BN or BN/2] (N-major)
+//                    of k-block kb into ring slot kb mod STAGES with the
+//                    128-byte swizzle; boxes that run past M, N or K are
+//                    zero-filled by the TMA unit (OCANNL "Module
+//                    Ir.Schedule", Pad-to-tile and Stage: out-of-range slots
+//                    hold the additive identity 0).
+//   warp 1, lane 0 : MMA issuer (the leader CTA of a pair).  BK/16
+//                    tcgen05.mma per slot into a tensor-memory accumulator;
+//                    the first one of a unit overwrites (the zero-initialised
+//                    accumulator of OCANNL Privatize).
 //   warps 2..5     : epilogue.  tcgen05.ld of the accumulator (warp w reads
-//                    TMEM lanes 32*(w%4) ..), then either a TMA store of
-//                    32 x 32 fp32 boxes through swizzled shared memory (the
-//                    store clips rows >= M and columns >= N), or plain masked
-//                    stores when C is not 16-byte aligned.
+//                    TMEM lanes 32*(w%4) ..) into a 128B-swizzled 32 x 32
+//                    fp32 box in shared memory, then a TMA store of the box
+//                    (clipped at M and N by the hardware) or, when C is not
+//                    16-byte aligned, coalesced masked stores of its rows.
 // Synchronisation is the issue / completion / release protocol of
 // LuisaCompute "Pipelines and stage boundaries" (section "Issue, completion
 // and release are different events"):
-//   full[s]    : TMA completion (expect_tx bytes)         -> MMA may read s
-//   empty[s]   : tcgen05.commit after the slot's MMAs     -> TMA may refill s
-//   tfull[b]   : tcgen05.commit after a unit's last MMA   -> epilogue may read b
-//   tempty[b]  : 128 epilogue arrivals after the last ld  -> MMA may reuse b
+//   full[s]       : the TMA bytes of slot s landed (expect_tx); in a pair the
+//                   leader's full[s] counts the bytes of both CTAs
+//   empty[s]      : tcgen05.commit after the slot's MMAs -> TMA may refill s
+//                   (pair: multicast to both CTAs)
+//   tfull[b]      : tcgen05.commit after a unit's last MMA -> epilogue may
+//                   read accumulator buffer b (pair: multicast)
+//   tempty[b]     : one arrival per epilogue warp (pair: of both CTAs, on
+//                   the leader) after its last tcgen05.ld -> MMA may reuse b
 // The ring of STAGES slots generalises OCANNL's pipeline_depth: slot and
 // phase are (it mod STAGES, (it / STAGES) & 1), and the values the MMA reads
 // do not depend on STAGES, so the result is bitwise independent of it.
 //
+// Two-SM tiles (PAIR): a cluster of two CTAs computes a 256 x BN tile with
+// tcgen05.mma.cta_group::2 (M = 256): each CTA loads its own 128 rows of A
+// and half of B's BN columns into its own shared memory (the copies of both
+// CTAs complete on the leader's full barrier), and receives its 128 x BN
+// accumulator in its own tensor memory.  Per SM this halves the B bytes of
+// every k-block (no TMA multicast is used).
+//
 // Split-K (OCANNL "Module Ir.Schedule", Deterministic two-pass split
-// reduction): every split writes its fp32 partial tile to scratch, then the
-// last split to arrive at the tile's counter sums all partials in the fixed
-// order s = 0, 1, ..., splits-1 and stores C.  No split ever waits for
-// another, so the combine needs no grid-wide barrier.
+// reduction): every split writes its fp32 partial (half-)tile to scratch,
+// then the last split to arrive at the tile's counter sums all partials in
+// the fixed order s = 0, 1, ..., splits-1 and stores C.  No split ever waits
+// for another, so the combine needs no grid-wide barrier.
 //
 // Every mbarrier wait is bounded (timeout_ns, %globaltimer).  On expiry the
-// waiting role records an error code in the device error word, raises a
-// CTA-wide abort flag that makes the other roles leave their loops, and the
-// CTA then waits (bounded) for its own TMA loads, MMAs and TMA stores in
-// flight, frees its tensor memory and returns.
+// waiting role records an error code in the device error word, raises the
+// abort flag of its CTA (and of the peer CTA) that makes the other roles
+// leave their loops, and every CTA then waits (bounded) for its own TMA
+// loads, MMAs and TMA stores in flight, frees its tensor memory and returns.
 #pragma once
 
 #include "tg_internal.h"
@@ -62,11 +75,11 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo,
 // Instruction descriptor of tcgen05.mma.kind::f16: D fp32 (bits 4-5 = 1),
 // A bf16 (bits 7-9 = 1), B bf16 (bits 10-12 = 1), A K-major (bit 15 = 0),
 // B MN-major (bit 16 = 1), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
-template <int BN>
+template <int M, int N>
 __host__ __device__ constexpr uint32_t instr_desc_bf16()
 {
-    return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
-           (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
+    return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 struct Unit {
@@ -104,6 +117,7 @@ struct Watchdog {
     uint64_t timeout_ns;
     volatile int32_t *abort_flag;
     uint32_t *err;
+    uint32_t peer_abort;  // cluster address of the peer CTA's abort flag (0: none)
 };
 
 // Bounded wait for the phase of parity `parity` of mbarrier `bar`.
@@ -138,6 +152,7 @@ __device__ __forceinline__ void raise_abort(const Watchdog &wd, uint32_t code)
 {
     atomicCAS(wd.err, 0u, code);
     *wd.abort_flag = 1;
+    if (wd.peer_abort) ptx::st_cluster_u32(wd.peer_abort, 1u);
     __threadfence_block();
 }
 
@@ -156,23 +171,34 @@ __device__ __forceinline__ bool epi_all(bool pred)
     return r != 0;
 }
 
-template <int BN, int STAGES>
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr)
+{
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+template <int BN, int STAGES, bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const KernelParams p)
 {
-    using G = Geometry<BN>;
+    using G = Geometry<BN, PAIR>;
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "tile width");
+    static_assert(!PAIR || G::B_COLS % 64 == 0, "two-SM tiles need 64-column halves of B");
     static_assert(G::smem_bytes(STAGES) <= SMEM_LIMIT, "shared memory budget");
+    constexpr int TILE_M = PAIR ? 2 * BM : BM;
+    constexpr int B_BOXES = G::B_COLS / 64;
     constexpr uint32_t B_BOX_BYTES = BK * 64 * 2;  // one 64-column box of B: 8 KB
     constexpr uint32_t EPI_BOX_BYTES = EPI_CHUNK * EPI_CHUNK * 4;  // 4 KB
+    constexpr uint32_t EPI_WARPS_TOTAL = PAIR ? 8 : 4;  // arrivals on tempty per tile
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
     const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
     uint8_t *smem = smem_raw + pad;
     const uint32_t sA = raw + pad;                  // STAGES x [BM x BK] bf16
-    const uint32_t sB = sA + STAGES * G::A_STAGE;   // STAGES x [BK x BN] bf16
+    const uint32_t sB = sA + STAGES * G::A_STAGE;   // STAGES x [BK x B_COLS] bf16
     const uint32_t sE = sB + STAGES * G::B_STAGE;   // 4 warps x EPI_BUFS x 4 KB
     uint8_t *bar_area = smem + STAGES * G::STAGE + G::EPI_BYTES;
     const uint32_t bar0 = ptx::smem_addr(bar_area);
@@ -184,6 +210,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_area + 8 * (2 * STAGES + 6));
     volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(tmem_slot + 1);
     volatile int32_t *last_flag = reinterpret_cast<volatile int32_t *>(tmem_slot + 2);
+    uint32_t *issued_slot = tmem_slot + 3;  // k-block loads this CTA's producer issued
     auto full_bar = [&](uint32_t s) { return bar0 + 8u * s; };
     auto empty_bar = [&](uint32_t s) { return bar0 + 8u * (STAGES + s); };
     auto tfull_bar = [&](uint32_t b) { return bar0 + 8u * (2 * STAGES + b); };
@@ -191,6 +218,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x >> 5), 0);
     const int lane = static_cast<int>(threadIdx.x & 31);
+    const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;
+    const bool leader = rank == 0;
+    const int64_t worker = PAIR ? (blockIdx.x >> 1) : blockIdx.x;
+    const int64_t n_workers = PAIR ? (gridDim.x >> 1) : gridDim.x;
 
     if (threadIdx.x == 0) {
         for (uint32_t s = 0; s < STAGES; ++s) {
@@ -199,12 +230,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (uint32_t b = 0; b < 2; ++b) {
             ptx::mbar_init(tfull_bar(b), 1);
-            ptx::mbar_init(tempty_bar(b), 128);
+            ptx::mbar_init(tempty_bar(b), EPI_WARPS_TOTAL);
         }
         ptx::mbar_init(done_bar, 1);
         ptx::mbar_init(stall_bar, 1);
         *abort_flag = 0;
         *last_flag = 0;
+        *issued_slot = 0;
         ptx::fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
@@ -213,24 +245,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (p.epi_tma) ptx::prefetch_tensormap(&tmC);
     }
     if (warp == 1) {
-        ptx::tmem_alloc(ptx::smem_addr(tmem_slot), G::TMEM_COLS);
-        ptx::tmem_relinquish();
+        if constexpr (PAIR) {
+            ptx::tmem_alloc_pair(ptx::smem_addr(tmem_slot), G::TMEM_COLS);
+            ptx::tmem_relinquish_pair();
+        } else {
+            ptx::tmem_alloc(ptx::smem_addr(tmem_slot), G::TMEM_COLS);
+            ptx::tmem_relinquish();
+        }
     }
     ptx::tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) ptx::cluster_sync_all();  // both CTAs' barriers exist
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const Watchdog wd{p.timeout_ns, abort_flag, p.err};
+    const uint32_t peer_abort =
+        PAIR ? ptx::map_to_cta(ptx::smem_addr(const_cast<int32_t *>(abort_flag)), rank ^ 1u) : 0u;
+    const Watchdog wd{p.timeout_ns, abort_flag, p.err, peer_abort};
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
-            for (int64_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+            // pair: both CTAs' copies complete on the leader's full barrier
+            const uint32_t full0 = PAIR ? ptx::map_to_cta(full_bar(0), 0u) : full_bar(0);
+            for (int64_t u = worker; ok && u < p.num_units; u += n_workers) {
                 const Unit w = decode_unit(p, u);
                 const int32_t zA = p.a_bcast ? 0 : w.b;
                 const int32_t zB = p.b_bcast ? 0 : w.b;
+                const int32_t m_rows = w.tm * TILE_M + static_cast<int32_t>(rank) * BM;
+                const int32_t n_cols = w.tn * BN + static_cast<int32_t>(rank) * G::B_COLS;
                 for (int32_t kb = w.kb0; kb < w.kb1; ++kb, ++it) {
                     const uint32_t s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1u;
@@ -240,26 +284,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         ok = false;
                         break;
                     }
-                    ptx::mbar_arrive_expect_tx(full_bar(s), G::STAGE);
-                    ptx::tma_load_3d(sA + s * G::A_STAGE, &tmA, full_bar(s), kb * BK, w.tm * BM, zA);
+                    if constexpr (PAIR) {
+                        if (leader) ptx::mbar_arrive_expect_tx(full_bar(s), 2 * G::STAGE);
+                        const uint32_t fb = full0 + 8u * s;
+                        ptx::tma_load_3d_pair(sA + s * G::A_STAGE, &tmA, fb, kb * BK, m_rows, zA);
 #pragma unroll
-                    for (int j = 0; j < BN / 64; ++j)
-                        ptx::tma_load_3d(sB + s * G::B_STAGE + j * B_BOX_BYTES, &tmB, full_bar(s),
-                                         w.tn * BN + 64 * j, kb * BK, zB);
+                        for (int j = 0; j < B_BOXES; ++j)
+                            ptx::tma_load_3d_pair(sB + s * G::B_STAGE + j * B_BOX_BYTES, &tmB, fb,
+                                                  n_cols + 64 * j, kb * BK, zB);
+                    } else {
+                        ptx::mbar_arrive_expect_tx(full_bar(s), G::STAGE);
+                        ptx::tma_load_3d(sA + s * G::A_STAGE, &tmA, full_bar(s), kb * BK, m_rows, zA);
+#pragma unroll
+                        for (int j = 0; j < B_BOXES; ++j)
+                            ptx::tma_load_3d(sB + s * G::B_STAGE + j * B_BOX_BYTES, &tmB, full_bar(s),
+                                             n_cols + 64 * j, kb * BK, zB);
+                    }
                 }
             }
-            // Drain: the last load issued into every slot has landed.
-            const uint32_t first = it > STAGES ? it - STAGES : 0u;
-            for (uint32_t j = first; j < it; ++j)
-                if (!wait_drain(full_bar(j % STAGES), (j / STAGES) & 1u, wd)) break;
+            *issued_slot = it;
+            if constexpr (!PAIR) {
+                // Drain: the last load issued into every slot has landed.
+                const uint32_t first = it > STAGES ? it - STAGES : 0u;
+                for (uint32_t j = first; j < it; ++j)
+                    if (!wait_drain(full_bar(j % STAGES), (j / STAGES) & 1u, wd)) break;
+            }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc = instr_desc_bf16<BN>();
+        if (lane == 0 && (!PAIR || leader)) {
+            // ------------------------------------------------ MMA issuer
+            constexpr uint32_t idesc = instr_desc_bf16<TILE_M, BN>();
             uint32_t it = 0, t = 0;
             bool ok = true;
-            for (int64_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++t) {
+            for (int64_t u = worker; ok && u < p.num_units; u += n_workers, ++t) {
                 const Unit w = decode_unit(p, u);
                 const uint32_t buf = t & 1u;
                 const uint32_t tph = (t >> 1) & 1u;
@@ -290,15 +347,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         // (leading offset), 8 k-rows 1024 B apart (stride
                         // offset); +16 rows x 128 B per 16 k.
                         const uint64_t bd = smem_desc_sw128(b_addr + kk * 2048, BK * 128, 1024);
-                        ptx::mma_bf16(d_tmem, ad, bd, idesc, (kb > w.kb0 || kk > 0) ? 1u : 0u);
+                        const uint32_t acc = (kb > w.kb0 || kk > 0) ? 1u : 0u;
+                        if constexpr (PAIR)
+                            ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, acc);
+                        else
+                            ptx::mma_bf16(d_tmem, ad, bd, idesc, acc);
                     }
-                    ptx::mma_commit(empty_bar(s));
+                    if constexpr (PAIR)
+                        ptx::mma_commit_pair_multicast(empty_bar(s), 0x3);
+                    else
+                        ptx::mma_commit(empty_bar(s));
                 }
                 if (!ok) break;
-                ptx::mma_commit(tfull_bar(buf));
+                if constexpr (PAIR)
+                    ptx::mma_commit_pair_multicast(tfull_bar(buf), 0x3);
+                else
+                    ptx::mma_commit(tfull_bar(buf));
             }
             // Every MMA issued above completes before tensor memory is freed.
-            ptx::mma_commit(done_bar);
+            if constexpr (PAIR)
+                ptx::mma_commit_pair_multicast(done_bar, 0x1);
+            else
+                ptx::mma_commit(done_bar);
             wait_drain(done_bar, 0, wd);
         }
     } else {
@@ -306,6 +376,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int q = warp & 3;  // tensor-memory lane quadrant of this warp
         const int row = q * 32 + lane;
         const uint32_t stage_base = sE + static_cast<uint32_t>(q * EPI_BUFS) * EPI_BOX_BYTES;
+        const uint32_t tempty_leader0 = PAIR ? ptx::map_to_cta(tempty_bar(0), 0u) : tempty_bar(0);
         uint32_t st_cnt = 0;
         bool ok = true;
         if (p.debug_stall) {
@@ -315,43 +386,63 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ok = epi_all(r == WAIT_OK);
         }
 
-        auto store_chunk = [&](const uint32_t (&v)[32], const Unit &w, int c) {
-            const int32_t m0 = w.tm * BM;
-            const int32_t col0 = w.tn * BN + c * EPI_CHUNK;
-            if (p.epi_tma) {
-                if (m0 + q * 32 < p.M && col0 < p.N) {  // warp-uniform
-                    const uint32_t box = stage_base + (st_cnt % EPI_BUFS) * EPI_BOX_BYTES;
-                    ++st_cnt;
-                    if (lane == 0) ptx::bulk_wait_group_read<EPI_BUFS - 1>();
-                    __syncwarp();
-                    // Row `lane` of the box, 16-byte unit jj stored at unit
-                    // jj ^ (lane mod 8): the 128B swizzle the TMA store reads.
+        // One 32 x 32 fp32 chunk (rows m_base + 32q .., columns col0 ..) of
+        // this warp's accumulator rows -> C.
+        auto store_chunk = [&](const uint32_t (&v)[32], int32_t m_base, int32_t col0, int32_t b) {
+            const int32_t row0 = m_base + q * 32;
+            if (row0 >= p.M || col0 >= p.N) return;  // warp-uniform
+            const uint32_t box = stage_base + (st_cnt % EPI_BUFS) * EPI_BOX_BYTES;
+            ++st_cnt;
+            if (p.epi_tma && lane == 0) ptx::bulk_wait_group_read<EPI_BUFS - 1>();
+            __syncwarp();
+            // Row `lane` of the box; its 16-byte unit jj is stored at unit
+            // jj ^ (lane mod 8): the 128B swizzle (Swizzle(2,3,3) on fp32).
 #pragma unroll
-                    for (int jj = 0; jj < 8; ++jj)
-                        ptx::st_shared_v4(box + lane * 128 + ((jj ^ (lane & 7)) << 4), v[4 * jj],
-                                          v[4 * jj + 1], v[4 * jj + 2], v[4 * jj + 3]);
-                    ptx::fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        ptx::tma_store_3d(&tmC, box, col0, m0 + q * 32, w.b);
-                        ptx::bulk_commit_group();
-                    }
+            for (int jj = 0; jj < 8; ++jj)
+                ptx::st_shared_v4(box + lane * 128 + ((jj ^ (lane & 7)) << 4), v[4 * jj],
+                                  v[4 * jj + 1], v[4 * jj + 2], v[4 * jj + 3]);
+            if (p.epi_tma) {
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    ptx::tma_store_3d(&tmC, box, col0, row0, b);
+                    ptx::bulk_commit_group();
                 }
             } else {
-                const int32_t m = m0 + row;
-                if (m < p.M && col0 < p.N) {
-                    float *dst = p.C + static_cast<int64_t>(w.b) * p.strideC +
-                                 static_cast<int64_t>(m) * p.ldc + col0;
-                    const int32_t nvalid = min(EPI_CHUNK, p.N - col0);
-#pragma unroll
-                    for (int j = 0; j < EPI_CHUNK; ++j)
-                        if (j < nvalid) dst[j] = __uint_as_float(v[j]);
+                __syncwarp();
+                // Coalesced: lane l writes column col0 + l of each row.
+                const int32_t col = col0 + lane;
+                if (col < p.N) {
+                    float *dst = p.C + static_cast<int64_t>(b) * p.strideC +
+                                 static_cast<int64_t>(row0) * p.ldc + col;
+                    const int32_t nrows = min(32, p.M - row0);
+                    const uint32_t src = box + (((lane >> 2)) << 4) + ((lane & 3) << 2);
+#pragma unroll 8
+                    for (int r = 0; r < 32; ++r) {
+                        if (r < nrows)
+                            dst[static_cast<int64_t>(r) * p.ldc] =
+                                ld_shared_f32((src ^ ((r & 7) << 4)) + r * 128);
+                    }
                 }
+                __syncwarp();
+            }
+        };
+
+        // Frees accumulator buffer `buf` for the MMA issuer (after this
+        // warp's last tcgen05.ld of it).
+        auto release_tmem = [&](uint32_t buf) {
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if constexpr (PAIR)
+                    ptx::mbar_arrive_cluster(tempty_leader0 + 8u * buf);
+                else
+                    ptx::mbar_arrive(tempty_bar(buf));
             }
         };
 
         uint32_t t = 0;
-        for (int64_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++t) {
+        for (int64_t u = worker; ok && u < p.num_units; u += n_workers, ++t) {
             const Unit w = decode_unit(p, u);
             const uint32_t buf = t & 1u;
             const uint32_t tph = (t >> 1) & 1u;
@@ -360,31 +451,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (!epi_all(r == WAIT_OK)) break;
             ptx::tc_fence_after();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
+            const int32_t m_base = w.tm * TILE_M + static_cast<int32_t>(rank) * BM;
+            const int32_t n_base = w.tn * BN;
             if (p.splits == 1) {
 #pragma unroll 1
                 for (int c = 0; c < BN / EPI_CHUNK; ++c) {
                     uint32_t v[32];
                     ptx::tmem_load_32cols(taddr + c * EPI_CHUNK, v);
-                    if (c == BN / EPI_CHUNK - 1) {
-                        ptx::tc_fence_before();
-                        ptx::mbar_arrive(tempty_bar(buf));
-                    }
-                    store_chunk(v, w, c);
+                    if (c == BN / EPI_CHUNK - 1) release_tmem(buf);
+                    store_chunk(v, m_base, n_base + c * EPI_CHUNK, w.b);
                 }
             } else {
-                // Partial tile -> scratch, column-major inside the tile so
-                // that a warp's 32 rows of one column are one 128-byte line.
-                const bool row_ok = (w.tm * BM + row) < p.M;
-                float *ws0 = p.partials + w.tile * static_cast<int64_t>(p.splits) * (BM * BN);
+                // Partial (half-)tile -> scratch, column-major inside the tile
+                // so that a warp's 32 rows of one column are one 128-byte line.
+                const int64_t half = w.tile * (PAIR ? 2 : 1) + rank;
+                const bool row_ok = (m_base + row) < p.M;
+                float *ws0 = p.partials + half * static_cast<int64_t>(p.splits) * (BM * BN);
                 float *mine = ws0 + static_cast<int64_t>(w.split) * (BM * BN);
 #pragma unroll 1
                 for (int c = 0; c < BN / EPI_CHUNK; ++c) {
                     uint32_t v[32];
                     ptx::tmem_load_32cols(taddr + c * EPI_CHUNK, v);
-                    if (c == BN / EPI_CHUNK - 1) {
-                        ptx::tc_fence_before();
-                        ptx::mbar_arrive(tempty_bar(buf));
-                    }
+                    if (c == BN / EPI_CHUNK - 1) release_tmem(buf);
                     if (row_ok) {
 #pragma unroll
                         for (int j = 0; j < EPI_CHUNK; ++j)
@@ -394,9 +482,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 __threadfence();
                 ptx::named_barrier_sync(1, 128);
                 if (warp == 2 && lane == 0) {
-                    const int32_t old = atomicAdd(p.counters + w.tile, 1);
+                    const int32_t old = atomicAdd(p.counters + half, 1);
                     const int32_t last = (old == p.splits - 1) ? 1 : 0;
-                    if (last) atomicExch(p.counters + w.tile, 0);  // ready for the next call
+                    if (last) atomicExch(p.counters + half, 0);  // ready for the next call
                     *last_flag = last;
                 }
                 ptx::named_barrier_sync(1, 128);
@@ -417,7 +505,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         uint32_t v[32];
 #pragma unroll
                         for (int j = 0; j < EPI_CHUNK; ++j) v[j] = __float_as_uint(acc[j]);
-                        store_chunk(v, w, c);
+                        store_chunk(v, m_base, n_base + c * EPI_CHUNK, w.b);
                     }
                 }
                 ptx::named_barrier_sync(1, 128);
@@ -429,23 +517,94 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 
     __syncthreads();
+    if constexpr (PAIR) {
+        // Neither CTA leaves (or frees tensor memory) while the other may
+        // still signal its barriers, the leader's MMAs may write its TMEM, or
+        // a copy of either CTA may still be landing.  Both producers' issue
+        // counts are final after the first cluster barrier; the leader then
+        // waits for the latest phase of every slot of its full barriers.  If
+        // an abort left the two producers at different counts, it first
+        // settles the phases only one of them issued: peer bytes that will
+        // never come are counted with complete_tx, and a missing leader
+        // arrival is made with expect_tx of the peer's bytes alone.
+        ptx::cluster_sync_all();
+        if (leader && warp == 0 && lane == 0) {
+            const uint32_t i_l = *issued_slot;
+            const uint32_t i_p = ptx::ld_cluster_u32(ptx::map_to_cta(ptx::smem_addr(issued_slot), 1u));
+            const uint32_t hi = i_l > i_p ? i_l : i_p;
+            const uint32_t lo = hi > STAGES ? hi - STAGES : 0u;
+            for (uint32_t j = lo; j < hi; ++j) {
+                const uint32_t s = j % STAGES;
+                if (j < i_l && j >= i_p)
+                    ptx::mbar_complete_tx(full_bar(s), G::STAGE);
+                else if (j >= i_l && j < i_p)
+                    ptx::mbar_arrive_expect_tx(full_bar(s), G::STAGE);
+                if (!wait_drain(full_bar(s), (j / STAGES) & 1u, wd)) break;
+            }
+        }
+        ptx::cluster_sync_all();
+    }
     if (warp == 1) {
         __syncwarp();
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem_base, G::TMEM_COLS);
+        if constexpr (PAIR)
+            ptx::tmem_dealloc_pair(tmem_base, G::TMEM_COLS);
+        else
+            ptx::tmem_dealloc(tmem_base, G::TMEM_COLS);
     }
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, bool PAIR>
 cudaError_t launch_fixed(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
                          const KernelParams &p, int grid, cudaStream_t s)
 {
-    constexpr int smem = Geometry<BN>::smem_bytes(STAGES);
-    auto kern = gemm_kernel<BN, STAGES>;
+    constexpr int smem = Geometry<BN, PAIR>::smem_bytes(STAGES);
+    auto kern = gemm_kernel<BN, STAGES, PAIR>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, NUM_THREADS, smem, s>>>(ta, tb, tc, p);
-    return cudaGetLastError();
+    if constexpr (!PAIR) {
+        kern<<<grid, NUM_THREADS, smem, s>>>(ta, tb, tc, p);
+        return cudaGetLastError();
+    } else {
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+        cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, p);
+    }
+}
+
+// Largest number of two-CTA clusters of this configuration that can be
+// resident at once (0 if the query fails).
+template <int BN, int STAGES>
+int max_active_pairs()
+{
+    constexpr int smem = Geometry<BN, true>::smem_bytes(STAGES);
+    auto kern = gemm_kernel<BN, STAGES, true>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) return 0;
+    return n;
 }
 
 }  // namespace tg

@@ -17,9 +17,20 @@
 
 namespace tg {
 
+// Widths that have a two-SM (cta_group::2) variant: each CTA of the pair
+// loads BN/2 columns of B, which must be whole 64-column boxes.
+constexpr bool pair_width(int bn) { return bn == 128 || bn == 256; }
+
 // Ring depths instantiated for each tile width (kept small for build time).
-constexpr bool stage_supported(int bn, int s)
+constexpr bool stage_supported(int bn, int s, bool pair = false)
 {
+    if (pair) {
+        switch (bn) {
+            case 128: return s == 2 || s == 4 || s == 8;
+            case 256: return s == 2 || s == 4 || s == 6;
+            default: return false;
+        }
+    }
     switch (bn) {
         case 64: return s == 2 || s == 4 || s == 6 || s == 8;
         case 128: return s == 2 || s == 3 || s == 4 || s == 6;
@@ -29,26 +40,40 @@ constexpr bool stage_supported(int bn, int s)
     }
 }
 
-constexpr int max_stages(int bn)
+template <bool PAIR>
+constexpr int max_stages_t(int bn)
 {
-    return bn == 64 ? Geometry<64>::MAX_STAGES
-           : bn == 128 ? Geometry<128>::MAX_STAGES
-           : bn == 192 ? Geometry<192>::MAX_STAGES
-           : bn == 256 ? Geometry<256>::MAX_STAGES
+    return bn == 64 ? Geometry<64, PAIR>::MAX_STAGES
+           : bn == 128 ? Geometry<128, PAIR>::MAX_STAGES
+           : bn == 192 ? Geometry<192, PAIR>::MAX_STAGES
+           : bn == 256 ? Geometry<256, PAIR>::MAX_STAGES
                        : 0;
+}
+
+constexpr int max_stages(int bn, bool pair = false)
+{
+    return pair ? max_stages_t<true>(bn) : max_stages_t<false>(bn);
 }
 
 static_assert(stage_supported(64, max_stages(64)), "deepest ring of BN=64 instantiated");
 static_assert(stage_supported(128, max_stages(128)), "deepest ring of BN=128 instantiated");
 static_assert(stage_supported(192, max_stages(192)), "deepest ring of BN=192 instantiated");
 static_assert(stage_supported(256, max_stages(256)), "deepest ring of BN=256 instantiated");
+static_assert(stage_supported(128, max_stages(128, true), true), "deepest pair ring of BN=128");
+static_assert(stage_supported(256, max_stages(256, true), true), "deepest pair ring of BN=256");
 
-constexpr int smem_bytes_for(int bn, int stages)
+template <bool PAIR>
+constexpr int smem_bytes_t(int bn, int stages)
 {
-    return bn == 64 ? Geometry<64>::smem_bytes(stages)
-           : bn == 128 ? Geometry<128>::smem_bytes(stages)
-           : bn == 192 ? Geometry<192>::smem_bytes(stages)
-                       : Geometry<256>::smem_bytes(stages);
+    return bn == 64 ? Geometry<64, PAIR>::smem_bytes(stages)
+           : bn == 128 ? Geometry<128, PAIR>::smem_bytes(stages)
+           : bn == 192 ? Geometry<192, PAIR>::smem_bytes(stages)
+                       : Geometry<256, PAIR>::smem_bytes(stages);
+}
+
+constexpr int smem_bytes_for(int bn, int stages, bool pair = false)
+{
+    return pair ? smem_bytes_t<true>(bn, stages) : smem_bytes_t<false>(bn, stages);
 }
 
 constexpr int tmem_cols_for(int bn)
@@ -66,9 +91,11 @@ struct PlanInput {
     int sm_count;
     // overrides (0 = choose)
     int block_n, stages, split_k, force_pack, epilogue, max_ctas;
+    int cta_pair;  // 0 = choose, 1 = one CTA per tile, 2 = two-SM tiles
 };
 
 struct Plan {
+    bool pair = false;  // two-SM tiles (256 rows, cluster of 2)
     int bn = 0, stages = 0;
     int tiles_m = 0, tiles_n = 0, k_blocks = 0, splits = 1;
     int64_t units = 0;
@@ -85,32 +112,44 @@ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 
 // Cost model (nanoseconds) used to rank candidate plans.  The MMA time of a
-// k-block is 2*BM*BN*BK flops at the SM's share of the dense bf16 peak,
-// divided by an efficiency that falls for narrow tiles.  The efficiencies are
-// the measured in-wave rates on GB300 (4096^3, 1 CTA per SM): a k-block costs
-// a near-constant ~250 ns of operand ingest plus the MMA time, so narrow tiles
-// waste most of it.  The memory time is the unique A/B/C bytes plus split-K
-// partial traffic at the lower of HBM bandwidth and what the active CTAs can
-// pull.
-inline double plan_cost_ns(const PlanInput &in, int bn, int splits, int k_blocks, int64_t tiles,
-                           int sms)
+// k-block is 2*BM*BN*BK flops per SM at the SM's share of the dense bf16
+// peak, divided by an efficiency.  One-CTA efficiencies are the measured
+// in-wave rates on GB300 (4096^3): a k-block costs a near-constant ~250 ns of
+// operand ingest plus the MMA time, so narrow tiles waste most of it.  A
+// two-SM tile halves the B bytes each SM ingests per k-block.  Work is
+// spread over `workers` = SMs (one CTA per tile) or SMs/2 (two-SM tiles).
+// The memory time is the unique A/B/C bytes plus split-K partial traffic at
+// the lower of HBM bandwidth and what the active SMs can pull.
+inline double tile_efficiency(int bn, bool pair)
+{
+    // measured in-wave rates on GB300 (fraction of the measured bf16 peak)
+    if (pair) return bn >= 256 ? 0.97 : 0.53;
+    return bn >= 256 ? 0.80 : bn >= 192 ? 0.645 : bn >= 128 ? 0.54 : 0.29;
+}
+
+inline double plan_cost_ns(const PlanInput &in, int bn, bool pair, int splits, int k_blocks,
+                           int64_t tiles, int sms)
 {
     const double sm_flops = 1.95e15 / 152.0;  // per-SM dense bf16, flop/s
-    const double eff = bn >= 256 ? 0.80 : bn >= 192 ? 0.645 : bn >= 128 ? 0.54 : 0.29;
-    const double kb_ns = (2.0 * BM * bn * BK) / sm_flops * 1e9 / eff;
+    const double kb_ns = (2.0 * BM * bn * BK) / sm_flops * 1e9 / tile_efficiency(bn, pair);
+    const int64_t workers = pair ? std::max(1, sms / 2) : sms;
     const int64_t units = tiles * splits;
-    const int64_t waves = ceil_div(units, sms);
+    const int64_t waves = ceil_div(units, workers);
     const int64_t kb_unit = ceil_div(k_blocks, splits);
     const double t_mma = static_cast<double>(waves) * static_cast<double>(kb_unit) * kb_ns;
     const double ab = 2.0 * in.batch * (in.M * in.K + in.K * in.N);
     const double c = 4.0 * in.batch * in.M * in.N;
     const double partial = splits > 1 ? 2.0 * 4.0 * in.batch * in.M * in.N * splits : 0.0;
-    const int64_t active = units < sms ? units : sms;
-    const double bw = std::min(6.5e12, static_cast<double>(active) * 50e9);
+    const int64_t active_sms = std::min<int64_t>(units, workers) * (pair ? 2 : 1);
+    const double bw = std::min(6.5e12, static_cast<double>(active_sms) * 50e9);
     const double t_mem = (ab + c + partial) / bw * 1e9;
     const double fixup = splits > 1 ? 2000.0 : 0.0;
     return (t_mma > t_mem ? t_mma : t_mem) + fixup;
 }
+
+// Whether the planner may pick two-SM tiles on its own (otherwise only when
+// asked with cta_pair = 2).
+constexpr bool PAIR_BY_DEFAULT = true;
 
 // Returns false (and leaves `out` unspecified) for an invalid override.
 inline bool make_plan(const PlanInput &in, Plan &out)
@@ -120,37 +159,50 @@ inline bool make_plan(const PlanInput &in, Plan &out)
     const int64_t kb = ceil_div(in.K, BK);
     if (kb > INT32_MAX) return false;
     p.k_blocks = static_cast<int>(kb);
-    p.tiles_m = static_cast<int>(ceil_div(in.M, BM));
 
-    const int cand_bn[4] = {256, 192, 128, 64};
     if (in.block_n != 0 && in.block_n != 64 && in.block_n != 128 && in.block_n != 192 &&
         in.block_n != 256)
         return false;
     if (in.split_k < 0 || in.stages < 0 || in.max_ctas < 0) return false;
     if (in.epilogue < 0 || in.epilogue > 2) return false;
+    if (in.cta_pair < 0 || in.cta_pair > 2) return false;
     if (in.split_k > 0 && in.split_k > p.k_blocks) return false;
+    if (in.cta_pair == 2 && in.block_n != 0 && !pair_width(in.block_n)) return false;
 
+    struct Cand {
+        int bn;
+        bool pair;
+    };
+    const Cand cands[6] = {{256, true}, {128, true}, {256, false}, {192, false}, {128, false}, {64, false}};
     double best = 0.0;
     bool have = false;
-    for (int bn : cand_bn) {
-        if (in.block_n != 0 && bn != in.block_n) continue;
-        const int64_t tiles_n = ceil_div(in.N, bn);
-        const int64_t tiles = in.batch * p.tiles_m * tiles_n;
+    for (const Cand &cd : cands) {
+        if (in.block_n != 0 && cd.bn != in.block_n) continue;
+        if (in.cta_pair == 1 && cd.pair) continue;
+        if (in.cta_pair == 2 && !cd.pair) continue;
+        if (in.cta_pair == 0 && cd.pair && !PAIR_BY_DEFAULT) continue;
+        const int tile_m = cd.pair ? 2 * BM : BM;
+        const int64_t tiles_m = ceil_div(in.M, tile_m);
+        const int64_t tiles_n = ceil_div(in.N, cd.bn);
+        const int64_t tiles = in.batch * tiles_m * tiles_n;
+        const int64_t workers = cd.pair ? std::max(1, sms / 2) : sms;
         int split_lo = 1, split_hi = 1;
         if (in.split_k > 0) {
             split_lo = split_hi = in.split_k;
-        } else if (tiles < sms) {
+        } else if (tiles < workers) {
             // Few tiles: consider splitting K so the grid fills the SMs,
             // keeping at least 8 k-blocks per split.
             split_hi = static_cast<int>(std::min<int64_t>(16, std::max<int64_t>(1, p.k_blocks / 8)));
         }
         for (int s = split_lo; s <= split_hi; ++s) {
-            const double c = plan_cost_ns(in, bn, s, p.k_blocks, tiles, sms);
+            const double c = plan_cost_ns(in, cd.bn, cd.pair, s, p.k_blocks, tiles, sms);
             if (!have || c < best * 0.999) {
                 have = true;
                 best = c;
-                p.bn = bn;
+                p.bn = cd.bn;
+                p.pair = cd.pair;
                 p.splits = s;
+                p.tiles_m = static_cast<int>(tiles_m);
                 p.tiles_n = static_cast<int>(tiles_n);
             }
         }
@@ -159,31 +211,36 @@ inline bool make_plan(const PlanInput &in, Plan &out)
 
     // Ring depth: the deepest instantiated one unless overridden.
     if (in.stages != 0) {
-        if (!stage_supported(p.bn, in.stages)) return false;
+        if (!stage_supported(p.bn, in.stages, p.pair)) return false;
         p.stages = in.stages;
     } else {
-        p.stages = max_stages(p.bn);
+        p.stages = max_stages(p.bn, p.pair);
     }
     p.units = in.batch * p.tiles_m * static_cast<int64_t>(p.tiles_n) * p.splits;
-    int64_t grid = p.units < sms ? p.units : sms;
-    if (in.max_ctas > 0 && grid > in.max_ctas) grid = in.max_ctas;
-    p.grid = static_cast<int>(grid);
+    const int64_t workers = p.pair ? std::max(1, sms / 2) : sms;
+    int64_t w = p.units < workers ? p.units : workers;
+    if (in.max_ctas > 0) {
+        const int64_t cap = p.pair ? std::max(1, in.max_ctas / 2) : in.max_ctas;
+        if (w > cap) w = cap;
+    }
+    p.grid = static_cast<int>(w * (p.pair ? 2 : 1));
     p.group_m = 8;
 
     p.pack_a = in.force_pack || !in.a_tma_ok;
     p.pack_b = in.force_pack || !in.b_tma_ok;
     if (in.epilogue == 1 && !in.c_tma_ok) return false;
     p.epilogue = in.epilogue != 0 ? in.epilogue : (in.c_tma_ok ? 1 : 2);
-    p.smem = smem_bytes_for(p.bn, p.stages);
+    p.smem = smem_bytes_for(p.bn, p.stages, p.pair);
     p.tmem = tmem_cols_for(p.bn);
 
     const int64_t batch_a = in.a_bcast ? 1 : in.batch;
     const int64_t batch_b = in.b_bcast ? 1 : in.batch;
     p.ws_pack_a = p.pack_a ? round_up(batch_a * in.M * round_up(in.K, 8) * 2, 256) : 0;
     p.ws_pack_b = p.pack_b ? round_up(batch_b * in.K * round_up(in.N, 8) * 2, 256) : 0;
-    const int64_t tiles_total = in.batch * p.tiles_m * static_cast<int64_t>(p.tiles_n);
-    p.ws_partials = p.splits > 1 ? tiles_total * p.splits * BM * p.bn * 4 : 0;
-    p.ws_counters = p.splits > 1 ? round_up(tiles_total * 4, 256) : 0;
+    // split-K scratch is kept per 128-row (half-)tile
+    const int64_t halves = in.batch * p.tiles_m * static_cast<int64_t>(p.tiles_n) * (p.pair ? 2 : 1);
+    p.ws_partials = p.splits > 1 ? halves * p.splits * BM * p.bn * 4 : 0;
+    p.ws_counters = p.splits > 1 ? round_up(halves * 4, 256) : 0;
     out = p;
     return true;
 }
