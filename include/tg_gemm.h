@@ -86,7 +86,18 @@ typedef struct tg_options {
     int32_t cta_pair;    /* 1 = one CTA per output tile; 2 = two-SM tiles:    */
                          /* a cluster of two CTAs computes 256 x block_n with */
                          /* one tcgen05 cta_group::2 MMA (block_n 128 or 256) */
-    int32_t reserved[6];
+    int32_t stream_k;    /* 1 = off; 2 = on when the last wave of tiles is    */
+                         /* partial: each worker takes its full waves of      */
+                         /* tiles, then an equal share of the remaining       */
+                         /* tiles' k-blocks; split tiles are combined in a    */
+                         /* fixed k order (cannot be combined with split_k)   */
+    int32_t reserved0;
+    uint64_t trace_buffer; /* device address of grid x 8 uint64 (0 = off): per */
+                         /* CTA %globaltimer stamps in ns: [0] entry, [1] set- */
+                         /* up done, [2] first k-block ready, [3] last MMA    */
+                         /* issued, [4] first epilogue start, [5] last store  */
+                         /* issued, [6] stores complete, [7] exit             */
+    int32_t reserved[2];
 } tg_options;
 
 /* What the planner chose (tg_plan output). */
@@ -104,7 +115,9 @@ typedef struct tg_plan_info {
                              /* partial tiles, tile counters)                  */
     int32_t cta_pair;    /* 1 = one CTA per tile, 2 = two-SM tiles (block_m  */
                          /* is then 256 and grid counts CTAs, 2 per cluster) */
-    int32_t reserved[5];
+    int32_t stream_k;    /* 1 = off, 2 = on                                  */
+    int32_t sk_tiles;    /* tiles whose k-blocks are shared between workers  */
+    int32_t reserved[3];
 } tg_plan_info;
 
 /* The GEMM (see the header comment for the operation and conventions). */

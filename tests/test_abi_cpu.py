@@ -160,12 +160,56 @@ def test_plan_pair_choices(lib):
     sq = _plan(synth.WORKLOADS["square_4096"])
     assert sq["cta_pair"] == 2 and sq["block_m"] == 256 and sq["block_n"] == 256
     assert sq["grid"] == 152 and sq["tiles_m"] == 16
+    # 256 tiles on 76 pairs: 3 whole waves, the last 28 tiles shared (stream-K)
+    assert sq["stream_k"] == 2 and sq["sk_tiles"] == 256 - 3 * 76
     sk = _plan(synth.WORKLOADS["skinny_64x28672x8192"])
     assert sk["cta_pair"] == 1
     forced = tg.plan(1000, 1000, 1000, sm_count=152, options=tg.make_options(cta_pair=2, block_n=128))
     assert forced["cta_pair"] == 2 and forced["block_m"] == 256 and forced["tiles_m"] == 4
     with pytest.raises(tg.TgError):
         tg.plan(1000, 1000, 1000, sm_count=152, options=tg.make_options(cta_pair=2, block_n=192))
+
+
+def test_stream_k_schedule_covers_every_k_block_once(lib):
+    """Host-side model of the stream-K schedule the kernel walks: whole
+    tiles for the full waves, then contiguous k-block ranges; every (tile,
+    k-block) is covered exactly once and parts are numbered in k order."""
+    def owner(x, W, L):
+        return min(W - 1, ((x + 1) * W - 1) // L)
+
+    for tiles, kb, W in [(256, 64, 76), (64, 32, 7), (10, 1, 7), (5, 3, 16), (29, 65, 4)]:
+        if tiles % W == 0:
+            continue
+        dp = tiles // W
+        sk_tiles = tiles - dp * W
+        L = sk_tiles * kb
+        cover = {}
+        for w in range(W):
+            for i in range(dp):
+                t = w + i * W
+                for k in range(kb):
+                    cover[(t, k)] = cover.get((t, k), 0) + 1
+            pos, end = w * L // W, (w + 1) * L // W
+            while pos < end:
+                ts = pos // kb
+                e = min(end, (ts + 1) * kb)
+                first, last = owner(ts * kb, W, L), owner((ts + 1) * kb - 1, W, L)
+                assert first <= w <= last
+                for k in range(pos - ts * kb, e - ts * kb):
+                    cover[(dp * W + ts, k)] = cover.get((dp * W + ts, k), 0) + 1
+                pos = e
+        assert len(cover) == tiles * kb and set(cover.values()) == {1}
+
+
+def test_plan_stream_k_overrides(lib):
+    off = tg.plan(4096, 4096, 4096, sm_count=152, options=tg.make_options(stream_k=1))
+    assert off["stream_k"] == 1 and off["sk_tiles"] == 0
+    with pytest.raises(tg.TgError):
+        tg.plan(4096, 4096, 4096, sm_count=152, options=tg.make_options(stream_k=2, split_k=2))
+    full = tg.plan(4096, 4096, 4096, sm_count=152,
+                   options=tg.make_options(stream_k=2, cta_pair=2, max_ctas=128))
+    # 256 tiles on 64 pairs: the last wave is full, nothing to balance
+    assert full["stream_k"] == 1
 
 
 def test_plan_honours_overrides(lib):

@@ -330,3 +330,48 @@ def test_plan_queries_device():
     info = tg.plan(4096, 4096, 4096)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     assert 1 <= info["grid"] <= sms
+
+
+@pytest.mark.parametrize("bn,pair,ctas,shape", [
+    (128, 1, 7, (1000, 1000, 2048)),   # 64 tiles on 7 CTAs: 1 tile split 7 ways
+    (64, 1, 5, (300, 700, 1000)),      # ragged tiles and k-blocks
+    (256, 2, 6, (1000, 900, 1500)),    # two-SM tiles on 3 pairs
+    (128, 2, 10, (777, 1300, 640)),
+    (128, 1, 7, (1000, 1000, 64)),     # one k-block: most ranges empty
+])
+def test_stream_k_exact_integer(bn, pair, ctas, shape):
+    """Stream-K: whole-tile waves, then shared k-block ranges combined in k
+    order; exact with integer inputs, and bitwise run to run."""
+    M, N, K = shape
+    A, B = synth.make_int_inputs(2 if bn == 64 else 1, M, N, K, seed=_seed(M, N, K, ctas))
+    opts = tg.make_options(block_n=bn, cta_pair=pair, max_ctas=ctas, stream_k=2)
+    info = tg.plan(M, N, K, 2 if bn == 64 else 1, sm_count=152, options=opts)
+    assert info["stream_k"] == 2 and info["sk_tiles"] > 0
+    got = run(A, B, options=opts)
+    assert np.array_equal(got, oracle_dense(A, B))
+    assert np.array_equal(run(A, B, options=opts), got)
+
+
+def test_stream_k_float_deterministic_and_close():
+    M, N, K = 1100, 1500, 3000
+    A, B = synth.make_inputs(1, M, N, K, "normal", seed=91)
+    opts = tg.make_options(block_n=256, cta_pair=2, max_ctas=10, stream_k=2)
+    o1 = run(A, B, options=opts)
+    o2 = run(A, B, options=opts)
+    assert np.array_equal(o1, o2)
+    ref = oracle_dense(A, B)
+    assert_close(o1, ref, K, "stream-K")
+    off = run(A, B, options=tg.make_options(block_n=256, cta_pair=2, max_ctas=10, stream_k=1))
+    assert_close(off, ref, K, "stream-K off")
+
+
+def test_stream_k_watchdog():
+    M, N, K = 1000, 1000, 2048
+    A, B = synth.make_int_inputs(1, M, N, K, seed=93)
+    ad, bd = A.to(dev()), B.to(dev())
+    tg.gemm(ad, bd, options=tg.make_options(debug_stall=1, timeout_ns=20_000_000, block_n=128,
+                                            max_ctas=7, stream_k=2))
+    assert tg.device_error() == tg.TG_ERR_TIMEOUT
+    got = tg.gemm(ad, bd, options=tg.make_options(block_n=128, max_ctas=7, stream_k=2))
+    assert tg.device_error() == tg.TG_OK
+    assert np.array_equal(got.cpu().double().numpy(), oracle_dense(A, B))

@@ -40,7 +40,10 @@ class tg_options(ctypes.Structure):
         ("timeout_ns", ctypes.c_uint64),
         ("debug_stall", ctypes.c_int32),
         ("cta_pair", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 6),
+        ("stream_k", ctypes.c_int32),
+        ("reserved0", ctypes.c_int32),
+        ("trace_buffer", ctypes.c_uint64),
+        ("reserved", ctypes.c_int32 * 2),
     ]
 
 
@@ -63,7 +66,9 @@ class tg_plan_info(ctypes.Structure):
         ("tmem_cols", ctypes.c_int32),
         ("workspace_bytes", ctypes.c_int64),
         ("cta_pair", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 5),
+        ("stream_k", ctypes.c_int32),
+        ("sk_tiles", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 3),
     ]
 
     def as_dict(self) -> dict:

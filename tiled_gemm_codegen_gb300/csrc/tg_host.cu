@@ -24,6 +24,13 @@ namespace tg {
 namespace {
 
 constexpr uint64_t DEFAULT_TIMEOUT_NS = 2000000000ull;  // 2 s
+
+// TG_TRACE=1 prints each call's plan to stderr (read once).
+bool trace_enabled()
+{
+    static const bool on = std::getenv("TG_TRACE") != nullptr;
+    return on;
+}
 constexpr int64_t EXTENT_LIMIT = INT32_MAX;
 
 // ------------------------------------------------------------ small kernels
@@ -162,6 +169,7 @@ PlanInput plan_input(const Args &a, int sms, const tg_options *opt)
         in.epilogue = opt->epilogue;
         in.max_ctas = opt->max_ctas;
         in.cta_pair = opt->cta_pair;
+        in.stream_k = opt->stream_k;
     }
     return in;
 }
@@ -171,6 +179,8 @@ void fill_info(const Plan &p, tg_plan_info *out)
     std::memset(out, 0, sizeof(*out));
     out->block_m = p.pair ? 2 * BM : BM;
     out->cta_pair = p.pair ? 2 : 1;
+    out->stream_k = p.stream_k ? 2 : 1;
+    out->sk_tiles = static_cast<int32_t>(p.sk_tiles);
     out->block_n = p.bn;
     out->block_k = BK;
     out->stages = p.stages;
@@ -301,12 +311,40 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
+// Recently encoded tensor maps (per host thread): repeated calls on the same
+// buffers skip the driver's encode.
+struct MapKey {
+    const void *base;
+    int dt;
+    uint64_t d0, d1, d2, s1, s2;
+    uint32_t b0, b1;
+    bool operator==(const MapKey &o) const
+    {
+        return base == o.base && dt == o.dt && d0 == o.d0 && d1 == o.d1 && d2 == o.d2 &&
+               s1 == o.s1 && s2 == o.s2 && b0 == o.b0 && b1 == o.b1;
+    }
+};
+struct MapCache {
+    static constexpr int N = 32;
+    MapKey key[N];
+    CUtensorMap map[N];
+    bool used[N] = {};
+    int next = 0;
+};
+thread_local MapCache t_maps;
+
 // A rank-3 tiled map: dim0 contiguous (d0 elements), dim1 rows (stride1
 // bytes), dim2 problems (stride2 bytes); box {box0, box1, 1}; 128B swizzle;
 // out-of-range elements read as zero.
 bool encode_3d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t d0, uint64_t d1,
                uint64_t d2, uint64_t stride1, uint64_t stride2, uint32_t box0, uint32_t box1)
 {
+    const MapKey k{base, static_cast<int>(dt), d0, d1, d2, stride1, stride2, box0, box1};
+    for (int i = 0; i < MapCache::N; ++i)
+        if (t_maps.used[i] && t_maps.key[i] == k) {
+            *m = t_maps.map[i];
+            return true;
+        }
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[3] = {d0, d1, d2};
@@ -316,7 +354,13 @@ bool encode_3d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_
     CUresult r = fn(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    if (r != CUDA_SUCCESS) return false;
+    const int slot = t_maps.next;
+    t_maps.next = (slot + 1) % MapCache::N;
+    t_maps.key[slot] = k;
+    t_maps.map[slot] = *m;
+    t_maps.used[slot] = true;
+    return true;
 }
 
 // Stride of the problem dimension when there is only one problem (any valid
@@ -418,6 +462,18 @@ tg_status run_gemm(const Args &a, cudaStream_t stream, const tg_options *opt)
         plan.ws_pack_b = round_up((in.b_bcast ? 1 : a.batch) * a.K * round_up(a.N, 8) * 2, 256);
     }
 
+    // The persistent grid actually launched: two-SM tiles never use more
+    // clusters than can be resident at once; the stream-K ranges follow it.
+    int grid = plan.grid;
+    if (plan.pair) {
+        const int pairs = max_pairs(dev, plan.bn, plan.stages);
+        if (pairs <= 0) return TG_ERR_UNSUPPORTED;
+        if (grid > 2 * pairs) grid = 2 * pairs;
+        if (trace_enabled())
+            std::fprintf(stderr, "tg_gemm: co-resident CTA pairs %d, launch grid %d\n", pairs, grid);
+        if (grid != plan.grid) replan_stream_k(in, plan, grid);
+    }
+
     const size_t arena_need = static_cast<size_t>(plan.ws_pack_a + plan.ws_pack_b + plan.ws_partials);
     if (arena_need > 0) {
         st = grow(&w.arena, &w.arena_cap, arena_need, stream);
@@ -484,29 +540,29 @@ tg_status run_gemm(const Args &a, cudaStream_t stream, const tg_options *opt)
     p.C = a.C;
     p.ldc = a.ldc;
     p.strideC = a.sC;
-    p.partials = plan.splits > 1 ? partials : nullptr;
-    p.counters = plan.splits > 1 ? w.counters : nullptr;
+    const bool partial_tiles = plan.splits > 1 || plan.stream_k;
+    p.partials = partial_tiles ? partials : nullptr;
+    p.counters = partial_tiles ? w.counters : nullptr;
+    p.stream_k = plan.stream_k ? 1 : 0;
+    p.dp_waves = plan.dp_waves;
+    p.sk_first_tile = static_cast<int32_t>(plan.sk_first_tile);
+    p.sk_iters = plan.sk_iters;
+    p.maxparts = plan.maxparts;
     p.err = w.err;
     p.timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : DEFAULT_TIMEOUT_NS;
     p.debug_stall = (opt && opt->debug_stall) ? 1 : 0;
+    p.trace = opt ? reinterpret_cast<unsigned long long *>(opt->trace_buffer) : nullptr;
 
-    if (std::getenv("TG_TRACE"))
+    if (trace_enabled())
         std::fprintf(stderr,
                      "tg_gemm M=%lld N=%lld K=%lld batch=%lld: BN=%d stages=%d tiles=%dx%d kb=%d "
-                     "split=%d pair=%d units=%lld grid=%d pack=%d/%d epi=%d\n",
+                     "split=%d pair=%d stream_k=%d (dp_waves=%d sk_tiles=%lld maxparts=%d) units=%lld grid=%d "
+                     "pack=%d/%d epi=%d\n",
                      (long long)a.M, (long long)a.N, (long long)a.K, (long long)a.batch, plan.bn,
                      plan.stages, plan.tiles_m, plan.tiles_n, plan.k_blocks, plan.splits, plan.pair ? 2 : 1,
+                     plan.stream_k ? 1 : 0, plan.dp_waves, (long long)plan.sk_tiles, plan.maxparts,
                      (long long)plan.units, plan.grid, plan.pack_a, plan.pack_b, plan.epilogue);
 
-    int grid = plan.grid;
-    if (plan.pair) {
-        // never more clusters than can be resident at once (persistent)
-        const int pairs = max_pairs(dev, plan.bn, plan.stages);
-        if (pairs <= 0) return TG_ERR_UNSUPPORTED;
-        if (grid > 2 * pairs) grid = 2 * pairs;
-        if (std::getenv("TG_TRACE"))
-            std::fprintf(stderr, "tg_gemm: co-resident CTA pairs %d, launch grid %d\n", pairs, grid);
-    }
     e = launch_gemm(plan.bn, plan.pair, ta, tb, tc, p, plan.stages, grid, stream);
     return cuda_status(e);
 }

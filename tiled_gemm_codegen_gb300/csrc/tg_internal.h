@@ -43,6 +43,17 @@ struct KernelParams {
     uint32_t *err;        // device error word
     uint64_t timeout_ns;
     int32_t debug_stall;
+    // Stream-K schedule (stream_k == 1): every worker takes dp_waves whole
+    // tiles (tile = worker + i * workers), then the k-block range
+    // [w * sk_iters / workers, (w + 1) * sk_iters / workers) of the sk_tiles
+    // tiles that follow; a tile covered by several ranges is combined from
+    // per-range partials.  maxparts = partial slots per tile (split-K: splits).
+    int32_t stream_k;
+    int32_t dp_waves;
+    int32_t sk_first_tile;
+    int32_t maxparts;
+    int64_t sk_iters;
+    unsigned long long *trace;  // grid x 8 timestamps, or null
 };
 
 // Shared-memory budget of one tile width.  PAIR: the tile is computed by a

@@ -42,11 +42,12 @@
 // accumulator in its own tensor memory.  Per SM this halves the B bytes of
 // every k-block (no TMA multicast is used).
 //
-// Split-K (OCANNL "Module Ir.Schedule", Deterministic two-pass split
-// reduction): every split writes its fp32 partial (half-)tile to scratch,
-// then the last split to arrive at the tile's counter sums all partials in
-// the fixed order s = 0, 1, ..., splits-1 and stores C.  No split ever waits
-// for another, so the combine needs no grid-wide barrier.
+// Split-K and stream-K (OCANNL "Module Ir.Schedule", Deterministic two-pass
+// split reduction): every contributor to a tile writes its fp32 partial
+// (half-)tile to scratch, then the last to arrive at the tile's counter sums
+// all partials in the fixed k order 0, 1, ..., nparts-1 and stores C.  No
+// contributor ever waits for another, so the combine needs no grid-wide
+// barrier, and the result is deterministic for a given plan.
 //
 // Every mbarrier wait is bounded (timeout_ns, %globaltimer).  On expiry the
 // waiting role records an error code in the device error word, raises the
@@ -54,6 +55,8 @@
 // leave their loops, and every CTA then waits (bounded) for its own TMA
 // loads, MMAs and TMA stores in flight, frees its tensor memory and returns.
 #pragma once
+
+#include <atomic>
 
 #include "tg_internal.h"
 #include "tg_ptx.cuh"
@@ -83,19 +86,17 @@ __host__ __device__ constexpr uint32_t instr_desc_bf16()
 }
 
 struct Unit {
-    int32_t b, tm, tn, split, kb0, kb1;
-    int64_t tile;  // linear output-tile index over (batch, tiles_m, tiles_n)
+    int32_t b, tm, tn, kb0, kb1;
+    int32_t nparts;  // contributors to this output tile (1: store C directly)
+    int32_t part;    // this contributor's index, in k order
+    int64_t slot;    // tile index of the partial slots and arrival counter
 };
 
-// Work unit u -> (problem, tile row, tile column, K split).  Splits of one
-// tile are adjacent; tiles are rasterised in groups of group_m tile rows so
-// that concurrently running CTAs share A and B panels in L2.
-__device__ __forceinline__ Unit decode_unit(const KernelParams &p, int64_t u)
+// Output tile t -> (problem, tile row, tile column).  Tiles are rasterised in
+// groups of group_m tile rows so that concurrently running workers share A
+// and B panels in L2.
+__device__ __forceinline__ void decode_tile(const KernelParams &p, int64_t t, Unit &w)
 {
-    Unit w;
-    w.split = static_cast<int32_t>(u % p.splits);
-    const int64_t t = u / p.splits;
-    w.tile = t;
     const int64_t per_batch = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
     w.b = static_cast<int32_t>(t / per_batch);
     const int64_t r = t % per_batch;
@@ -106,9 +107,82 @@ __device__ __forceinline__ Unit decode_unit(const KernelParams &p, int64_t u)
     const int32_t in = static_cast<int32_t>(r % group_tiles);
     w.tm = first_m + in % gsize;
     w.tn = in / gsize;
-    w.kb0 = static_cast<int32_t>((static_cast<int64_t>(w.split) * p.k_blocks) / p.splits);
-    w.kb1 = static_cast<int32_t>((static_cast<int64_t>(w.split + 1) * p.k_blocks) / p.splits);
-    return w;
+}
+
+// The sequence of work units one worker (a CTA, or a CTA pair) processes.
+// Every role of the worker walks its own copy of this iterator and sees the
+// same sequence.
+//  - split-K / plain: units u = worker + i * workers over tiles x splits;
+//    split s of a tile covers k-blocks [s*KB/S, (s+1)*KB/S) (OCANNL two-pass
+//    split reduction).
+//  - stream-K: first the worker's contiguous range of the stream-K tiles'
+//    k-blocks, cut at tile boundaries (the parts of a tile are numbered by
+//    the order of their k ranges), then its dp_waves whole tiles.  Shared
+//    tiles come first so that their partial writes and combines run in the
+//    epilogue while the MMA works on the whole tiles.
+struct WorkIter {
+    int64_t i;
+    int64_t sk_pos, sk_end;
+};
+
+__device__ __forceinline__ void work_begin(const KernelParams &p, int64_t worker, int64_t workers,
+                                           WorkIter &it)
+{
+    it.i = 0;
+    it.sk_pos = p.stream_k ? worker * p.sk_iters / workers : 0;
+    it.sk_end = p.stream_k ? (worker + 1) * p.sk_iters / workers : 0;
+}
+
+// The worker whose stream-K range holds position x (ranges may be empty).
+__device__ __forceinline__ int64_t sk_owner(const KernelParams &p, int64_t x, int64_t workers)
+{
+    const int64_t w = ((x + 1) * workers - 1) / p.sk_iters;
+    return w < workers - 1 ? w : workers - 1;
+}
+
+__device__ __forceinline__ bool work_next(const KernelParams &p, int64_t worker, int64_t workers,
+                                          WorkIter &it, Unit &w)
+{
+    const int64_t KB = p.k_blocks;
+    if (!p.stream_k) {
+        const int64_t u = worker + it.i * workers;
+        if (u >= p.num_units) return false;
+        ++it.i;
+        const int32_t split = static_cast<int32_t>(u % p.splits);
+        const int64_t t = u / p.splits;
+        decode_tile(p, t, w);
+        w.kb0 = static_cast<int32_t>((static_cast<int64_t>(split) * KB) / p.splits);
+        w.kb1 = static_cast<int32_t>((static_cast<int64_t>(split + 1) * KB) / p.splits);
+        w.nparts = p.splits;
+        w.part = split;
+        w.slot = t;
+        return true;
+    }
+    if (it.sk_pos < it.sk_end) {
+        const int64_t ts = it.sk_pos / KB;
+        const int64_t tile_end = (ts + 1) * KB;
+        const int64_t end = it.sk_end < tile_end ? it.sk_end : tile_end;
+        decode_tile(p, p.sk_first_tile + ts, w);
+        w.kb0 = static_cast<int32_t>(it.sk_pos - ts * KB);
+        w.kb1 = static_cast<int32_t>(end - ts * KB);
+        const int64_t first = sk_owner(p, ts * KB, workers);
+        const int64_t last = sk_owner(p, tile_end - 1, workers);
+        w.nparts = static_cast<int32_t>(last - first + 1);
+        w.part = static_cast<int32_t>(worker - first);
+        w.slot = ts;
+        it.sk_pos = end;
+        return true;
+    }
+    if (it.i >= p.dp_waves) return false;
+    const int64_t t = worker + it.i * workers;
+    ++it.i;
+    decode_tile(p, t, w);
+    w.kb0 = 0;
+    w.kb1 = static_cast<int32_t>(KB);
+    w.nparts = 1;
+    w.part = 0;
+    w.slot = t;
+    return true;
 }
 
 enum WaitResult : int { WAIT_OK = 0, WAIT_TIMEOUT = 1, WAIT_ABORTED = 2 };
@@ -218,6 +292,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x >> 5), 0);
     const int lane = static_cast<int>(threadIdx.x & 31);
+    // optional timeline: 8 %globaltimer stamps per CTA
+    unsigned long long *trace = p.trace ? p.trace + 8ull * blockIdx.x : nullptr;
+    auto stamp = [&](int k) {
+        if (trace) trace[k] = ptx::global_timer_ns();
+    };
+    if (threadIdx.x == 0) stamp(0);
     const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;
     const bool leader = rank == 0;
     const int64_t worker = PAIR ? (blockIdx.x >> 1) : blockIdx.x;
@@ -261,6 +341,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t peer_abort =
         PAIR ? ptx::map_to_cta(ptx::smem_addr(const_cast<int32_t *>(abort_flag)), rank ^ 1u) : 0u;
     const Watchdog wd{p.timeout_ns, abort_flag, p.err, peer_abort};
+    if (threadIdx.x == 0) stamp(1);
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
@@ -269,8 +350,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool ok = true;
             // pair: both CTAs' copies complete on the leader's full barrier
             const uint32_t full0 = PAIR ? ptx::map_to_cta(full_bar(0), 0u) : full_bar(0);
-            for (int64_t u = worker; ok && u < p.num_units; u += n_workers) {
-                const Unit w = decode_unit(p, u);
+            WorkIter wi;
+            work_begin(p, worker, n_workers, wi);
+            Unit w;
+            while (ok && work_next(p, worker, n_workers, wi, w)) {
                 const int32_t zA = p.a_bcast ? 0 : w.b;
                 const int32_t zB = p.b_bcast ? 0 : w.b;
                 const int32_t m_rows = w.tm * TILE_M + static_cast<int32_t>(rank) * BM;
@@ -316,8 +399,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             constexpr uint32_t idesc = instr_desc_bf16<TILE_M, BN>();
             uint32_t it = 0, t = 0;
             bool ok = true;
-            for (int64_t u = worker; ok && u < p.num_units; u += n_workers, ++t) {
-                const Unit w = decode_unit(p, u);
+            WorkIter wi;
+            work_begin(p, worker, n_workers, wi);
+            Unit w;
+            for (; ok && work_next(p, worker, n_workers, wi, w); ++t) {
                 const uint32_t buf = t & 1u;
                 const uint32_t tph = (t >> 1) & 1u;
                 int r = wait_bounded(tempty_bar(buf), tph ^ 1u, wd);
@@ -336,6 +421,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         ok = false;
                         break;
                     }
+                    if (it == 0) stamp(2);
                     ptx::tc_fence_after();
                     const uint32_t a_addr = sA + s * G::A_STAGE;
                     const uint32_t b_addr = sB + s * G::B_STAGE;
@@ -364,6 +450,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 else
                     ptx::mma_commit(tfull_bar(buf));
             }
+            stamp(3);
             // Every MMA issued above completes before tensor memory is freed.
             if constexpr (PAIR)
                 ptx::mma_commit_pair_multicast(done_bar, 0x1);
@@ -442,32 +529,49 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         };
 
         uint32_t t = 0;
-        for (int64_t u = worker; ok && u < p.num_units; u += n_workers, ++t) {
-            const Unit w = decode_unit(p, u);
+        WorkIter wi;
+        work_begin(p, worker, n_workers, wi);
+        Unit w;
+        for (; ok && work_next(p, worker, n_workers, wi, w); ++t) {
             const uint32_t buf = t & 1u;
             const uint32_t tph = (t >> 1) & 1u;
             const int r = wait_bounded(tfull_bar(buf), tph, wd);
             if (r == WAIT_TIMEOUT) raise_abort(wd, ERR_TIMEOUT_EPILOGUE);
             if (!epi_all(r == WAIT_OK)) break;
+            if (t == 0 && warp == 2 && lane == 0) stamp(4);
             ptx::tc_fence_after();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
             const int32_t m_base = w.tm * TILE_M + static_cast<int32_t>(rank) * BM;
             const int32_t n_base = w.tn * BN;
-            if (p.splits == 1) {
+            if (w.nparts == 1) {
+                // Two register sets: the load of chunk c+1 is in flight while
+                // chunk c is staged and stored.
+                constexpr int NCH = BN / EPI_CHUNK;
+                static_assert(NCH % 2 == 0, "chunk count");
+                uint32_t va[32], vb[32];
+                ptx::tmem_load_32cols(taddr, va);
 #pragma unroll 1
-                for (int c = 0; c < BN / EPI_CHUNK; ++c) {
-                    uint32_t v[32];
-                    ptx::tmem_load_32cols(taddr + c * EPI_CHUNK, v);
-                    if (c == BN / EPI_CHUNK - 1) release_tmem(buf);
-                    store_chunk(v, m_base, n_base + c * EPI_CHUNK, w.b);
+                for (int c = 0; c < NCH; c += 2) {
+                    ptx::tmem_load_32cols_async(taddr + (c + 1) * EPI_CHUNK, vb);
+                    store_chunk(va, m_base, n_base + c * EPI_CHUNK, w.b);
+                    ptx::tmem_wait_ld(vb);
+                    if (c + 2 < NCH) ptx::tmem_load_32cols_async(taddr + (c + 2) * EPI_CHUNK, va);
+                    else release_tmem(buf);
+                    store_chunk(vb, m_base, n_base + (c + 1) * EPI_CHUNK, w.b);
+                    if (c + 2 < NCH) ptx::tmem_wait_ld(va);
                 }
             } else {
-                // Partial (half-)tile -> scratch, column-major inside the tile
-                // so that a warp's 32 rows of one column are one 128-byte line.
-                const int64_t half = w.tile * (PAIR ? 2 : 1) + rank;
+                // Partial (half-)tile -> scratch.  Layout inside one part:
+                // [chunk c][column quad j4][row][4 columns], so a warp's 32
+                // rows of one column quad are 512 contiguous bytes and every
+                // access below is a coalesced 16-byte vector per thread.
+                const int64_t half = w.slot * (PAIR ? 2 : 1) + rank;
                 const bool row_ok = (m_base + row) < p.M;
-                float *ws0 = p.partials + half * static_cast<int64_t>(p.splits) * (BM * BN);
-                float *mine = ws0 + static_cast<int64_t>(w.split) * (BM * BN);
+                const float4 *ws0 = reinterpret_cast<const float4 *>(
+                    p.partials + half * static_cast<int64_t>(p.maxparts) * (BM * BN));
+                float4 *mine = reinterpret_cast<float4 *>(p.partials) +
+                               (half * static_cast<int64_t>(p.maxparts) + w.part) * (BM * BN / 4);
+                constexpr int64_t PART4 = BM * BN / 4;  // float4s per part
 #pragma unroll 1
                 for (int c = 0; c < BN / EPI_CHUNK; ++c) {
                     uint32_t v[32];
@@ -475,15 +579,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (c == BN / EPI_CHUNK - 1) release_tmem(buf);
                     if (row_ok) {
 #pragma unroll
-                        for (int j = 0; j < EPI_CHUNK; ++j)
-                            __stcg(mine + (c * EPI_CHUNK + j) * BM + row, __uint_as_float(v[j]));
+                        for (int j4 = 0; j4 < 8; ++j4)
+                            __stcg(mine + (c * 8 + j4) * BM + row,
+                                   make_float4(__uint_as_float(v[4 * j4]), __uint_as_float(v[4 * j4 + 1]),
+                                               __uint_as_float(v[4 * j4 + 2]), __uint_as_float(v[4 * j4 + 3])));
                     }
                 }
                 __threadfence();
                 ptx::named_barrier_sync(1, 128);
                 if (warp == 2 && lane == 0) {
                     const int32_t old = atomicAdd(p.counters + half, 1);
-                    const int32_t last = (old == p.splits - 1) ? 1 : 0;
+                    const int32_t last = (old == w.nparts - 1) ? 1 : 0;
                     if (last) atomicExch(p.counters + half, 0);  // ready for the next call
                     *last_flag = last;
                 }
@@ -492,28 +598,55 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     __threadfence();
 #pragma unroll 1
                     for (int c = 0; c < BN / EPI_CHUNK; ++c) {
-                        float acc[32];
+                        float4 acc[8];
+                        const float4 *src = ws0 + c * 8 * BM + row;
 #pragma unroll
-                        for (int j = 0; j < EPI_CHUNK; ++j)
-                            acc[j] = row_ok ? __ldcg(ws0 + (c * EPI_CHUNK + j) * BM + row) : 0.0f;
-                        for (int s = 1; s < p.splits; ++s) {
-                            const float *ps = ws0 + static_cast<int64_t>(s) * (BM * BN);
+                        for (int j4 = 0; j4 < 8; ++j4)
+                            acc[j4] = row_ok ? __ldcg(src + j4 * BM) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        // parts 1 .. nparts-1 in order, two parts' loads in flight
+                        int s = 1;
+                        for (; row_ok && s + 1 < w.nparts; s += 2) {
+                            float4 t0[8], t1[8];
 #pragma unroll
-                            for (int j = 0; j < EPI_CHUNK; ++j)
-                                if (row_ok) acc[j] += __ldcg(ps + (c * EPI_CHUNK + j) * BM + row);
+                            for (int j4 = 0; j4 < 8; ++j4) {
+                                t0[j4] = __ldcg(src + s * PART4 + j4 * BM);
+                                t1[j4] = __ldcg(src + (s + 1) * PART4 + j4 * BM);
+                            }
+#pragma unroll
+                            for (int j4 = 0; j4 < 8; ++j4) {
+                                acc[j4].x += t0[j4].x; acc[j4].y += t0[j4].y;
+                                acc[j4].z += t0[j4].z; acc[j4].w += t0[j4].w;
+                                acc[j4].x += t1[j4].x; acc[j4].y += t1[j4].y;
+                                acc[j4].z += t1[j4].z; acc[j4].w += t1[j4].w;
+                            }
+                        }
+                        if (row_ok && s < w.nparts) {
+#pragma unroll
+                            for (int j4 = 0; j4 < 8; ++j4) {
+                                const float4 t0 = __ldcg(src + s * PART4 + j4 * BM);
+                                acc[j4].x += t0.x; acc[j4].y += t0.y; acc[j4].z += t0.z; acc[j4].w += t0.w;
+                            }
                         }
                         uint32_t v[32];
 #pragma unroll
-                        for (int j = 0; j < EPI_CHUNK; ++j) v[j] = __float_as_uint(acc[j]);
+                        for (int j4 = 0; j4 < 8; ++j4) {
+                            v[4 * j4] = __float_as_uint(acc[j4].x);
+                            v[4 * j4 + 1] = __float_as_uint(acc[j4].y);
+                            v[4 * j4 + 2] = __float_as_uint(acc[j4].z);
+                            v[4 * j4 + 3] = __float_as_uint(acc[j4].w);
+                        }
                         store_chunk(v, m_base, n_base + c * EPI_CHUNK, w.b);
                     }
                 }
                 ptx::named_barrier_sync(1, 128);
             }
         }
-        // Every TMA store issued by this warp has completed its writes.
-        if (lane == 0) ptx::bulk_wait_group<0>();
+        if (warp == 2 && lane == 0) stamp(5);
+        // Every TMA store issued by this warp has read its shared-memory
+        // source (the global writes complete with the grid).
+        if (lane == 0) ptx::bulk_wait_group_read<0>();
         __syncwarp();
+        if (warp == 2 && lane == 0) stamp(6);
     }
 
     __syncthreads();
@@ -552,6 +685,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         else
             ptx::tmem_dealloc(tmem_base, G::TMEM_COLS);
     }
+    if (threadIdx.x == 0) stamp(7);
 }
 
 template <int BN, int STAGES, bool PAIR>
@@ -560,8 +694,17 @@ cudaError_t launch_fixed(const CUtensorMap &ta, const CUtensorMap &tb, const CUt
 {
     constexpr int smem = Geometry<BN, PAIR>::smem_bytes(STAGES);
     auto kern = gemm_kernel<BN, STAGES, PAIR>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    // the shared-memory opt-in is per device; set it once per device
+    static std::atomic<unsigned long long> configured{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
+    if (!bit || !(configured.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit, std::memory_order_acq_rel);
+    }
     if constexpr (!PAIR) {
         kern<<<grid, NUM_THREADS, smem, s>>>(ta, tb, tc, p);
         return cudaGetLastError();

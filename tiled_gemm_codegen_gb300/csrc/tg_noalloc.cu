@@ -80,6 +80,7 @@ TG_API tg_status tg_gemm_splitk_static(const void *A, const void *B, float *C, i
     tg_options opt{};
     opt.split_k = split_k;
     opt.cta_pair = 1;  // one CTA per tile: the launch below is the single-CTA kernel
+    opt.stream_k = 1;  // the split factor is the caller's
     Plan plan;
     PlanInput in;
     if (!shared_plan(A, B, C, M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC, sms, &opt, &plan, &in))
@@ -132,6 +133,7 @@ TG_API tg_status tg_gemm_splitk_static(const void *A, const void *B, float *C, i
     p.ldc = ldc;
     p.strideC = strideC;
     p.partials = partials;
+    p.maxparts = plan.splits;
     p.counters = counters;
     p.err = err;
     p.timeout_ns = 2000000000ull;

@@ -92,6 +92,7 @@ struct PlanInput {
     // overrides (0 = choose)
     int block_n, stages, split_k, force_pack, epilogue, max_ctas;
     int cta_pair;  // 0 = choose, 1 = one CTA per tile, 2 = two-SM tiles
+    int stream_k;  // 0 = choose, 1 = off, 2 = on (when the last wave is partial)
 };
 
 struct Plan {
@@ -104,12 +105,51 @@ struct Plan {
     int epilogue = 1;  // 1 TMA store, 2 plain stores
     int smem = 0, tmem = 0;
     int group_m = 8;
+    // stream-K schedule (see KernelParams)
+    bool stream_k = false;
+    int dp_waves = 0, maxparts = 1;
+    int64_t sk_first_tile = 0, sk_tiles = 0, sk_iters = 0;
     int64_t ws_pack_a = 0, ws_pack_b = 0, ws_partials = 0, ws_counters = 0;
     int64_t workspace() const { return ws_pack_a + ws_pack_b + ws_partials + ws_counters; }
 };
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+
+// Stream-K schedule of `tiles` tiles of `kb` k-blocks on `workers` workers:
+// whole tiles for dp_waves full waves, then the remaining sk_tiles tiles'
+// k-blocks split into `workers` contiguous ranges.  maxparts = the largest
+// number of ranges one tile meets (its partial slots).  Returns false when
+// the last wave is already full (nothing to balance).
+struct SkSchedule {
+    int dp_waves = 0, maxparts = 1;
+    int64_t sk_first_tile = 0, sk_tiles = 0, sk_iters = 0;
+};
+
+inline int64_t sk_owner_host(int64_t x, int64_t workers, int64_t iters)
+{
+    const int64_t w = ((x + 1) * workers - 1) / iters;
+    return w < workers - 1 ? w : workers - 1;
+}
+
+inline bool sk_schedule(int64_t tiles, int64_t kb, int64_t workers, SkSchedule &out)
+{
+    if (workers <= 1 || tiles % workers == 0 || kb < 1) return false;
+    SkSchedule s;
+    s.dp_waves = static_cast<int>(tiles / workers);
+    s.sk_first_tile = static_cast<int64_t>(s.dp_waves) * workers;
+    s.sk_tiles = tiles - s.sk_first_tile;
+    s.sk_iters = s.sk_tiles * kb;
+    int maxp = 1;
+    for (int64_t ts = 0; ts < s.sk_tiles; ++ts) {
+        const int64_t first = sk_owner_host(ts * kb, workers, s.sk_iters);
+        const int64_t last = sk_owner_host((ts + 1) * kb - 1, workers, s.sk_iters);
+        maxp = std::max<int>(maxp, static_cast<int>(last - first + 1));
+    }
+    s.maxparts = maxp;
+    out = s;
+    return true;
+}
 
 // Cost model (nanoseconds) used to rank candidate plans.  The MMA time of a
 // k-block is 2*BM*BN*BK flops per SM at the SM's share of the dense bf16
@@ -128,28 +168,71 @@ inline double tile_efficiency(int bn, bool pair)
 }
 
 inline double plan_cost_ns(const PlanInput &in, int bn, bool pair, int splits, int k_blocks,
-                           int64_t tiles, int sms)
+                           int64_t tiles, int sms, bool stream_k = false)
 {
     const double sm_flops = 1.95e15 / 152.0;  // per-SM dense bf16, flop/s
     const double kb_ns = (2.0 * BM * bn * BK) / sm_flops * 1e9 / tile_efficiency(bn, pair);
     const int64_t workers = pair ? std::max(1, sms / 2) : sms;
     const int64_t units = tiles * splits;
-    const int64_t waves = ceil_div(units, workers);
-    const int64_t kb_unit = ceil_div(k_blocks, splits);
-    const double t_mma = static_cast<double>(waves) * static_cast<double>(kb_unit) * kb_ns;
+    double t_mma = 0.0, partial = 0.0;
+    if (stream_k) {
+        // whole waves, then an even share of the remaining k-blocks
+        const int64_t dp = tiles / workers;
+        const int64_t sk_iters = (tiles - dp * workers) * k_blocks;
+        t_mma = (static_cast<double>(dp * k_blocks) + static_cast<double>(ceil_div(sk_iters, workers))) * kb_ns;
+        partial = 2.0 * 4.0 * (pair ? 2 : 1) * BM * bn * 2.0 * static_cast<double>(tiles - dp * workers);
+    } else {
+        const int64_t waves = ceil_div(units, workers);
+        const int64_t kb_unit = ceil_div(k_blocks, splits);
+        t_mma = static_cast<double>(waves) * static_cast<double>(kb_unit) * kb_ns;
+        partial = splits > 1 ? 2.0 * 4.0 * in.batch * in.M * in.N * splits : 0.0;
+    }
     const double ab = 2.0 * in.batch * (in.M * in.K + in.K * in.N);
     const double c = 4.0 * in.batch * in.M * in.N;
-    const double partial = splits > 1 ? 2.0 * 4.0 * in.batch * in.M * in.N * splits : 0.0;
     const int64_t active_sms = std::min<int64_t>(units, workers) * (pair ? 2 : 1);
     const double bw = std::min(6.5e12, static_cast<double>(active_sms) * 50e9);
     const double t_mem = (ab + c + partial) / bw * 1e9;
-    const double fixup = splits > 1 ? 2000.0 : 0.0;
+    const double fixup = (splits > 1 || stream_k) ? 2000.0 : 0.0;
     return (t_mma > t_mem ? t_mma : t_mem) + fixup;
 }
 
 // Whether the planner may pick two-SM tiles on its own (otherwise only when
 // asked with cta_pair = 2).
 constexpr bool PAIR_BY_DEFAULT = true;
+
+// Split-K / stream-K scratch, kept per 128-row (half-)tile.
+inline void set_partial_workspace(const PlanInput &in, Plan &p)
+{
+    const int64_t per_tile = p.pair ? 2 : 1;
+    int64_t slot_tiles = 0;
+    if (p.stream_k)
+        slot_tiles = p.sk_tiles;
+    else if (p.splits > 1)
+        slot_tiles = in.batch * p.tiles_m * static_cast<int64_t>(p.tiles_n);
+    p.ws_partials = slot_tiles * per_tile * p.maxparts * BM * static_cast<int64_t>(p.bn) * 4;
+    p.ws_counters = slot_tiles > 0 ? round_up(slot_tiles * per_tile * 4, 256) : 0;
+}
+
+// Re-derives the stream-K schedule for the grid actually launched (the
+// co-resident cluster limit can lower it); false if it no longer applies.
+inline void replan_stream_k(const PlanInput &in, Plan &p, int grid)
+{
+    if (!p.stream_k) return;
+    const int64_t workers = grid / (p.pair ? 2 : 1);
+    const int64_t tiles_total = in.batch * p.tiles_m * static_cast<int64_t>(p.tiles_n);
+    SkSchedule sk;
+    if (sk_schedule(tiles_total, p.k_blocks, workers, sk)) {
+        p.dp_waves = sk.dp_waves;
+        p.sk_first_tile = sk.sk_first_tile;
+        p.sk_tiles = sk.sk_tiles;
+        p.sk_iters = sk.sk_iters;
+        p.maxparts = sk.maxparts;
+    } else {
+        p.stream_k = false;
+        p.maxparts = p.splits;
+    }
+    set_partial_workspace(in, p);
+}
 
 // Returns false (and leaves `out` unspecified) for an invalid override.
 inline bool make_plan(const PlanInput &in, Plan &out)
@@ -166,6 +249,8 @@ inline bool make_plan(const PlanInput &in, Plan &out)
     if (in.split_k < 0 || in.stages < 0 || in.max_ctas < 0) return false;
     if (in.epilogue < 0 || in.epilogue > 2) return false;
     if (in.cta_pair < 0 || in.cta_pair > 2) return false;
+    if (in.stream_k < 0 || in.stream_k > 2) return false;
+    if (in.stream_k == 2 && in.split_k > 1) return false;  // one way of splitting K at a time
     if (in.split_k > 0 && in.split_k > p.k_blocks) return false;
     if (in.cta_pair == 2 && in.block_n != 0 && !pair_width(in.block_n)) return false;
 
@@ -195,15 +280,21 @@ inline bool make_plan(const PlanInput &in, Plan &out)
             split_hi = static_cast<int>(std::min<int64_t>(16, std::max<int64_t>(1, p.k_blocks / 8)));
         }
         for (int s = split_lo; s <= split_hi; ++s) {
-            const double c = plan_cost_ns(in, cd.bn, cd.pair, s, p.k_blocks, tiles, sms);
-            if (!have || c < best * 0.999) {
-                have = true;
-                best = c;
-                p.bn = cd.bn;
-                p.pair = cd.pair;
-                p.splits = s;
-                p.tiles_m = static_cast<int>(tiles_m);
-                p.tiles_n = static_cast<int>(tiles_n);
+            for (int sk = 0; sk < 2; ++sk) {
+                const bool use_sk = sk == 1;
+                if (use_sk && (s > 1 || in.stream_k == 1 || tiles % workers == 0)) continue;
+                if (!use_sk && in.stream_k == 2 && tiles % workers != 0) continue;
+                const double c = plan_cost_ns(in, cd.bn, cd.pair, s, p.k_blocks, tiles, sms, use_sk);
+                if (!have || c < best * 0.999) {
+                    have = true;
+                    best = c;
+                    p.bn = cd.bn;
+                    p.pair = cd.pair;
+                    p.splits = s;
+                    p.stream_k = use_sk;
+                    p.tiles_m = static_cast<int>(tiles_m);
+                    p.tiles_n = static_cast<int>(tiles_n);
+                }
             }
         }
     }
@@ -225,6 +316,20 @@ inline bool make_plan(const PlanInput &in, Plan &out)
     }
     p.grid = static_cast<int>(w * (p.pair ? 2 : 1));
     p.group_m = 8;
+    if (p.stream_k) {
+        SkSchedule sk;
+        const int64_t tiles_total = in.batch * p.tiles_m * static_cast<int64_t>(p.tiles_n);
+        if (!sk_schedule(tiles_total, p.k_blocks, w, sk)) {
+            p.stream_k = false;  // e.g. max_ctas made the last wave full
+        } else {
+            p.dp_waves = sk.dp_waves;
+            p.sk_first_tile = sk.sk_first_tile;
+            p.sk_tiles = sk.sk_tiles;
+            p.sk_iters = sk.sk_iters;
+            p.maxparts = sk.maxparts;
+        }
+    }
+    if (!p.stream_k) p.maxparts = p.splits;
 
     p.pack_a = in.force_pack || !in.a_tma_ok;
     p.pack_b = in.force_pack || !in.b_tma_ok;
@@ -237,10 +342,7 @@ inline bool make_plan(const PlanInput &in, Plan &out)
     const int64_t batch_b = in.b_bcast ? 1 : in.batch;
     p.ws_pack_a = p.pack_a ? round_up(batch_a * in.M * round_up(in.K, 8) * 2, 256) : 0;
     p.ws_pack_b = p.pack_b ? round_up(batch_b * in.K * round_up(in.N, 8) * 2, 256) : 0;
-    // split-K scratch is kept per 128-row (half-)tile
-    const int64_t halves = in.batch * p.tiles_m * static_cast<int64_t>(p.tiles_n) * (p.pair ? 2 : 1);
-    p.ws_partials = p.splits > 1 ? halves * p.splits * BM * p.bn * 4 : 0;
-    p.ws_counters = p.splits > 1 ? round_up(halves * 4, 256) : 0;
+    set_partial_workspace(in, p);
     out = p;
     return true;
 }
