@@ -38,28 +38,76 @@ constexpr int64_t EXTENT_LIMIT = INT32_MAX;
 // arbitrary element strides into a dense buffer whose rows are padded to a
 // multiple of 8 elements (16 bytes) - the address form TMA can load.  The
 // pad columns are written as 0; the GEMM never reads them (its tensor map
-// extent is the true column count).
-__global__ void pack_bf16_kernel(const uint16_t *__restrict__ src, uint16_t *__restrict__ dst,
-                                 int64_t rows, int64_t cols, int64_t ld_src, int64_t s_src,
-                                 int64_t ld_dst, int64_t total_chunks)
+// extent is the true column count).  One launch packs A and B (two jobs).
+//
+// Each thread writes one 16-byte chunk (8 elements).  Its source is read
+// with the widest aligned loads the source address allows: one 16-byte,
+// two 8-byte or four 4-byte loads, or, for a 2-byte-aligned source, five
+// aligned 4-byte words realigned with funnel shifts.  A wider load is used
+// only when every byte it touches lies inside the operand's span
+// [span_begin, span_end); otherwise, and in a row's ragged tail, elements
+// are read one by one.
+struct PackJob {
+    const uint16_t *src;
+    uint16_t *dst;
+    int64_t rows, cols, ld_src, s_src, ld_dst, chunks;
+    uintptr_t span_begin, span_end;  // bytes of the source this job may read
+};
+
+__device__ __forceinline__ uint32_t pack_pair(uint16_t lo, uint16_t hi)
 {
-    const int64_t chunks_per_row = ld_dst / 8;
-    for (int64_t c = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; c < total_chunks;
-         c += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
+__device__ __forceinline__ uint4 load8_bf16(const uint16_t *s, const PackJob &j)
+{
+    const uintptr_t a = reinterpret_cast<uintptr_t>(s);
+    if ((a & 15u) == 0) return *reinterpret_cast<const uint4 *>(s);
+    if ((a & 7u) == 0) {
+        const uint2 lo = *reinterpret_cast<const uint2 *>(s);
+        const uint2 hi = *reinterpret_cast<const uint2 *>(s + 4);
+        return make_uint4(lo.x, lo.y, hi.x, hi.y);
+    }
+    if ((a & 3u) == 0) {
+        const uint32_t *w = reinterpret_cast<const uint32_t *>(s);
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    if (a - 2 >= j.span_begin && a + 18 <= j.span_end) {
+        // words at a-2, a+2, .., a+14: element e of s sits in the high half
+        // of word (e+1)/2 (e odd: low half of word (e+1)/2)
+        const uint32_t *w = reinterpret_cast<const uint32_t *>(a - 2);
+        const uint32_t w0 = w[0], w1 = w[1], w2 = w[2], w3 = w[3], w4 = w[4];
+        return make_uint4(__funnelshift_r(w0, w1, 16), __funnelshift_r(w1, w2, 16),
+                          __funnelshift_r(w2, w3, 16), __funnelshift_r(w3, w4, 16));
+    }
+    return make_uint4(pack_pair(s[0], s[1]), pack_pair(s[2], s[3]), pack_pair(s[4], s[5]),
+                      pack_pair(s[6], s[7]));
+}
+
+__global__ void pack_bf16_kernel(PackJob ja, PackJob jb, int blocks_a)
+{
+    const bool is_a = static_cast<int>(blockIdx.x) < blocks_a;
+    const PackJob j = is_a ? ja : jb;
+    const int64_t bid = is_a ? blockIdx.x : blockIdx.x - blocks_a;
+    const int64_t nblocks = is_a ? blocks_a : gridDim.x - blocks_a;
+    const int64_t chunks_per_row = j.ld_dst / 8;
+    for (int64_t c = bid * blockDim.x + threadIdx.x; c < j.chunks; c += nblocks * blockDim.x) {
         const int64_t row_g = c / chunks_per_row;
         const int64_t col0 = (c - row_g * chunks_per_row) * 8;
-        const int64_t b = row_g / rows;
-        const int64_t r = row_g - b * rows;
-        const uint16_t *s = src + b * s_src + r * ld_src + col0;
-        uint16_t v[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] = (col0 + e < cols) ? s[e] : static_cast<uint16_t>(0);
+        const int64_t b = row_g / j.rows;
+        const int64_t r = row_g - b * j.rows;
+        const uint16_t *s = j.src + b * j.s_src + r * j.ld_src + col0;
         uint4 out;
-        out.x = static_cast<uint32_t>(v[0]) | (static_cast<uint32_t>(v[1]) << 16);
-        out.y = static_cast<uint32_t>(v[2]) | (static_cast<uint32_t>(v[3]) << 16);
-        out.z = static_cast<uint32_t>(v[4]) | (static_cast<uint32_t>(v[5]) << 16);
-        out.w = static_cast<uint32_t>(v[6]) | (static_cast<uint32_t>(v[7]) << 16);
-        *reinterpret_cast<uint4 *>(dst + row_g * ld_dst + col0) = out;
+        if (col0 + 8 <= j.cols) {
+            out = load8_bf16(s, j);
+        } else {
+            uint16_t v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = (col0 + e < j.cols) ? s[e] : static_cast<uint16_t>(0);
+            out = make_uint4(pack_pair(v[0], v[1]), pack_pair(v[2], v[3]), pack_pair(v[4], v[5]),
+                             pack_pair(v[6], v[7]));
+        }
+        *reinterpret_cast<uint4 *>(j.dst + row_g * j.ld_dst + col0) = out;
     }
 }
 
@@ -488,29 +536,40 @@ tg_status run_gemm(const Args &a, cudaStream_t stream, const tg_options *opt)
     uint16_t *pack_b_buf = reinterpret_cast<uint16_t *>(arena + plan.ws_pack_a);
     float *partials = reinterpret_cast<float *>(arena + plan.ws_pack_a + plan.ws_pack_b);
 
-    if (plan.pack_a) {
-        const int64_t nb = in.a_bcast ? 1 : a.batch;
-        const int64_t ld2 = round_up(a.K, 8);
-        const int64_t chunks = nb * a.M * (ld2 / 8);
-        pack_bf16_kernel<<<grid_for(chunks, sms), 256, 0, stream>>>(
-            static_cast<const uint16_t *>(a.A), pack_a_buf, a.M, a.K, a.lda, a.sA, ld2, chunks);
+    if (plan.pack_a || plan.pack_b) {
+        PackJob ja{}, jb{};
+        if (plan.pack_a) {
+            const int64_t nb = in.a_bcast ? 1 : a.batch;
+            const int64_t ld2 = round_up(a.K, 8);
+            const uintptr_t base = reinterpret_cast<uintptr_t>(a.A);
+            ja = PackJob{static_cast<const uint16_t *>(a.A), pack_a_buf, a.M, a.K, a.lda, a.sA, ld2,
+                         nb * a.M * (ld2 / 8), base,
+                         base + 2u * static_cast<uintptr_t>(span_elems(a.M, a.K, a.lda, nb, a.sA))};
+        }
+        if (plan.pack_b) {
+            const int64_t nb = in.b_bcast ? 1 : a.batch;
+            const int64_t ld2 = round_up(a.N, 8);
+            const uintptr_t base = reinterpret_cast<uintptr_t>(a.B);
+            jb = PackJob{static_cast<const uint16_t *>(a.B), pack_b_buf, a.K, a.N, a.ldb, a.sB, ld2,
+                         nb * a.K * (ld2 / 8), base,
+                         base + 2u * static_cast<uintptr_t>(span_elems(a.K, a.N, a.ldb, nb, a.sB))};
+        }
+        const int blocks_a = plan.pack_a ? grid_for(ja.chunks, sms) : 0;
+        const int blocks_b = plan.pack_b ? grid_for(jb.chunks, sms) : 0;
+        pack_bf16_kernel<<<blocks_a + blocks_b, 256, 0, stream>>>(ja, jb, blocks_a);
         if ((e = cudaGetLastError()) != cudaSuccess) return cuda_status(e);
-        A = pack_a_buf;
-        lda = ld2;
-        sA = in.a_bcast ? 0 : a.M * ld2;
-        if (!encode_a()) return TG_ERR_CUDA;
-    }
-    if (plan.pack_b) {
-        const int64_t nb = in.b_bcast ? 1 : a.batch;
-        const int64_t ld2 = round_up(a.N, 8);
-        const int64_t chunks = nb * a.K * (ld2 / 8);
-        pack_bf16_kernel<<<grid_for(chunks, sms), 256, 0, stream>>>(
-            static_cast<const uint16_t *>(a.B), pack_b_buf, a.K, a.N, a.ldb, a.sB, ld2, chunks);
-        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_status(e);
-        B = pack_b_buf;
-        ldb = ld2;
-        sB = in.b_bcast ? 0 : a.K * ld2;
-        if (!encode_b()) return TG_ERR_CUDA;
+        if (plan.pack_a) {
+            A = pack_a_buf;
+            lda = ja.ld_dst;
+            sA = in.a_bcast ? 0 : a.M * ja.ld_dst;
+            if (!encode_a()) return TG_ERR_CUDA;
+        }
+        if (plan.pack_b) {
+            B = pack_b_buf;
+            ldb = jb.ld_dst;
+            sB = in.b_bcast ? 0 : a.K * jb.ld_dst;
+            if (!encode_b()) return TG_ERR_CUDA;
+        }
     }
     if (plan.epilogue == 1) {
         const uint64_t z = static_cast<uint64_t>(a.batch);
