@@ -497,21 +497,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             } else {
                 __syncwarp();
-                // Coalesced: lane l writes column col0 + l of each row.
+                // Coalesced: lane l writes column col0 + l of each row.  All
+                // 32 values are read from the box first, then the 32 row
+                // stores go out back to back.
                 const int32_t col = col0 + lane;
+                const uint32_t src = box + ((lane >> 2) << 4) + ((lane & 3) << 2);
+                float vals[32];
+#pragma unroll
+                for (int r = 0; r < 32; ++r) vals[r] = ld_shared_f32((src ^ ((r & 7) << 4)) + r * 128);
+                __syncwarp();
                 if (col < p.N) {
                     float *dst = p.C + static_cast<int64_t>(b) * p.strideC +
                                  static_cast<int64_t>(row0) * p.ldc + col;
                     const int32_t nrows = min(32, p.M - row0);
-                    const uint32_t src = box + (((lane >> 2)) << 4) + ((lane & 3) << 2);
-#pragma unroll 8
-                    for (int r = 0; r < 32; ++r) {
-                        if (r < nrows)
-                            dst[static_cast<int64_t>(r) * p.ldc] =
-                                ld_shared_f32((src ^ ((r & 7) << 4)) + r * 128);
-                    }
+#pragma unroll
+                    for (int r = 0; r < 32; ++r)
+                        if (r < nrows) dst[static_cast<int64_t>(r) * p.ldc] = vals[r];
                 }
-                __syncwarp();
             }
         };
 
