@@ -135,6 +135,54 @@ tg_status tg_gemm_ex(const void *A, const void *B, float *C,
                      int64_t batch, int64_t strideA, int64_t strideB, int64_t strideC,
                      tg_stream_t stream, const tg_options *opt);
 
+/* Fused epilogue (OCANNL "Module Ir.Schedule", Epilogue fusion: the
+ * elementwise tail of a reduction - bias add, activation, residual - folded
+ * into the accumulator's store-back instead of a separate memory pass).
+ *
+ *     D_b[i][j] = act(alpha * (A_b B_b)[i][j] + bias_b[j]) + beta * R_b[i][j]
+ *
+ * applied once to the final fp32 value of every element (after any split-K
+ * or stream-K combine), each product and sum rounded separately in fp32 (no
+ * fused multiply-add).  With activation NONE or RELU the result therefore
+ * equals, bit for bit, the same formula applied in fp32 to tg_gemm's output;
+ * a bf16 D is that fp32 value rounded to nearest even. */
+typedef enum tg_activation {
+    TG_ACT_NONE = 0,
+    TG_ACT_RELU = 1,      /* max(x, 0)                                        */
+    TG_ACT_GELU_TANH = 2, /* x/2 (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3)))    */
+    TG_ACT_SILU = 3       /* x / (1 + exp(-x))                                */
+} tg_activation;
+
+typedef enum tg_dtype { TG_F32 = 0, TG_BF16 = 1 } tg_dtype;
+
+typedef struct tg_epilogue {
+    float alpha;           /* scales A B                                       */
+    float beta;            /* scales the residual (ignored without residual)   */
+    const float *bias;     /* device, fp32: bias_b[j] = bias[b*bias_stride + j] */
+                           /* (j < N), or NULL for none                        */
+    int64_t bias_stride;   /* elements between problems' bias vectors (0: one  */
+                           /* vector for all problems)                         */
+    const void *residual;  /* device, same type as D: R_b[i][j] =              */
+                           /* residual[b*strideR + i*ldr + j], or NULL. It may */
+                           /* be D itself (same pointer and strides); any      */
+                           /* other overlap with D is rejected                 */
+    int64_t ldr, strideR;
+    int32_t activation;    /* tg_activation                                    */
+    int32_t out_type;      /* tg_dtype of D (and of the residual)              */
+    int32_t reserved[6];
+} tg_epilogue;
+
+/* The GEMM with a fused epilogue writing D (fp32 or bf16, ep->out_type),
+ * row-major with ldd / strideD in elements of D's type.  ep must not be
+ * NULL.  Same conventions, checks and options as tg_gemm_ex; K == 0 gives
+ * D = act(bias) + beta * R.  TG_ERR_INVALID_ARG also for an unknown
+ * activation or out_type, or a residual with ldr < N. */
+tg_status tg_gemm_fused(const void *A, const void *B, void *D,
+                        int64_t M, int64_t N, int64_t K,
+                        int64_t lda, int64_t ldb, int64_t ldd,
+                        int64_t batch, int64_t strideA, int64_t strideB, int64_t strideD,
+                        const tg_epilogue *ep, tg_stream_t stream, const tg_options *opt);
+
 /* The GEMM on HOST buffers: copies the spans of A and B that the strides
  * reach to device scratch owned by the library, runs tg_gemm_ex there, and
  * copies the reached span of C back.  Synchronous: returns after C is on the

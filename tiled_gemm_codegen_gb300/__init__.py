@@ -12,14 +12,18 @@ from __future__ import annotations
 
 import ctypes
 
-from ._abi import (TG_ERR_CUDA, TG_ERR_INVALID_ARG, TG_ERR_OOM, TG_ERR_TIMEOUT,
-                   TG_ERR_UNSUPPORTED, TG_OK, STATUS_NAMES, library_path, load, tg_options,
-                   tg_plan_info)
+from ._abi import (TG_ACT_GELU_TANH, TG_ACT_NONE, TG_ACT_RELU, TG_ACT_SILU, TG_BF16, TG_ERR_CUDA,
+                   TG_ERR_INVALID_ARG, TG_ERR_OOM, TG_ERR_TIMEOUT, TG_ERR_UNSUPPORTED, TG_F32, TG_OK,
+                   STATUS_NAMES, library_path, load, tg_epilogue, tg_options, tg_plan_info)
+
+ACTIVATIONS = {"none": TG_ACT_NONE, "relu": TG_ACT_RELU, "gelu_tanh": TG_ACT_GELU_TANH,
+               "silu": TG_ACT_SILU}
 
 __all__ = [
     "TG_OK", "TG_ERR_INVALID_ARG", "TG_ERR_UNSUPPORTED", "TG_ERR_CUDA", "TG_ERR_OOM",
     "TG_ERR_TIMEOUT", "TgError", "tg_options", "tg_plan_info", "load", "library_path",
-    "tg_gemm", "tg_gemm_ex", "tg_gemm_host", "tg_gemm_splitk_static", "tg_plan", "tg_device_error", "tg_status_string",
+    "tg_gemm", "tg_gemm_ex", "tg_gemm_host", "tg_gemm_fused", "tg_gemm_splitk_static", "tg_plan",
+    "tg_epilogue", "gemm_fused", "ACTIVATIONS", "tg_device_error", "tg_status_string",
     "tg_shutdown", "make_options", "gemm", "gemm_host", "plan", "device_error",
 ]
 
@@ -46,6 +50,13 @@ def tg_gemm_host(A, B, C, M, N, K, lda, ldb, ldc, batch, strideA, strideB, strid
                  opt=None) -> int:
     return load().tg_gemm_host(A, B, C, M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC,
                                stream, ctypes.byref(opt) if opt is not None else None)
+
+
+def tg_gemm_fused(A, B, D, M, N, K, lda, ldb, ldd, batch, strideA, strideB, strideD, ep,
+                  stream=None, opt=None) -> int:
+    return load().tg_gemm_fused(A, B, D, M, N, K, lda, ldb, ldd, batch, strideA, strideB, strideD,
+                                ctypes.byref(ep), stream,
+                                ctypes.byref(opt) if opt is not None else None)
 
 
 def tg_gemm_splitk_static(A, B, C, M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC,
@@ -144,6 +155,60 @@ def gemm(A, B, C=None, *, options: tg_options | None = None, stream=None):
     if st != TG_OK:
         raise TgError(st, "tg_gemm_ex")
     return C
+
+
+def gemm_fused(A, B, D=None, *, bias=None, residual=None, alpha: float = 1.0, beta: float = 1.0,
+               activation: str = "none", out_dtype=None, options: tg_options | None = None,
+               stream=None):
+    """D = act(alpha * (A @ B) + bias) + beta * residual, fused into the GEMM's
+    store-back.  bias: fp32 CUDA tensor [N] or [batch, N]; residual: CUDA
+    tensor shaped like D; D: fp32 or bf16 (out_dtype, default fp32)."""
+    import torch
+
+    if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
+        raise TypeError("A and B must be bf16")
+    pa, M, K, lda, ba, sA = _operand_geometry(A, -2, "A")
+    pb, K2, N, ldb, bb, sB = _operand_geometry(B, -2, "B")
+    if K2 != K:
+        raise ValueError(f"inner dimensions differ: {K} vs {K2}")
+    batch = max(ba, bb)
+    if ba == 1:
+        sA = 0
+    if bb == 1:
+        sB = 0
+    if D is None:
+        dt = out_dtype if out_dtype is not None else torch.float32
+        shape = (batch, M, N) if (A.dim() == 3 or B.dim() == 3) else (M, N)
+        D = torch.empty(shape, dtype=dt, device=A.device)
+    if D.dtype not in (torch.float32, torch.bfloat16) or not D.is_cuda:
+        raise TypeError("D must be an fp32 or bf16 CUDA tensor")
+    pd, Md, Nd, ldd, bd, sD = _operand_geometry(D, -2, "D")
+    if (Md, Nd) != (M, N) or bd != batch:
+        raise ValueError("D has the wrong shape")
+    ep = tg_epilogue()
+    ep.alpha = float(alpha)
+    ep.beta = float(beta)
+    ep.activation = ACTIVATIONS[activation]
+    ep.out_type = TG_BF16 if D.dtype == torch.bfloat16 else TG_F32
+    if bias is not None:
+        if bias.dtype != torch.float32 or not bias.is_cuda or bias.stride(-1) != 1:
+            raise TypeError("bias must be a contiguous fp32 CUDA tensor")
+        ep.bias = bias.data_ptr()
+        ep.bias_stride = bias.stride(0) if bias.dim() == 2 and bias.shape[0] > 1 else 0
+    if residual is not None:
+        if residual.dtype != D.dtype or not residual.is_cuda:
+            raise TypeError("residual must have D's dtype and live on the GPU")
+        pr, Mr, Nr, ldr, br, sR = _operand_geometry(residual, -2, "residual")
+        if (Mr, Nr) != (M, N) or br not in (1, batch):
+            raise ValueError("residual has the wrong shape")
+        ep.residual = pr
+        ep.ldr = ldr
+        ep.strideR = sR if br > 1 else 0
+    st = tg_gemm_fused(pa, pb, pd, M, N, K, lda, ldb, ldd, batch, sA, sB, sD, ep,
+                       _stream_ptr(stream), options)
+    if st != TG_OK:
+        raise TgError(st, "tg_gemm_fused")
+    return D
 
 
 def gemm_host(A, B, C=None, *, options: tg_options | None = None, stream=None):

@@ -75,6 +75,24 @@ class tg_plan_info(ctypes.Structure):
         return {name: getattr(self, name) for name, _ in self._fields_ if name != "reserved"}
 
 
+class tg_epilogue(ctypes.Structure):
+    _fields_ = [
+        ("alpha", ctypes.c_float),
+        ("beta", ctypes.c_float),
+        ("bias", ctypes.c_void_p),
+        ("bias_stride", ctypes.c_int64),
+        ("residual", ctypes.c_void_p),
+        ("ldr", ctypes.c_int64),
+        ("strideR", ctypes.c_int64),
+        ("activation", ctypes.c_int32),
+        ("out_type", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 6),
+    ]
+
+
+TG_ACT_NONE, TG_ACT_RELU, TG_ACT_GELU_TANH, TG_ACT_SILU = 0, 1, 2, 3
+TG_F32, TG_BF16 = 0, 1
+
 _i64 = ctypes.c_int64
 _vp = ctypes.c_void_p
 _GEMM_ARGS = [_vp, _vp, _vp] + [_i64] * 10 + [_vp]
@@ -85,6 +103,8 @@ SIGNATURES = {
     "tg_gemm_host": (_GEMM_ARGS + [ctypes.POINTER(tg_options)], ctypes.c_int),
     "tg_plan": ([_vp, _vp, _vp] + [_i64] * 10 + [ctypes.c_int32, ctypes.POINTER(tg_options),
                                                    ctypes.POINTER(tg_plan_info)], ctypes.c_int),
+    "tg_gemm_fused": ([_vp, _vp, _vp] + [_i64] * 10 + [ctypes.POINTER(tg_epilogue), _vp,
+                                                         ctypes.POINTER(tg_options)], ctypes.c_int),
     "tg_gemm_splitk_static": ([_vp, _vp, _vp] + [_i64] * 10 + [ctypes.c_int32, _vp], ctypes.c_int),
     "tg_device_error": ([_vp], ctypes.c_int),
     "tg_status_string": ([ctypes.c_int], ctypes.c_char_p),

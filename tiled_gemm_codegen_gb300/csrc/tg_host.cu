@@ -14,6 +14,7 @@
 #include <tuple>
 #include <utility>
 
+#include "tg_epilogue.cuh"
 #include "tg_gemm.h"
 #include "tg_internal.h"
 #include "tg_plan.h"
@@ -129,8 +130,9 @@ __global__ void zero_c_kernel(float *C, int64_t M, int64_t N, int64_t ldc, int64
 struct Args {
     const void *A;
     const void *B;
-    float *C;
+    void *C;  // C (fp32), or D of the fused epilogue (fp32 or bf16)
     int64_t M, N, K, lda, ldb, ldc, batch, sA, sB, sC;
+    int64_t c_bytes = 4;  // element size of C
 };
 
 // Elements spanned by one operand over all problems (0 if empty).  Callers
@@ -181,7 +183,8 @@ tg_status validate(const Args &a)
     if (a.batch > 1 && a.sC < one_c) return TG_ERR_INVALID_ARG;
     if (a.K > 0) {
         const uintptr_t c0 = reinterpret_cast<uintptr_t>(a.C);
-        const uintptr_t c1 = c0 + 4u * static_cast<uintptr_t>(span_elems(a.M, a.N, a.ldc, a.batch, a.sC));
+        const uintptr_t c1 =
+            c0 + static_cast<uintptr_t>(a.c_bytes) * static_cast<uintptr_t>(span_elems(a.M, a.N, a.ldc, a.batch, a.sC));
         const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.A);
         const uintptr_t a1 = a0 + 2u * static_cast<uintptr_t>(span_elems(a.M, a.K, a.lda, a.batch, a.sA));
         const uintptr_t b0 = reinterpret_cast<uintptr_t>(a.B);
@@ -207,7 +210,8 @@ PlanInput plan_input(const Args &a, int sms, const tg_options *opt)
     const bool batched_b = a.batch > 1 && !in.b_bcast;
     in.a_tma_ok = aligned16(a.A) && (a.lda * 2) % 16 == 0 && (!batched_a || (a.sA * 2) % 16 == 0);
     in.b_tma_ok = aligned16(a.B) && (a.ldb * 2) % 16 == 0 && (!batched_b || (a.sB * 2) % 16 == 0);
-    in.c_tma_ok = aligned16(a.C) && (a.ldc * 4) % 16 == 0 && (a.batch == 1 || (a.sC * 4) % 16 == 0);
+    in.c_tma_ok = aligned16(a.C) && (a.ldc * a.c_bytes) % 16 == 0 &&
+                  (a.batch == 1 || (a.sC * a.c_bytes) % 16 == 0);
     in.sm_count = sms;
     if (opt) {
         in.block_n = opt->block_n;
@@ -385,9 +389,11 @@ thread_local MapCache t_maps;
 // bytes), dim2 problems (stride2 bytes); box {box0, box1, 1}; 128B swizzle;
 // out-of-range elements read as zero.
 bool encode_3d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t d0, uint64_t d1,
-               uint64_t d2, uint64_t stride1, uint64_t stride2, uint32_t box0, uint32_t box1)
+               uint64_t d2, uint64_t stride1, uint64_t stride2, uint32_t box0, uint32_t box1,
+               CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B)
 {
-    const MapKey k{base, static_cast<int>(dt), d0, d1, d2, stride1, stride2, box0, box1};
+    const MapKey k{base, static_cast<int>(dt) * 16 + static_cast<int>(swz), d0, d1, d2, stride1, stride2,
+                   box0, box1};
     for (int i = 0; i < MapCache::N; ++i)
         if (t_maps.used[i] && t_maps.key[i] == k) {
             *m = t_maps.map[i];
@@ -400,8 +406,8 @@ bool encode_3d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_
     const cuuint32_t box[3] = {box0, box1, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return false;
     const int slot = t_maps.next;
     t_maps.next = (slot + 1) % MapCache::N;
@@ -449,6 +455,53 @@ int max_pairs(int dev, int bn, int stages)
     return n;
 }
 
+// Fused-epilogue fields of the kernel parameters.
+void fill_epilogue(KernelParams &p, const Args &a, const tg_epilogue *ep)
+{
+    p.C = a.C;
+    p.ldc = a.ldc;
+    p.strideC = a.sC;
+    p.M = static_cast<int32_t>(a.M);
+    p.N = static_cast<int32_t>(a.N);
+    p.fused = 1;
+    p.act = ep->activation;
+    p.out_bf16 = ep->out_type == TG_BF16 ? 1 : 0;
+    p.alpha = ep->alpha;
+    p.beta = ep->beta;
+    p.bias = ep->bias;
+    p.bias_stride = ep->bias_stride;
+    p.residual = ep->residual;
+    p.ldr = ep->ldr;
+    p.strideR = ep->strideR;
+}
+
+// K == 0 with an epilogue: D = act(bias) + beta * R (the empty sum is 0).
+__global__ void epilogue_only_kernel(const KernelParams p, int64_t total)
+{
+    for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
+         e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t b = e / (static_cast<int64_t>(p.M) * p.N);
+        const int64_t r = e - b * p.M * p.N;
+        const int64_t i = r / p.N;
+        const int64_t j = r - i * p.N;
+        float x = __fmul_rn(p.alpha, 0.0f);
+        if (p.bias) x = __fadd_rn(x, p.bias[b * p.bias_stride + j]);
+        x = activation(x, p.act);
+        const int64_t ro = b * p.strideR + i * p.ldr + j;
+        const int64_t o = b * p.strideC + i * p.ldc + j;
+        if (p.out_bf16) {
+            if (p.residual) {
+                const float rv = __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t *>(p.residual)[ro]) << 16);
+                x = __fadd_rn(x, __fmul_rn(p.beta, rv));
+            }
+            static_cast<__nv_bfloat16 *>(p.C)[o] = __float2bfloat16_rn(x);
+        } else {
+            if (p.residual) x = __fadd_rn(x, __fmul_rn(p.beta, static_cast<const float *>(p.residual)[ro]));
+            static_cast<float *>(p.C)[o] = x;
+        }
+    }
+}
+
 int grid_for(int64_t work, int sms)
 {
     int64_t g = (work + 255) / 256;
@@ -459,7 +512,8 @@ int grid_for(int64_t work, int sms)
 }
 
 // The whole device-side path of one call (arguments already validated).
-tg_status run_gemm(const Args &a, cudaStream_t stream, const tg_options *opt)
+tg_status run_gemm(const Args &a, cudaStream_t stream, const tg_options *opt,
+                   const tg_epilogue *ep = nullptr)
 {
     if (a.M == 0 || a.N == 0) return TG_OK;
     int dev = 0;
@@ -472,7 +526,14 @@ tg_status run_gemm(const Args &a, cudaStream_t stream, const tg_options *opt)
 
     if (a.K == 0) {
         const int64_t total = a.batch * a.M * a.N;
-        zero_c_kernel<<<grid_for(total, sms), 256, 0, stream>>>(a.C, a.M, a.N, a.ldc, a.sC, total);
+        if (ep) {
+            KernelParams p{};
+            fill_epilogue(p, a, ep);
+            epilogue_only_kernel<<<grid_for(total, sms), 256, 0, stream>>>(p, total);
+        } else {
+            zero_c_kernel<<<grid_for(total, sms), 256, 0, stream>>>(static_cast<float *>(a.C), a.M, a.N,
+                                                                     a.ldc, a.sC, total);
+        }
         return cuda_status(cudaGetLastError());
     }
 
@@ -573,9 +634,12 @@ tg_status run_gemm(const Args &a, cudaStream_t stream, const tg_options *opt)
     }
     if (plan.epilogue == 1) {
         const uint64_t z = static_cast<uint64_t>(a.batch);
-        const uint64_t s2 = z == 1 ? single_problem_stride(a.M, a.ldc * 4) : static_cast<uint64_t>(a.sC) * 4;
-        if (!encode_3d(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.C, a.N, a.M, z, a.ldc * 4, s2,
-                       EPI_CHUNK, EPI_CHUNK)) {
+        const uint64_t s2 = z == 1 ? single_problem_stride(a.M, a.ldc * a.c_bytes)
+                                   : static_cast<uint64_t>(a.sC) * a.c_bytes;
+        const bool bf16 = a.c_bytes == 2;
+        if (!encode_3d(&tc, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.C,
+                       a.N, a.M, z, a.ldc * a.c_bytes, s2, EPI_CHUNK, EPI_CHUNK,
+                       bf16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B)) {
             if (opt && opt->epilogue == 1) return TG_ERR_UNSUPPORTED;
             plan.epilogue = 2;
         }
@@ -599,6 +663,7 @@ tg_status run_gemm(const Args &a, cudaStream_t stream, const tg_options *opt)
     p.C = a.C;
     p.ldc = a.ldc;
     p.strideC = a.sC;
+    if (ep) fill_epilogue(p, a, ep);
     const bool partial_tiles = plan.splits > 1 || plan.stream_k;
     p.partials = partial_tiles ? partials : nullptr;
     p.counters = partial_tiles ? w.counters : nullptr;
@@ -714,6 +779,41 @@ TG_API tg_status tg_gemm(const void *A, const void *B, float *C, int64_t M, int6
 {
     return tg_gemm_ex(A, B, C, M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC, stream,
                       nullptr);
+}
+
+TG_API tg_status tg_gemm_fused(const void *A, const void *B, void *D, int64_t M, int64_t N,
+                               int64_t K, int64_t lda, int64_t ldb, int64_t ldd, int64_t batch,
+                               int64_t strideA, int64_t strideB, int64_t strideD, const tg_epilogue *ep,
+                               tg_stream_t stream, const tg_options *opt)
+{
+    if (!ep) return TG_ERR_INVALID_ARG;
+    if (ep->activation < TG_ACT_NONE || ep->activation > TG_ACT_SILU) return TG_ERR_INVALID_ARG;
+    if (ep->out_type != TG_F32 && ep->out_type != TG_BF16) return TG_ERR_INVALID_ARG;
+    Args a{A, B, D, M, N, K, lda, ldb, ldd, batch, strideA, strideB, strideD};
+    a.c_bytes = ep->out_type == TG_BF16 ? 2 : 4;
+    tg_status st = validate(a);
+    if (st != TG_OK) return st;
+    if (M == 0 || N == 0) return TG_OK;
+    if (ep->bias_stride < 0) return TG_ERR_INVALID_ARG;
+    if (ep->residual) {
+        if (ep->ldr < N || ep->strideR < 0) return TG_ERR_INVALID_ARG;
+        if (batch > 1 && ep->strideR < (M - 1) * ep->ldr + N && ep->strideR != 0) return TG_ERR_INVALID_ARG;
+        const bool same = ep->residual == D && ep->ldr == ldd && ep->strideR == strideD;
+        if (!same) {
+            const uintptr_t d0 = reinterpret_cast<uintptr_t>(D);
+            const uintptr_t d1 = d0 + a.c_bytes * static_cast<uintptr_t>(span_elems(M, N, ldd, batch, strideD));
+            const uintptr_t r0 = reinterpret_cast<uintptr_t>(ep->residual);
+            const uintptr_t r1 =
+                r0 + a.c_bytes * static_cast<uintptr_t>(span_elems(M, N, ep->ldr, batch, ep->strideR));
+            if (ranges_overlap(d0, d1, r0, r1)) return TG_ERR_INVALID_ARG;
+        }
+    }
+    if (opt) {
+        PlanInput in = plan_input(a, 148, opt);
+        Plan pl;
+        if (K > 0 && !make_plan(in, pl)) return TG_ERR_INVALID_ARG;
+    }
+    return run_gemm(a, reinterpret_cast<cudaStream_t>(stream), opt, ep);
 }
 
 TG_API tg_status tg_plan(const void *A, const void *B, const float *C, int64_t M, int64_t N,

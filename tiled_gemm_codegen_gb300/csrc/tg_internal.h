@@ -36,8 +36,16 @@ struct KernelParams {
     int32_t a_bcast;      // 1: A has batch stride 0 (same A for every problem)
     int32_t b_bcast;      // 1: B has batch stride 0
     int32_t epi_tma;      // 1: TMA store of C; 0: plain masked stores
-    float *C;             // plain-store epilogue target
+    void *C;              // plain-store epilogue target (fp32, or bf16 when out_bf16)
     int64_t ldc, strideC;
+    // Fused epilogue (fused == 1): D = act(alpha * acc + bias[j]) + beta * R,
+    // applied once to the final fp32 value; D and R are bf16 when out_bf16.
+    int32_t fused, act, out_bf16;
+    float alpha, beta;
+    const float *bias;
+    int64_t bias_stride;
+    const void *residual;
+    int64_t ldr, strideR;
     float *partials;      // split-K partial tiles
     int32_t *counters;    // split-K arrival counters, one per output tile
     uint32_t *err;        // device error word

@@ -58,6 +58,7 @@
 
 #include <atomic>
 
+#include "tg_epilogue.cuh"
 #include "tg_internal.h"
 #include "tg_ptx.cuh"
 
@@ -250,6 +251,70 @@ __device__ __forceinline__ float ld_shared_f32(uint32_t addr)
     float v;
     asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
     return v;
+}
+
+__device__ __forceinline__ uint16_t ld_shared_u16(uint32_t addr)
+{
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// OCANNL "Module Ir.Schedule", Epilogue fusion: the elementwise tail of the
+// reduction, applied to the final fp32 values of one thread's 32 columns:
+//   D = act(alpha * acc + bias[col]) + beta * R[row][col]
+// The products and sums are rounded one by one (no fused multiply-add), so
+// with no activation or relu the fused result equals, bit for bit, the same
+// formula applied in fp32 to the stored product.
+__device__ __forceinline__ void apply_epilogue(const KernelParams &p, uint32_t (&v)[32], int32_t row,
+                                               int32_t col0, int32_t b)
+{
+    const bool row_ok = row < p.M;
+    float bias[32], res[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        bias[j] = 0.0f;
+        res[j] = 0.0f;
+    }
+    if (p.bias) {
+        const float *bp = p.bias + static_cast<int64_t>(b) * p.bias_stride + col0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (col0 + j < p.N) bias[j] = __ldg(bp + j);
+    }
+    if (p.residual && row_ok) {
+        const int64_t off = static_cast<int64_t>(b) * p.strideR + static_cast<int64_t>(row) * p.ldr + col0;
+        if (p.out_bf16) {
+            const uint16_t *rp = static_cast<const uint16_t *>(p.residual) + off;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (col0 + j < p.N) res[j] = __uint_as_float(static_cast<uint32_t>(rp[j]) << 16);
+        } else {
+            const float *rp = static_cast<const float *>(p.residual) + off;
+            if ((reinterpret_cast<uintptr_t>(rp) & 15u) == 0 && col0 + 32 <= p.N) {
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {
+                    const float4 t = *reinterpret_cast<const float4 *>(rp + j);
+                    res[j] = t.x;
+                    res[j + 1] = t.y;
+                    res[j + 2] = t.z;
+                    res[j + 3] = t.w;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (col0 + j < p.N) res[j] = rp[j];
+            }
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        float x = __fmul_rn(p.alpha, __uint_as_float(v[j]));
+        if (p.bias) x = __fadd_rn(x, bias[j]);
+        x = activation(x, p.act);
+        if (p.residual) x = __fadd_rn(x, __fmul_rn(p.beta, res[j]));
+        v[j] = __float_as_uint(x);
+    }
 }
 
 template <int BN, int STAGES, bool PAIR>
@@ -475,44 +540,81 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
         // One 32 x 32 fp32 chunk (rows m_base + 32q .., columns col0 ..) of
         // this warp's accumulator rows -> C.
-        auto store_chunk = [&](const uint32_t (&v)[32], int32_t m_base, int32_t col0, int32_t b) {
+        auto store_chunk = [&](uint32_t (&v)[32], int32_t m_base, int32_t col0, int32_t b) {
             const int32_t row0 = m_base + q * 32;
             if (row0 >= p.M || col0 >= p.N) return;  // warp-uniform
+            if (p.fused) apply_epilogue(p, v, row0 + lane, col0, b);
             const uint32_t box = stage_base + (st_cnt % EPI_BUFS) * EPI_BOX_BYTES;
             ++st_cnt;
             if (p.epi_tma && lane == 0) ptx::bulk_wait_group_read<EPI_BUFS - 1>();
             __syncwarp();
-            // Row `lane` of the box; its 16-byte unit jj is stored at unit
-            // jj ^ (lane mod 8): the 128B swizzle (Swizzle(2,3,3) on fp32).
+            const int32_t col = col0 + lane;
+            const int32_t nrows = min(32, p.M - row0);
+            if (!p.out_bf16) {
+                // Row `lane` of the box; its 16-byte unit jj is stored at unit
+                // jj ^ (lane mod 8): the 128B swizzle (Swizzle(2,3,3) on fp32).
 #pragma unroll
-            for (int jj = 0; jj < 8; ++jj)
-                ptx::st_shared_v4(box + lane * 128 + ((jj ^ (lane & 7)) << 4), v[4 * jj],
-                                  v[4 * jj + 1], v[4 * jj + 2], v[4 * jj + 3]);
-            if (p.epi_tma) {
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    ptx::tma_store_3d(&tmC, box, col0, row0, b);
-                    ptx::bulk_commit_group();
+                for (int jj = 0; jj < 8; ++jj)
+                    ptx::st_shared_v4(box + lane * 128 + ((jj ^ (lane & 7)) << 4), v[4 * jj],
+                                      v[4 * jj + 1], v[4 * jj + 2], v[4 * jj + 3]);
+                if (p.epi_tma) {
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        ptx::tma_store_3d(&tmC, box, col0, row0, b);
+                        ptx::bulk_commit_group();
+                    }
+                } else {
+                    __syncwarp();
+                    // Coalesced: lane l writes column col0 + l of each row.  All
+                    // 32 values are read from the box first, then the 32 row
+                    // stores go out back to back.
+                    const uint32_t src = box + ((lane >> 2) << 4) + ((lane & 3) << 2);
+                    float vals[32];
+#pragma unroll
+                    for (int r = 0; r < 32; ++r) vals[r] = ld_shared_f32((src ^ ((r & 7) << 4)) + r * 128);
+                    __syncwarp();
+                    if (col < p.N) {
+                        float *dst = static_cast<float *>(p.C) + static_cast<int64_t>(b) * p.strideC +
+                                     static_cast<int64_t>(row0) * p.ldc + col;
+#pragma unroll
+                        for (int r = 0; r < 32; ++r)
+                            if (r < nrows) dst[static_cast<int64_t>(r) * p.ldc] = vals[r];
+                    }
                 }
             } else {
-                __syncwarp();
-                // Coalesced: lane l writes column col0 + l of each row.  All
-                // 32 values are read from the box first, then the 32 row
-                // stores go out back to back.
-                const int32_t col = col0 + lane;
-                const uint32_t src = box + ((lane >> 2) << 4) + ((lane & 3) << 2);
-                float vals[32];
+                // bf16 output (round to nearest even): a 32 x 32 box of 64-byte
+                // rows with the 64B swizzle (Swizzle(3,2,3) on bf16): 16-byte
+                // unit u of row r sits at unit u ^ ((r / 2) mod 4).
+                uint32_t w[16];
 #pragma unroll
-                for (int r = 0; r < 32; ++r) vals[r] = ld_shared_f32((src ^ ((r & 7) << 4)) + r * 128);
-                __syncwarp();
-                if (col < p.N) {
-                    float *dst = p.C + static_cast<int64_t>(b) * p.strideC +
-                                 static_cast<int64_t>(row0) * p.ldc + col;
-                    const int32_t nrows = min(32, p.M - row0);
+                for (int k = 0; k < 16; ++k) w[k] = pack_bf16x2(v[2 * k], v[2 * k + 1]);
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    ptx::st_shared_v4(box + lane * 64 + ((u ^ ((lane >> 1) & 3)) << 4), w[4 * u],
+                                      w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+                if (p.epi_tma) {
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        ptx::tma_store_3d(&tmC, box, col0, row0, b);
+                        ptx::bulk_commit_group();
+                    }
+                } else {
+                    __syncwarp();
+                    const uint32_t src = box + ((lane >> 3) << 4) + ((lane & 7) << 1);
+                    uint16_t vals[32];
 #pragma unroll
                     for (int r = 0; r < 32; ++r)
-                        if (r < nrows) dst[static_cast<int64_t>(r) * p.ldc] = vals[r];
+                        vals[r] = ld_shared_u16((src ^ (((r >> 1) & 3) << 4)) + r * 64);
+                    __syncwarp();
+                    if (col < p.N) {
+                        uint16_t *dst = static_cast<uint16_t *>(p.C) + static_cast<int64_t>(b) * p.strideC +
+                                        static_cast<int64_t>(row0) * p.ldc + col;
+#pragma unroll
+                        for (int r = 0; r < 32; ++r)
+                            if (r < nrows) dst[static_cast<int64_t>(r) * p.ldc] = vals[r];
+                    }
                 }
             }
         };
