@@ -23,6 +23,10 @@
  *     (split-K with a fixed combine order).
  *
  * Conventions shared by every entry point:
+ *   - Operand storage: by default A is row-major M x K (lda >= K) and B
+ *     row-major K x N (ldb >= N); tg_options.a_col_major / b_col_major select
+ *     the transposed storage (A as K x M with lda >= M, B as N x K with
+ *     ldb >= K).  C (D) is always row-major M x N.
  *   - Pointers are DEVICE pointers unless the name says _host.  The caller
  *     owns A, B, C and the stream; the library never frees caller memory.
  *   - Calls are asynchronous on `stream` (NULL = the legacy default stream)
@@ -30,7 +34,9 @@
  *     expiry) are reported later by tg_device_error().
  *   - Arguments are validated before anything is enqueued:
  *       TG_ERR_INVALID_ARG  for a NULL pointer with a nonzero extent, M, N or
- *                           K < 0, batch < 1, lda < K, ldb < N, ldc < N, a
+ *                           K < 0, batch < 1, a leading dimension shorter
+ *                           than its stored row (lda < K, or < M when A is
+ *                           column-major; ldb < N, or < K; ldc < N), a
  *                           negative batch stride, batch strides that make
  *                           two problems share an element of C, C
  *                           overlapping A or B, or an extent > 2^31 - 1.
@@ -97,7 +103,10 @@ typedef struct tg_options {
                          /* up done, [2] first k-block ready, [3] last MMA    */
                          /* issued, [4] first epilogue start, [5] last store  */
                          /* issued, [6] stores complete, [7] exit             */
-    int32_t reserved[2];
+    int32_t a_col_major; /* nonzero: A is stored K x M (element A_b[i][k] at   */
+                         /* A[b*strideA + k*lda + i], lda >= M)               */
+    int32_t b_col_major; /* nonzero: B is stored N x K (element B_b[k][j] at   */
+                         /* B[b*strideB + j*ldb + k], ldb >= K)               */
 } tg_options;
 
 /* What the planner chose (tg_plan output). */

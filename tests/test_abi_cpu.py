@@ -96,6 +96,20 @@ def test_invalid_arguments_rejected_before_any_cuda_call(lib, args):
     assert st == tg.TG_ERR_INVALID_ARG
 
 
+def test_column_major_leading_dimensions(lib):
+    """With column-major storage the leading dimension bounds the stored
+    row: lda >= M for A stored K x M, ldb >= K for B stored N x K."""
+    base = [A0, B0, C0, 8, 6, 4]
+    ok = tg.make_options(a_col_major=1, b_col_major=1)
+    # lda = 8 >= M, ldb = 4 >= K: plan accepted (host-only planning)
+    st, _ = tg.tg_plan(*base, 8, 4, 6, 1, 32, 24, 48, 152, ok)
+    assert st == tg.TG_OK
+    st, _ = tg.tg_plan(*base, 7, 4, 6, 1, 32, 24, 48, 152, ok)
+    assert st == tg.TG_ERR_INVALID_ARG
+    st, _ = tg.tg_plan(*base, 8, 3, 6, 1, 32, 24, 48, 152, ok)
+    assert st == tg.TG_ERR_INVALID_ARG
+
+
 def test_empty_output_is_ok_without_gpu(lib):
     assert tg.tg_gemm(0, 0, 0, 0, 5, 7, 7, 5, 5, 1, 0, 0, 0, None) == tg.TG_OK
     assert tg.tg_gemm(0, 0, 0, 5, 0, 7, 7, 0, 0, 1, 0, 0, 0, None) == tg.TG_OK

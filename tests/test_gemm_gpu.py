@@ -375,3 +375,80 @@ def test_stream_k_watchdog():
     got = tg.gemm(ad, bd, options=tg.make_options(block_n=128, max_ctas=7, stream_k=2))
     assert tg.device_error() == tg.TG_OK
     assert np.array_equal(got.cpu().double().numpy(), oracle_dense(A, B))
+
+
+def _stored(t_logical, col_major, pad=0, offset=0):
+    """Device copy of a logical [batch?, rows, cols] bf16 matrix in row- or
+    column-major storage with `pad` extra elements per stored row and an
+    element offset from an allocation start.  Returns (view, ld)."""
+    t = t_logical if t_logical.dim() == 3 else t_logical.unsqueeze(0)
+    batch, rows, cols = t.shape
+    srows, scols = (cols, rows) if col_major else (rows, cols)
+    ld = scols + pad
+    per = srows * ld
+    buf = torch.zeros(offset + batch * per, dtype=torch.bfloat16)
+    for b in range(batch):
+        block = buf[offset + b * per: offset + (b + 1) * per].view(srows, ld)
+        block[:, :scols] = t[b].t() if col_major else t[b]
+    d = buf.to(dev())
+    if col_major:
+        v = torch.as_strided(d, (batch, rows, cols), (per, 1, ld), offset)
+    else:
+        v = torch.as_strided(d, (batch, rows, cols), (per, ld, 1), offset)
+    return (v if t_logical.dim() == 3 else v[0]), ld
+
+
+@pytest.mark.parametrize("a_cm,b_cm", [(0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("cfg", [(128, 1), (256, 1), (256, 2), (128, 2), (64, 1), (192, 1)], ids=_cfg_id)
+def test_transposed_layouts_exact(a_cm, b_cm, cfg):
+    """Column-major A (stored K x M) and/or B (stored N x K): K-major and
+    MN-major shared-memory atoms swap roles; exact with integer inputs."""
+    bn, pair = cfg
+    M, N, K = 277, 389, 333
+    A, B = synth.make_int_inputs(1, M, N, K, seed=_seed(a_cm, b_cm, bn, pair))
+    Ad, lda = _stored(A, a_cm)
+    Bd, ldb = _stored(B, b_cm)
+    got = tg.gemm(Ad, Bd, options=tg.make_options(block_n=bn, cta_pair=pair))
+    assert tg.device_error() == tg.TG_OK
+    assert np.array_equal(got.cpu().double().numpy(), oracle_dense(A, B))
+
+
+@pytest.mark.parametrize("a_cm,b_cm", [(1, 0), (0, 1), (1, 1)])
+def test_transposed_batched_split_stream_and_pack(a_cm, b_cm):
+    batch, M, N, K = 3, 190, 300, 1000
+    A, B = synth.make_int_inputs(batch, M, N, K, seed=a_cm * 2 + b_cm)
+    ref = oracle_dense(A, B)
+    for pad, off, extra in [(0, 0, dict(split_k=3)), (8, 0, dict(stream_k=2, max_ctas=7)),
+                            (3, 1, dict()), (0, 0, dict(cta_pair=2, block_n=256, stream_k=2, max_ctas=10))]:
+        Ad, _ = _stored(A, a_cm, pad=pad, offset=off)
+        Bd, _ = _stored(B, b_cm, pad=pad, offset=off)
+        got = tg.gemm(Ad, Bd, options=tg.make_options(**extra))
+        assert tg.device_error() == tg.TG_OK
+        assert np.array_equal(got.cpu().double().numpy(), ref), (pad, off, extra)
+
+
+def test_transposed_float_and_fused():
+    M, N, K = 300, 260, 777
+    A, B = synth.make_inputs(1, M, N, K, "normal", seed=17)
+    At = A.t().contiguous().to(dev()).t()   # column-major view
+    Bt = B.t().contiguous().to(dev()).t()
+    got = tg.gemm(At, Bt)
+    assert tg.device_error() == tg.TG_OK
+    assert_close(got.cpu().double().numpy(), oracle_dense(A, B), K)
+    plain = tg.gemm(A.to(dev()), B.to(dev()))
+    fused = tg.gemm_fused(At, Bt, activation="relu")
+    assert tg.device_error() == tg.TG_OK
+    assert np.array_equal(fused.cpu().numpy(), np.maximum(plain.cpu().numpy(), 0))
+
+
+def test_transposed_host_entry():
+    M, N, K = 150, 170, 190
+    A, B = synth.make_int_inputs(1, M, N, K, seed=23)
+    At = A.t().contiguous()
+    Bt = B.t().contiguous()
+    C = torch.zeros(M, N)
+    st = tg.tg_gemm_host(At.data_ptr(), Bt.data_ptr(), C.data_ptr(), M, N, K, M, K, N, 1, 0, 0, 0,
+                         torch.cuda.current_stream().cuda_stream,
+                         tg.make_options(a_col_major=1, b_col_major=1))
+    assert st == tg.TG_OK
+    assert np.array_equal(C.double().numpy(), oracle_dense(A, B))

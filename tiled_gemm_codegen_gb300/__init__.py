@@ -121,6 +121,29 @@ def _operand_geometry(t, rows_dim, what):
     return t.data_ptr(), rows, cols, max(ld, cols), batch, sb
 
 
+def _operand(t, what):
+    """(ptr, rows, cols, ld, batch, batch_stride, col_major) of a logical
+    rows x cols operand: row-major when its last dim has unit stride,
+    column-major (a transposed view) when its second-last dim has."""
+    rows, cols = t.shape[-2], t.shape[-1]
+    if t.dim() in (2, 3) and cols > 1 and t.stride(-1) != 1 and (t.stride(-2) == 1 or rows == 1):
+        ld = max(t.stride(-1), rows, 1)
+        batch, sb = (t.shape[0], t.stride(0) if t.shape[0] > 1 else 0) if t.dim() == 3 else (1, 0)
+        return t.data_ptr(), rows, cols, ld, batch, sb, True
+    return (*_operand_geometry(t, -2, what), False)
+
+
+def _with_layout(options, a_cm, b_cm):
+    if not (a_cm or b_cm):
+        return options
+    o = tg_options()
+    if options is not None:
+        ctypes.memmove(ctypes.byref(o), ctypes.byref(options), ctypes.sizeof(o))
+    o.a_col_major = int(a_cm)
+    o.b_col_major = int(b_cm)
+    return o
+
+
 def gemm(A, B, C=None, *, options: tg_options | None = None, stream=None):
     """C = A @ B (per problem) for CUDA bf16 tensors A [.., M, K], B [.., K, N];
     C is an fp32 CUDA tensor [.., M, N] (allocated when None).  Asynchronous
@@ -131,8 +154,9 @@ def gemm(A, B, C=None, *, options: tg_options | None = None, stream=None):
         raise TypeError("A and B must be bf16")
     if not (A.is_cuda and B.is_cuda):
         raise ValueError("A and B must be CUDA tensors (use gemm_host for host buffers)")
-    pa, M, K, lda, ba, sA = _operand_geometry(A, -2, "A")
-    pb, K2, N, ldb, bb, sB = _operand_geometry(B, -2, "B")
+    pa, M, K, lda, ba, sA, a_cm = _operand(A, "A")
+    pb, K2, N, ldb, bb, sB, b_cm = _operand(B, "B")
+    options = _with_layout(options, a_cm, b_cm)
     if K2 != K:
         raise ValueError(f"inner dimensions differ: {K} vs {K2}")
     batch = max(ba, bb)
@@ -167,8 +191,9 @@ def gemm_fused(A, B, D=None, *, bias=None, residual=None, alpha: float = 1.0, be
 
     if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
         raise TypeError("A and B must be bf16")
-    pa, M, K, lda, ba, sA = _operand_geometry(A, -2, "A")
-    pb, K2, N, ldb, bb, sB = _operand_geometry(B, -2, "B")
+    pa, M, K, lda, ba, sA, a_cm = _operand(A, "A")
+    pb, K2, N, ldb, bb, sB, b_cm = _operand(B, "B")
+    options = _with_layout(options, a_cm, b_cm)
     if K2 != K:
         raise ValueError(f"inner dimensions differ: {K} vs {K2}")
     batch = max(ba, bb)

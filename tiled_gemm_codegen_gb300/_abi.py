@@ -43,7 +43,8 @@ class tg_options(ctypes.Structure):
         ("stream_k", ctypes.c_int32),
         ("reserved0", ctypes.c_int32),
         ("trace_buffer", ctypes.c_uint64),
-        ("reserved", ctypes.c_int32 * 2),
+        ("a_col_major", ctypes.c_int32),
+        ("b_col_major", ctypes.c_int32),
     ]
 
 

@@ -133,7 +133,25 @@ struct Args {
     void *C;  // C (fp32), or D of the fused epilogue (fp32 or bf16)
     int64_t M, N, K, lda, ldb, ldc, batch, sA, sB, sC;
     int64_t c_bytes = 4;  // element size of C
+    bool a_cm = false;    // A stored K x M (column-major)
+    bool b_cm = false;    // B stored N x K (column-major)
+    // stored (rows, columns) of A and B
+    int64_t a_rows() const { return a_cm ? K : M; }
+    int64_t a_cols() const { return a_cm ? M : K; }
+    int64_t b_rows() const { return b_cm ? N : K; }
+    int64_t b_cols() const { return b_cm ? K : N; }
 };
+
+// Args with the operand layouts of `opt` (the layout fields are part of the
+// operation, not tuning).
+Args with_layout(Args a, const tg_options *opt)
+{
+    if (opt) {
+        a.a_cm = opt->a_col_major != 0;
+        a.b_cm = opt->b_col_major != 0;
+    }
+    return a;
+}
 
 // Elements spanned by one operand over all problems (0 if empty).  Callers
 // have bounded every factor (extents < 2^31, strides <= 2^40) and checked
@@ -166,15 +184,15 @@ tg_status validate(const Args &a)
     if (a.M > EXTENT_LIMIT || a.N > EXTENT_LIMIT || a.K > EXTENT_LIMIT || a.batch > EXTENT_LIMIT)
         return TG_ERR_INVALID_ARG;
     if (a.sA < 0 || a.sB < 0 || a.sC < 0) return TG_ERR_INVALID_ARG;
-    if (a.lda < a.K || a.ldb < a.N || a.ldc < a.N) return TG_ERR_INVALID_ARG;
+    if (a.lda < a.a_cols() || a.ldb < a.b_cols() || a.ldc < a.N) return TG_ERR_INVALID_ARG;
     // strides beyond 2^40 elements are not addressable in any case
     const int64_t STRIDE_LIMIT = int64_t(1) << 40;
     if (a.lda > STRIDE_LIMIT || a.ldb > STRIDE_LIMIT || a.ldc > STRIDE_LIMIT ||
         a.sA > STRIDE_LIMIT || a.sB > STRIDE_LIMIT || a.sC > STRIDE_LIMIT)
         return TG_ERR_INVALID_ARG;
     if (a.M == 0 || a.N == 0) return TG_OK;
-    if (!span_ok(a.M, a.N, a.ldc, a.batch, a.sC) || !span_ok(a.M, a.K, a.lda, a.batch, a.sA) ||
-        !span_ok(a.K, a.N, a.ldb, a.batch, a.sB))
+    if (!span_ok(a.M, a.N, a.ldc, a.batch, a.sC) || !span_ok(a.a_rows(), a.a_cols(), a.lda, a.batch, a.sA) ||
+        !span_ok(a.b_rows(), a.b_cols(), a.ldb, a.batch, a.sB))
         return TG_ERR_INVALID_ARG;
     if (a.C == nullptr) return TG_ERR_INVALID_ARG;
     if (a.K > 0 && (a.A == nullptr || a.B == nullptr)) return TG_ERR_INVALID_ARG;
@@ -186,9 +204,11 @@ tg_status validate(const Args &a)
         const uintptr_t c1 =
             c0 + static_cast<uintptr_t>(a.c_bytes) * static_cast<uintptr_t>(span_elems(a.M, a.N, a.ldc, a.batch, a.sC));
         const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.A);
-        const uintptr_t a1 = a0 + 2u * static_cast<uintptr_t>(span_elems(a.M, a.K, a.lda, a.batch, a.sA));
+        const uintptr_t a1 =
+            a0 + 2u * static_cast<uintptr_t>(span_elems(a.a_rows(), a.a_cols(), a.lda, a.batch, a.sA));
         const uintptr_t b0 = reinterpret_cast<uintptr_t>(a.B);
-        const uintptr_t b1 = b0 + 2u * static_cast<uintptr_t>(span_elems(a.K, a.N, a.ldb, a.batch, a.sB));
+        const uintptr_t b1 =
+            b0 + 2u * static_cast<uintptr_t>(span_elems(a.b_rows(), a.b_cols(), a.ldb, a.batch, a.sB));
         if (ranges_overlap(c0, c1, a0, a1) || ranges_overlap(c0, c1, b0, b1))
             return TG_ERR_INVALID_ARG;
     }
@@ -213,6 +233,8 @@ PlanInput plan_input(const Args &a, int sms, const tg_options *opt)
     in.c_tma_ok = aligned16(a.C) && (a.ldc * a.c_bytes) % 16 == 0 &&
                   (a.batch == 1 || (a.sC * a.c_bytes) % 16 == 0);
     in.sm_count = sms;
+    in.a_cm = a.a_cm;
+    in.b_cm = a.b_cm;
     if (opt) {
         in.block_n = opt->block_n;
         in.stages = opt->stages;
@@ -551,24 +573,30 @@ tg_status run_gemm(const Args &a, cudaStream_t stream, const tg_options *opt,
 
     // Encode the operand maps; an operand TMA cannot describe is packed.
     CUtensorMap ta{}, tb{}, tc{};
+    // Row-major A: boxes [128 rows x 64 k]; column-major A: [64 k x 64 rows].
+    // Row-major B: [64 k x 64 columns]; column-major B: [B columns x 64 k].
+    const uint32_t b_cols_cta = static_cast<uint32_t>(plan.pair ? plan.bn / 2 : plan.bn);
     auto encode_a = [&]() {
         const uint64_t z = in.a_bcast || a.batch == 1 ? 1 : static_cast<uint64_t>(a.batch);
-        const uint64_t s2 = z == 1 ? single_problem_stride(a.M, lda * 2) : static_cast<uint64_t>(sA) * 2;
+        const uint64_t s2 = z == 1 ? single_problem_stride(a.a_rows(), lda * 2) : static_cast<uint64_t>(sA) * 2;
+        if (a.a_cm) return encode_3d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, a.M, a.K, z, lda * 2, s2, 64, BK);
         return encode_3d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, a.K, a.M, z, lda * 2, s2, BK, BM);
     };
     auto encode_b = [&]() {
         const uint64_t z = in.b_bcast || a.batch == 1 ? 1 : static_cast<uint64_t>(a.batch);
-        const uint64_t s2 = z == 1 ? single_problem_stride(a.K, ldb * 2) : static_cast<uint64_t>(sB) * 2;
+        const uint64_t s2 = z == 1 ? single_problem_stride(a.b_rows(), ldb * 2) : static_cast<uint64_t>(sB) * 2;
+        if (a.b_cm)
+            return encode_3d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, a.K, a.N, z, ldb * 2, s2, BK, b_cols_cta);
         return encode_3d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, a.N, a.K, z, ldb * 2, s2, 64, BK);
     };
     if (!encode_fn()) return TG_ERR_CUDA;
     if (!plan.pack_a && !encode_a()) {
         plan.pack_a = true;
-        plan.ws_pack_a = round_up((in.a_bcast ? 1 : a.batch) * a.M * round_up(a.K, 8) * 2, 256);
+        plan.ws_pack_a = round_up((in.a_bcast ? 1 : a.batch) * a.a_rows() * round_up(a.a_cols(), 8) * 2, 256);
     }
     if (!plan.pack_b && !encode_b()) {
         plan.pack_b = true;
-        plan.ws_pack_b = round_up((in.b_bcast ? 1 : a.batch) * a.K * round_up(a.N, 8) * 2, 256);
+        plan.ws_pack_b = round_up((in.b_bcast ? 1 : a.batch) * a.b_rows() * round_up(a.b_cols(), 8) * 2, 256);
     }
 
     // The persistent grid actually launched: two-SM tiles never use more
@@ -601,19 +629,21 @@ tg_status run_gemm(const Args &a, cudaStream_t stream, const tg_options *opt,
         PackJob ja{}, jb{};
         if (plan.pack_a) {
             const int64_t nb = in.a_bcast ? 1 : a.batch;
-            const int64_t ld2 = round_up(a.K, 8);
+            const int64_t rows = a.a_rows(), cols = a.a_cols();
+            const int64_t ld2 = round_up(cols, 8);
             const uintptr_t base = reinterpret_cast<uintptr_t>(a.A);
-            ja = PackJob{static_cast<const uint16_t *>(a.A), pack_a_buf, a.M, a.K, a.lda, a.sA, ld2,
-                         nb * a.M * (ld2 / 8), base,
-                         base + 2u * static_cast<uintptr_t>(span_elems(a.M, a.K, a.lda, nb, a.sA))};
+            ja = PackJob{static_cast<const uint16_t *>(a.A), pack_a_buf, rows, cols, a.lda, a.sA, ld2,
+                         nb * rows * (ld2 / 8), base,
+                         base + 2u * static_cast<uintptr_t>(span_elems(rows, cols, a.lda, nb, a.sA))};
         }
         if (plan.pack_b) {
             const int64_t nb = in.b_bcast ? 1 : a.batch;
-            const int64_t ld2 = round_up(a.N, 8);
+            const int64_t rows = a.b_rows(), cols = a.b_cols();
+            const int64_t ld2 = round_up(cols, 8);
             const uintptr_t base = reinterpret_cast<uintptr_t>(a.B);
-            jb = PackJob{static_cast<const uint16_t *>(a.B), pack_b_buf, a.K, a.N, a.ldb, a.sB, ld2,
-                         nb * a.K * (ld2 / 8), base,
-                         base + 2u * static_cast<uintptr_t>(span_elems(a.K, a.N, a.ldb, nb, a.sB))};
+            jb = PackJob{static_cast<const uint16_t *>(a.B), pack_b_buf, rows, cols, a.ldb, a.sB, ld2,
+                         nb * rows * (ld2 / 8), base,
+                         base + 2u * static_cast<uintptr_t>(span_elems(rows, cols, a.ldb, nb, a.sB))};
         }
         const int blocks_a = plan.pack_a ? grid_for(ja.chunks, sms) : 0;
         const int blocks_b = plan.pack_b ? grid_for(jb.chunks, sms) : 0;
@@ -622,13 +652,13 @@ tg_status run_gemm(const Args &a, cudaStream_t stream, const tg_options *opt,
         if (plan.pack_a) {
             A = pack_a_buf;
             lda = ja.ld_dst;
-            sA = in.a_bcast ? 0 : a.M * ja.ld_dst;
+            sA = in.a_bcast ? 0 : a.a_rows() * ja.ld_dst;
             if (!encode_a()) return TG_ERR_CUDA;
         }
         if (plan.pack_b) {
             B = pack_b_buf;
             ldb = jb.ld_dst;
-            sB = in.b_bcast ? 0 : a.K * jb.ld_dst;
+            sB = in.b_bcast ? 0 : a.b_rows() * jb.ld_dst;
             if (!encode_b()) return TG_ERR_CUDA;
         }
     }
@@ -659,6 +689,8 @@ tg_status run_gemm(const Args &a, cudaStream_t stream, const tg_options *opt,
     p.group_m = plan.group_m;
     p.a_bcast = in.a_bcast ? 1 : 0;
     p.b_bcast = in.b_bcast ? 1 : 0;
+    p.a_mn = a.a_cm ? 1 : 0;
+    p.b_k = a.b_cm ? 1 : 0;
     p.epi_tma = plan.epilogue == 1 ? 1 : 0;
     p.C = a.C;
     p.ldc = a.ldc;
@@ -761,7 +793,7 @@ TG_API tg_status tg_gemm_ex(const void *A, const void *B, float *C, int64_t M, i
                             int64_t strideB, int64_t strideC, tg_stream_t stream,
                             const tg_options *opt)
 {
-    const Args a{A, B, C, M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC};
+    const Args a = with_layout(Args{A, B, C, M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC}, opt);
     tg_status st = validate(a);
     if (st != TG_OK) return st;
     if (opt) {
@@ -789,7 +821,7 @@ TG_API tg_status tg_gemm_fused(const void *A, const void *B, void *D, int64_t M,
     if (!ep) return TG_ERR_INVALID_ARG;
     if (ep->activation < TG_ACT_NONE || ep->activation > TG_ACT_SILU) return TG_ERR_INVALID_ARG;
     if (ep->out_type != TG_F32 && ep->out_type != TG_BF16) return TG_ERR_INVALID_ARG;
-    Args a{A, B, D, M, N, K, lda, ldb, ldd, batch, strideA, strideB, strideD};
+    Args a = with_layout(Args{A, B, D, M, N, K, lda, ldb, ldd, batch, strideA, strideB, strideD}, opt);
     a.c_bytes = ep->out_type == TG_BF16 ? 2 : 4;
     tg_status st = validate(a);
     if (st != TG_OK) return st;
@@ -822,7 +854,8 @@ TG_API tg_status tg_plan(const void *A, const void *B, const float *C, int64_t M
                          const tg_options *opt, tg_plan_info *out)
 {
     if (!out || sm_count < 0) return TG_ERR_INVALID_ARG;
-    const Args a{A, B, const_cast<float *>(C), M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC};
+    const Args a =
+        with_layout(Args{A, B, const_cast<float *>(C), M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC}, opt);
     tg_status st = validate(a);
     if (st != TG_OK) return st;
     int sms = sm_count;
@@ -847,7 +880,8 @@ TG_API tg_status tg_gemm_host(const void *A_host, const void *B_host, float *C_h
                               int64_t batch, int64_t strideA, int64_t strideB, int64_t strideC,
                               tg_stream_t stream_, const tg_options *opt)
 {
-    const Args a{A_host, B_host, C_host, M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC};
+    const Args a =
+        with_layout(Args{A_host, B_host, C_host, M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC}, opt);
     tg_status st = validate(a);
     if (st != TG_OK) return st;
     if (M == 0 || N == 0) return TG_OK;
@@ -856,8 +890,8 @@ TG_API tg_status tg_gemm_host(const void *A_host, const void *B_host, float *C_h
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_status(e);
 
-    const int64_t na = K > 0 ? span_elems(M, K, lda, batch, strideA) : 0;
-    const int64_t nb = K > 0 ? span_elems(K, N, ldb, batch, strideB) : 0;
+    const int64_t na = K > 0 ? span_elems(a.a_rows(), a.a_cols(), lda, batch, strideA) : 0;
+    const int64_t nb = K > 0 ? span_elems(a.b_rows(), a.b_cols(), ldb, batch, strideB) : 0;
     const int64_t nc = span_elems(M, N, ldc, batch, strideC);
     const size_t off_b = static_cast<size_t>(round_up(na * 2, 256));
     const size_t off_c = off_b + static_cast<size_t>(round_up(nb * 2, 256));
@@ -877,7 +911,8 @@ TG_API tg_status tg_gemm_host(const void *A_host, const void *B_host, float *C_h
         return cuda_status(e);
     if (nb > 0 && (e = cudaMemcpyAsync(dB, B_host, nb * 2, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
         return cuda_status(e);
-    st = run_gemm(Args{dA, dB, dC, M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC}, stream, opt);
+    st = run_gemm(with_layout(Args{dA, dB, dC, M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC}, opt),
+                  stream, opt);
     if (st != TG_OK) return st;
     // Copy back only the M x N block of every problem (gaps keep host data).
     if (ldc == N && (batch == 1 || strideC == M * N)) {

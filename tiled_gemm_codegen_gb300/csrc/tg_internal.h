@@ -33,6 +33,8 @@ struct KernelParams {
     int32_t k_blocks;     // ceil(K / BK)
     int64_t num_units;    // batch * tiles_m * tiles_n * splits
     int32_t group_m;      // tile-row group of the rasterisation
+    int32_t a_mn;         // 1: A's M dimension is contiguous (column-major A)
+    int32_t b_k;          // 1: B's K dimension is contiguous (column-major B)
     int32_t a_bcast;      // 1: A has batch stride 0 (same A for every problem)
     int32_t b_bcast;      // 1: B has batch stride 0
     int32_t epi_tma;      // 1: TMA store of C; 0: plain masked stores

@@ -77,12 +77,13 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo,
 }
 
 // Instruction descriptor of tcgen05.mma.kind::f16: D fp32 (bits 4-5 = 1),
-// A bf16 (bits 7-9 = 1), B bf16 (bits 10-12 = 1), A K-major (bit 15 = 0),
-// B MN-major (bit 16 = 1), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+// A bf16 (bits 7-9 = 1), B bf16 (bits 10-12 = 1), bit 15 = A MN-major,
+// bit 16 = B MN-major, N >> 3 at bits 17-22, M >> 4 at bits 24-28.
 template <int M, int N>
-__host__ __device__ constexpr uint32_t instr_desc_bf16()
+__host__ __device__ constexpr uint32_t instr_desc_bf16(bool a_mn, bool b_mn)
 {
-    return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
+           (static_cast<uint32_t>(b_mn) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 
@@ -432,21 +433,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         ok = false;
                         break;
                     }
+                    // One copy: this CTA's own barrier; a pair: the leader's.
+                    uint32_t fb;
                     if constexpr (PAIR) {
                         if (leader) ptx::mbar_arrive_expect_tx(full_bar(s), 2 * G::STAGE);
-                        const uint32_t fb = full0 + 8u * s;
-                        ptx::tma_load_3d_pair(sA + s * G::A_STAGE, &tmA, fb, kb * BK, m_rows, zA);
-#pragma unroll
-                        for (int j = 0; j < B_BOXES; ++j)
-                            ptx::tma_load_3d_pair(sB + s * G::B_STAGE + j * B_BOX_BYTES, &tmB, fb,
-                                                  n_cols + 64 * j, kb * BK, zB);
+                        fb = full0 + 8u * s;
                     } else {
                         ptx::mbar_arrive_expect_tx(full_bar(s), G::STAGE);
-                        ptx::tma_load_3d(sA + s * G::A_STAGE, &tmA, full_bar(s), kb * BK, m_rows, zA);
+                        fb = full_bar(s);
+                    }
+                    auto load = [&](uint32_t dst, const CUtensorMap *map, int32_t c0, int32_t c1, int32_t c2) {
+                        if constexpr (PAIR)
+                            ptx::tma_load_3d_pair(dst, map, fb, c0, c1, c2);
+                        else
+                            ptx::tma_load_3d(dst, map, fb, c0, c1, c2);
+                    };
+                    const uint32_t a_dst = sA + s * G::A_STAGE;
+                    const uint32_t b_dst = sB + s * G::B_STAGE;
+                    if (!p.a_mn) {
+                        // A row-major: one box [128 rows x 64 k], K-major atoms
+                        load(a_dst, &tmA, kb * BK, m_rows, zA);
+                    } else {
+                        // A column-major: two boxes [64 k x 64 rows], MN-major atoms
+                        load(a_dst, &tmA, m_rows, kb * BK, zA);
+                        load(a_dst + B_BOX_BYTES, &tmA, m_rows + 64, kb * BK, zA);
+                    }
+                    if (!p.b_k) {
+                        // B row-major: boxes [64 k x 64 columns], MN-major atoms
 #pragma unroll
                         for (int j = 0; j < B_BOXES; ++j)
-                            ptx::tma_load_3d(sB + s * G::B_STAGE + j * B_BOX_BYTES, &tmB, full_bar(s),
-                                             n_cols + 64 * j, kb * BK, zB);
+                            load(b_dst + j * B_BOX_BYTES, &tmB, n_cols + 64 * j, kb * BK, zB);
+                    } else {
+                        // B column-major: one box [B_COLS columns x 64 k], K-major atoms
+                        load(b_dst, &tmB, kb * BK, n_cols, zB);
                     }
                 }
             }
@@ -461,7 +480,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else if (warp == 1) {
         if (lane == 0 && (!PAIR || leader)) {
             // ------------------------------------------------ MMA issuer
-            constexpr uint32_t idesc = instr_desc_bf16<TILE_M, BN>();
+            const uint32_t idesc = instr_desc_bf16<TILE_M, BN>(p.a_mn != 0, p.b_k == 0);
+            // Layout-dependent descriptor parts, fixed for the whole kernel:
+            // a K-major operand steps 32 B per 16 k (leading offset unused);
+            // an MN-major one steps 16 rows x 128 B and its 64-element atoms
+            // sit one box (BK x 128 B) apart.  Per MMA only the start address
+            // changes.
+            const uint64_t a_desc0 = smem_desc_sw128(0, p.a_mn ? BK * 128 : 16, 1024);
+            const uint64_t b_desc0 = smem_desc_sw128(0, p.b_k ? 16 : BK * 128, 1024);
+            const uint32_t a_step = p.a_mn ? 2048u : 32u;
+            const uint32_t b_step = p.b_k ? 32u : 2048u;
             uint32_t it = 0, t = 0;
             bool ok = true;
             WorkIter wi;
@@ -492,12 +520,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t b_addr = sB + s * G::B_STAGE;
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
-                        // A: K-major, 8-row atoms 1024 B apart; +32 B per 16 k.
-                        const uint64_t ad = smem_desc_sw128(a_addr + kk * 32, 16, 1024);
-                        // B: N-major, 64-column atoms one box (BK x 128 B) apart
-                        // (leading offset), 8 k-rows 1024 B apart (stride
-                        // offset); +16 rows x 128 B per 16 k.
-                        const uint64_t bd = smem_desc_sw128(b_addr + kk * 2048, BK * 128, 1024);
+                        const uint64_t ad = a_desc0 | (((a_addr + kk * a_step) >> 4) & 0x3FFFu);
+                        const uint64_t bd = b_desc0 | (((b_addr + kk * b_step) >> 4) & 0x3FFFu);
                         const uint32_t acc = (kb > w.kb0 || kk > 0) ? 1u : 0u;
                         if constexpr (PAIR)
                             ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, acc);

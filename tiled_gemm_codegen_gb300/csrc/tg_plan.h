@@ -93,6 +93,7 @@ struct PlanInput {
     int block_n, stages, split_k, force_pack, epilogue, max_ctas;
     int cta_pair;  // 0 = choose, 1 = one CTA per tile, 2 = two-SM tiles
     int stream_k;  // 0 = choose, 1 = off, 2 = on (when the last wave is partial)
+    bool a_cm = false, b_cm = false;  // column-major (transposed) operand storage
 };
 
 struct Plan {
@@ -340,8 +341,11 @@ inline bool make_plan(const PlanInput &in, Plan &out)
 
     const int64_t batch_a = in.a_bcast ? 1 : in.batch;
     const int64_t batch_b = in.b_bcast ? 1 : in.batch;
-    p.ws_pack_a = p.pack_a ? round_up(batch_a * in.M * round_up(in.K, 8) * 2, 256) : 0;
-    p.ws_pack_b = p.pack_b ? round_up(batch_b * in.K * round_up(in.N, 8) * 2, 256) : 0;
+    // pack copies keep the stored layout: rows x round_up(columns, 8)
+    const int64_t a_rows = in.a_cm ? in.K : in.M, a_cols = in.a_cm ? in.M : in.K;
+    const int64_t b_rows = in.b_cm ? in.N : in.K, b_cols = in.b_cm ? in.K : in.N;
+    p.ws_pack_a = p.pack_a ? round_up(batch_a * a_rows * round_up(a_cols, 8) * 2, 256) : 0;
+    p.ws_pack_b = p.pack_b ? round_up(batch_b * b_rows * round_up(b_cols, 8) * 2, 256) : 0;
     set_partial_workspace(in, p);
     out = p;
     return true;
