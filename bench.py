@@ -4,7 +4,9 @@
 
 A step is one tg_gemm call over the workload (4096^3 by default: the square
 problem the headline TFLOP/s is quoted on), inputs already resident in HBM.
-L2 is flushed (a 512 MB write) between steps, outside the timed events.
+L2 is flushed between steps, outside the timed events: a 512 MB write (evicts
+A, B and C) followed by a 256 MB read (evicts the flush's own dirty lines, so
+their write-back does not land inside the next timed step).
 Prints one JSON line (rank 0).  With --impl reference the oracle (fp64 CPU
 triple loop) is timed instead, on a bounded sample of rows of the same
 workload.
@@ -69,7 +71,7 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -85,7 +87,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (FileNotFoundError, OSError):
             self.proc = None
             return
@@ -231,13 +233,19 @@ def run_gpu(args, rank, world, local, dist):
     info = tg.plan(w.M, w.N, w.K, w.batch, A=A.data_ptr(), B=B.data_ptr(), C=C.data_ptr())
     launches_per_step = 1 + info["pack_a"] + info["pack_b"]
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+    flush_read = torch.ones(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+    sink = torch.empty((), dtype=torch.float32, device=device)
+
+    def flush_l2(v: float):
+        flush.fill_(v)                          # write > L2: A, B, C evicted
+        torch.sum(flush_read, dim=0, out=sink)  # read > L2: dirty flush lines written back now
 
     def step():
         tg.gemm(A, B, C)
 
     # warm-up (also JIT-loads the module, allocates workspaces)
     for _ in range(args.warmup):
-        flush.fill_(1.0)
+        flush_l2(1.0)
         step()
     torch.cuda.synchronize()
     st = tg.device_error()
@@ -248,19 +256,21 @@ def run_gpu(args, rank, world, local, dist):
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     clocks = ClockSampler(local)
     clocks.start()
-    # A one-second load window of back-to-back steps right before the timed
-    # region, so that the 200 ms clock samples see the GPU under this load
-    # even when the timed region itself is only milliseconds long.
+    # A load window right before the timed region that repeats the timed
+    # steps themselves (flush, then GEMM), so that the clock samples see the
+    # GPU under this benchmark's load even when the timed region itself is
+    # only milliseconds long.
     t_end = time.perf_counter() + args.clock_window
     while time.perf_counter() < t_end:
-        for _ in range(50):
+        for _ in range(20):
+            flush_l2(0.5)
             step()
         torch.cuda.synchronize()
     barrier(dist)
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
     for i in range(args.steps):
-        flush.fill_(float(i))  # evict A, B, C from L2 (outside the timed events)
+        flush_l2(float(i))  # outside the timed events
         starts[i].record(stream)
         step()
         ends[i].record(stream)
@@ -284,7 +294,7 @@ def run_gpu(args, rank, world, local, dist):
     tg.gemm_host(Ah, Bh, Ch)
     e2e_ms = []
     for _ in range(max(3, min(args.steps, 10))):
-        flush.fill_(2.0)
+        flush_l2(2.0)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         tg.gemm_host(Ah, Bh, Ch)
@@ -311,7 +321,8 @@ def run_gpu(args, rank, world, local, dist):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
             "config": {"workload": w.name, "batch": w.batch, "M": w.M, "N": w.N, "K": w.K,
-                       "accumulate": "fp32", "l2": "flushed (512 MB write) between steps",
+                       "accumulate": "fp32",
+                       "l2": "flushed between steps (512 MB write, then 256 MB read)",
                        "parallelism": "replicas" if world > 1 else "single GPU",
                        "plan": {k: info[k] for k in ("block_n", "stages", "split_k", "grid", "pack_a",
                                                      "pack_b", "epilogue")}},
@@ -321,8 +332,8 @@ def run_gpu(args, rank, world, local, dist):
                     "h2d_bytes_per_step": int(A_cpu.numel() * 2 + B_cpu.numel() * 2),
                     "d2h_bytes_per_step": int(C.numel() * 4)},
             "gpu_launches": launches_per_step * args.steps,
-            "clocks": dict(clk, window=f"{args.clock_window:.1f} s of back-to-back steps just before "
-                                          "the timed region, and the timed region"),
+            "clocks": dict(clk, window=f"{args.clock_window:.1f} s of the same steps (flush, GEMM) just "
+                                          "before the timed region, and the timed region"),
             "ms_min": round(min(per), 4),
             "wall_s": round(wall, 3),
         }
@@ -337,7 +348,7 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--impl", default="tg", choices=["tg", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--clock-window", type=float, default=1.0)
+    ap.add_argument("--clock-window", type=float, default=0.5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "tg":
