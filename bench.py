@@ -31,7 +31,7 @@ import synth  # noqa: E402
 DEFAULT_WORKLOAD = "square_4096"
 METRIC = "bf16->fp32 GEMM TFLOP/s at 1 GB300 and % of dense BF16 tensor (or HBM) roofline"
 KERNEL_SOURCES = ["tiled_gemm_codegen_gb300/csrc/tg_kernel.cuh", "tiled_gemm_codegen_gb300/csrc/tg_ptx.cuh",
-                  "tiled_gemm_codegen_gb300/csrc/tg_internal.h"]
+                  "tiled_gemm_codegen_gb300/csrc/tg_internal.h", "tiled_gemm_codegen_gb300/csrc/tg_epilogue.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -325,7 +325,8 @@ def run_gpu(args, rank, world, local, dist):
                        "l2": "flushed between steps (512 MB write, then 256 MB read)",
                        "parallelism": "replicas" if world > 1 else "single GPU",
                        "plan": {k: info[k] for k in ("block_n", "stages", "split_k", "grid", "pack_a",
-                                                     "pack_b", "epilogue")}},
+                                                     "pack_b", "epilogue", "cta_pair", "stream_k",
+                                                     "sk_tiles")}},
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s",

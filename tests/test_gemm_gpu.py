@@ -222,6 +222,33 @@ def test_misaligned_operands_use_pack(a_off, b_off, lda_pad, ldb_pad):
     assert np.array_equal(C.cpu().double().numpy(), oracle_dense(Ai, Bi))
 
 
+@pytest.mark.parametrize("a_off,b_off,lda_pad,ldb_pad,M,N,K", [
+    (1, 7, 0, 0, 131, 257, 300),     # every row start misaligned, odd ld
+    (0, 0, 0, 1, 64, 95, 4100),      # A rows alternate 8- and 16-byte alignment
+    (3, 5, 2, 3, 5, 9, 7),           # rows shorter than one 16-byte chunk
+    (0, 2, 0, 1, 33, 1031, 1031),    # a ragged last chunk in every row
+])
+def test_pack_reads_nothing_outside_rows(a_off, b_off, lda_pad, ldb_pad, M, N, K):
+    """Every element around and between the operands' rows is NaN: the
+    realigning pack reads whole aligned 16-byte blocks, so a stray byte
+    shifted into a packed row, or a tail not masked, would turn outputs
+    into NaN.  Integer inputs make the product exact."""
+    lda, ldb = K + lda_pad, N + ldb_pad
+    Ai, Bi = synth.make_int_inputs(1, M, N, K, seed=M + N)
+    nan = float("nan")
+    abuf = torch.full((a_off + M * lda + 16,), nan, dtype=torch.bfloat16)
+    bbuf = torch.full((b_off + K * ldb + 16,), nan, dtype=torch.bfloat16)
+    abuf[a_off:a_off + M * lda].view(M, lda)[:, :K] = Ai
+    bbuf[b_off:b_off + K * ldb].view(K, ldb)[:, :N] = Bi
+    ad, bd = abuf.to(dev()), bbuf.to(dev())
+    A = ad[a_off:a_off + M * lda].view(M, lda)[:, :K]
+    B = bd[b_off:b_off + K * ldb].view(K, ldb)[:, :N]
+    C = torch.empty(M, N, dtype=torch.float32, device=dev())
+    tg.gemm(A, B, C)
+    assert tg.device_error() == tg.TG_OK
+    assert np.array_equal(C.cpu().double().numpy(), oracle_dense(Ai, Bi))
+
+
 def test_strided_batches_with_gaps():
     batch, M, N, K = 4, 70, 90, 110
     Ai, Bi = synth.make_int_inputs(batch, M, N, K, seed=21)
