@@ -590,20 +590,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 } else {
                     __syncwarp();
-                    // Coalesced: lane l writes column col0 + l of each row.  All
-                    // 32 values are read from the box first, then the 32 row
-                    // stores go out back to back.
+                    // Coalesced: lane l writes column col0 + l of each row.  Eight
+                    // rows a step: their values are read from the box first,
+                    // then their stores go out back to back.  The loop is kept
+                    // rolled: a small tile's epilogue runs its code once, from a
+                    // cold instruction cache.
                     const uint32_t src = box + ((lane >> 2) << 4) + ((lane & 3) << 2);
-                    float vals[32];
+                    float *dst = static_cast<float *>(p.C) + static_cast<int64_t>(b) * p.strideC +
+                                 static_cast<int64_t>(row0) * p.ldc + col;
+#pragma unroll 1
+                    for (int r0 = 0; r0 < 32; r0 += 8) {
+                        float vals[8];
 #pragma unroll
-                    for (int r = 0; r < 32; ++r) vals[r] = ld_shared_f32((src ^ ((r & 7) << 4)) + r * 128);
-                    __syncwarp();
-                    if (col < p.N) {
-                        float *dst = static_cast<float *>(p.C) + static_cast<int64_t>(b) * p.strideC +
-                                     static_cast<int64_t>(row0) * p.ldc + col;
+                        for (int r = 0; r < 8; ++r)
+                            vals[r] = ld_shared_f32((src ^ (((r0 + r) & 7) << 4)) + (r0 + r) * 128);
+                        if (col < p.N) {
 #pragma unroll
-                        for (int r = 0; r < 32; ++r)
-                            if (r < nrows) dst[static_cast<int64_t>(r) * p.ldc] = vals[r];
+                            for (int r = 0; r < 8; ++r)
+                                if (r0 + r < nrows) dst[static_cast<int64_t>(r0 + r) * p.ldc] = vals[r];
+                        }
                     }
                 }
             } else {
@@ -627,17 +632,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 } else {
                     __syncwarp();
                     const uint32_t src = box + ((lane >> 3) << 4) + ((lane & 7) << 1);
-                    uint16_t vals[32];
+                    uint16_t *dst = static_cast<uint16_t *>(p.C) + static_cast<int64_t>(b) * p.strideC +
+                                    static_cast<int64_t>(row0) * p.ldc + col;
+#pragma unroll 1
+                    for (int r0 = 0; r0 < 32; r0 += 8) {
+                        uint16_t vals[8];
 #pragma unroll
-                    for (int r = 0; r < 32; ++r)
-                        vals[r] = ld_shared_u16((src ^ (((r >> 1) & 3) << 4)) + r * 64);
-                    __syncwarp();
-                    if (col < p.N) {
-                        uint16_t *dst = static_cast<uint16_t *>(p.C) + static_cast<int64_t>(b) * p.strideC +
-                                        static_cast<int64_t>(row0) * p.ldc + col;
+                        for (int r = 0; r < 8; ++r)
+                            vals[r] = ld_shared_u16((src ^ ((((r0 + r) >> 1) & 3) << 4)) + (r0 + r) * 64);
+                        if (col < p.N) {
 #pragma unroll
-                        for (int r = 0; r < 32; ++r)
-                            if (r < nrows) dst[static_cast<int64_t>(r) * p.ldc] = vals[r];
+                            for (int r = 0; r < 8; ++r)
+                                if (r0 + r < nrows) dst[static_cast<int64_t>(r0 + r) * p.ldc] = vals[r];
+                        }
                     }
                 }
             }
