@@ -193,10 +193,18 @@ tg_status tg_gemm_fused(const void *A, const void *B, void *D,
                         const tg_epilogue *ep, tg_stream_t stream, const tg_options *opt);
 
 /* The GEMM on HOST buffers: copies the spans of A and B that the strides
- * reach to device scratch owned by the library, runs tg_gemm_ex there, and
- * copies the reached span of C back.  Synchronous: returns after C is on the
- * host (pinned host memory makes the copies faster; pageable also works).
- * Elements of C between rows (ldc > N) or between problems are preserved. */
+ * reach to device scratch owned by the library, runs tg_gemm_ex there into
+ * a device C with 16-byte rows, and copies the M x N block of every problem
+ * back.  The copies and the GEMM are pipelined over pieces that are
+ * contiguous in host memory (problems of a stacked batch, rows of a
+ * row-major A, columns of a column-major B; at most 8): copies in, GEMMs and
+ * copies out run on three streams and overlap.  An operand copied whole
+ * whose rows are not 16-byte aligned is realigned once on the device.
+ * Synchronous: returns after C is on the host (pinned host memory makes the
+ * copies faster; pageable also works).  Elements of C between rows
+ * (ldc > N) or between problems are preserved.  Results equal tg_gemm_ex's
+ * on the same data except where the pieces change the plan's split-K or
+ * stream-K partition (then within the usual rounding of a split sum). */
 tg_status tg_gemm_host(const void *A_host, const void *B_host, float *C_host,
                        int64_t M, int64_t N, int64_t K,
                        int64_t lda, int64_t ldb, int64_t ldc,

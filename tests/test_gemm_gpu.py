@@ -479,3 +479,83 @@ def test_transposed_host_entry():
                          tg.make_options(a_col_major=1, b_col_major=1))
     assert st == tg.TG_OK
     assert np.array_equal(C.double().numpy(), oracle_dense(A, B))
+
+
+def _host_strided(rows, cols, ld, fill=float("nan")):
+    """A host bf16 buffer of `rows` rows of pitch `ld` and a view of its
+    rows x cols block."""
+    buf = torch.full((rows * ld,), fill, dtype=torch.bfloat16)
+    return buf, buf.view(rows, ld)[:, :cols]
+
+
+@pytest.mark.parametrize("M,N,K,lda_pad,ldb_pad,ldc_pad", [
+    (2048, 256, 300, 0, 0, 0),     # A the larger operand: streamed in pieces of rows
+    (1031, 300, 200, 3, 5, 7),     # row pieces, host rows not 16-byte aligned, C row gaps
+    (100, 3000, 200, 1, 0, 2),     # B the larger operand: streamed in pieces of columns
+    (64, 1300, 520, 0, 3, 1),      # column pieces with a ragged last piece
+])
+def test_host_entry_pipelined_pieces(M, N, K, lda_pad, ldb_pad, ldc_pad):
+    """tg_gemm_host stages the operands with 16-byte row pitches and
+    multiplies piece by piece while copies overlap: exact integer products,
+    and the host C keeps every element outside the M x N block."""
+    Ai, Bi = synth.make_int_inputs(1, M, N, K, seed=M + 7 * N)
+    lda, ldb, ldc = K + lda_pad, N + ldb_pad, N + ldc_pad
+    _, A = _host_strided(M, K, lda)
+    _, B = _host_strided(K, N, ldb)
+    A.copy_(Ai)
+    B.copy_(Bi)
+    cbuf = torch.full((M * ldc,), float("nan"), dtype=torch.float32)
+    C = cbuf.view(M, ldc)[:, :N]
+    tg.gemm_host(A, B, C)
+    assert np.array_equal(C.double().numpy(), oracle_dense(Ai, Bi))
+    if ldc_pad:
+        assert torch.all(torch.isnan(cbuf.view(M, ldc)[:, N:]))
+
+
+def test_host_entry_pipelined_batches():
+    """Batched host operands with gaps between problems: pieces of problems."""
+    batch, M, N, K = 11, 70, 90, 110
+    Ai, Bi = synth.make_int_inputs(batch, M, N, K, seed=99)
+    sA, sB, sC = M * K + 24, K * N + 8, M * N + 40
+    abuf = torch.full((batch * sA,), float("nan"), dtype=torch.bfloat16)
+    bbuf = torch.full((batch * sB,), float("nan"), dtype=torch.bfloat16)
+    cbuf = torch.full((batch * sC,), float("nan"), dtype=torch.float32)
+    for b in range(batch):
+        abuf[b * sA: b * sA + M * K] = Ai[b].reshape(-1)
+        bbuf[b * sB: b * sB + K * N] = Bi[b].reshape(-1)
+    st = tg.tg_gemm_host(abuf.data_ptr(), bbuf.data_ptr(), cbuf.data_ptr(), M, N, K, K, N, N, batch,
+                         sA, sB, sC, torch.cuda.current_stream().cuda_stream, None)
+    assert st == tg.TG_OK
+    want = oracle_dense(Ai, Bi)
+    for b in range(batch):
+        got = cbuf[b * sC: b * sC + M * N].view(M, N).double().numpy()
+        assert np.array_equal(got, want[b]), b
+        assert torch.all(torch.isnan(cbuf[b * sC + M * N: (b + 1) * sC]))
+
+
+@pytest.mark.parametrize("M,N,K,a_cm,b_cm", [(1500, 200, 300, 1, 0), (90, 1800, 250, 0, 1),
+                                             (1100, 150, 260, 1, 1)])
+def test_host_entry_pipelined_transposed(M, N, K, a_cm, b_cm):
+    """Column-major operands through the host entry point, with pieces of
+    rows (A streamed) or columns (B streamed)."""
+    Ai, Bi = synth.make_int_inputs(1, M, N, K, seed=M + N + a_cm)
+    A = Ai.t().contiguous() if a_cm else Ai.contiguous()
+    B = Bi.t().contiguous() if b_cm else Bi.contiguous()
+    lda = M if a_cm else K
+    ldb = K if b_cm else N
+    C = torch.full((M, N), float("nan"))
+    st = tg.tg_gemm_host(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, lda, ldb, N, 1, 0, 0, 0,
+                         torch.cuda.current_stream().cuda_stream,
+                         tg.make_options(a_col_major=a_cm, b_col_major=b_cm))
+    assert st == tg.TG_OK
+    assert np.array_equal(C.double().numpy(), oracle_dense(Ai, Bi))
+
+
+def test_host_entry_empty_sum():
+    """K == 0 through the host entry point: C is all zeros."""
+    M, N = 37, 45
+    A = torch.empty(M, 0, dtype=torch.bfloat16)
+    B = torch.empty(0, N, dtype=torch.bfloat16)
+    C = torch.full((M, N), float("nan"))
+    tg.gemm_host(A, B, C)
+    assert torch.all(C == 0)

@@ -286,6 +286,10 @@ struct Workspace {
     uint32_t *err = nullptr;  // device error word of this stream
     void *host_arena = nullptr;  // device copies of tg_gemm_host operands
     size_t host_cap = 0;
+    // tg_gemm_host's copy streams and events (created on first use)
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    static constexpr int HOST_EVENTS = 1 + 3 * 8;
+    cudaEvent_t ev[HOST_EVENTS] = {};
 };
 
 std::mutex g_mutex;
@@ -533,6 +537,17 @@ int grid_for(int64_t work, int sms)
     return static_cast<int>(g);
 }
 
+// The pack job of one operand: rows x cols bf16 (batch nb, element stride
+// between problems), into dst with rows padded to 8 elements.
+PackJob pack_job(const void *src, uint16_t *dst, int64_t rows, int64_t cols, int64_t ld, int64_t nb,
+                 int64_t stride)
+{
+    const int64_t ld2 = round_up(cols, 8);
+    const uintptr_t base = reinterpret_cast<uintptr_t>(src);
+    return PackJob{static_cast<const uint16_t *>(src), dst, rows, cols, ld, stride, ld2, nb * rows * (ld2 / 8), base,
+                   base + 2u * static_cast<uintptr_t>(span_elems(rows, cols, ld, nb, stride))};
+}
+
 // The whole device-side path of one call (arguments already validated).
 tg_status run_gemm(const Args &a, cudaStream_t stream, const tg_options *opt,
                    const tg_epilogue *ep = nullptr)
@@ -627,24 +642,10 @@ tg_status run_gemm(const Args &a, cudaStream_t stream, const tg_options *opt,
 
     if (plan.pack_a || plan.pack_b) {
         PackJob ja{}, jb{};
-        if (plan.pack_a) {
-            const int64_t nb = in.a_bcast ? 1 : a.batch;
-            const int64_t rows = a.a_rows(), cols = a.a_cols();
-            const int64_t ld2 = round_up(cols, 8);
-            const uintptr_t base = reinterpret_cast<uintptr_t>(a.A);
-            ja = PackJob{static_cast<const uint16_t *>(a.A), pack_a_buf, rows, cols, a.lda, a.sA, ld2,
-                         nb * rows * (ld2 / 8), base,
-                         base + 2u * static_cast<uintptr_t>(span_elems(rows, cols, a.lda, nb, a.sA))};
-        }
-        if (plan.pack_b) {
-            const int64_t nb = in.b_bcast ? 1 : a.batch;
-            const int64_t rows = a.b_rows(), cols = a.b_cols();
-            const int64_t ld2 = round_up(cols, 8);
-            const uintptr_t base = reinterpret_cast<uintptr_t>(a.B);
-            jb = PackJob{static_cast<const uint16_t *>(a.B), pack_b_buf, rows, cols, a.ldb, a.sB, ld2,
-                         nb * rows * (ld2 / 8), base,
-                         base + 2u * static_cast<uintptr_t>(span_elems(rows, cols, a.ldb, nb, a.sB))};
-        }
+        if (plan.pack_a)
+            ja = pack_job(a.A, pack_a_buf, a.a_rows(), a.a_cols(), a.lda, in.a_bcast ? 1 : a.batch, a.sA);
+        if (plan.pack_b)
+            jb = pack_job(a.B, pack_b_buf, a.b_rows(), a.b_cols(), a.ldb, in.b_bcast ? 1 : a.batch, a.sB);
         const int blocks_a = plan.pack_a ? grid_for(ja.chunks, sms) : 0;
         const int blocks_b = plan.pack_b ? grid_for(jb.chunks, sms) : 0;
         pack_bf16_kernel<<<blocks_a + blocks_b, 256, 0, stream>>>(ja, jb, blocks_a);
@@ -875,11 +876,73 @@ TG_API tg_status tg_plan(const void *A, const void *B, const float *C, int64_t M
     return TG_OK;
 }
 
+namespace tg {
+namespace {
+
+// Copy rows [r0, r0 + nrows) x columns [c0, c0 + ncols) of a matrix between
+// two pitches (elements of `eb` bytes).
+cudaError_t copy_block(void *dst, int64_t dpitch, const void *src, int64_t spitch, int64_t r0, int64_t nrows,
+                       int64_t c0, int64_t ncols, int64_t eb, cudaMemcpyKind kind, cudaStream_t s)
+{
+    if (nrows <= 0 || ncols <= 0) return cudaSuccess;
+    auto *d = static_cast<uint8_t *>(dst) + (r0 * dpitch + c0) * eb;
+    const auto *x = static_cast<const uint8_t *>(src) + (r0 * spitch + c0) * eb;
+    if (ncols == dpitch && ncols == spitch)
+        return cudaMemcpyAsync(d, x, static_cast<size_t>(nrows * ncols * eb), kind, s);
+    return cudaMemcpy2DAsync(d, static_cast<size_t>(dpitch * eb), x, static_cast<size_t>(spitch * eb),
+                             static_cast<size_t>(ncols * eb), static_cast<size_t>(nrows), kind, s);
+}
+
+// Problems [b0, b1) of a batch: one copy when the problems are stacked
+// (stride = rows * pitch on both sides), else one per problem.
+cudaError_t copy_problems(void *dst, int64_t dpitch, int64_t dstride, const void *src, int64_t spitch,
+                          int64_t sstride, int64_t b0, int64_t b1, int64_t r0, int64_t nrows, int64_t rows,
+                          int64_t c0, int64_t ncols, int64_t eb, cudaMemcpyKind kind, cudaStream_t s)
+{
+    if (b1 - b0 > 1 && nrows == rows && dstride == rows * dpitch && sstride == rows * spitch) {
+        auto *d = static_cast<uint8_t *>(dst) + b0 * dstride * eb;
+        const auto *x = static_cast<const uint8_t *>(src) + b0 * sstride * eb;
+        return copy_block(d, dpitch, x, spitch, 0, (b1 - b0) * rows, c0, ncols, eb, kind, s);
+    }
+    for (int64_t b = b0; b < b1; ++b) {
+        cudaError_t e = copy_block(static_cast<uint8_t *>(dst) + b * dstride * eb, dpitch,
+                                   static_cast<const uint8_t *>(src) + b * sstride * eb, spitch, r0, nrows, c0,
+                                   ncols, eb, kind, s);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+tg_status host_streams(Workspace &w)
+{
+    cudaError_t e = cudaSuccess;
+    if (!w.h2d && (e = cudaStreamCreateWithFlags(&w.h2d, cudaStreamNonBlocking)) != cudaSuccess) return cuda_status(e);
+    if (!w.d2h && (e = cudaStreamCreateWithFlags(&w.d2h, cudaStreamNonBlocking)) != cudaSuccess) return cuda_status(e);
+    for (cudaEvent_t &ev : w.ev)
+        if (!ev && (e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess) return cuda_status(e);
+    return TG_OK;
+}
+
+}  // namespace
+}  // namespace tg
+
+// Host buffers in, host buffer out.  The operands are copied to the device
+// as they are laid out on the host (contiguous spans, so every copy is a
+// plain 1-D copy at full link speed; strided 2-D copies of host memory run
+// up to ~40% slower), C is written to a device buffer with 16-byte rows (so
+// the epilogue stores with the tensor memory accelerator) and copied back
+// row by row into the host layout.  The work is pipelined over pieces that
+// are contiguous on the host (see host_pieces): one stream copies operand
+// pieces in, the caller's stream multiplies each piece as soon as it has
+// landed, a third stream copies each finished piece of C out, so the copies
+// in both directions overlap the GEMMs and each other.  An operand copied
+// whole whose rows are not 16-byte aligned is realigned once on the device.
 TG_API tg_status tg_gemm_host(const void *A_host, const void *B_host, float *C_host, int64_t M,
                               int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
                               int64_t batch, int64_t strideA, int64_t strideB, int64_t strideC,
                               tg_stream_t stream_, const tg_options *opt)
 {
+    using namespace tg;
     const Args a =
         with_layout(Args{A_host, B_host, C_host, M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC}, opt);
     tg_status st = validate(a);
@@ -889,42 +952,137 @@ TG_API tg_status tg_gemm_host(const void *A_host, const void *B_host, float *C_h
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_status(e);
+    int sms = 0;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        if ((st = device_sms(dev, &sms)) != TG_OK) return st;
+    }
 
-    const int64_t na = K > 0 ? span_elems(a.a_rows(), a.a_cols(), lda, batch, strideA) : 0;
-    const int64_t nb = K > 0 ? span_elems(a.b_rows(), a.b_cols(), ldb, batch, strideB) : 0;
-    const int64_t nc = span_elems(M, N, ldc, batch, strideC);
-    const size_t off_b = static_cast<size_t>(round_up(na * 2, 256));
-    const size_t off_c = off_b + static_cast<size_t>(round_up(nb * 2, 256));
-    const size_t need = off_c + static_cast<size_t>(round_up(nc * 4, 256));
+    const bool a_bcast = batch > 1 && strideA == 0, b_bcast = batch > 1 && strideB == 0;
+    const int64_t a_rows = a.a_rows(), a_cols = a.a_cols(), b_rows = a.b_rows(), b_cols = a.b_cols();
+    // device copies of A and B keep the host's element offsets: the span of
+    // every operand is copied from its first element
+    const int64_t na = K > 0 ? span_elems(a_rows, a_cols, lda, a_bcast ? 1 : batch, strideA) : 0;
+    const int64_t nb = K > 0 ? span_elems(b_rows, b_cols, ldb, b_bcast ? 1 : batch, strideB) : 0;
+    const int64_t ldc_d = round_up(N, 4), sC_d = M * ldc_d;
+    const HostPieces hp = host_pieces(M, N, K, batch, a_bcast, b_bcast, a.a_cm, a.b_cm,
+                                      strideA == a_rows * lda, strideB == b_rows * ldb);
+    // the operand copied whole is realigned once if its rows are not 16-byte aligned
+    const bool a_whole = hp.dim == 0 || hp.dim == 3, b_whole = hp.dim == 0 || hp.dim == 2;
+    const bool a_fix = K > 0 && a_whole && (lda % 8 != 0 || (batch > 1 && !a_bcast && strideA % 8 != 0));
+    const bool b_fix = K > 0 && b_whole && (ldb % 8 != 0 || (batch > 1 && !b_bcast && strideB % 8 != 0));
+    const int64_t lda_f = round_up(a_cols, 8), ldb_f = round_up(b_cols, 8);
+    const int64_t sA_f = a_bcast ? 0 : a_rows * lda_f, sB_f = b_bcast ? 0 : b_rows * ldb_f;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off += static_cast<size_t>(round_up(static_cast<int64_t>(bytes), 256));
+        return o;
+    };
+    const size_t off_a = take(na * 2), off_b = take(nb * 2), off_c = take(batch * sC_d * 4);
+    const size_t off_af = a_fix ? take((a_bcast ? 1 : batch) * a_rows * lda_f * 2) : 0;
+    const size_t off_bf = b_fix ? take((b_bcast ? 1 : batch) * b_rows * ldb_f * 2) : 0;
     uint8_t *dbuf = nullptr;
+    Workspace *wp = nullptr;
     {
         std::lock_guard<std::mutex> lock(g_mutex);
         Workspace &w = workspace_for(dev, stream);
-        st = grow(&w.host_arena, &w.host_cap, need, stream);
+        st = grow(&w.host_arena, &w.host_cap, off, stream);
+        if (st == TG_OK) st = host_streams(w);
         if (st != TG_OK) return st;
         dbuf = static_cast<uint8_t *>(w.host_arena);
+        wp = &w;  // map nodes are stable; calls on one stream are serial
     }
-    void *dA = dbuf;
-    void *dB = dbuf + off_b;
+    Workspace &w = *wp;
+    const uint16_t *dA = reinterpret_cast<uint16_t *>(dbuf + off_a);
+    const uint16_t *dB = reinterpret_cast<uint16_t *>(dbuf + off_b);
     float *dC = reinterpret_cast<float *>(dbuf + off_c);
-    if (na > 0 && (e = cudaMemcpyAsync(dA, A_host, na * 2, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
-        return cuda_status(e);
-    if (nb > 0 && (e = cudaMemcpyAsync(dB, B_host, nb * 2, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
-        return cuda_status(e);
-    st = run_gemm(with_layout(Args{dA, dB, dC, M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC}, opt),
-                  stream, opt);
-    if (st != TG_OK) return st;
-    // Copy back only the M x N block of every problem (gaps keep host data).
-    if (ldc == N && (batch == 1 || strideC == M * N)) {
-        e = cudaMemcpyAsync(C_host, dC, static_cast<size_t>(batch * M * N) * 4, cudaMemcpyDeviceToHost, stream);
-        if (e != cudaSuccess) return cuda_status(e);
-    } else {
-        for (int64_t b = 0; b < batch; ++b) {
-            e = cudaMemcpy2DAsync(C_host + b * strideC, ldc * 4, dC + b * strideC, ldc * 4, N * 4, M,
-                                  cudaMemcpyDeviceToHost, stream);
-            if (e != cudaSuccess) return cuda_status(e);
+    const cudaMemcpyKind H2D = cudaMemcpyHostToDevice;
+
+    // the copy streams start after the caller's earlier work
+    if ((e = cudaEventRecord(w.ev[0], stream)) != cudaSuccess) return cuda_status(e);
+    if ((e = cudaStreamWaitEvent(w.h2d, w.ev[0], 0)) != cudaSuccess) return cuda_status(e);
+    if ((e = cudaStreamWaitEvent(w.d2h, w.ev[0], 0)) != cudaSuccess) return cuda_status(e);
+    // elements [e0, e1) of an operand's span, host -> device
+    auto copy_in = [&](const uint16_t *dst, const void *src, int64_t e0, int64_t e1) {
+        if (e1 <= e0) return cudaSuccess;
+        return cudaMemcpyAsync(const_cast<uint16_t *>(dst) + e0, static_cast<const uint16_t *>(src) + e0,
+                               static_cast<size_t>((e1 - e0) * 2), H2D, w.h2d);
+    };
+    // the span of problems [b0, b1), or of rows [r0, r1) of one problem
+    auto span = [&](int64_t rows, int64_t cols, int64_t ld, int64_t stride, int64_t b0, int64_t b1, int64_t r0,
+                    int64_t r1) {
+        const int64_t lo = b0 * stride + r0 * ld;
+        const int64_t hi = (b1 - 1) * stride + (r1 - 1) * ld + cols;
+        (void)rows;
+        return std::make_pair(lo, hi);
+    };
+    const uint16_t *A_use = dA, *B_use = dB;
+    int64_t lda_use = lda, ldb_use = ldb, sA_use = a_bcast ? 0 : strideA, sB_use = b_bcast ? 0 : strideB;
+    if (K > 0 && a_whole) {
+        const auto sp = span(a_rows, a_cols, lda, strideA, 0, a_bcast ? 1 : batch, 0, a_rows);
+        if ((e = copy_in(dA, A_host, sp.first, sp.second)) != cudaSuccess) return cuda_status(e);
+        if (a_fix) {
+            uint16_t *dst = reinterpret_cast<uint16_t *>(dbuf + off_af);
+            const PackJob j = pack_job(dA, dst, a_rows, a_cols, lda, a_bcast ? 1 : batch, strideA);
+            pack_bf16_kernel<<<grid_for(j.chunks, sms), 256, 0, w.h2d>>>(j, PackJob{}, grid_for(j.chunks, sms));
+            if ((e = cudaGetLastError()) != cudaSuccess) return cuda_status(e);
+            A_use = dst, lda_use = lda_f, sA_use = sA_f;
         }
     }
+    if (K > 0 && b_whole) {
+        const auto sp = span(b_rows, b_cols, ldb, strideB, 0, b_bcast ? 1 : batch, 0, b_rows);
+        if ((e = copy_in(dB, B_host, sp.first, sp.second)) != cudaSuccess) return cuda_status(e);
+        if (b_fix) {
+            uint16_t *dst = reinterpret_cast<uint16_t *>(dbuf + off_bf);
+            const PackJob j = pack_job(dB, dst, b_rows, b_cols, ldb, b_bcast ? 1 : batch, strideB);
+            pack_bf16_kernel<<<grid_for(j.chunks, sms), 256, 0, w.h2d>>>(j, PackJob{}, grid_for(j.chunks, sms));
+            if ((e = cudaGetLastError()) != cudaSuccess) return cuda_status(e);
+            B_use = dst, ldb_use = ldb_f, sB_use = sB_f;
+        }
+    }
+    cudaEvent_t last_out = nullptr;
+    for (int i = 0; i < hp.pieces; ++i) {
+        const int64_t lo = hp.dim ? hp.bound(i) : 0, hi = hp.dim ? hp.bound(i + 1) : 0;
+        int64_t b0 = 0, b1 = batch, m0 = 0, m1 = M, n0 = 0, n1 = N;
+        if (hp.dim == 1) { b0 = lo; b1 = hi; }
+        if (hp.dim == 2) { m0 = lo; m1 = hi; }
+        if (hp.dim == 3) { n0 = lo; n1 = hi; }
+        if (b1 <= b0 || m1 <= m0 || n1 <= n0) continue;
+        if (hp.dim == 1) {
+            const auto sa = span(a_rows, a_cols, lda, strideA, b0, b1, 0, a_rows);
+            const auto sb = span(b_rows, b_cols, ldb, strideB, b0, b1, 0, b_rows);
+            e = copy_in(dA, A_host, sa.first, sa.second);
+            if (e == cudaSuccess) e = copy_in(dB, B_host, sb.first, sb.second);
+        } else if (hp.dim == 2) {  // rows m0..m1 of a row-major A
+            const auto sa = span(a_rows, a_cols, lda, strideA, 0, 1, m0, m1);
+            e = copy_in(dA, A_host, sa.first, sa.second);
+        } else if (hp.dim == 3) {  // columns n0..n1 of B: rows of a column-major B
+            const auto sb = span(b_rows, b_cols, ldb, strideB, 0, 1, n0, n1);
+            e = copy_in(dB, B_host, sb.first, sb.second);
+        }
+        cudaEvent_t ev_in = w.ev[1 + 3 * i], ev_gemm = w.ev[2 + 3 * i], ev_out = w.ev[3 + 3 * i];
+        if (e == cudaSuccess) e = cudaEventRecord(ev_in, w.h2d);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, ev_in, 0);
+        if (e != cudaSuccess) return cuda_status(e);
+        // the piece's GEMM on the device copies
+        const int64_t a_off = a.a_cm ? m0 : m0 * lda_use;
+        const int64_t b_off = a.b_cm ? n0 * ldb_use : n0;
+        Args piece{A_use + b0 * sA_use + a_off, B_use + b0 * sB_use + b_off, dC + b0 * sC_d + m0 * ldc_d + n0,
+                   m1 - m0, n1 - n0, K, lda_use, ldb_use, ldc_d, b1 - b0, sA_use, sB_use, sC_d};
+        st = run_gemm(with_layout(piece, opt), stream, opt);
+        if (st != TG_OK) return st;
+        if ((e = cudaEventRecord(ev_gemm, stream)) != cudaSuccess) return cuda_status(e);
+        if ((e = cudaStreamWaitEvent(w.d2h, ev_gemm, 0)) != cudaSuccess) return cuda_status(e);
+        // only the M x N block of every problem goes back (gaps keep host data)
+        e = copy_problems(C_host, ldc, strideC, dC, ldc_d, sC_d, b0, b1, m0, m1 - m0, M, n0, n1 - n0, 4,
+                          cudaMemcpyDeviceToHost, w.d2h);
+        if (e == cudaSuccess) e = cudaEventRecord(ev_out, w.d2h);
+        if (e != cudaSuccess) return cuda_status(e);
+        last_out = ev_out;
+    }
+    // the caller's stream resumes after the last piece of C is home
+    if (last_out && (e = cudaStreamWaitEvent(stream, last_out, 0)) != cudaSuccess) return cuda_status(e);
     e = cudaStreamSynchronize(stream);
     return cuda_status(e);
 }
@@ -965,6 +1123,10 @@ TG_API void tg_shutdown(void)
         if (w.counters) cudaFree(w.counters);
         if (w.err) cudaFree(w.err);
         if (w.host_arena) cudaFree(w.host_arena);
+        if (w.h2d) cudaStreamDestroy(w.h2d);
+        if (w.d2h) cudaStreamDestroy(w.d2h);
+        for (cudaEvent_t ev : w.ev)
+            if (ev) cudaEventDestroy(ev);
     }
     g_workspaces.clear();
     g_devices.clear();

@@ -351,6 +351,52 @@ inline bool make_plan(const PlanInput &in, Plan &out)
     return true;
 }
 
+// Pieces of the host-buffer entry point's pipeline: while piece p is
+// multiplied, piece p+1 of the streamed operand is copied in and the C of
+// piece p-1 copied out.  A piece is always contiguous in host memory, so
+// its copy is one 1-D copy: stacked batches split by problem; a single
+// problem streams its larger operand if that operand's pieces are
+// contiguous - A (row-major) by rows of M, B (column-major) by columns of
+// N - in at most MAX_PIECES pieces of at least PIECE_MIN (boundaries on
+// multiples of 256, a tile edge).  Otherwise, or for K == 0 or small
+// extents: one piece.
+struct HostPieces {
+    int dim = 0;         // 0 one piece, 1 batch, 2 M (rows of A and C), 3 N (columns of B and C)
+    int pieces = 1;
+    int64_t extent = 0;  // extent of the split dimension
+    int64_t bound(int i) const  // start of piece i (bound(pieces) == extent)
+    {
+        if (dim == 1) return extent * i / pieces;
+        const int64_t b = (extent * i / pieces + 255) / 256 * 256;
+        return b < extent ? b : extent;
+    }
+};
+
+inline HostPieces host_pieces(int64_t M, int64_t N, int64_t K, int64_t batch, bool a_bcast, bool b_bcast,
+                              bool a_cm, bool b_cm, bool a_stacked, bool b_stacked)
+{
+    constexpr int MAX_PIECES = 8;
+    constexpr int64_t PIECE_MIN = 512;
+    HostPieces h;
+    if (K == 0 || M == 0 || N == 0) return h;
+    if (batch > 1) {
+        if (a_bcast || b_bcast || !a_stacked || !b_stacked) return h;
+        h.dim = 1;
+        h.extent = batch;
+        h.pieces = static_cast<int>(std::min<int64_t>(batch, MAX_PIECES));
+        return h;
+    }
+    const bool by_m = M * K >= K * N;
+    if (by_m ? a_cm : !b_cm) return h;  // that operand's pieces would be strided
+    const int64_t ext = by_m ? M : N;
+    const int64_t p = std::min<int64_t>(ext / PIECE_MIN, MAX_PIECES);
+    if (p < 2) return h;
+    h.dim = by_m ? 2 : 3;
+    h.extent = ext;
+    h.pieces = static_cast<int>(p);
+    return h;
+}
+
 }  // namespace tg
 
 // Host helpers shared between the library's translation units (defined in
