@@ -138,3 +138,29 @@ def bits_u16(t: torch.Tensor) -> np.ndarray:
     if t.dtype != torch.bfloat16:
         raise TypeError("expected bf16")
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+# ------------------------------------------------------------ 8-bit operands
+FP8_DTYPES = {0: torch.float8_e4m3fn, 1: torch.float8_e5m2}  # format code -> torch dtype
+
+
+def make_fp8_codes(shape, fmt: int, seed: int, kind: str = "int") -> torch.Tensor:
+    """Seeded 8-bit floating-point codes (uint8) of format ``fmt`` (0 E4M3,
+    1 E5M2).  ``int``: integers drawn uniformly from [-16, 16] (E4M3) or
+    [-8, 8] (E5M2), every one of them exact in the format; ``finite``: codes
+    drawn uniformly among the format's finite values; ``normal``: N(0, 1)
+    draws cast to the format by PyTorch (round to nearest)."""
+    gen = torch.Generator("cpu").manual_seed(seed)
+    dt = FP8_DTYPES[fmt]
+    if kind == "int":
+        mag = 16 if fmt == 0 else 8
+        v = torch.randint(-mag, mag + 1, tuple(shape), generator=gen).to(torch.float32)
+        return v.to(dt).view(torch.uint8)
+    if kind == "finite":
+        allc = torch.arange(256, dtype=torch.uint8)
+        ok = allc[torch.isfinite(allc.view(dt).to(torch.float32))]
+        idx = torch.randint(0, ok.numel(), tuple(shape), generator=gen)
+        return ok[idx]
+    if kind == "normal":
+        return torch.randn(tuple(shape), generator=gen).to(dt).view(torch.uint8)
+    raise ValueError(kind)
