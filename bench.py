@@ -304,12 +304,23 @@ def run_gpu(args, rank, world, local, dist):
 
     peaks, peak_src = load_peaks()
     peak = float(peaks["bf16_tflops"])
+    hbm = float(peaks["hbm_gbs"])
     achieved = flops / (ms_mean * 1e-3) / 1e12  # this rank's kernel
-    roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4), "traffic": measured_traffic(w.name),
-                "peak_source": f"{peak_src} bf16_tflops (burst; kernel timed alone)",
-                "algorithmic_flops_per_launch": int(flops),
-                "hbm_frac": round(w.bytes_moved / (ms_mean * 1e-3) / 1e9 / float(peaks["hbm_gbs"]), 4)}
+    gbs = w.bytes_moved / (ms_mean * 1e-3) / 1e9
+    # the binding roofline: HBM when the workload's arithmetic intensity
+    # (algorithmic flop per algorithmic byte) is below the ridge point
+    if flops / w.bytes_moved < peak * 1e12 / (hbm * 1e9):
+        roofline = {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                    "frac": round(gbs / hbm, 4), "traffic": measured_traffic(w.name),
+                    "peak_source": f"{peak_src} hbm_gbs (copy)",
+                    "algorithmic_bytes_per_launch": int(w.bytes_moved),
+                    "tensor_frac": round(achieved / peak, 4)}
+    else:
+        roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                    "frac": round(achieved / peak, 4), "traffic": measured_traffic(w.name),
+                    "peak_source": f"{peak_src} bf16_tflops (burst; kernel timed alone)",
+                    "algorithmic_flops_per_launch": int(flops),
+                    "hbm_frac": round(gbs / hbm, 4)}
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = oracle_sample(w, seconds=args.cpu_seconds)

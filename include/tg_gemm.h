@@ -192,6 +192,29 @@ tg_status tg_gemm_fused(const void *A, const void *B, void *D,
                         int64_t batch, int64_t strideA, int64_t strideB, int64_t strideD,
                         const tg_epilogue *ep, tg_stream_t stream, const tg_options *opt);
 
+/* 8-bit floating-point operand formats (OCP FP8: E4M3 with no infinities,
+ * E5M2 with IEEE-style infinities and NaNs). */
+typedef enum { TG_FP8_E4M3 = 0, TG_FP8_E5M2 = 1 } tg_fp8_format;
+
+/* The GEMM with 8-bit floating-point A and B (a_format, b_format), fp32
+ * accumulation and the fused epilogue of tg_gemm_fused (ep may be NULL:
+ * D = A B in fp32).  Per-tensor scales of the operands go into ep->alpha.
+ * Layout: A row-major M x K (element (i,k) at A[i*lda + k], lda >= K); B
+ * column-major K x N, i.e. stored N x K (element (k,j) at B[j*ldb + k],
+ * ldb >= K) - both operands contiguous along K, the layout the tensor cores
+ * read for 8-bit types.  Strides count elements (bytes).  Requirements:
+ * A and B 16-byte aligned, lda, ldb and the batch strides multiples of 16
+ * (else TG_ERR_UNSUPPORTED); a_col_major, b_col_major and force_pack in opt
+ * must be 0 (TG_ERR_INVALID_ARG).  Otherwise as tg_gemm_fused.  (The pages
+ * define the contraction over any element type; 8-bit operands are the
+ * block-scaled family's element types without the per-block scales.) */
+tg_status tg_gemm_fp8(const void *A, const void *B, void *D,
+                      int64_t M, int64_t N, int64_t K,
+                      int64_t lda, int64_t ldb, int64_t ldd,
+                      int64_t batch, int64_t strideA, int64_t strideB, int64_t strideD,
+                      int32_t a_format, int32_t b_format,
+                      const tg_epilogue *ep, tg_stream_t stream, const tg_options *opt);
+
 /* The GEMM on HOST buffers: copies the spans of A and B that the strides
  * reach to device scratch owned by the library, runs tg_gemm_ex there into
  * a device C with 16-byte rows, and copies the M x N block of every problem

@@ -3,6 +3,7 @@
 The product is the C-ABI CUDA library declared in ``include/tg_gemm.h``.
 This package is its thin Python binding: the C functions under the same
 names (``tg_gemm``, ``tg_gemm_ex``, ``tg_gemm_host``, ``tg_gemm_splitk_static``, ``tg_plan``,
+``tg_gemm_fp8``,
 ``tg_device_error``, ``tg_status_string``, ``tg_shutdown``) taking raw
 pointers and sizes, plus conveniences that read pointers, shapes and
 strides off torch tensors.  PyTorch only provides device memory and
@@ -13,6 +14,7 @@ from __future__ import annotations
 import ctypes
 
 from ._abi import (TG_ACT_GELU_TANH, TG_ACT_NONE, TG_ACT_RELU, TG_ACT_SILU, TG_BF16, TG_ERR_CUDA,
+                   TG_FP8_E4M3, TG_FP8_E5M2,
                    TG_ERR_INVALID_ARG, TG_ERR_OOM, TG_ERR_TIMEOUT, TG_ERR_UNSUPPORTED, TG_F32, TG_OK,
                    STATUS_NAMES, library_path, load, tg_epilogue, tg_options, tg_plan_info)
 
@@ -23,6 +25,7 @@ __all__ = [
     "TG_OK", "TG_ERR_INVALID_ARG", "TG_ERR_UNSUPPORTED", "TG_ERR_CUDA", "TG_ERR_OOM",
     "TG_ERR_TIMEOUT", "TgError", "tg_options", "tg_plan_info", "load", "library_path",
     "tg_gemm", "tg_gemm_ex", "tg_gemm_host", "tg_gemm_fused", "tg_gemm_splitk_static", "tg_plan",
+    "tg_gemm_fp8", "gemm_fp8", "TG_FP8_E4M3", "TG_FP8_E5M2",
     "tg_epilogue", "gemm_fused", "ACTIVATIONS", "tg_device_error", "tg_status_string",
     "tg_shutdown", "make_options", "gemm", "gemm_host", "plan", "device_error",
 ]
@@ -63,6 +66,13 @@ def tg_gemm_splitk_static(A, B, C, M, N, K, lda, ldb, ldc, batch, strideA, strid
                           split_k, stream=None) -> int:
     return load().tg_gemm_splitk_static(A, B, C, M, N, K, lda, ldb, ldc, batch, strideA, strideB,
                                         strideC, split_k, stream)
+
+
+def tg_gemm_fp8(A, B, D, M, N, K, lda, ldb, ldd, batch, strideA, strideB, strideD, a_format,
+                b_format, ep=None, stream=None, opt=None) -> int:
+    return load().tg_gemm_fp8(A, B, D, M, N, K, lda, ldb, ldd, batch, strideA, strideB, strideD,
+                              a_format, b_format, ctypes.byref(ep) if ep is not None else None, stream,
+                              ctypes.byref(opt) if opt is not None else None)
 
 
 def tg_plan(A, B, C, M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC, sm_count=0,
@@ -233,6 +243,71 @@ def gemm_fused(A, B, D=None, *, bias=None, residual=None, alpha: float = 1.0, be
                        _stream_ptr(stream), options)
     if st != TG_OK:
         raise TgError(st, "tg_gemm_fused")
+    return D
+
+
+def _fp8_format(t, what):
+    import torch
+
+    if t.dtype == torch.float8_e4m3fn:
+        return TG_FP8_E4M3
+    if t.dtype == torch.float8_e5m2:
+        return TG_FP8_E5M2
+    raise TypeError(f"{what} must be float8_e4m3fn or float8_e5m2")
+
+
+def gemm_fp8(A, Bt, D=None, *, scale: float = 1.0, bias=None, residual=None, beta: float = 1.0,
+             activation: str = "none", out_dtype=None, options: tg_options | None = None,
+             stream=None):
+    """D = act(scale * (A @ Bt^T) + bias) + beta * residual with 8-bit
+    floating-point A [.., M, K] and Bt [.., N, K] (B column-major), both
+    contiguous along K; scale carries the operands' per-tensor scales."""
+    import torch
+
+    fa, fb = _fp8_format(A, "A"), _fp8_format(Bt, "Bt")
+    if not (A.is_cuda and Bt.is_cuda):
+        raise ValueError("A and Bt must be CUDA tensors")
+    pa, M, K, lda, ba, sA = _operand_geometry(A, -2, "A")
+    pb, N, K2, ldb, bb, sB = _operand_geometry(Bt, -2, "Bt")
+    if K2 != K:
+        raise ValueError(f"inner dimensions differ: {K} vs {K2}")
+    batch = max(ba, bb)
+    if ba == 1:
+        sA = 0
+    if bb == 1:
+        sB = 0
+    if D is None:
+        dt = out_dtype if out_dtype is not None else torch.float32
+        shape = (batch, M, N) if (A.dim() == 3 or Bt.dim() == 3) else (M, N)
+        D = torch.empty(shape, dtype=dt, device=A.device)
+    if D.dtype not in (torch.float32, torch.bfloat16) or not D.is_cuda:
+        raise TypeError("D must be an fp32 or bf16 CUDA tensor")
+    pd, Md, Nd, ldd, bd, sD = _operand_geometry(D, -2, "D")
+    if (Md, Nd) != (M, N) or bd != batch:
+        raise ValueError("D has the wrong shape")
+    ep = tg_epilogue()
+    ep.alpha = float(scale)
+    ep.beta = float(beta)
+    ep.activation = ACTIVATIONS[activation]
+    ep.out_type = TG_BF16 if D.dtype == torch.bfloat16 else TG_F32
+    if bias is not None:
+        if bias.dtype != torch.float32 or not bias.is_cuda or bias.stride(-1) != 1:
+            raise TypeError("bias must be a contiguous fp32 CUDA tensor")
+        ep.bias = bias.data_ptr()
+        ep.bias_stride = bias.stride(0) if bias.dim() == 2 and bias.shape[0] > 1 else 0
+    if residual is not None:
+        if residual.dtype != D.dtype or not residual.is_cuda:
+            raise TypeError("residual must have D's dtype and live on the GPU")
+        pr, Mr, Nr, ldr, br, sR = _operand_geometry(residual, -2, "residual")
+        if (Mr, Nr) != (M, N) or br not in (1, batch):
+            raise ValueError("residual has the wrong shape")
+        ep.residual = pr
+        ep.ldr = ldr
+        ep.strideR = sR if br > 1 else 0
+    st = tg_gemm_fp8(pa, pb, pd, M, N, K, lda, ldb, ldd, batch, sA, sB, sD, fa, fb, ep,
+                     _stream_ptr(stream), options)
+    if st != TG_OK:
+        raise TgError(st, "tg_gemm_fp8")
     return D
 
 

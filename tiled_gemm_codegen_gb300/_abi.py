@@ -93,6 +93,7 @@ class tg_epilogue(ctypes.Structure):
 
 TG_ACT_NONE, TG_ACT_RELU, TG_ACT_GELU_TANH, TG_ACT_SILU = 0, 1, 2, 3
 TG_F32, TG_BF16 = 0, 1
+TG_FP8_E4M3, TG_FP8_E5M2 = 0, 1
 
 _i64 = ctypes.c_int64
 _vp = ctypes.c_void_p
@@ -107,6 +108,9 @@ SIGNATURES = {
     "tg_gemm_fused": ([_vp, _vp, _vp] + [_i64] * 10 + [ctypes.POINTER(tg_epilogue), _vp,
                                                          ctypes.POINTER(tg_options)], ctypes.c_int),
     "tg_gemm_splitk_static": ([_vp, _vp, _vp] + [_i64] * 10 + [ctypes.c_int32, _vp], ctypes.c_int),
+    "tg_gemm_fp8": ([_vp, _vp, _vp] + [_i64] * 10 + [ctypes.c_int32, ctypes.c_int32,
+                                                       ctypes.POINTER(tg_epilogue), _vp,
+                                                       ctypes.POINTER(tg_options)], ctypes.c_int),
     "tg_device_error": ([_vp], ctypes.c_int),
     "tg_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "tg_shutdown": ([], None),

@@ -133,6 +133,8 @@ struct Args {
     void *C;  // C (fp32), or D of the fused epilogue (fp32 or bf16)
     int64_t M, N, K, lda, ldb, ldc, batch, sA, sB, sC;
     int64_t c_bytes = 4;  // element size of C
+    int64_t ab_bytes = 2; // element size of A and B (1: 8-bit floating point)
+    uint32_t mma_fmt = 0; // 8-bit operands: instruction-descriptor format fields
     bool a_cm = false;    // A stored K x M (column-major)
     bool b_cm = false;    // B stored N x K (column-major)
     // stored (rows, columns) of A and B
@@ -205,10 +207,12 @@ tg_status validate(const Args &a)
             c0 + static_cast<uintptr_t>(a.c_bytes) * static_cast<uintptr_t>(span_elems(a.M, a.N, a.ldc, a.batch, a.sC));
         const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.A);
         const uintptr_t a1 =
-            a0 + 2u * static_cast<uintptr_t>(span_elems(a.a_rows(), a.a_cols(), a.lda, a.batch, a.sA));
+            a0 + static_cast<uintptr_t>(a.ab_bytes) *
+                     static_cast<uintptr_t>(span_elems(a.a_rows(), a.a_cols(), a.lda, a.batch, a.sA));
         const uintptr_t b0 = reinterpret_cast<uintptr_t>(a.B);
         const uintptr_t b1 =
-            b0 + 2u * static_cast<uintptr_t>(span_elems(a.b_rows(), a.b_cols(), a.ldb, a.batch, a.sB));
+            b0 + static_cast<uintptr_t>(a.ab_bytes) *
+                     static_cast<uintptr_t>(span_elems(a.b_rows(), a.b_cols(), a.ldb, a.batch, a.sB));
         if (ranges_overlap(c0, c1, a0, a1) || ranges_overlap(c0, c1, b0, b1))
             return TG_ERR_INVALID_ARG;
     }
@@ -228,8 +232,10 @@ PlanInput plan_input(const Args &a, int sms, const tg_options *opt)
     in.b_bcast = a.batch > 1 && a.sB == 0;
     const bool batched_a = a.batch > 1 && !in.a_bcast;
     const bool batched_b = a.batch > 1 && !in.b_bcast;
-    in.a_tma_ok = aligned16(a.A) && (a.lda * 2) % 16 == 0 && (!batched_a || (a.sA * 2) % 16 == 0);
-    in.b_tma_ok = aligned16(a.B) && (a.ldb * 2) % 16 == 0 && (!batched_b || (a.sB * 2) % 16 == 0);
+    const int64_t eb = a.ab_bytes;
+    in.a_tma_ok = aligned16(a.A) && (a.lda * eb) % 16 == 0 && (!batched_a || (a.sA * eb) % 16 == 0);
+    in.b_tma_ok = aligned16(a.B) && (a.ldb * eb) % 16 == 0 && (!batched_b || (a.sB * eb) % 16 == 0);
+    in.f8 = a.ab_bytes == 1;
     in.c_tma_ok = aligned16(a.C) && (a.ldc * a.c_bytes) % 16 == 0 &&
                   (a.batch == 1 || (a.sC * a.c_bytes) % 16 == 0);
     in.sm_count = sms;
@@ -256,7 +262,7 @@ void fill_info(const Plan &p, tg_plan_info *out)
     out->stream_k = p.stream_k ? 2 : 1;
     out->sk_tiles = static_cast<int32_t>(p.sk_tiles);
     out->block_n = p.bn;
-    out->block_k = BK;
+    out->block_k = p.f8 ? 2 * BK : BK;
     out->stages = p.stages;
     out->tiles_m = p.tiles_m;
     out->tiles_n = p.tiles_n;
@@ -451,30 +457,30 @@ uint64_t single_problem_stride(uint64_t rows, uint64_t stride1)
     return (s + 15) / 16 * 16;
 }
 
-cudaError_t launch_gemm(int bn, bool pair, const CUtensorMap &ta, const CUtensorMap &tb,
+cudaError_t launch_gemm(int bn, bool pair, bool f8, const CUtensorMap &ta, const CUtensorMap &tb,
                         const CUtensorMap &tc, const KernelParams &p, int stages, int grid,
                         cudaStream_t s)
 {
     switch (bn) {
-        case 64: return launch_gemm_bn64(ta, tb, tc, p, stages, pair, grid, s);
-        case 128: return launch_gemm_bn128(ta, tb, tc, p, stages, pair, grid, s);
-        case 192: return launch_gemm_bn192(ta, tb, tc, p, stages, pair, grid, s);
-        case 256: return launch_gemm_bn256(ta, tb, tc, p, stages, pair, grid, s);
+        case 64: return launch_gemm_bn64(ta, tb, tc, p, stages, pair, f8, grid, s);
+        case 128: return launch_gemm_bn128(ta, tb, tc, p, stages, pair, f8, grid, s);
+        case 192: return launch_gemm_bn192(ta, tb, tc, p, stages, pair, f8, grid, s);
+        case 256: return launch_gemm_bn256(ta, tb, tc, p, stages, pair, f8, grid, s);
         default: return cudaErrorInvalidValue;
     }
 }
 
 // Co-resident two-CTA clusters of a pair configuration, cached per device.
-int max_pairs(int dev, int bn, int stages)
+int max_pairs(int dev, int bn, int stages, bool f8)
 {
-    static std::map<std::tuple<int, int, int>, int> cache;
-    const auto key = std::make_tuple(dev, bn, stages);
+    static std::map<std::tuple<int, int, int, bool>, int> cache;
+    const auto key = std::make_tuple(dev, bn, stages, f8);
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
     int n = 0;
     switch (bn) {
-        case 128: n = max_pairs_bn128(stages); break;
-        case 256: n = max_pairs_bn256(stages); break;
+        case 128: n = max_pairs_bn128(stages, f8); break;
+        case 256: n = max_pairs_bn256(stages, f8); break;
         default: n = 0;
     }
     cache[key] = n;
@@ -591,20 +597,26 @@ tg_status run_gemm(const Args &a, cudaStream_t stream, const tg_options *opt,
     // Row-major A: boxes [128 rows x 64 k]; column-major A: [64 k x 64 rows].
     // Row-major B: [64 k x 64 columns]; column-major B: [B columns x 64 k].
     const uint32_t b_cols_cta = static_cast<uint32_t>(plan.pair ? plan.bn / 2 : plan.bn);
+    // Element type and the K extent of a 128-byte box row: 64 bf16 or 128
+    // 8-bit elements (8-bit operands are K-major: row-major A, column-major B).
+    const int64_t eb = a.ab_bytes;
+    const CUtensorMapDataType dt = eb == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const uint32_t kbox = static_cast<uint32_t>(128 / eb);
     auto encode_a = [&]() {
         const uint64_t z = in.a_bcast || a.batch == 1 ? 1 : static_cast<uint64_t>(a.batch);
-        const uint64_t s2 = z == 1 ? single_problem_stride(a.a_rows(), lda * 2) : static_cast<uint64_t>(sA) * 2;
-        if (a.a_cm) return encode_3d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, a.M, a.K, z, lda * 2, s2, 64, BK);
-        return encode_3d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, a.K, a.M, z, lda * 2, s2, BK, BM);
+        const uint64_t s2 = z == 1 ? single_problem_stride(a.a_rows(), lda * eb) : static_cast<uint64_t>(sA) * eb;
+        if (a.a_cm) return encode_3d(&ta, dt, A, a.M, a.K, z, lda * eb, s2, 64, BK);
+        return encode_3d(&ta, dt, A, a.K, a.M, z, lda * eb, s2, kbox, BM);
     };
     auto encode_b = [&]() {
         const uint64_t z = in.b_bcast || a.batch == 1 ? 1 : static_cast<uint64_t>(a.batch);
-        const uint64_t s2 = z == 1 ? single_problem_stride(a.b_rows(), ldb * 2) : static_cast<uint64_t>(sB) * 2;
-        if (a.b_cm)
-            return encode_3d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, a.K, a.N, z, ldb * 2, s2, BK, b_cols_cta);
-        return encode_3d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, a.N, a.K, z, ldb * 2, s2, 64, BK);
+        const uint64_t s2 = z == 1 ? single_problem_stride(a.b_rows(), ldb * eb) : static_cast<uint64_t>(sB) * eb;
+        if (a.b_cm) return encode_3d(&tb, dt, B, a.K, a.N, z, ldb * eb, s2, kbox, b_cols_cta);
+        return encode_3d(&tb, dt, B, a.N, a.K, z, ldb * eb, s2, 64, BK);
     };
     if (!encode_fn()) return TG_ERR_CUDA;
+    // 8-bit operands are never packed (the entry point requires 16-byte rows)
+    if (plan.f8 && (plan.pack_a || plan.pack_b || !encode_a() || !encode_b())) return TG_ERR_UNSUPPORTED;
     if (!plan.pack_a && !encode_a()) {
         plan.pack_a = true;
         plan.ws_pack_a = round_up((in.a_bcast ? 1 : a.batch) * a.a_rows() * round_up(a.a_cols(), 8) * 2, 256);
@@ -618,7 +630,7 @@ tg_status run_gemm(const Args &a, cudaStream_t stream, const tg_options *opt,
     // clusters than can be resident at once; the stream-K ranges follow it.
     int grid = plan.grid;
     if (plan.pair) {
-        const int pairs = max_pairs(dev, plan.bn, plan.stages);
+        const int pairs = max_pairs(dev, plan.bn, plan.stages, plan.f8);
         if (pairs <= 0) return TG_ERR_UNSUPPORTED;
         if (grid > 2 * pairs) grid = 2 * pairs;
         if (trace_enabled())
@@ -720,7 +732,8 @@ tg_status run_gemm(const Args &a, cudaStream_t stream, const tg_options *opt,
                      plan.stream_k ? 1 : 0, plan.dp_waves, (long long)plan.sk_tiles, plan.maxparts,
                      (long long)plan.units, plan.grid, plan.pack_a, plan.pack_b, plan.epilogue);
 
-    e = launch_gemm(plan.bn, plan.pair, ta, tb, tc, p, plan.stages, grid, stream);
+    p.mma_fmt = a.mma_fmt;
+    e = launch_gemm(plan.bn, plan.pair, plan.f8, ta, tb, tc, p, plan.stages, grid, stream);
     return cuda_status(e);
 }
 
@@ -761,7 +774,7 @@ cudaError_t shared_launch_gemm(int bn, const CUtensorMap &ta, const CUtensorMap 
                                const CUtensorMap &tc, const KernelParams &p, int stages, int grid,
                                cudaStream_t s)
 {
-    return launch_gemm(bn, false, ta, tb, tc, p, stages, grid, s);
+    return launch_gemm(bn, false, false, ta, tb, tc, p, stages, grid, s);
 }
 
 cudaError_t shared_zero_fill(float *C, int64_t M, int64_t N, int64_t ldc, int64_t sC, int64_t batch,
@@ -814,37 +827,87 @@ TG_API tg_status tg_gemm(const void *A, const void *B, float *C, int64_t M, int6
                       nullptr);
 }
 
+namespace tg {
+namespace {
+
+// The fused-epilogue arguments against a validated call.
+tg_status check_epilogue(const Args &a, const tg_epilogue *ep)
+{
+    if (ep->activation < TG_ACT_NONE || ep->activation > TG_ACT_SILU) return TG_ERR_INVALID_ARG;
+    if (ep->bias_stride < 0) return TG_ERR_INVALID_ARG;
+    if (ep->residual) {
+        if (ep->ldr < a.N || ep->strideR < 0) return TG_ERR_INVALID_ARG;
+        if (a.batch > 1 && ep->strideR < (a.M - 1) * ep->ldr + a.N && ep->strideR != 0) return TG_ERR_INVALID_ARG;
+        const bool same = ep->residual == a.C && ep->ldr == a.ldc && ep->strideR == a.sC;
+        if (!same) {
+            const uintptr_t d0 = reinterpret_cast<uintptr_t>(a.C);
+            const uintptr_t d1 = d0 + a.c_bytes * static_cast<uintptr_t>(span_elems(a.M, a.N, a.ldc, a.batch, a.sC));
+            const uintptr_t r0 = reinterpret_cast<uintptr_t>(ep->residual);
+            const uintptr_t r1 =
+                r0 + a.c_bytes * static_cast<uintptr_t>(span_elems(a.M, a.N, ep->ldr, a.batch, ep->strideR));
+            if (ranges_overlap(d0, d1, r0, r1)) return TG_ERR_INVALID_ARG;
+        }
+    }
+    return TG_OK;
+}
+
+}  // namespace
+}  // namespace tg
+
 TG_API tg_status tg_gemm_fused(const void *A, const void *B, void *D, int64_t M, int64_t N,
                                int64_t K, int64_t lda, int64_t ldb, int64_t ldd, int64_t batch,
                                int64_t strideA, int64_t strideB, int64_t strideD, const tg_epilogue *ep,
                                tg_stream_t stream, const tg_options *opt)
 {
+    using namespace tg;
     if (!ep) return TG_ERR_INVALID_ARG;
-    if (ep->activation < TG_ACT_NONE || ep->activation > TG_ACT_SILU) return TG_ERR_INVALID_ARG;
     if (ep->out_type != TG_F32 && ep->out_type != TG_BF16) return TG_ERR_INVALID_ARG;
     Args a = with_layout(Args{A, B, D, M, N, K, lda, ldb, ldd, batch, strideA, strideB, strideD}, opt);
     a.c_bytes = ep->out_type == TG_BF16 ? 2 : 4;
     tg_status st = validate(a);
     if (st != TG_OK) return st;
     if (M == 0 || N == 0) return TG_OK;
-    if (ep->bias_stride < 0) return TG_ERR_INVALID_ARG;
-    if (ep->residual) {
-        if (ep->ldr < N || ep->strideR < 0) return TG_ERR_INVALID_ARG;
-        if (batch > 1 && ep->strideR < (M - 1) * ep->ldr + N && ep->strideR != 0) return TG_ERR_INVALID_ARG;
-        const bool same = ep->residual == D && ep->ldr == ldd && ep->strideR == strideD;
-        if (!same) {
-            const uintptr_t d0 = reinterpret_cast<uintptr_t>(D);
-            const uintptr_t d1 = d0 + a.c_bytes * static_cast<uintptr_t>(span_elems(M, N, ldd, batch, strideD));
-            const uintptr_t r0 = reinterpret_cast<uintptr_t>(ep->residual);
-            const uintptr_t r1 =
-                r0 + a.c_bytes * static_cast<uintptr_t>(span_elems(M, N, ep->ldr, batch, ep->strideR));
-            if (ranges_overlap(d0, d1, r0, r1)) return TG_ERR_INVALID_ARG;
-        }
-    }
+    if ((st = check_epilogue(a, ep)) != TG_OK) return st;
     if (opt) {
         PlanInput in = plan_input(a, 148, opt);
         Plan pl;
         if (K > 0 && !make_plan(in, pl)) return TG_ERR_INVALID_ARG;
+    }
+    return run_gemm(a, reinterpret_cast<cudaStream_t>(stream), opt, ep);
+}
+
+TG_API tg_status tg_gemm_fp8(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K,
+                             int64_t lda, int64_t ldb, int64_t ldd, int64_t batch, int64_t strideA,
+                             int64_t strideB, int64_t strideD, int32_t a_format, int32_t b_format,
+                             const tg_epilogue *ep, tg_stream_t stream, const tg_options *opt)
+{
+    using namespace tg;
+    if (a_format != TG_FP8_E4M3 && a_format != TG_FP8_E5M2) return TG_ERR_INVALID_ARG;
+    if (b_format != TG_FP8_E4M3 && b_format != TG_FP8_E5M2) return TG_ERR_INVALID_ARG;
+    if (opt && (opt->a_col_major || opt->b_col_major || opt->force_pack)) return TG_ERR_INVALID_ARG;
+    if (ep && ep->out_type != TG_F32 && ep->out_type != TG_BF16) return TG_ERR_INVALID_ARG;
+    // A row-major M x K, B stored N x K (column-major K x N): both K-major
+    Args a{A, B, D, M, N, K, lda, ldb, ldd, batch, strideA, strideB, strideD};
+    a.b_cm = true;
+    a.ab_bytes = 1;
+    a.c_bytes = ep && ep->out_type == TG_BF16 ? 2 : 4;
+    // kind::f8f6f4 operand formats: E4M3 = 0, E5M2 = 1 (bits 7-9 A, 10-12 B)
+    a.mma_fmt = (static_cast<uint32_t>(a_format) << 7) | (static_cast<uint32_t>(b_format) << 10);
+    tg_status st = validate(a);
+    if (st != TG_OK) return st;
+    if (M == 0 || N == 0) return TG_OK;
+    if (ep && (st = check_epilogue(a, ep)) != TG_OK) return st;
+    if (K > 0) {
+        // 16-byte rows: the TMA unit loads the operands as they are
+        const bool batched_a = batch > 1 && strideA != 0, batched_b = batch > 1 && strideB != 0;
+        if ((reinterpret_cast<uintptr_t>(A) & 15u) || (reinterpret_cast<uintptr_t>(B) & 15u) || lda % 16 ||
+            ldb % 16 || (batched_a && strideA % 16) || (batched_b && strideB % 16))
+            return TG_ERR_UNSUPPORTED;
+        if (opt) {
+            PlanInput in = plan_input(a, 148, opt);
+            Plan pl;
+            if (!make_plan(in, pl)) return TG_ERR_INVALID_ARG;
+        }
     }
     return run_gemm(a, reinterpret_cast<cudaStream_t>(stream), opt, ep);
 }

@@ -64,6 +64,7 @@ struct KernelParams {
     int32_t maxparts;
     int64_t sk_iters;
     unsigned long long *trace;  // grid x 8 timestamps, or null
+    uint32_t mma_fmt;           // 8-bit operands: A format << 7 | B format << 10
 };
 
 // Shared-memory budget of one tile width.  PAIR: the tile is computed by a
@@ -93,12 +94,13 @@ struct Geometry {
 
 // Launch of the persistent GEMM kernel for one tile width (defined in the
 // per-width translation units).  pair: two-SM tiles (grid counts CTAs, a
-// multiple of 2).  Returns the launch's cudaError_t.
+// multiple of 2); f8: 8-bit floating-point operands.  Returns the launch's
+// cudaError_t.
 #define TG_DECLARE_LAUNCH(BN_)                                                                   \
     cudaError_t launch_gemm_bn##BN_(const CUtensorMap &ta, const CUtensorMap &tb,                \
                                     const CUtensorMap &tc, const KernelParams &p, int stages,   \
-                                    bool pair, int grid, cudaStream_t s);                       \
-    int max_pairs_bn##BN_(int stages);
+                                    bool pair, bool f8, int grid, cudaStream_t s);              \
+    int max_pairs_bn##BN_(int stages, bool f8);
 TG_DECLARE_LAUNCH(64)
 TG_DECLARE_LAUNCH(128)
 TG_DECLARE_LAUNCH(192)

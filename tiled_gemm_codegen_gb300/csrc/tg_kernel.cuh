@@ -318,7 +318,10 @@ __device__ __forceinline__ void apply_epilogue(const KernelParams &p, uint32_t (
     }
 }
 
-template <int BN, int STAGES, bool PAIR>
+// F8: 8-bit floating-point operands (tcgen05 kind::f8f6f4, formats in
+// p.mma_fmt), K-major A and B only; a k-block is then 128 elements (still
+// 128 bytes a row) and each of its 4 MMAs takes K = 32.
+template <int BN, int STAGES, bool PAIR, bool F8 = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const KernelParams p)
@@ -332,6 +335,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     constexpr uint32_t B_BOX_BYTES = BK * 64 * 2;  // one 64-column box of B: 8 KB
     constexpr uint32_t EPI_BOX_BYTES = EPI_CHUNK * EPI_CHUNK * 4;  // 4 KB
     constexpr uint32_t EPI_WARPS_TOTAL = PAIR ? 8 : 4;  // arrivals on tempty per tile
+    constexpr int KBLK = F8 ? 2 * BK : BK;              // elements of K per k-block (128 bytes)
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
@@ -452,20 +456,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t b_dst = sB + s * G::B_STAGE;
                     if (!p.a_mn) {
                         // A row-major: one box [128 rows x 64 k], K-major atoms
-                        load(a_dst, &tmA, kb * BK, m_rows, zA);
+                        load(a_dst, &tmA, kb * KBLK, m_rows, zA);
                     } else {
                         // A column-major: two boxes [64 k x 64 rows], MN-major atoms
-                        load(a_dst, &tmA, m_rows, kb * BK, zA);
-                        load(a_dst + B_BOX_BYTES, &tmA, m_rows + 64, kb * BK, zA);
+                        load(a_dst, &tmA, m_rows, kb * KBLK, zA);
+                        load(a_dst + B_BOX_BYTES, &tmA, m_rows + 64, kb * KBLK, zA);
                     }
                     if (!p.b_k) {
                         // B row-major: boxes [64 k x 64 columns], MN-major atoms
 #pragma unroll
                         for (int j = 0; j < B_BOXES; ++j)
-                            load(b_dst + j * B_BOX_BYTES, &tmB, n_cols + 64 * j, kb * BK, zB);
+                            load(b_dst + j * B_BOX_BYTES, &tmB, n_cols + 64 * j, kb * KBLK, zB);
                     } else {
                         // B column-major: one box [B_COLS columns x 64 k], K-major atoms
-                        load(b_dst, &tmB, kb * BK, n_cols, zB);
+                        load(b_dst, &tmB, kb * KBLK, n_cols, zB);
                     }
                 }
             }
@@ -480,7 +484,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else if (warp == 1) {
         if (lane == 0 && (!PAIR || leader)) {
             // ------------------------------------------------ MMA issuer
-            const uint32_t idesc = instr_desc_bf16<TILE_M, BN>(p.a_mn != 0, p.b_k == 0);
+            // kind::f8f6f4 keeps the layout of the descriptor; only the A and
+            // B format fields (bits 7-12) differ
+            const uint32_t idesc_bf16 = instr_desc_bf16<TILE_M, BN>(p.a_mn != 0, p.b_k == 0);
+            const uint32_t idesc = F8 ? ((idesc_bf16 & ~(0x3Fu << 7)) | p.mma_fmt) : idesc_bf16;
             // Layout-dependent descriptor parts, fixed for the whole kernel:
             // a K-major operand steps 32 B per 16 k (leading offset unused);
             // an MN-major one steps 16 rows x 128 B and its 64-element atoms
@@ -523,8 +530,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const uint64_t ad = a_desc0 | (((a_addr + kk * a_step) >> 4) & 0x3FFFu);
                         const uint64_t bd = b_desc0 | (((b_addr + kk * b_step) >> 4) & 0x3FFFu);
                         const uint32_t acc = (kb > w.kb0 || kk > 0) ? 1u : 0u;
-                        if constexpr (PAIR)
+                        if constexpr (PAIR && F8)
+                            ptx::mma_f8_pair(d_tmem, ad, bd, idesc, acc);
+                        else if constexpr (PAIR)
                             ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, acc);
+                        else if constexpr (F8)
+                            ptx::mma_f8(d_tmem, ad, bd, idesc, acc);
                         else
                             ptx::mma_bf16(d_tmem, ad, bd, idesc, acc);
                     }
@@ -823,12 +834,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (threadIdx.x == 0) stamp(7);
 }
 
-template <int BN, int STAGES, bool PAIR>
+template <int BN, int STAGES, bool PAIR, bool F8 = false>
 cudaError_t launch_fixed(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
                          const KernelParams &p, int grid, cudaStream_t s)
 {
     constexpr int smem = Geometry<BN, PAIR>::smem_bytes(STAGES);
-    auto kern = gemm_kernel<BN, STAGES, PAIR>;
+    auto kern = gemm_kernel<BN, STAGES, PAIR, F8>;
     // the shared-memory opt-in is per device; set it once per device
     static std::atomic<unsigned long long> configured{0};
     int dev = 0;
@@ -862,11 +873,11 @@ cudaError_t launch_fixed(const CUtensorMap &ta, const CUtensorMap &tb, const CUt
 
 // Largest number of two-CTA clusters of this configuration that can be
 // resident at once (0 if the query fails).
-template <int BN, int STAGES>
+template <int BN, int STAGES, bool F8 = false>
 int max_active_pairs()
 {
     constexpr int smem = Geometry<BN, true>::smem_bytes(STAGES);
-    auto kern = gemm_kernel<BN, STAGES, true>;
+    auto kern = gemm_kernel<BN, STAGES, true, F8>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg{};

@@ -1,8 +1,9 @@
 // Instantiations of the persistent GEMM kernel: one translation unit per tile
 // width (selected at build time with -DTG_BN=...), so the widths compile in
 // parallel.  Each width instantiates a few ring depths, with one CTA per tile
-// and (widths 128 and 256) two-SM tiles; stage_supported() in tg_plan.h lists
-// them and the host planner only picks listed configurations.
+// and (widths 128 and 256) two-SM tiles, for bf16 operands and (a subset)
+// 8-bit floating-point ones; stage_supported() in tg_plan.h lists them and
+// the host planner only picks listed configurations.
 #include "tg_kernel.cuh"
 #include "tg_plan.h"
 
@@ -12,62 +13,61 @@
 
 namespace tg {
 
-#define TG_CASE(S)                                                             \
-    case S:                                                                    \
-        if constexpr (stage_supported(TG_BN, S, false))                        \
-            return launch_fixed<TG_BN, S, false>(ta, tb, tc, p, grid, s);      \
-        else                                                                   \
+#define TG_CASE(S, PAIR, F8)                                                        \
+    case S:                                                                         \
+        if constexpr ((!PAIR || pair_width(TG_BN)) && stage_supported(TG_BN, S, PAIR, F8)) \
+            return launch_fixed<TG_BN, S, PAIR, F8>(ta, tb, tc, p, grid, s);        \
+        else                                                                        \
             return cudaErrorInvalidValue;
 
-#define TG_CASE_PAIR(S)                                                        \
-    case S:                                                                    \
-        if constexpr (pair_width(TG_BN) && stage_supported(TG_BN, S, true))    \
-            return launch_fixed<TG_BN, S, true>(ta, tb, tc, p, grid, s);       \
-        else                                                                   \
-            return cudaErrorInvalidValue;
-
-#define TG_CASE_PAIRS(S)                                                       \
-    case S:                                                                    \
-        if constexpr (pair_width(TG_BN) && stage_supported(TG_BN, S, true))    \
-            return max_active_pairs<TG_BN, S>();                               \
-        else                                                                   \
+#define TG_CASE_PAIRS(S, F8)                                                        \
+    case S:                                                                         \
+        if constexpr (pair_width(TG_BN) && stage_supported(TG_BN, S, true, F8))     \
+            return max_active_pairs<TG_BN, S, F8>();                                \
+        else                                                                        \
             return 0;
 
 #define TG_CAT2(a, b) a##b
 #define TG_CAT(a, b) TG_CAT2(a, b)
 
+#define TG_SWITCH(PAIR, F8)                                                         \
+    switch (stages) {                                                               \
+        TG_CASE(2, PAIR, F8)                                                        \
+        TG_CASE(3, PAIR, F8)                                                        \
+        TG_CASE(4, PAIR, F8)                                                        \
+        TG_CASE(6, PAIR, F8)                                                        \
+        TG_CASE(8, PAIR, F8)                                                        \
+        default:                                                                    \
+            return cudaErrorInvalidValue;                                           \
+    }
+
 cudaError_t TG_CAT(launch_gemm_bn, TG_BN)(const CUtensorMap &ta, const CUtensorMap &tb,
                                           const CUtensorMap &tc, const KernelParams &p,
-                                          int stages, bool pair, int grid, cudaStream_t s)
+                                          int stages, bool pair, bool f8, int grid, cudaStream_t s)
 {
-    if (pair) {
+    if (pair && f8) TG_SWITCH(true, true)
+    if (pair) TG_SWITCH(true, false)
+    if (f8) TG_SWITCH(false, true)
+    TG_SWITCH(false, false)
+}
+
+int TG_CAT(max_pairs_bn, TG_BN)(int stages, bool f8)
+{
+    if (f8) {
         switch (stages) {
-            TG_CASE_PAIR(2)
-            TG_CASE_PAIR(4)
-            TG_CASE_PAIR(6)
-            TG_CASE_PAIR(8)
+            TG_CASE_PAIRS(2, true)
+            TG_CASE_PAIRS(4, true)
+            TG_CASE_PAIRS(6, true)
+            TG_CASE_PAIRS(8, true)
             default:
-                return cudaErrorInvalidValue;
+                return 0;
         }
     }
     switch (stages) {
-        TG_CASE(2)
-        TG_CASE(3)
-        TG_CASE(4)
-        TG_CASE(6)
-        TG_CASE(8)
-        default:
-            return cudaErrorInvalidValue;
-    }
-}
-
-int TG_CAT(max_pairs_bn, TG_BN)(int stages)
-{
-    switch (stages) {
-        TG_CASE_PAIRS(2)
-        TG_CASE_PAIRS(4)
-        TG_CASE_PAIRS(6)
-        TG_CASE_PAIRS(8)
+        TG_CASE_PAIRS(2, false)
+        TG_CASE_PAIRS(4, false)
+        TG_CASE_PAIRS(6, false)
+        TG_CASE_PAIRS(8, false)
         default:
             return 0;
     }

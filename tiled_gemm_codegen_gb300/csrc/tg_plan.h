@@ -22,8 +22,14 @@ namespace tg {
 constexpr bool pair_width(int bn) { return bn == 128 || bn == 256; }
 
 // Ring depths instantiated for each tile width (kept small for build time).
-constexpr bool stage_supported(int bn, int s, bool pair = false)
+// 8-bit operands (f8): two-SM tiles of width 256 and one-CTA tiles of widths
+// 128 and 256 only.
+constexpr bool stage_supported(int bn, int s, bool pair = false, bool f8 = false)
 {
+    if (f8) {
+        if (pair) return bn == 256 && (s == 2 || s == 4 || s == 6);
+        return (bn == 128 && (s == 2 || s == 4 || s == 6)) || (bn == 256 && (s == 2 || s == 4));
+    }
     if (pair) {
         switch (bn) {
             case 128: return s == 2 || s == 4 || s == 8;
@@ -94,10 +100,12 @@ struct PlanInput {
     int cta_pair;  // 0 = choose, 1 = one CTA per tile, 2 = two-SM tiles
     int stream_k;  // 0 = choose, 1 = off, 2 = on (when the last wave is partial)
     bool a_cm = false, b_cm = false;  // column-major (transposed) operand storage
+    bool f8 = false;                  // 8-bit floating-point A and B (K-major)
 };
 
 struct Plan {
     bool pair = false;  // two-SM tiles (256 rows, cluster of 2)
+    bool f8 = false;    // 8-bit operands: 128 elements of K per k-block
     int bn = 0, stages = 0;
     int tiles_m = 0, tiles_n = 0, k_blocks = 0, splits = 1;
     int64_t units = 0;
@@ -239,8 +247,10 @@ inline void replan_stream_k(const PlanInput &in, Plan &p, int grid)
 inline bool make_plan(const PlanInput &in, Plan &out)
 {
     Plan p;
+    p.f8 = in.f8;
     const int sms = in.sm_count > 0 ? in.sm_count : 1;
-    const int64_t kb = ceil_div(in.K, BK);
+    const int64_t kb = ceil_div(in.K, in.f8 ? 2 * BK : BK);  // a k-block is 128 bytes of K
+    if (in.f8 && (in.a_cm || !in.b_cm || in.force_pack || !in.a_tma_ok || !in.b_tma_ok)) return false;
     if (kb > INT32_MAX) return false;
     p.k_blocks = static_cast<int>(kb);
 
@@ -267,6 +277,7 @@ inline bool make_plan(const PlanInput &in, Plan &out)
         if (in.cta_pair == 1 && cd.pair) continue;
         if (in.cta_pair == 2 && !cd.pair) continue;
         if (in.cta_pair == 0 && cd.pair && !PAIR_BY_DEFAULT) continue;
+        if (in.f8 && !stage_supported(cd.bn, 2, cd.pair, true)) continue;  // no 8-bit instance
         const int tile_m = cd.pair ? 2 * BM : BM;
         const int64_t tiles_m = ceil_div(in.M, tile_m);
         const int64_t tiles_n = ceil_div(in.N, cd.bn);
@@ -303,10 +314,11 @@ inline bool make_plan(const PlanInput &in, Plan &out)
 
     // Ring depth: the deepest instantiated one unless overridden.
     if (in.stages != 0) {
-        if (!stage_supported(p.bn, in.stages, p.pair)) return false;
+        if (!stage_supported(p.bn, in.stages, p.pair, in.f8)) return false;
         p.stages = in.stages;
     } else {
         p.stages = max_stages(p.bn, p.pair);
+        while (in.f8 && p.stages > 2 && !stage_supported(p.bn, p.stages, p.pair, true)) --p.stages;
     }
     p.units = in.batch * p.tiles_m * static_cast<int64_t>(p.tiles_n) * p.splits;
     const int64_t workers = p.pair ? std::max(1, sms / 2) : sms;
