@@ -225,13 +225,26 @@ def run_gpu(args, rank, world, local, dist):
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     w = synth.WORKLOADS[args.workload]
-    A_cpu, B_cpu = synth.workload_inputs(w)
-    A = A_cpu.to(device)
-    B = B_cpu.to(device)
+    f8 = args.dtype == "e4m3"
     C = torch.empty((w.batch, w.M, w.N) if w.batch > 1 else (w.M, w.N), dtype=torch.float32, device=device)
+    if f8:
+        # the same shape with E4M3 operands (N(0,1) draws rounded to E4M3),
+        # A row-major and B column-major (stored N x K)
+        lead = (w.batch,) if w.batch > 1 else ()
+        A = synth.make_fp8_codes(lead + (w.M, w.K), 0, seed=w.seed, kind="normal").to(device)
+        A = A.view(torch.float8_e4m3fn)
+        B = synth.make_fp8_codes(lead + (w.N, w.K), 0, seed=w.seed + 1, kind="normal").to(device)
+        B = B.view(torch.float8_e4m3fn)
+        launches_per_step = 1
+        info = {k: None for k in ("block_n", "stages", "split_k", "grid", "pack_a", "pack_b", "epilogue",
+                                  "cta_pair", "stream_k", "sk_tiles")}
+    else:
+        A_cpu, B_cpu = synth.workload_inputs(w)
+        A = A_cpu.to(device)
+        B = B_cpu.to(device)
+        info = tg.plan(w.M, w.N, w.K, w.batch, A=A.data_ptr(), B=B.data_ptr(), C=C.data_ptr())
+        launches_per_step = 1 + info["pack_a"] + info["pack_b"]
     stream = torch.cuda.current_stream(device)
-    info = tg.plan(w.M, w.N, w.K, w.batch, A=A.data_ptr(), B=B.data_ptr(), C=C.data_ptr())
-    launches_per_step = 1 + info["pack_a"] + info["pack_b"]
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
     flush_read = torch.ones(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
     sink = torch.empty((), dtype=torch.float32, device=device)
@@ -241,7 +254,10 @@ def run_gpu(args, rank, world, local, dist):
         torch.sum(flush_read, dim=0, out=sink)  # read > L2: dirty flush lines written back now
 
     def step():
-        tg.gemm(A, B, C)
+        if f8:
+            tg.gemm_fp8(A, B, C)
+        else:
+            tg.gemm(A, B, C)
 
     # warm-up (also JIT-loads the module, allocates workspaces)
     for _ in range(args.warmup):
@@ -287,6 +303,8 @@ def run_gpu(args, rank, world, local, dist):
     flops = float(w.flops)
     value = world * flops / (ms_max * 1e-3) / 1e12
 
+    if f8:
+        return report_f8(args, w, per, ms_mean, ms_max, world, rank, clk, wall, launches_per_step)
     # end to end through the host-buffer entry point (pinned memory)
     Ah = A_cpu.pin_memory()
     Bh = B_cpu.pin_memory()
@@ -352,6 +370,38 @@ def run_gpu(args, rank, world, local, dist):
         print(json.dumps(line), flush=True)
 
 
+def report_f8(args, w, per, ms_mean, ms_max, world, rank, clk, wall, launches_per_step):
+    """The line of an --dtype e4m3 run: the same shape with 8-bit operands,
+    against the bf16 measured peak times the nominal 8-bit/16-bit tensor
+    ratio (2)."""
+    peaks, peak_src = load_peaks()
+    peak = 2.0 * float(peaks["bf16_tflops"])
+    flops = float(w.flops)
+    achieved = flops / (ms_mean * 1e-3) / 1e12
+    bytes_moved = w.batch * (w.M * w.K + w.K * w.N + 4 * w.M * w.N)
+    if rank == 0:
+        line = {
+            "metric": "e4m3->fp32 GEMM TFLOP/s at 1 GB300 and % of dense FP8 tensor roofline",
+            "value": round(world * flops / (ms_max * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+            "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.batch, "M": w.M, "N": w.N, "K": w.K,
+                       "layout": "A row-major, B column-major (both K-major)", "accumulate": "fp32",
+                       "l2": "flushed between steps (512 MB write, then 256 MB read)"},
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                         "frac": round(achieved / peak, 4), "traffic": None,
+                         "peak_source": f"{peak_src} bf16_tflops x 2 (nominal fp8/bf16 dense ratio)",
+                         "hbm_frac": round(bytes_moved / (ms_mean * 1e-3) / 1e9 / float(peaks["hbm_gbs"]), 4)},
+            "cpu_baseline": None, "e2e": None,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": dict(clk, window=f"{args.clock_window:.1f} s of the same steps before the timed region, "
+                                          "and the timed region"),
+            "ms_min": round(min(per), 4), "wall_s": round(wall, 3),
+        }
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -362,6 +412,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--clock-window", type=float, default=0.5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--dtype", default="bf16", choices=["bf16", "e4m3"],
+                    help="operand type; e4m3 runs the same shape through tg_gemm_fp8 (an extra line, "
+                         "not the contract's metric)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "tg":
         ap.error("--warmup must be at least 3")
