@@ -37,7 +37,8 @@ constexpr int64_t EXTENT_LIMIT = INT32_MAX;
 // ------------------------------------------------------------ small kernels
 // Pack (the realign pass): copy a batch of rows x cols bf16 matrices with
 // arbitrary element strides into a dense buffer whose rows are padded to a
-// multiple of 8 elements (16 bytes) - the address form TMA can load.  The
+// multiple of 64 elements (pack_pitch: 128 bytes, so rows start on cache
+// lines; TMA itself needs only 16-byte rows).  The
 // pad columns are written as 0; the GEMM never reads them (its tensor map
 // extent is the true column count).  One launch packs A and B (two jobs).
 //
@@ -548,7 +549,7 @@ int grid_for(int64_t work, int sms)
 PackJob pack_job(const void *src, uint16_t *dst, int64_t rows, int64_t cols, int64_t ld, int64_t nb,
                  int64_t stride)
 {
-    const int64_t ld2 = round_up(cols, 8);
+    const int64_t ld2 = pack_pitch(cols);
     const uintptr_t base = reinterpret_cast<uintptr_t>(src);
     return PackJob{static_cast<const uint16_t *>(src), dst, rows, cols, ld, stride, ld2, nb * rows * (ld2 / 8), base,
                    base + 2u * static_cast<uintptr_t>(span_elems(rows, cols, ld, nb, stride))};
@@ -619,11 +620,11 @@ tg_status run_gemm(const Args &a, cudaStream_t stream, const tg_options *opt,
     if (plan.f8 && (plan.pack_a || plan.pack_b || !encode_a() || !encode_b())) return TG_ERR_UNSUPPORTED;
     if (!plan.pack_a && !encode_a()) {
         plan.pack_a = true;
-        plan.ws_pack_a = round_up((in.a_bcast ? 1 : a.batch) * a.a_rows() * round_up(a.a_cols(), 8) * 2, 256);
+        plan.ws_pack_a = round_up((in.a_bcast ? 1 : a.batch) * a.a_rows() * pack_pitch(a.a_cols()) * 2, 256);
     }
     if (!plan.pack_b && !encode_b()) {
         plan.pack_b = true;
-        plan.ws_pack_b = round_up((in.b_bcast ? 1 : a.batch) * a.b_rows() * round_up(a.b_cols(), 8) * 2, 256);
+        plan.ws_pack_b = round_up((in.b_bcast ? 1 : a.batch) * a.b_rows() * pack_pitch(a.b_cols()) * 2, 256);
     }
 
     // The persistent grid actually launched: two-SM tiles never use more
@@ -1034,7 +1035,7 @@ TG_API tg_status tg_gemm_host(const void *A_host, const void *B_host, float *C_h
     const bool a_whole = hp.dim == 0 || hp.dim == 3, b_whole = hp.dim == 0 || hp.dim == 2;
     const bool a_fix = K > 0 && a_whole && (lda % 8 != 0 || (batch > 1 && !a_bcast && strideA % 8 != 0));
     const bool b_fix = K > 0 && b_whole && (ldb % 8 != 0 || (batch > 1 && !b_bcast && strideB % 8 != 0));
-    const int64_t lda_f = round_up(a_cols, 8), ldb_f = round_up(b_cols, 8);
+    const int64_t lda_f = pack_pitch(a_cols), ldb_f = pack_pitch(b_cols);
     const int64_t sA_f = a_bcast ? 0 : a_rows * lda_f, sB_f = b_bcast ? 0 : b_rows * ldb_f;
     size_t off = 0;
     auto take = [&](size_t bytes) {

@@ -125,6 +125,13 @@ struct Plan {
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 
+// Row pitch (elements) of a packed bf16 operand: a multiple of 64 elements,
+// so that every row starts on a 128-byte line.  A 16-byte-aligned pitch is
+// enough for the TMA unit, but rows that straddle lines cost the loads an
+// extra sector each (4096^3 with A rows of 8208 bytes instead of 8192: 4.4
+// us slower).
+inline int64_t pack_pitch(int64_t cols) { return round_up(cols, 64); }
+
 // Stream-K schedule of `tiles` tiles of `kb` k-blocks on `workers` workers:
 // whole tiles for dp_waves full waves, then the remaining sk_tiles tiles'
 // k-blocks split into `workers` contiguous ranges.  maxparts = the largest
@@ -353,11 +360,11 @@ inline bool make_plan(const PlanInput &in, Plan &out)
 
     const int64_t batch_a = in.a_bcast ? 1 : in.batch;
     const int64_t batch_b = in.b_bcast ? 1 : in.batch;
-    // pack copies keep the stored layout: rows x round_up(columns, 8)
+    // pack copies keep the stored layout: rows x pack_pitch(columns)
     const int64_t a_rows = in.a_cm ? in.K : in.M, a_cols = in.a_cm ? in.M : in.K;
     const int64_t b_rows = in.b_cm ? in.N : in.K, b_cols = in.b_cm ? in.K : in.N;
-    p.ws_pack_a = p.pack_a ? round_up(batch_a * a_rows * round_up(a_cols, 8) * 2, 256) : 0;
-    p.ws_pack_b = p.pack_b ? round_up(batch_b * b_rows * round_up(b_cols, 8) * 2, 256) : 0;
+    p.ws_pack_a = p.pack_a ? round_up(batch_a * a_rows * pack_pitch(a_cols) * 2, 256) : 0;
+    p.ws_pack_b = p.pack_b ? round_up(batch_b * b_rows * pack_pitch(b_cols) * 2, 256) : 0;
     set_partial_workspace(in, p);
     out = p;
     return true;
