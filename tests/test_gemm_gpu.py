@@ -559,3 +559,30 @@ def test_host_entry_empty_sum():
     C = torch.full((M, N), float("nan"))
     tg.gemm_host(A, B, C)
     assert torch.all(C == 0)
+
+
+@pytest.mark.parametrize("N", [423, 422, 421, 420])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_store_never_writes_row_padding(N, out):
+    """C rows 16-byte aligned (the tensor-memory-accelerator store path) but
+    N not ending on a 16-byte boundary: the padding between rows stays
+    untouched (a TMA store clips only at 16-byte granularity)."""
+    M, K = 70, 64
+    A, B = synth.make_int_inputs(1, M, N, K, seed=N)
+    ldc = (N + 8) // 8 * 8 + 8
+    dt = torch.float32 if out == "f32" else torch.bfloat16
+    buf = torch.full((M * ldc,), float("nan"), dtype=dt, device=dev())
+    D = buf.view(M, ldc)[:, :N]
+    if out == "f32":
+        tg.gemm(A.to(dev()), B.to(dev()), D)
+    else:
+        tg.gemm_fused(A.to(dev()), B.to(dev()), D)
+    assert tg.device_error() == tg.TG_OK
+    host = buf.view(M, ldc).float().cpu().numpy()
+    assert np.all(np.isnan(host[:, N:])), "write into the row padding"
+    want = oracle_dense(A, B)
+    got = host[:, :N].astype(np.float64)
+    if out == "f32":
+        assert np.array_equal(got, want)
+    else:
+        assert np.array_equal(got, torch.from_numpy(want).to(torch.bfloat16).double().numpy())

@@ -585,6 +585,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             __syncwarp();
             const int32_t col = col0 + lane;
             const int32_t nrows = min(32, p.M - row0);
+            // A TMA store clips the row at 16-byte granularity: the box that
+            // holds the row's last column writes on to the next 16-byte
+            // boundary, into the caller's row padding, unless N ends on one.
+            // That box goes out with plain stores instead.
+            const int32_t per16 = p.out_bf16 ? 8 : 4;
+            const bool tma = p.epi_tma && (col0 + EPI_CHUNK <= p.N || p.N % per16 == 0);
             if (!p.out_bf16) {
                 // Row `lane` of the box; its 16-byte unit jj is stored at unit
                 // jj ^ (lane mod 8): the 128B swizzle (Swizzle(2,3,3) on fp32).
@@ -592,7 +598,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int jj = 0; jj < 8; ++jj)
                     ptx::st_shared_v4(box + lane * 128 + ((jj ^ (lane & 7)) << 4), v[4 * jj],
                                       v[4 * jj + 1], v[4 * jj + 2], v[4 * jj + 3]);
-                if (p.epi_tma) {
+                if (tma) {
                     ptx::fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
@@ -633,7 +639,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int u = 0; u < 4; ++u)
                     ptx::st_shared_v4(box + lane * 64 + ((u ^ ((lane >> 1) & 3)) << 4), w[4 * u],
                                       w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
-                if (p.epi_tma) {
+                if (tma) {
                     ptx::fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
