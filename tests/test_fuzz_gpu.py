@@ -87,3 +87,61 @@ def test_random_exact_cases(i):
             mask[lo: lo + N] = True
             assert np.array_equal(host[lo: lo + N].astype(np.float64), want[b, i_]), (c, b, i_)
     assert np.all(np.isnan(host[~mask])), ("write outside C", c)
+
+
+def _case_fp8(i):
+    r = random.Random(5000 + i)
+    M, N = r.randint(1, 600), r.randint(1, 600)
+    K = 16 * r.randint(1, 50)
+    batch = r.choice([1, 1, 2])
+    cfg = r.choice([(0, 0), (128, 1), (256, 1), (256, 2)])
+    opts = {}
+    if cfg[0]:
+        opts = {"block_n": cfg[0], "cta_pair": cfg[1]}
+    if r.random() < 0.25 and K >= 256:
+        opts["split_k"] = 2
+        opts["cta_pair"] = 1
+    return dict(M=M, N=N, K=K, batch=batch, opts=opts, fa=r.choice([0, 1]), fb=r.choice([0, 1]),
+                lda_pad=16 * r.choice([0, 0, 1]), ldb_pad=16 * r.choice([0, 1]), ldd_pad=r.choice([0, 3, 8]),
+                out=r.choice(["f32", "bf16"]), seed=r.randint(0, 10 ** 6))
+
+
+@pytest.mark.parametrize("i", range(24))
+def test_random_fp8_cases(i):
+    """8-bit operands: random extents, pitches, formats, plans and output
+    types; exact against the oracle (bf16 output: the exact product rounded
+    once), and nothing written outside D."""
+    from oracle import fp8 as ofp8
+
+    c = _case_fp8(i)
+    M, N, K, batch = c["M"], c["N"], c["K"], c["batch"]
+    A = synth.make_fp8_codes((batch, M, K), c["fa"], seed=c["seed"])
+    Bt = synth.make_fp8_codes((batch, N, K), c["fb"], seed=c["seed"] + 1)
+    lda, ldb, ldd = K + c["lda_pad"], K + c["ldb_pad"], N + c["ldd_pad"]
+    abuf = torch.zeros(batch * M * lda, dtype=torch.uint8)
+    bbuf = torch.zeros(batch * N * ldb, dtype=torch.uint8)
+    abuf.view(batch, M, lda)[:, :, :K] = A
+    bbuf.view(batch, N, ldb)[:, :, :K] = Bt
+    ad, bd = abuf.to(dev()), bbuf.to(dev())
+    dt = torch.float32 if c["out"] == "f32" else torch.bfloat16
+    sD = M * ldd + 8
+    dbuf = torch.full(((batch - 1) * sD + M * ldd + 8,), float("nan"), dtype=dt, device=dev())
+    ep = tg.tg_epilogue()
+    ep.alpha, ep.beta = 1.0, 0.0
+    ep.out_type = tg.TG_F32 if c["out"] == "f32" else tg.TG_BF16
+    st = tg.tg_gemm_fp8(ad.data_ptr(), bd.data_ptr(), dbuf.data_ptr(), M, N, K, lda, ldb, ldd, batch,
+                        M * lda if batch > 1 else 0, N * ldb if batch > 1 else 0, sD if batch > 1 else 0,
+                        c["fa"], c["fb"], ep, torch.cuda.current_stream().cuda_stream, tg.make_options(**c["opts"]))
+    assert st == tg.TG_OK, (c, tg.STATUS_NAMES.get(st, st))
+    assert tg.device_error() == tg.TG_OK, c
+    host = dbuf.float().cpu().numpy()
+    want = ofp8.gemm_fp8_f64(A.numpy(), Bt.numpy(), c["fa"], c["fb"])
+    if c["out"] == "bf16":
+        want = torch.from_numpy(want).to(torch.bfloat16).double().numpy()
+    mask = np.zeros(host.shape, dtype=bool)
+    for b in range(batch):
+        for i_ in range(M):
+            lo = b * sD + i_ * ldd
+            mask[lo: lo + N] = True
+            assert np.array_equal(host[lo: lo + N].astype(np.float64), want[b, i_]), (c, b, i_)
+    assert np.all(np.isnan(host[~mask])), ("write outside D", c)
