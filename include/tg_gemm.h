@@ -234,6 +234,23 @@ tg_status tg_gemm_host(const void *A_host, const void *B_host, float *C_host,
                        int64_t batch, int64_t strideA, int64_t strideB, int64_t strideC,
                        tg_stream_t stream, const tg_options *opt);
 
+/* Run-time plan search (a tuner): times candidate plans for these arguments
+ * on the caller's buffers and stream - every instantiated tile width, one
+ * CTA or two-SM tiles, the two deepest ring depths, stream-K on and off,
+ * and split-K factors where there are fewer tiles than SMs - each `reps`
+ * times (1..100) with CUDA events, and returns the fastest (median) as
+ * options in *best (the layout fields and other fields of `base` kept; base
+ * may be NULL) and its time in microseconds in *best_us (may be NULL).
+ * C is written with the product.  Synchronous.  (The pages call for a
+ * search dimension over tile and depth choices; OCANNL "Module
+ * Ir.Schedule", pipeline_depth.) */
+tg_status tg_tune(const void *A, const void *B, float *C,
+                  int64_t M, int64_t N, int64_t K,
+                  int64_t lda, int64_t ldb, int64_t ldc,
+                  int64_t batch, int64_t strideA, int64_t strideB, int64_t strideC,
+                  tg_stream_t stream, const tg_options *base, int32_t reps,
+                  tg_options *best, float *best_us);
+
 /* The plan tg_gemm_ex would use for these arguments, without touching the
  * pointers' memory.  sm_count > 0 plans for that many SMs and makes no CUDA
  * call at all (host-only); sm_count == 0 queries the current device. */

@@ -239,3 +239,19 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_abi, "library_path", lambda: str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         _abi.load()
+
+
+def test_tune_rejects_bad_arguments_before_any_cuda_call(lib):
+    best = tg.tg_options()
+    us = ctypes.c_float(0)
+    good = (1 << 30, 1 << 36, 1 << 40, 64, 64, 64, 64, 64, 64, 1, 0, 0, 0)
+    assert tg.tg_tune(*good, None, None, 0, best, us) == tg.TG_ERR_INVALID_ARG      # reps < 1
+    assert tg.tg_tune(*good, None, None, 101, best, us) == tg.TG_ERR_INVALID_ARG    # reps > 100
+    assert tg.tg_tune(*good, None, None, 3, None, us) == tg.TG_ERR_INVALID_ARG      # no output
+    bad = (1 << 30, 1 << 36, 1 << 40, 64, 64, 64, 32, 64, 64, 1, 0, 0, 0)           # lda < K
+    assert tg.tg_tune(*bad, None, None, 3, best, us) == tg.TG_ERR_INVALID_ARG
+    # empty problem: nothing to time, the base options come back
+    empty = (1 << 30, 1 << 36, 1 << 40, 0, 64, 64, 64, 64, 64, 1, 0, 0, 0)
+    base = tg.make_options(a_col_major=0, stages=4)
+    assert tg.tg_tune(*empty, None, base, 3, best, us) == tg.TG_OK
+    assert best.stages == 4 and us.value == 0.0

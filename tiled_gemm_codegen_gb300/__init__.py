@@ -3,7 +3,7 @@
 The product is the C-ABI CUDA library declared in ``include/tg_gemm.h``.
 This package is its thin Python binding: the C functions under the same
 names (``tg_gemm``, ``tg_gemm_ex``, ``tg_gemm_host``, ``tg_gemm_splitk_static``, ``tg_plan``,
-``tg_gemm_fp8``,
+``tg_gemm_fp8``, ``tg_tune``,
 ``tg_device_error``, ``tg_status_string``, ``tg_shutdown``) taking raw
 pointers and sizes, plus conveniences that read pointers, shapes and
 strides off torch tensors.  PyTorch only provides device memory and
@@ -25,7 +25,7 @@ __all__ = [
     "TG_OK", "TG_ERR_INVALID_ARG", "TG_ERR_UNSUPPORTED", "TG_ERR_CUDA", "TG_ERR_OOM",
     "TG_ERR_TIMEOUT", "TgError", "tg_options", "tg_plan_info", "load", "library_path",
     "tg_gemm", "tg_gemm_ex", "tg_gemm_host", "tg_gemm_fused", "tg_gemm_splitk_static", "tg_plan",
-    "tg_gemm_fp8", "gemm_fp8", "TG_FP8_E4M3", "TG_FP8_E5M2",
+    "tg_gemm_fp8", "gemm_fp8", "TG_FP8_E4M3", "TG_FP8_E5M2", "tg_tune", "tune",
     "tg_epilogue", "gemm_fused", "ACTIVATIONS", "tg_device_error", "tg_status_string",
     "tg_shutdown", "make_options", "gemm", "gemm_host", "plan", "device_error",
 ]
@@ -73,6 +73,14 @@ def tg_gemm_fp8(A, B, D, M, N, K, lda, ldb, ldd, batch, strideA, strideB, stride
     return load().tg_gemm_fp8(A, B, D, M, N, K, lda, ldb, ldd, batch, strideA, strideB, strideD,
                               a_format, b_format, ctypes.byref(ep) if ep is not None else None, stream,
                               ctypes.byref(opt) if opt is not None else None)
+
+
+def tg_tune(A, B, C, M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC, stream=None,
+            base=None, reps=3, best=None, best_us=None) -> int:
+    return load().tg_tune(A, B, C, M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC, stream,
+                          ctypes.byref(base) if base is not None else None, reps,
+                          ctypes.byref(best) if best is not None else None,
+                          ctypes.byref(best_us) if best_us is not None else None)
 
 
 def tg_plan(A, B, C, M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC, sm_count=0,
@@ -309,6 +317,37 @@ def gemm_fp8(A, Bt, D=None, *, scale: float = 1.0, bias=None, residual=None, bet
     if st != TG_OK:
         raise TgError(st, "tg_gemm_fp8")
     return D
+
+
+def tune(A, B, C=None, *, options: tg_options | None = None, reps: int = 3, stream=None):
+    """Run-time plan search on these CUDA tensors (tg_tune): returns
+    (options of the fastest plan, its median time in microseconds).  C is
+    written with the product."""
+    import torch
+
+    if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
+        raise TypeError("A and B must be bf16")
+    pa, M, K, lda, ba, sA, a_cm = _operand(A, "A")
+    pb, K2, N, ldb, bb, sB, b_cm = _operand(B, "B")
+    options = _with_layout(options, a_cm, b_cm)
+    if K2 != K:
+        raise ValueError(f"inner dimensions differ: {K} vs {K2}")
+    batch = max(ba, bb)
+    if ba == 1:
+        sA = 0
+    if bb == 1:
+        sB = 0
+    if C is None:
+        shape = (batch, M, N) if (A.dim() == 3 or B.dim() == 3) else (M, N)
+        C = torch.empty(shape, dtype=torch.float32, device=A.device)
+    pc, Mc, Nc, ldc, bc, sC = _operand_geometry(C, -2, "C")
+    best = tg_options()
+    us = ctypes.c_float(0.0)
+    st = tg_tune(pa, pb, pc, M, N, K, lda, ldb, ldc, batch, sA, sB, sC, _stream_ptr(stream), options,
+                 reps, best, us)
+    if st != TG_OK:
+        raise TgError(st, "tg_tune")
+    return best, us.value
 
 
 def gemm_host(A, B, C=None, *, options: tg_options | None = None, stream=None):

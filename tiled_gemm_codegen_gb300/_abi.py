@@ -108,6 +108,8 @@ SIGNATURES = {
     "tg_gemm_fused": ([_vp, _vp, _vp] + [_i64] * 10 + [ctypes.POINTER(tg_epilogue), _vp,
                                                          ctypes.POINTER(tg_options)], ctypes.c_int),
     "tg_gemm_splitk_static": ([_vp, _vp, _vp] + [_i64] * 10 + [ctypes.c_int32, _vp], ctypes.c_int),
+    "tg_tune": (_GEMM_ARGS + [ctypes.POINTER(tg_options), ctypes.c_int32, ctypes.POINTER(tg_options),
+                              ctypes.POINTER(ctypes.c_float)], ctypes.c_int),
     "tg_gemm_fp8": ([_vp, _vp, _vp] + [_i64] * 10 + [ctypes.c_int32, ctypes.c_int32,
                                                        ctypes.POINTER(tg_epilogue), _vp,
                                                        ctypes.POINTER(tg_options)], ctypes.c_int),

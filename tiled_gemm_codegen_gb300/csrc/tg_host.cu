@@ -820,6 +820,97 @@ TG_API tg_status tg_gemm_ex(const void *A, const void *B, float *C, int64_t M, i
     return run_gemm(a, reinterpret_cast<cudaStream_t>(stream), opt);
 }
 
+// Run-time plan search: every instantiated (width, two-SM, ring depth)
+// with stream-K on or off and, when there are fewer tiles than workers,
+// split-K factors; each timed `reps` times with events on the caller's
+// stream, the median kept, the fastest returned.
+TG_API tg_status tg_tune(const void *A, const void *B, float *C, int64_t M, int64_t N, int64_t K, int64_t lda,
+                         int64_t ldb, int64_t ldc, int64_t batch, int64_t strideA, int64_t strideB,
+                         int64_t strideC, tg_stream_t stream_, const tg_options *base, int32_t reps,
+                         tg_options *best, float *best_us)
+{
+    using namespace tg;
+    if (!best || reps < 1 || reps > 100) return TG_ERR_INVALID_ARG;
+    const Args a = with_layout(Args{A, B, C, M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC}, base);
+    tg_status st = validate(a);
+    if (st != TG_OK) return st;
+    tg_options start{};
+    if (base) start = *base;
+    *best = start;
+    if (best_us) *best_us = 0.0f;
+    if (M == 0 || N == 0 || K == 0) return TG_OK;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_status(e);
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        if ((st = device_sms(dev, &sms)) != TG_OK) return st;
+    }
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if ((e = cudaEventCreate(&e0)) != cudaSuccess || (e = cudaEventCreate(&e1)) != cudaSuccess) {
+        if (e0) cudaEventDestroy(e0);
+        return cuda_status(e);
+    }
+    float best_t = -1.0f;
+    tg_options best_o = start;
+    st = TG_OK;
+    const int widths[4] = {64, 128, 192, 256};
+    const int depths[5] = {2, 3, 4, 6, 8};
+    const int splits[6] = {1, 2, 3, 4, 6, 8};
+    for (int wi = 0; wi < 4 && st == TG_OK; ++wi) {
+        for (int pr = 1; pr <= 2 && st == TG_OK; ++pr) {
+            const bool pair = pr == 2;
+            if (pair && !pair_width(widths[wi])) continue;
+            for (int di = 0; di < 5 && st == TG_OK; ++di) {
+                if (!stage_supported(widths[wi], depths[di], pair)) continue;
+                for (int si = 0; si < 6 && st == TG_OK; ++si) {
+                    for (int sk = 1; sk <= 2 && st == TG_OK; ++sk) {
+                        if (sk == 2 && splits[si] > 1) continue;
+                        tg_options o = start;
+                        o.block_n = widths[wi];
+                        o.cta_pair = pr;
+                        o.stages = depths[di];
+                        o.split_k = splits[si];
+                        o.stream_k = sk;
+                        PlanInput in = plan_input(a, sms, &o);
+                        Plan pl;
+                        if (!make_plan(in, pl)) continue;
+                        // keep split-K to the cases it exists for: fewer units than workers
+                        const int64_t workers = pair ? sms / 2 : sms;
+                        if (splits[si] > 1 && pl.units / splits[si] >= workers) continue;
+                        if (sk == 2 && !pl.stream_k) continue;  // same plan as stream_k = 1
+                        // the deeper half of the instantiated ring depths
+                        if (depths[di] < max_stages(widths[wi], pair) / 2) continue;
+                        float ts[100];
+                        st = run_gemm(a, stream, &o);  // warm-up (workspaces, maps)
+                        for (int r = 0; r < reps && st == TG_OK; ++r) {
+                            cudaEventRecord(e0, stream);
+                            st = run_gemm(a, stream, &o);
+                            cudaEventRecord(e1, stream);
+                            if ((e = cudaEventSynchronize(e1)) != cudaSuccess) st = cuda_status(e);
+                            if (st == TG_OK) cudaEventElapsedTime(&ts[r], e0, e1);
+                        }
+                        if (st != TG_OK) break;
+                        std::sort(ts, ts + reps);
+                        const float t = ts[reps / 2] * 1000.0f;
+                        if (best_t < 0.0f || t < best_t) {
+                            best_t = t;
+                            best_o = o;
+                        }
+                    }
+                }
+            }
+        }
+    }
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    if (st != TG_OK) return st;
+    *best = best_o;
+    if (best_us) *best_us = best_t;
+    return TG_OK;
+}
+
 TG_API tg_status tg_gemm(const void *A, const void *B, float *C, int64_t M, int64_t N, int64_t K,
                          int64_t lda, int64_t ldb, int64_t ldc, int64_t batch, int64_t strideA,
                          int64_t strideB, int64_t strideC, tg_stream_t stream)
