@@ -18,6 +18,7 @@
 #include "tg_gemm.h"
 #include "tg_internal.h"
 #include "tg_plan.h"
+#include "tg_ptx.cuh"
 
 #define TG_API extern "C" __attribute__((visibility("default")))
 
@@ -88,6 +89,9 @@ __device__ __forceinline__ uint4 load8_bf16(const uint16_t *s, const PackJob &j)
 
 __global__ void pack_bf16_kernel(PackJob ja, PackJob jb, int blocks_a)
 {
+    // the GEMM that follows may be scheduled now: it waits for this grid to
+    // complete before it reads the packed operands
+    ptx::griddep_launch_dependents();
     const bool is_a = static_cast<int>(blockIdx.x) < blocks_a;
     const PackJob j = is_a ? ja : jb;
     const int64_t bid = is_a ? blockIdx.x : blockIdx.x - blocks_a;

@@ -408,6 +408,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if constexpr (PAIR) ptx::cluster_sync_all();  // both CTAs' barriers exist
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // Everything above touched only this CTA's shared and tensor memory (and
+    // the optional trace); A, B, C and the workspace only after the kernels
+    // before this one in the stream are complete and visible.
+    ptx::griddep_wait();
     const uint32_t peer_abort =
         PAIR ? ptx::map_to_cta(ptx::smem_addr(const_cast<int32_t *>(abort_flag)), rank ^ 1u) : 0u;
     const Watchdog wd{p.timeout_ns, abort_flag, p.err, peer_abort};
@@ -857,24 +861,25 @@ cudaError_t launch_fixed(const CUtensorMap &ta, const CUtensorMap &tb, const CUt
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
-    if constexpr (!PAIR) {
-        kern<<<grid, NUM_THREADS, smem, s>>>(ta, tb, tc, p);
-        return cudaGetLastError();
-    } else {
-        cudaLaunchConfig_t cfg{};
-        cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-        cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-        cfg.dynamicSmemBytes = smem;
-        cfg.stream = s;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, p);
-    }
+    // Programmatic dependent launch: the kernel may start while the previous
+    // kernel of the stream finishes; it sets up (barriers, tensor memory,
+    // cluster) and then waits on the grid dependency before its first access
+    // to any operand or workspace.
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = PAIR ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, p);
 }
 
 // Largest number of two-CTA clusters of this configuration that can be

@@ -65,6 +65,14 @@ __device__ __forceinline__ void prefetch_tensormap(const void *tmap)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
+// Programmatic dependent launch: wait until every kernel this grid depends
+// on has completed and its memory is visible; let dependents be scheduled.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // 3-D tiled load global -> shared, completing `bytes` on mbarrier `bar`.
 // Out-of-range elements of the box are filled with zeros.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, uint32_t bar,
