@@ -1158,15 +1158,21 @@ TG_API tg_status tg_gemm_host(const void *A_host, const void *B_host, float *C_h
     float *dC = reinterpret_cast<float *>(dbuf + off_c);
     const cudaMemcpyKind H2D = cudaMemcpyHostToDevice;
 
-    // the copy streams start after the caller's earlier work
-    if ((e = cudaEventRecord(w.ev[0], stream)) != cudaSuccess) return cuda_status(e);
-    if ((e = cudaStreamWaitEvent(w.h2d, w.ev[0], 0)) != cudaSuccess) return cuda_status(e);
-    if ((e = cudaStreamWaitEvent(w.d2h, w.ev[0], 0)) != cudaSuccess) return cuda_status(e);
+    // One piece: everything on the caller's stream (cross-stream events would
+    // only add latency).  Several: the copy streams start after the caller's
+    // earlier work.
+    const bool overlap = hp.pieces > 1;
+    cudaStream_t s_in = overlap ? w.h2d : stream, s_out = overlap ? w.d2h : stream;
+    if (overlap) {
+        if ((e = cudaEventRecord(w.ev[0], stream)) != cudaSuccess) return cuda_status(e);
+        if ((e = cudaStreamWaitEvent(w.h2d, w.ev[0], 0)) != cudaSuccess) return cuda_status(e);
+        if ((e = cudaStreamWaitEvent(w.d2h, w.ev[0], 0)) != cudaSuccess) return cuda_status(e);
+    }
     // elements [e0, e1) of an operand's span, host -> device
     auto copy_in = [&](const uint16_t *dst, const void *src, int64_t e0, int64_t e1) {
         if (e1 <= e0) return cudaSuccess;
         return cudaMemcpyAsync(const_cast<uint16_t *>(dst) + e0, static_cast<const uint16_t *>(src) + e0,
-                               static_cast<size_t>((e1 - e0) * 2), H2D, w.h2d);
+                               static_cast<size_t>((e1 - e0) * 2), H2D, s_in);
     };
     // the span of problems [b0, b1), or of rows [r0, r1) of one problem
     auto span = [&](int64_t rows, int64_t cols, int64_t ld, int64_t stride, int64_t b0, int64_t b1, int64_t r0,
@@ -1184,7 +1190,7 @@ TG_API tg_status tg_gemm_host(const void *A_host, const void *B_host, float *C_h
         if (a_fix) {
             uint16_t *dst = reinterpret_cast<uint16_t *>(dbuf + off_af);
             const PackJob j = pack_job(dA, dst, a_rows, a_cols, lda, a_bcast ? 1 : batch, strideA);
-            pack_bf16_kernel<<<grid_for(j.chunks, sms), 256, 0, w.h2d>>>(j, PackJob{}, grid_for(j.chunks, sms));
+            pack_bf16_kernel<<<grid_for(j.chunks, sms), 256, 0, s_in>>>(j, PackJob{}, grid_for(j.chunks, sms));
             if ((e = cudaGetLastError()) != cudaSuccess) return cuda_status(e);
             A_use = dst, lda_use = lda_f, sA_use = sA_f;
         }
@@ -1195,7 +1201,7 @@ TG_API tg_status tg_gemm_host(const void *A_host, const void *B_host, float *C_h
         if (b_fix) {
             uint16_t *dst = reinterpret_cast<uint16_t *>(dbuf + off_bf);
             const PackJob j = pack_job(dB, dst, b_rows, b_cols, ldb, b_bcast ? 1 : batch, strideB);
-            pack_bf16_kernel<<<grid_for(j.chunks, sms), 256, 0, w.h2d>>>(j, PackJob{}, grid_for(j.chunks, sms));
+            pack_bf16_kernel<<<grid_for(j.chunks, sms), 256, 0, s_in>>>(j, PackJob{}, grid_for(j.chunks, sms));
             if ((e = cudaGetLastError()) != cudaSuccess) return cuda_status(e);
             B_use = dst, ldb_use = ldb_f, sB_use = sB_f;
         }
@@ -1221,8 +1227,8 @@ TG_API tg_status tg_gemm_host(const void *A_host, const void *B_host, float *C_h
             e = copy_in(dB, B_host, sb.first, sb.second);
         }
         cudaEvent_t ev_in = w.ev[1 + 3 * i], ev_gemm = w.ev[2 + 3 * i], ev_out = w.ev[3 + 3 * i];
-        if (e == cudaSuccess) e = cudaEventRecord(ev_in, w.h2d);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, ev_in, 0);
+        if (e == cudaSuccess && overlap) e = cudaEventRecord(ev_in, w.h2d);
+        if (e == cudaSuccess && overlap) e = cudaStreamWaitEvent(stream, ev_in, 0);
         if (e != cudaSuccess) return cuda_status(e);
         // the piece's GEMM on the device copies
         const int64_t a_off = a.a_cm ? m0 : m0 * lda_use;
@@ -1231,14 +1237,14 @@ TG_API tg_status tg_gemm_host(const void *A_host, const void *B_host, float *C_h
                    m1 - m0, n1 - n0, K, lda_use, ldb_use, ldc_d, b1 - b0, sA_use, sB_use, sC_d};
         st = run_gemm(with_layout(piece, opt), stream, opt);
         if (st != TG_OK) return st;
-        if ((e = cudaEventRecord(ev_gemm, stream)) != cudaSuccess) return cuda_status(e);
-        if ((e = cudaStreamWaitEvent(w.d2h, ev_gemm, 0)) != cudaSuccess) return cuda_status(e);
+        if (overlap && (e = cudaEventRecord(ev_gemm, stream)) != cudaSuccess) return cuda_status(e);
+        if (overlap && (e = cudaStreamWaitEvent(w.d2h, ev_gemm, 0)) != cudaSuccess) return cuda_status(e);
         // only the M x N block of every problem goes back (gaps keep host data)
         e = copy_problems(C_host, ldc, strideC, dC, ldc_d, sC_d, b0, b1, m0, m1 - m0, M, n0, n1 - n0, 4,
-                          cudaMemcpyDeviceToHost, w.d2h);
-        if (e == cudaSuccess) e = cudaEventRecord(ev_out, w.d2h);
+                          cudaMemcpyDeviceToHost, s_out);
+        if (e == cudaSuccess && overlap) e = cudaEventRecord(ev_out, w.d2h);
         if (e != cudaSuccess) return cuda_status(e);
-        last_out = ev_out;
+        if (overlap) last_out = ev_out;
     }
     // the caller's stream resumes after the last piece of C is home
     if (last_out && (e = cudaStreamWaitEvent(stream, last_out, 0)) != cudaSuccess) return cuda_status(e);
