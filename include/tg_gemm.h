@@ -215,6 +215,37 @@ tg_status tg_gemm_fp8(const void *A, const void *B, void *D,
                       int32_t a_format, int32_t b_format,
                       const tg_epilogue *ep, tg_stream_t stream, const tg_options *opt);
 
+/* Block-scaled 8-bit GEMM (MXFP8: TVM "Tensor Layout", Case study: Blackwell
+ * tensor memory, the per-block scale factors SFA / SFB of a block-scaled
+ * MMA):
+ *     D[b][i][j] = sum_k  2^(SFA[b][i][k/32] - 127) * A[b][i][k]
+ *                       * 2^(SFB[b][j][k/32] - 127) * B[b][k][j]
+ * then the fused epilogue of tg_gemm_fused (ep may be NULL: D in fp32).
+ * Every run of 32 consecutive elements along K of a row of A (of a column of
+ * B) shares one E8M0 scale: an unsigned byte e meaning 2^(e - 127) (e = 255
+ * is NaN; the last run of a row may be shorter when K is not a multiple of
+ * 32).  A, B, their formats, layouts and requirements as tg_gemm_fp8.
+ * SFA (device bytes): the scale of row i, run r of problem b at
+ * SFA[b*stride_sfa + i*ld_sfa + r], ld_sfa >= ceil(K/32); SFB likewise per
+ * column j of B (SFB[b*stride_sfb + j*ld_sfb + r], ld_sfb >= ceil(K/32)).
+ * A scale stride of 0 shares one scale matrix across the batch; where A (B)
+ * is shared (strideA == 0 with batch > 1) its scales must be too.  Scales
+ * are read, never written, and may alias anything but D.  The library
+ * re-arranges them into device scratch it owns (one 512-byte block per 128
+ * rows or columns and 128 elements of K) on `stream` before the GEMM.
+ * Tiles are 128 x 128 (one CTA each); opt->block_n must be 0 or 128,
+ * opt->cta_pair 0 or 1, opt->stages 0, 2 or 4 (else TG_ERR_INVALID_ARG).
+ * TG_ERR_INVALID_ARG also for a NULL scale pointer with K > 0, ld_sfa or
+ * ld_sfb < ceil(K/32), or a negative scale stride. */
+tg_status tg_gemm_mxfp8(const void *A, const void *B, void *D,
+                        int64_t M, int64_t N, int64_t K,
+                        int64_t lda, int64_t ldb, int64_t ldd,
+                        int64_t batch, int64_t strideA, int64_t strideB, int64_t strideD,
+                        int32_t a_format, int32_t b_format,
+                        const uint8_t *SFA, int64_t ld_sfa, int64_t stride_sfa,
+                        const uint8_t *SFB, int64_t ld_sfb, int64_t stride_sfb,
+                        const tg_epilogue *ep, tg_stream_t stream, const tg_options *opt);
+
 /* The GEMM on HOST buffers: copies the spans of A and B that the strides
  * reach to device scratch owned by the library, runs tg_gemm_ex there into
  * a device C with 16-byte rows, and copies the M x N block of every problem

@@ -164,3 +164,10 @@ def make_fp8_codes(shape, fmt: int, seed: int, kind: str = "int") -> torch.Tenso
     if kind == "normal":
         return torch.randn(tuple(shape), generator=gen).to(dt).view(torch.uint8)
     raise ValueError(kind)
+
+
+def make_e8m0_codes(shape, seed: int, lo: int = 124, hi: int = 130) -> torch.Tensor:
+    """Seeded E8M0 scale codes (uint8) drawn uniformly from [lo, hi]; the
+    default range is scales 2^-3 .. 2^3."""
+    gen = torch.Generator("cpu").manual_seed(seed)
+    return torch.randint(lo, hi + 1, tuple(shape), generator=gen).to(torch.uint8)

@@ -255,3 +255,35 @@ def test_tune_rejects_bad_arguments_before_any_cuda_call(lib):
     base = tg.make_options(a_col_major=0, stages=4)
     assert tg.tg_tune(*empty, None, base, 3, best, us) == tg.TG_OK
     assert best.stages == 4 and us.value == 0.0
+
+
+def test_mxfp8_rejects_bad_arguments_before_any_cuda_call(lib):
+    """Block-scaled entry: scale pointers, pitches, strides, options and
+    overlaps are checked on the host (fake device addresses, no GPU)."""
+    M, N, K = 256, 256, 256
+    A, B, D = 0x100000, 0x200000, 0x300000
+    SF = 0x400000
+
+    def call(sfa=SF, ld_sfa=8, s_sfa=0, sfb=SF, ld_sfb=8, s_sfb=0, opt=None, batch=1, sA=0, sB=0,
+             fa=0, K=K):
+        return tg.tg_gemm_mxfp8(A, B, D, M, N, K, K, K, N, batch, sA, sB, M * N, fa, 0,
+                                sfa, ld_sfa, s_sfa, sfb, ld_sfb, s_sfb, None, None, opt)
+
+    bad = tg.TG_ERR_INVALID_ARG
+    assert call(sfa=None) == bad
+    assert call(sfb=None) == bad
+    assert call(ld_sfa=7) == bad                        # < ceil(K/32)
+    assert call(ld_sfb=7) == bad
+    assert call(s_sfa=-8) == bad
+    assert call(fa=2) == bad                            # unknown format
+    assert call(opt=tg.make_options(block_n=256)) == bad
+    assert call(opt=tg.make_options(cta_pair=2)) == bad
+    assert call(opt=tg.make_options(stages=6)) == bad
+    assert call(opt=tg.make_options(a_col_major=1)) == bad
+    # A shared across the batch but its scales not
+    assert call(batch=2, sA=0, sB=N * K, s_sfa=M * 8) == bad
+    # scales overlapping D
+    assert call(sfa=D + 64) == bad
+    # K == 0: no scales needed, nothing to check (and M == 0: nothing to do)
+    assert tg.tg_gemm_mxfp8(A, B, D, 0, N, K, K, K, N, 1, 0, 0, 0, 0, 0,
+                            SF, 8, 0, SF, 8, 0, None, None, None) == tg.TG_OK

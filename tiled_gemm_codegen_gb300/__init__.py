@@ -3,7 +3,7 @@
 The product is the C-ABI CUDA library declared in ``include/tg_gemm.h``.
 This package is its thin Python binding: the C functions under the same
 names (``tg_gemm``, ``tg_gemm_ex``, ``tg_gemm_host``, ``tg_gemm_splitk_static``, ``tg_plan``,
-``tg_gemm_fp8``, ``tg_tune``,
+``tg_gemm_fp8``, ``tg_gemm_mxfp8``, ``tg_tune``,
 ``tg_device_error``, ``tg_status_string``, ``tg_shutdown``) taking raw
 pointers and sizes, plus conveniences that read pointers, shapes and
 strides off torch tensors.  PyTorch only provides device memory and
@@ -25,7 +25,8 @@ __all__ = [
     "TG_OK", "TG_ERR_INVALID_ARG", "TG_ERR_UNSUPPORTED", "TG_ERR_CUDA", "TG_ERR_OOM",
     "TG_ERR_TIMEOUT", "TgError", "tg_options", "tg_plan_info", "load", "library_path",
     "tg_gemm", "tg_gemm_ex", "tg_gemm_host", "tg_gemm_fused", "tg_gemm_splitk_static", "tg_plan",
-    "tg_gemm_fp8", "gemm_fp8", "TG_FP8_E4M3", "TG_FP8_E5M2", "tg_tune", "tune",
+    "tg_gemm_fp8", "gemm_fp8", "TG_FP8_E4M3", "TG_FP8_E5M2",
+    "tg_gemm_mxfp8", "gemm_mxfp8", "tg_tune", "tune",
     "tg_epilogue", "gemm_fused", "ACTIVATIONS", "tg_device_error", "tg_status_string",
     "tg_shutdown", "make_options", "gemm", "gemm_host", "plan", "device_error",
 ]
@@ -73,6 +74,15 @@ def tg_gemm_fp8(A, B, D, M, N, K, lda, ldb, ldd, batch, strideA, strideB, stride
     return load().tg_gemm_fp8(A, B, D, M, N, K, lda, ldb, ldd, batch, strideA, strideB, strideD,
                               a_format, b_format, ctypes.byref(ep) if ep is not None else None, stream,
                               ctypes.byref(opt) if opt is not None else None)
+
+
+def tg_gemm_mxfp8(A, B, D, M, N, K, lda, ldb, ldd, batch, strideA, strideB, strideD, a_format,
+                  b_format, SFA, ld_sfa, stride_sfa, SFB, ld_sfb, stride_sfb, ep=None, stream=None,
+                  opt=None) -> int:
+    return load().tg_gemm_mxfp8(A, B, D, M, N, K, lda, ldb, ldd, batch, strideA, strideB, strideD,
+                                a_format, b_format, SFA, ld_sfa, stride_sfa, SFB, ld_sfb, stride_sfb,
+                                ctypes.byref(ep) if ep is not None else None, stream,
+                                ctypes.byref(opt) if opt is not None else None)
 
 
 def tg_tune(A, B, C, M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC, stream=None,
@@ -264,12 +274,8 @@ def _fp8_format(t, what):
     raise TypeError(f"{what} must be float8_e4m3fn or float8_e5m2")
 
 
-def gemm_fp8(A, Bt, D=None, *, scale: float = 1.0, bias=None, residual=None, beta: float = 1.0,
-             activation: str = "none", out_dtype=None, options: tg_options | None = None,
-             stream=None):
-    """D = act(scale * (A @ Bt^T) + bias) + beta * residual with 8-bit
-    floating-point A [.., M, K] and Bt [.., N, K] (B column-major), both
-    contiguous along K; scale carries the operands' per-tensor scales."""
+def _fp8_call(A, Bt, D, scale, bias, residual, beta, activation, out_dtype):
+    """Shapes, D and the epilogue of the 8-bit entry points."""
     import torch
 
     fa, fb = _fp8_format(A, "A"), _fp8_format(Bt, "Bt")
@@ -312,10 +318,46 @@ def gemm_fp8(A, Bt, D=None, *, scale: float = 1.0, bias=None, residual=None, bet
         ep.residual = pr
         ep.ldr = ldr
         ep.strideR = sR if br > 1 else 0
-    st = tg_gemm_fp8(pa, pb, pd, M, N, K, lda, ldb, ldd, batch, sA, sB, sD, fa, fb, ep,
-                     _stream_ptr(stream), options)
+    args = (pa, pb, pd, M, N, K, lda, ldb, ldd, batch, sA, sB, sD, fa, fb)
+    return D, ep, args
+
+
+def gemm_fp8(A, Bt, D=None, *, scale: float = 1.0, bias=None, residual=None, beta: float = 1.0,
+             activation: str = "none", out_dtype=None, options: tg_options | None = None,
+             stream=None):
+    """D = act(scale * (A @ Bt^T) + bias) + beta * residual with 8-bit
+    floating-point A [.., M, K] and Bt [.., N, K] (B column-major), both
+    contiguous along K; scale carries the operands' per-tensor scales."""
+    D, ep, args = _fp8_call(A, Bt, D, scale, bias, residual, beta, activation, out_dtype)
+    st = tg_gemm_fp8(*args, ep, _stream_ptr(stream), options)
     if st != TG_OK:
         raise TgError(st, "tg_gemm_fp8")
+    return D
+
+
+def gemm_mxfp8(A, Bt, SFA, SFB, D=None, *, scale: float = 1.0, bias=None, residual=None,
+               beta: float = 1.0, activation: str = "none", out_dtype=None,
+               options: tg_options | None = None, stream=None):
+    """Block-scaled (MXFP8) GEMM: as gemm_fp8, with every 32 consecutive
+    elements along K of a row of A (of Bt) scaled by 2^(e - 127), e the
+    uint8 E8M0 code in SFA [.., M, ceil(K/32)] (SFB [.., N, ceil(K/32)])."""
+    import torch
+
+    D, ep, args = _fp8_call(A, Bt, D, scale, bias, residual, beta, activation, out_dtype)
+    M, N, K, batch = args[3], args[4], args[5], args[9]
+    runs = -(-K // 32)
+    geo = []
+    for sf, rows, name in ((SFA, M, "SFA"), (SFB, N, "SFB")):
+        if sf.dtype != torch.uint8 or not sf.is_cuda:
+            raise TypeError(f"{name} must be a uint8 CUDA tensor")
+        p, r, c, ld, b, sb = _operand_geometry(sf, -2, name)
+        if (r, c) != (rows, runs) or b not in (1, batch):
+            raise ValueError(f"{name} must have shape [.., {rows}, {runs}]")
+        geo.append((p, ld, sb if b > 1 else 0))
+    (pfa, ldfa, sfa_s), (pfb, ldfb, sfb_s) = geo
+    st = tg_gemm_mxfp8(*args, pfa, ldfa, sfa_s, pfb, ldfb, sfb_s, ep, _stream_ptr(stream), options)
+    if st != TG_OK:
+        raise TgError(st, "tg_gemm_mxfp8")
     return D
 
 

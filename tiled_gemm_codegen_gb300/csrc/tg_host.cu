@@ -117,6 +117,53 @@ __global__ void pack_bf16_kernel(PackJob ja, PackJob jb, int blocks_a)
     }
 }
 
+// Block-scaled operands: re-arrange one operand's E8M0 scales (rows x
+// ceil(K/32) bytes a problem, any pitch) into the blocks the GEMM kernel
+// copies with each k-block: 512 bytes per 128 rows and 128 elements of K,
+// the byte of row 32g + l and run j of the k-block at l * 16 + g * 4 + j
+// (tensor-memory lane l of cell column g after the warpx4 copy; TVM "Tensor
+// Layout", Case study: Blackwell tensor memory, the scale-factor atom of 32
+// rows on lanes, 4 scales per 32-bit column cell, replicated over the four
+// lane quadrants).  Rows and runs past the operand read as 127 (2^0): their
+// operand elements are the TMA unit's zero fill.
+struct ScaleJob {
+    const uint8_t *src;
+    uint8_t *dst;
+    int64_t rows, runs, ld, stride;  // stride: between problems (0: shared)
+    int64_t tiles, k_blocks, chunks;  // chunks = problems * tiles * k_blocks * 32
+};
+
+__global__ void scale_tile_kernel(ScaleJob ja, ScaleJob jb, int blocks_a)
+{
+    ptx::griddep_launch_dependents();
+    const bool is_a = static_cast<int>(blockIdx.x) < blocks_a;
+    const ScaleJob j = is_a ? ja : jb;
+    const int64_t bid = is_a ? blockIdx.x : blockIdx.x - blocks_a;
+    const int64_t nblocks = is_a ? blocks_a : gridDim.x - blocks_a;
+    for (int64_t c = bid * blockDim.x + threadIdx.x; c < j.chunks; c += nblocks * blockDim.x) {
+        const int64_t l = c & 31;
+        const int64_t blk = c >> 5;
+        const int64_t kb = blk % j.k_blocks;
+        const int64_t t = (blk / j.k_blocks) % j.tiles;
+        const int64_t z = blk / (j.k_blocks * j.tiles);
+        const uint8_t *src = j.src + z * j.stride;
+        uint32_t w[4];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const int64_t row = t * 128 + 32 * g + l;
+            uint32_t cell = 0;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int64_t run = 4 * kb + r;
+                const uint32_t e = (row < j.rows && run < j.runs) ? src[row * j.ld + run] : 127u;
+                cell |= e << (8 * r);
+            }
+            w[g] = cell;
+        }
+        *reinterpret_cast<uint4 *>(j.dst + c * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
 // K == 0: every entry of C is the empty sum.
 __global__ void zero_c_kernel(float *C, int64_t M, int64_t N, int64_t ldc, int64_t sC,
                               int64_t total)
@@ -142,6 +189,10 @@ struct Args {
     uint32_t mma_fmt = 0; // 8-bit operands: instruction-descriptor format fields
     bool a_cm = false;    // A stored K x M (column-major)
     bool b_cm = false;    // B stored N x K (column-major)
+    // block-scaled 8-bit operands: E8M0 scales per 32 elements of K
+    bool mx = false;
+    const uint8_t *sfa = nullptr, *sfb = nullptr;
+    int64_t ld_sfa = 0, s_sfa = 0, ld_sfb = 0, s_sfb = 0;
     // stored (rows, columns) of A and B
     int64_t a_rows() const { return a_cm ? K : M; }
     int64_t a_cols() const { return a_cm ? M : K; }
@@ -241,6 +292,7 @@ PlanInput plan_input(const Args &a, int sms, const tg_options *opt)
     in.a_tma_ok = aligned16(a.A) && (a.lda * eb) % 16 == 0 && (!batched_a || (a.sA * eb) % 16 == 0);
     in.b_tma_ok = aligned16(a.B) && (a.ldb * eb) % 16 == 0 && (!batched_b || (a.sB * eb) % 16 == 0);
     in.f8 = a.ab_bytes == 1;
+    in.mx = a.mx;
     in.c_tma_ok = aligned16(a.C) && (a.ldc * a.c_bytes) % 16 == 0 &&
                   (a.batch == 1 || (a.sC * a.c_bytes) % 16 == 0);
     in.sm_count = sms;
@@ -462,15 +514,15 @@ uint64_t single_problem_stride(uint64_t rows, uint64_t stride1)
     return (s + 15) / 16 * 16;
 }
 
-cudaError_t launch_gemm(int bn, bool pair, bool f8, const CUtensorMap &ta, const CUtensorMap &tb,
+cudaError_t launch_gemm(int bn, bool pair, bool f8, bool mx, const CUtensorMap &ta, const CUtensorMap &tb,
                         const CUtensorMap &tc, const KernelParams &p, int stages, int grid,
                         cudaStream_t s)
 {
     switch (bn) {
-        case 64: return launch_gemm_bn64(ta, tb, tc, p, stages, pair, f8, grid, s);
-        case 128: return launch_gemm_bn128(ta, tb, tc, p, stages, pair, f8, grid, s);
-        case 192: return launch_gemm_bn192(ta, tb, tc, p, stages, pair, f8, grid, s);
-        case 256: return launch_gemm_bn256(ta, tb, tc, p, stages, pair, f8, grid, s);
+        case 64: return launch_gemm_bn64(ta, tb, tc, p, stages, pair, f8, mx, grid, s);
+        case 128: return launch_gemm_bn128(ta, tb, tc, p, stages, pair, f8, mx, grid, s);
+        case 192: return launch_gemm_bn192(ta, tb, tc, p, stages, pair, f8, mx, grid, s);
+        case 256: return launch_gemm_bn256(ta, tb, tc, p, stages, pair, f8, mx, grid, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -643,7 +695,8 @@ tg_status run_gemm(const Args &a, cudaStream_t stream, const tg_options *opt,
         if (grid != plan.grid) replan_stream_k(in, plan, grid);
     }
 
-    const size_t arena_need = static_cast<size_t>(plan.ws_pack_a + plan.ws_pack_b + plan.ws_partials);
+    const size_t arena_need = static_cast<size_t>(plan.ws_pack_a + plan.ws_pack_b + plan.ws_partials +
+                                                  plan.ws_scales_a + plan.ws_scales_b);
     if (arena_need > 0) {
         st = grow(&w.arena, &w.arena_cap, arena_need, stream);
         if (st != TG_OK) return st;
@@ -656,6 +709,19 @@ tg_status run_gemm(const Args &a, cudaStream_t stream, const tg_options *opt,
     uint16_t *pack_a_buf = reinterpret_cast<uint16_t *>(arena);
     uint16_t *pack_b_buf = reinterpret_cast<uint16_t *>(arena + plan.ws_pack_a);
     float *partials = reinterpret_cast<float *>(arena + plan.ws_pack_a + plan.ws_pack_b);
+    uint8_t *scales_a = arena + plan.ws_pack_a + plan.ws_pack_b + plan.ws_partials;
+    uint8_t *scales_b = scales_a + plan.ws_scales_a;
+    if (plan.mx) {
+        const int64_t runs = ceil_div(a.K, 32);
+        const int64_t za = in.a_bcast ? 1 : a.batch, zb = in.b_bcast ? 1 : a.batch;
+        const ScaleJob ja{a.sfa, scales_a, a.M, runs, a.ld_sfa, a.batch > 1 ? a.s_sfa : 0,
+                          plan.tiles_m, plan.k_blocks, za * plan.tiles_m * static_cast<int64_t>(plan.k_blocks) * 32};
+        const ScaleJob jb{a.sfb, scales_b, a.N, runs, a.ld_sfb, a.batch > 1 ? a.s_sfb : 0,
+                          plan.tiles_n, plan.k_blocks, zb * plan.tiles_n * static_cast<int64_t>(plan.k_blocks) * 32};
+        const int blocks_a = grid_for(ja.chunks, sms), blocks_b = grid_for(jb.chunks, sms);
+        scale_tile_kernel<<<blocks_a + blocks_b, 256, 0, stream>>>(ja, jb, blocks_a);
+        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_status(e);
+    }
 
     if (plan.pack_a || plan.pack_b) {
         PackJob ja{}, jb{};
@@ -738,7 +804,9 @@ tg_status run_gemm(const Args &a, cudaStream_t stream, const tg_options *opt,
                      (long long)plan.units, plan.grid, plan.pack_a, plan.pack_b, plan.epilogue);
 
     p.mma_fmt = a.mma_fmt;
-    e = launch_gemm(plan.bn, plan.pair, plan.f8, ta, tb, tc, p, plan.stages, grid, stream);
+    p.sfa = plan.mx ? scales_a : nullptr;
+    p.sfb = plan.mx ? scales_b : nullptr;
+    e = launch_gemm(plan.bn, plan.pair, plan.f8, plan.mx, ta, tb, tc, p, plan.stages, grid, stream);
     return cuda_status(e);
 }
 
@@ -779,7 +847,7 @@ cudaError_t shared_launch_gemm(int bn, const CUtensorMap &ta, const CUtensorMap 
                                const CUtensorMap &tc, const KernelParams &p, int stages, int grid,
                                cudaStream_t s)
 {
-    return launch_gemm(bn, false, false, ta, tb, tc, p, stages, grid, s);
+    return launch_gemm(bn, false, false, false, ta, tb, tc, p, stages, grid, s);
 }
 
 cudaError_t shared_zero_fill(float *C, int64_t M, int64_t N, int64_t ldc, int64_t sC, int64_t batch,
@@ -972,32 +1040,48 @@ TG_API tg_status tg_gemm_fused(const void *A, const void *B, void *D, int64_t M,
     return run_gemm(a, reinterpret_cast<cudaStream_t>(stream), opt, ep);
 }
 
-TG_API tg_status tg_gemm_fp8(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K,
-                             int64_t lda, int64_t ldb, int64_t ldd, int64_t batch, int64_t strideA,
-                             int64_t strideB, int64_t strideD, int32_t a_format, int32_t b_format,
-                             const tg_epilogue *ep, tg_stream_t stream, const tg_options *opt)
+namespace tg {
+namespace {
+
+// The shared part of the 8-bit entry points: the layout, formats and
+// requirements of tg_gemm_fp8, then the call.  `a` holds the operands, D and
+// (block-scaled) the scales; its checks of the scales are the caller's.
+tg_status run_fp8(Args a, int32_t a_format, int32_t b_format, const tg_epilogue *ep, cudaStream_t stream,
+                  const tg_options *opt)
 {
-    using namespace tg;
     if (a_format != TG_FP8_E4M3 && a_format != TG_FP8_E5M2) return TG_ERR_INVALID_ARG;
     if (b_format != TG_FP8_E4M3 && b_format != TG_FP8_E5M2) return TG_ERR_INVALID_ARG;
     if (opt && (opt->a_col_major || opt->b_col_major || opt->force_pack)) return TG_ERR_INVALID_ARG;
     if (ep && ep->out_type != TG_F32 && ep->out_type != TG_BF16) return TG_ERR_INVALID_ARG;
     // A row-major M x K, B stored N x K (column-major K x N): both K-major
-    Args a{A, B, D, M, N, K, lda, ldb, ldd, batch, strideA, strideB, strideD};
     a.b_cm = true;
     a.ab_bytes = 1;
     a.c_bytes = ep && ep->out_type == TG_BF16 ? 2 : 4;
-    // kind::f8f6f4 operand formats: E4M3 = 0, E5M2 = 1 (bits 7-9 A, 10-12 B)
+    // kind::f8f6f4 / kind::mxf8f6f4 operand formats: E4M3 = 0, E5M2 = 1
+    // (bits 7-9 A, 10-12 B)
     a.mma_fmt = (static_cast<uint32_t>(a_format) << 7) | (static_cast<uint32_t>(b_format) << 10);
     tg_status st = validate(a);
     if (st != TG_OK) return st;
-    if (M == 0 || N == 0) return TG_OK;
+    if (a.M == 0 || a.N == 0) return TG_OK;
     if (ep && (st = check_epilogue(a, ep)) != TG_OK) return st;
-    if (K > 0) {
+    if (a.mx && a.K > 0) {
+        // the scale matrices lie apart from D
+        const int64_t runs = ceil_div(a.K, 32);
+        if (!span_ok(a.M, runs, a.ld_sfa, a.batch, a.s_sfa) || !span_ok(a.N, runs, a.ld_sfb, a.batch, a.s_sfb))
+            return TG_ERR_INVALID_ARG;
+        const uintptr_t d0 = reinterpret_cast<uintptr_t>(a.C);
+        const uintptr_t d1 = d0 + a.c_bytes * static_cast<uintptr_t>(span_elems(a.M, a.N, a.ldc, a.batch, a.sC));
+        const uintptr_t f0 = reinterpret_cast<uintptr_t>(a.sfa);
+        const uintptr_t f1 = f0 + static_cast<uintptr_t>(span_elems(a.M, runs, a.ld_sfa, a.batch, a.s_sfa));
+        const uintptr_t g0 = reinterpret_cast<uintptr_t>(a.sfb);
+        const uintptr_t g1 = g0 + static_cast<uintptr_t>(span_elems(a.N, runs, a.ld_sfb, a.batch, a.s_sfb));
+        if (ranges_overlap(d0, d1, f0, f1) || ranges_overlap(d0, d1, g0, g1)) return TG_ERR_INVALID_ARG;
+    }
+    if (a.K > 0) {
         // 16-byte rows: the TMA unit loads the operands as they are
-        const bool batched_a = batch > 1 && strideA != 0, batched_b = batch > 1 && strideB != 0;
-        if ((reinterpret_cast<uintptr_t>(A) & 15u) || (reinterpret_cast<uintptr_t>(B) & 15u) || lda % 16 ||
-            ldb % 16 || (batched_a && strideA % 16) || (batched_b && strideB % 16))
+        const bool batched_a = a.batch > 1 && a.sA != 0, batched_b = a.batch > 1 && a.sB != 0;
+        if ((reinterpret_cast<uintptr_t>(a.A) & 15u) || (reinterpret_cast<uintptr_t>(a.B) & 15u) || a.lda % 16 ||
+            a.ldb % 16 || (batched_a && a.sA % 16) || (batched_b && a.sB % 16))
             return TG_ERR_UNSUPPORTED;
         if (opt) {
             PlanInput in = plan_input(a, 148, opt);
@@ -1005,7 +1089,53 @@ TG_API tg_status tg_gemm_fp8(const void *A, const void *B, void *D, int64_t M, i
             if (!make_plan(in, pl)) return TG_ERR_INVALID_ARG;
         }
     }
-    return run_gemm(a, reinterpret_cast<cudaStream_t>(stream), opt, ep);
+    return run_gemm(a, stream, opt, ep);
+}
+
+}  // namespace
+}  // namespace tg
+
+TG_API tg_status tg_gemm_fp8(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K,
+                             int64_t lda, int64_t ldb, int64_t ldd, int64_t batch, int64_t strideA,
+                             int64_t strideB, int64_t strideD, int32_t a_format, int32_t b_format,
+                             const tg_epilogue *ep, tg_stream_t stream, const tg_options *opt)
+{
+    using namespace tg;
+    const Args a{A, B, D, M, N, K, lda, ldb, ldd, batch, strideA, strideB, strideD};
+    return run_fp8(a, a_format, b_format, ep, reinterpret_cast<cudaStream_t>(stream), opt);
+}
+
+TG_API tg_status tg_gemm_mxfp8(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K,
+                               int64_t lda, int64_t ldb, int64_t ldd, int64_t batch, int64_t strideA,
+                               int64_t strideB, int64_t strideD, int32_t a_format, int32_t b_format,
+                               const uint8_t *SFA, int64_t ld_sfa, int64_t stride_sfa, const uint8_t *SFB,
+                               int64_t ld_sfb, int64_t stride_sfb, const tg_epilogue *ep, tg_stream_t stream,
+                               const tg_options *opt)
+{
+    using namespace tg;
+    Args a{A, B, D, M, N, K, lda, ldb, ldd, batch, strideA, strideB, strideD};
+    a.mx = true;
+    a.sfa = SFA;
+    a.sfb = SFB;
+    a.ld_sfa = ld_sfa;
+    a.s_sfa = stride_sfa;
+    a.ld_sfb = ld_sfb;
+    a.s_sfb = stride_sfb;
+    if (opt && ((opt->block_n != 0 && opt->block_n != 128) || opt->cta_pair == 2 ||
+                (opt->stages != 0 && opt->stages != 2 && opt->stages != 4)))
+        return TG_ERR_INVALID_ARG;
+    if (stride_sfa < 0 || stride_sfb < 0 || K < 0) return TG_ERR_INVALID_ARG;
+    if (K > 0) {
+        const int64_t runs = (K + 31) / 32;
+        if (!SFA || !SFB || ld_sfa < runs || ld_sfb < runs) return TG_ERR_INVALID_ARG;
+        const int64_t LIMIT = int64_t(1) << 40;
+        if (ld_sfa > LIMIT || ld_sfb > LIMIT || stride_sfa > LIMIT || stride_sfb > LIMIT) return TG_ERR_INVALID_ARG;
+        // shared operands have shared scales (the re-arranged scales follow
+        // the operand's problem index)
+        if (batch > 1 && ((strideA == 0 && stride_sfa != 0) || (strideB == 0 && stride_sfb != 0)))
+            return TG_ERR_INVALID_ARG;
+    }
+    return run_fp8(a, a_format, b_format, ep, reinterpret_cast<cudaStream_t>(stream), opt);
 }
 
 TG_API tg_status tg_plan(const void *A, const void *B, const float *C, int64_t M, int64_t N,

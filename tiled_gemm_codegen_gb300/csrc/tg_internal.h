@@ -65,6 +65,11 @@ struct KernelParams {
     int64_t sk_iters;
     unsigned long long *trace;  // grid x 8 timestamps, or null
     uint32_t mma_fmt;           // 8-bit operands: A format << 7 | B format << 10
+    // Block-scaled operands: E8M0 scales pre-arranged in 512-byte blocks,
+    // block ((z * tiles + t) * k_blocks + kb) for problem z, 128-row (A) or
+    // 128-column (B) tile t and k-block kb.
+    const uint8_t *sfa;
+    const uint8_t *sfb;
 };
 
 // Shared-memory budget of one tile width.  PAIR: the tile is computed by a
@@ -78,6 +83,7 @@ struct Geometry {
     static constexpr int STAGE = A_STAGE + B_STAGE;
     static constexpr int EPI_BYTES = 4 * EPI_BUFS * EPI_CHUNK * EPI_CHUNK * 4;  // 32 KB
     static constexpr int BAR_BYTES = 512;
+    static constexpr int SF_STAGE = 1024;  // block-scaled operands: scales of one slot
     static constexpr int ALIGN_SLACK = 1024;
     static constexpr int MAX_STAGES_RAW = (SMEM_LIMIT - EPI_BYTES - BAR_BYTES - ALIGN_SLACK) / STAGE;
     static constexpr int MAX_STAGES = MAX_STAGES_RAW > 8 ? 8 : MAX_STAGES_RAW;
@@ -90,16 +96,17 @@ struct Geometry {
                    ? stages * STAGE + EPI_BYTES + BAR_BYTES + ALIGN_SLACK
                    : ONE_CTA_PER_SM;
     }
+    static constexpr int smem_bytes_mx(int stages) { return smem_bytes(stages) + stages * SF_STAGE; }
 };
 
 // Launch of the persistent GEMM kernel for one tile width (defined in the
 // per-width translation units).  pair: two-SM tiles (grid counts CTAs, a
-// multiple of 2); f8: 8-bit floating-point operands.  Returns the launch's
-// cudaError_t.
+// multiple of 2); f8: 8-bit floating-point operands; mx: block-scaled 8-bit
+// operands (width 128, one CTA per tile).  Returns the launch's cudaError_t.
 #define TG_DECLARE_LAUNCH(BN_)                                                                   \
     cudaError_t launch_gemm_bn##BN_(const CUtensorMap &ta, const CUtensorMap &tb,                \
                                     const CUtensorMap &tc, const KernelParams &p, int stages,   \
-                                    bool pair, bool f8, int grid, cudaStream_t s);              \
+                                    bool pair, bool f8, bool mx, int grid, cudaStream_t s);     \
     int max_pairs_bn##BN_(int stages, bool f8);
 TG_DECLARE_LAUNCH(64)
 TG_DECLARE_LAUNCH(128)

@@ -321,7 +321,16 @@ __device__ __forceinline__ void apply_epilogue(const KernelParams &p, uint32_t (
 // F8: 8-bit floating-point operands (tcgen05 kind::f8f6f4, formats in
 // p.mma_fmt), K-major A and B only; a k-block is then 128 elements (still
 // 128 bytes a row) and each of its 4 MMAs takes K = 32.
-template <int BN, int STAGES, bool PAIR, bool F8 = false>
+// MX (with F8, one-CTA 128 x 128 tiles): block-scaled operands
+// (kind::mxf8f6f4): every 32 consecutive elements of a row of A (of a
+// column of B) along K share one E8M0 power-of-two scale.  The scales of a
+// k-block come pre-arranged as one 512-byte block per 128 rows of A and one
+// per 128 columns of B (the byte of row 32g + l and K group j at
+// l * 16 + g * 4 + j); the producer bulk-copies both with the slot's
+// operands, and the MMA thread moves them to tensor memory (tcgen05.cp,
+// columns 256 + 8s ..) ahead of the slot's four MMAs, the j-th of which
+// reads byte j of each 32-bit scale cell.
+template <int BN, int STAGES, bool PAIR, bool F8 = false, bool MX = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const KernelParams p)
@@ -330,12 +339,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "tile width");
     static_assert(!PAIR || G::B_COLS % 64 == 0, "two-SM tiles need 64-column halves of B");
     static_assert(G::smem_bytes(STAGES) <= SMEM_LIMIT, "shared memory budget");
+    static_assert(!MX || (F8 && !PAIR && BN == 128), "block scaling: one-CTA 128 x 128 tiles");
+    static_assert(!MX || G::smem_bytes_mx(STAGES) <= SMEM_LIMIT, "shared memory budget (scales)");
     constexpr int TILE_M = PAIR ? 2 * BM : BM;
     constexpr int B_BOXES = G::B_COLS / 64;
     constexpr uint32_t B_BOX_BYTES = BK * 64 * 2;  // one 64-column box of B: 8 KB
     constexpr uint32_t EPI_BOX_BYTES = EPI_CHUNK * EPI_CHUNK * 4;  // 4 KB
     constexpr uint32_t EPI_WARPS_TOTAL = PAIR ? 8 : 4;  // arrivals on tempty per tile
     constexpr int KBLK = F8 ? 2 * BK : BK;              // elements of K per k-block (128 bytes)
+    // MX: the scale blocks of a slot (512 B of A's, 512 B of B's) travel with
+    // its operands; tensor memory holds both accumulators (columns 0-255)
+    // and the slots' scales (columns 256 + 8s: A's 4, then B's 4).
+    constexpr uint32_t TX_BYTES = G::STAGE + (MX ? G::SF_STAGE : 0);
+    constexpr uint32_t TMEM_ALLOC = MX ? 512u : static_cast<uint32_t>(G::TMEM_COLS);
+    constexpr uint32_t SF_COL0 = 2 * BN;
+    static_assert(!MX || SF_COL0 + 8 * STAGES <= TMEM_ALLOC, "scale columns");
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
@@ -346,6 +364,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t sE = sB + STAGES * G::B_STAGE;   // 4 warps x EPI_BUFS x 4 KB
     uint8_t *bar_area = smem + STAGES * G::STAGE + G::EPI_BYTES;
     const uint32_t bar0 = ptx::smem_addr(bar_area);
+    const uint32_t sSF = bar0 + G::BAR_BYTES;  // MX: STAGES x 1 KB of scales
     // barrier k lives at bar0 + 8k:
     //   [0, S) full   [S, 2S) empty   2S+{0,1} tfull   2S+{2,3} tempty
     //   2S+4 mma-done   2S+5 stall (never completed)
@@ -396,10 +415,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     if (warp == 1) {
         if constexpr (PAIR) {
-            ptx::tmem_alloc_pair(ptx::smem_addr(tmem_slot), G::TMEM_COLS);
+            ptx::tmem_alloc_pair(ptx::smem_addr(tmem_slot), TMEM_ALLOC);
             ptx::tmem_relinquish_pair();
         } else {
-            ptx::tmem_alloc(ptx::smem_addr(tmem_slot), G::TMEM_COLS);
+            ptx::tmem_alloc(ptx::smem_addr(tmem_slot), TMEM_ALLOC);
             ptx::tmem_relinquish();
         }
     }
@@ -447,7 +466,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         if (leader) ptx::mbar_arrive_expect_tx(full_bar(s), 2 * G::STAGE);
                         fb = full0 + 8u * s;
                     } else {
-                        ptx::mbar_arrive_expect_tx(full_bar(s), G::STAGE);
+                        ptx::mbar_arrive_expect_tx(full_bar(s), TX_BYTES);
                         fb = full_bar(s);
                     }
                     auto load = [&](uint32_t dst, const CUtensorMap *map, int32_t c0, int32_t c1, int32_t c2) {
@@ -475,6 +494,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         // B column-major: one box [B_COLS columns x 64 k], K-major atoms
                         load(b_dst, &tmB, kb * KBLK, n_cols, zB);
                     }
+                    if constexpr (MX) {
+                        const int64_t fa = (static_cast<int64_t>(zA) * p.tiles_m + w.tm) * p.k_blocks + kb;
+                        const int64_t fbk = (static_cast<int64_t>(zB) * p.tiles_n + w.tn) * p.k_blocks + kb;
+                        ptx::bulk_load(sSF + s * G::SF_STAGE, p.sfa + fa * 512, 512, fb);
+                        ptx::bulk_load(sSF + s * G::SF_STAGE + 512, p.sfb + fbk * 512, 512, fb);
+                    }
                 }
             }
             *issued_slot = it;
@@ -492,6 +517,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // B format fields (bits 7-12) differ
             const uint32_t idesc_bf16 = instr_desc_bf16<TILE_M, BN>(p.a_mn != 0, p.b_k == 0);
             const uint32_t idesc = F8 ? ((idesc_bf16 & ~(0x3Fu << 7)) | p.mma_fmt) : idesc_bf16;
+            // kind::mxf8f6f4: no D format field (bits 4-5 hold B's scale
+            // byte), scale type E8M0 (bit 23), A's scale byte at bits 29-30
+            const uint32_t idesc_mx = p.mma_fmt | (static_cast<uint32_t>(BN >> 3) << 17) | (1u << 23) |
+                                      (static_cast<uint32_t>(TILE_M >> 4) << 24);
             // Layout-dependent descriptor parts, fixed for the whole kernel:
             // a K-major operand steps 32 B per 16 k (leading offset unused);
             // an MN-major one steps 16 rows x 128 B and its 64-element atoms
@@ -529,12 +558,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     ptx::tc_fence_after();
                     const uint32_t a_addr = sA + s * G::A_STAGE;
                     const uint32_t b_addr = sB + s * G::B_STAGE;
+                    const uint32_t sf_tmem = tmem_base + SF_COL0 + 8u * s;
+                    if constexpr (MX) {
+                        // no-swizzle descriptors of the two 512-byte scale
+                        // blocks: 8-row core matrices 128 B apart
+                        const uint64_t sf_desc = (static_cast<uint64_t>(128 >> 4) << 16) |
+                                                 (static_cast<uint64_t>(128 >> 4) << 32) | (1ull << 46);
+                        const uint32_t sf_smem = sSF + s * G::SF_STAGE;
+                        ptx::tmem_cp_32x128b_x4(sf_tmem, sf_desc | ((sf_smem >> 4) & 0x3FFFu));
+                        ptx::tmem_cp_32x128b_x4(sf_tmem + 4, sf_desc | (((sf_smem + 512) >> 4) & 0x3FFFu));
+                    }
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
                         const uint64_t ad = a_desc0 | (((a_addr + kk * a_step) >> 4) & 0x3FFFu);
                         const uint64_t bd = b_desc0 | (((b_addr + kk * b_step) >> 4) & 0x3FFFu);
                         const uint32_t acc = (kb > w.kb0 || kk > 0) ? 1u : 0u;
-                        if constexpr (PAIR && F8)
+                        if constexpr (MX)
+                            ptx::mma_mx(d_tmem, ad, bd,
+                                        idesc_mx | (static_cast<uint32_t>(kk) << 29) | (static_cast<uint32_t>(kk) << 4),
+                                        sf_tmem, sf_tmem + 4, acc);
+                        else if constexpr (PAIR && F8)
                             ptx::mma_f8_pair(d_tmem, ad, bd, idesc, acc);
                         else if constexpr (PAIR)
                             ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, acc);
@@ -837,19 +880,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncwarp();
         ptx::tc_fence_after();
         if constexpr (PAIR)
-            ptx::tmem_dealloc_pair(tmem_base, G::TMEM_COLS);
+            ptx::tmem_dealloc_pair(tmem_base, TMEM_ALLOC);
         else
-            ptx::tmem_dealloc(tmem_base, G::TMEM_COLS);
+            ptx::tmem_dealloc(tmem_base, TMEM_ALLOC);
     }
     if (threadIdx.x == 0) stamp(7);
 }
 
-template <int BN, int STAGES, bool PAIR, bool F8 = false>
+template <int BN, int STAGES, bool PAIR, bool F8 = false, bool MX = false>
 cudaError_t launch_fixed(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
                          const KernelParams &p, int grid, cudaStream_t s)
 {
-    constexpr int smem = Geometry<BN, PAIR>::smem_bytes(STAGES);
-    auto kern = gemm_kernel<BN, STAGES, PAIR, F8>;
+    constexpr int smem = MX ? Geometry<BN, PAIR>::smem_bytes_mx(STAGES) : Geometry<BN, PAIR>::smem_bytes(STAGES);
+    auto kern = gemm_kernel<BN, STAGES, PAIR, F8, MX>;
     // the shared-memory opt-in is per device; set it once per device
     static std::atomic<unsigned long long> configured{0};
     int dev = 0;

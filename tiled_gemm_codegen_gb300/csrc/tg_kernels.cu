@@ -2,8 +2,9 @@
 // width (selected at build time with -DTG_BN=...), so the widths compile in
 // parallel.  Each width instantiates a few ring depths, with one CTA per tile
 // and (widths 128 and 256) two-SM tiles, for bf16 operands and (a subset)
-// 8-bit floating-point ones; stage_supported() in tg_plan.h lists them and
-// the host planner only picks listed configurations.
+// 8-bit floating-point ones (width 128 also block-scaled 8-bit ones, rings
+// 2 and 4); stage_supported() and mx_stage_supported() in tg_plan.h list
+// them and the host planner only picks listed configurations.
 #include "tg_kernel.cuh"
 #include "tg_plan.h"
 
@@ -43,8 +44,21 @@ namespace tg {
 
 cudaError_t TG_CAT(launch_gemm_bn, TG_BN)(const CUtensorMap &ta, const CUtensorMap &tb,
                                           const CUtensorMap &tc, const KernelParams &p,
-                                          int stages, bool pair, bool f8, int grid, cudaStream_t s)
+                                          int stages, bool pair, bool f8, bool mx, int grid, cudaStream_t s)
 {
+    if (mx) {
+        // block-scaled 8-bit operands: width 128, one CTA per tile
+        if (pair || !f8) return cudaErrorInvalidValue;
+#if TG_BN == 128
+        switch (stages) {
+            case 2: return launch_fixed<128, 2, false, true, true>(ta, tb, tc, p, grid, s);
+            case 4: return launch_fixed<128, 4, false, true, true>(ta, tb, tc, p, grid, s);
+            default: return cudaErrorInvalidValue;
+        }
+#else
+        return cudaErrorInvalidValue;
+#endif
+    }
     if (pair && f8) TG_SWITCH(true, true)
     if (pair) TG_SWITCH(true, false)
     if (f8) TG_SWITCH(false, true)

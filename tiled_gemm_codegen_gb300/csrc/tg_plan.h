@@ -46,6 +46,12 @@ constexpr bool stage_supported(int bn, int s, bool pair = false, bool f8 = false
     }
 }
 
+// Block-scaled 8-bit operands: one-CTA tiles of width 128, rings 2 and 4.
+constexpr bool mx_stage_supported(int bn, int s, bool pair = false)
+{
+    return !pair && bn == 128 && (s == 2 || s == 4);
+}
+
 template <bool PAIR>
 constexpr int max_stages_t(int bn)
 {
@@ -101,11 +107,13 @@ struct PlanInput {
     int stream_k;  // 0 = choose, 1 = off, 2 = on (when the last wave is partial)
     bool a_cm = false, b_cm = false;  // column-major (transposed) operand storage
     bool f8 = false;                  // 8-bit floating-point A and B (K-major)
+    bool mx = false;                  // f8 with per-32-element E8M0 block scales
 };
 
 struct Plan {
     bool pair = false;  // two-SM tiles (256 rows, cluster of 2)
     bool f8 = false;    // 8-bit operands: 128 elements of K per k-block
+    bool mx = false;    // block-scaled 8-bit operands
     int bn = 0, stages = 0;
     int tiles_m = 0, tiles_n = 0, k_blocks = 0, splits = 1;
     int64_t units = 0;
@@ -119,7 +127,13 @@ struct Plan {
     int dp_waves = 0, maxparts = 1;
     int64_t sk_first_tile = 0, sk_tiles = 0, sk_iters = 0;
     int64_t ws_pack_a = 0, ws_pack_b = 0, ws_partials = 0, ws_counters = 0;
-    int64_t workspace() const { return ws_pack_a + ws_pack_b + ws_partials + ws_counters; }
+    // block-scaled operands: the scales re-arranged into 512-byte blocks
+    // (one per 128 rows or columns and k-block), A's then B's
+    int64_t ws_scales_a = 0, ws_scales_b = 0;
+    int64_t workspace() const
+    {
+        return ws_pack_a + ws_pack_b + ws_partials + ws_counters + ws_scales_a + ws_scales_b;
+    }
 };
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -255,6 +269,8 @@ inline bool make_plan(const PlanInput &in, Plan &out)
 {
     Plan p;
     p.f8 = in.f8;
+    p.mx = in.mx;
+    if (in.mx && !in.f8) return false;
     const int sms = in.sm_count > 0 ? in.sm_count : 1;
     const int64_t kb = ceil_div(in.K, in.f8 ? 2 * BK : BK);  // a k-block is 128 bytes of K
     if (in.f8 && (in.a_cm || !in.b_cm || in.force_pack || !in.a_tma_ok || !in.b_tma_ok)) return false;
@@ -285,6 +301,7 @@ inline bool make_plan(const PlanInput &in, Plan &out)
         if (in.cta_pair == 2 && !cd.pair) continue;
         if (in.cta_pair == 0 && cd.pair && !PAIR_BY_DEFAULT) continue;
         if (in.f8 && !stage_supported(cd.bn, 2, cd.pair, true)) continue;  // no 8-bit instance
+        if (in.mx && !mx_stage_supported(cd.bn, 2, cd.pair)) continue;
         const int tile_m = cd.pair ? 2 * BM : BM;
         const int64_t tiles_m = ceil_div(in.M, tile_m);
         const int64_t tiles_n = ceil_div(in.N, cd.bn);
@@ -320,7 +337,10 @@ inline bool make_plan(const PlanInput &in, Plan &out)
     if (!have) return false;
 
     // Ring depth: the deepest instantiated one unless overridden.
-    if (in.stages != 0) {
+    if (in.mx) {
+        if (in.stages != 0 && !mx_stage_supported(p.bn, in.stages, p.pair)) return false;
+        p.stages = in.stages != 0 ? in.stages : 4;
+    } else if (in.stages != 0) {
         if (!stage_supported(p.bn, in.stages, p.pair, in.f8)) return false;
         p.stages = in.stages;
     } else {
@@ -357,6 +377,10 @@ inline bool make_plan(const PlanInput &in, Plan &out)
     p.epilogue = in.epilogue != 0 ? in.epilogue : (in.c_tma_ok ? 1 : 2);
     p.smem = smem_bytes_for(p.bn, p.stages, p.pair);
     p.tmem = tmem_cols_for(p.bn);
+    if (p.mx) {
+        p.smem = Geometry<128>::smem_bytes_mx(p.stages);
+        p.tmem = 512;  // accumulators and the slots' scales
+    }
 
     const int64_t batch_a = in.a_bcast ? 1 : in.batch;
     const int64_t batch_b = in.b_bcast ? 1 : in.batch;
@@ -365,6 +389,10 @@ inline bool make_plan(const PlanInput &in, Plan &out)
     const int64_t b_rows = in.b_cm ? in.N : in.K, b_cols = in.b_cm ? in.K : in.N;
     p.ws_pack_a = p.pack_a ? round_up(batch_a * a_rows * pack_pitch(a_cols) * 2, 256) : 0;
     p.ws_pack_b = p.pack_b ? round_up(batch_b * b_rows * pack_pitch(b_cols) * 2, 256) : 0;
+    if (p.mx) {
+        p.ws_scales_a = round_up(batch_a * p.tiles_m * static_cast<int64_t>(p.k_blocks) * 512, 256);
+        p.ws_scales_b = round_up(batch_b * p.tiles_n * static_cast<int64_t>(p.k_blocks) * 512, 256);
+    }
     set_partial_workspace(in, p);
     out = p;
     return true;

@@ -309,6 +309,40 @@ __device__ __forceinline__ void mma_f8_pair(uint32_t d_tmem, uint64_t a_desc, ui
         : "memory");
 }
 
+// Block-scaled 8-bit MMA (kind::mxf8f6f4, one E8M0 scale per 32 elements of
+// K): D (+)= (SFA . A) x (SFB . B).  sfa / sfb are the tensor-memory
+// addresses of the scale factors; idesc selects which byte of their 32-bit
+// cells this instruction's K = 32 uses.
+__device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t sfa, uint32_t sfb, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+}
+
+// Shared memory -> tensor memory: 32 rows of 16 bytes (described by the
+// no-swizzle matrix descriptor sdesc) into 4 columns of lanes 0-31,
+// replicated into each of the four 32-lane quadrants.  Ordered with the
+// issuing thread's later tcgen05.mma.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc)
+{
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Plain bulk copy global -> this CTA's shared memory, completing `bytes` on
+// mbarrier `bar` (addresses 16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
 // Arrive once on the mbarrier at offset `bar` in every CTA of `cta_mask` when
 // this thread's earlier tcgen05 ops are done.
 __device__ __forceinline__ void mma_commit_pair_multicast(uint32_t bar, uint16_t cta_mask)
