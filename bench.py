@@ -225,7 +225,8 @@ def run_gpu(args, rank, world, local, dist):
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     w = synth.WORKLOADS[args.workload]
-    f8 = args.dtype == "e4m3"
+    f8 = args.dtype in ("e4m3", "mxfp8")
+    mx = args.dtype == "mxfp8"
     C = torch.empty((w.batch, w.M, w.N) if w.batch > 1 else (w.M, w.N), dtype=torch.float32, device=device)
     if f8:
         # the same shape with E4M3 operands (N(0,1) draws rounded to E4M3),
@@ -236,6 +237,13 @@ def run_gpu(args, rank, world, local, dist):
         B = synth.make_fp8_codes(lead + (w.N, w.K), 0, seed=w.seed + 1, kind="normal").to(device)
         B = B.view(torch.float8_e4m3fn)
         launches_per_step = 1
+        if mx:
+            # block-scaled: one E8M0 scale (2^-3 .. 2^3) per 32 elements of K;
+            # the scale re-arrangement is a second launch
+            runs = -(-w.K // 32)
+            SFA = synth.make_e8m0_codes(lead + (w.M, runs), seed=w.seed + 2).to(device)
+            SFB = synth.make_e8m0_codes(lead + (w.N, runs), seed=w.seed + 3).to(device)
+            launches_per_step = 2
         info = {k: None for k in ("block_n", "stages", "split_k", "grid", "pack_a", "pack_b", "epilogue",
                                   "cta_pair", "stream_k", "sk_tiles")}
     else:
@@ -254,7 +262,9 @@ def run_gpu(args, rank, world, local, dist):
         torch.sum(flush_read, dim=0, out=sink)  # read > L2: dirty flush lines written back now
 
     def step():
-        if f8:
+        if mx:
+            tg.gemm_mxfp8(A, B, SFA, SFB, C)
+        elif f8:
             tg.gemm_fp8(A, B, C)
         else:
             tg.gemm(A, B, C)
@@ -371,20 +381,24 @@ def run_gpu(args, rank, world, local, dist):
 
 
 def report_f8(args, w, per, ms_mean, ms_max, world, rank, clk, wall, launches_per_step):
-    """The line of an --dtype e4m3 run: the same shape with 8-bit operands,
-    against the bf16 measured peak times the nominal 8-bit/16-bit tensor
-    ratio (2)."""
+    """The line of an --dtype e4m3 / mxfp8 run: the same shape with 8-bit
+    operands (mxfp8: with E8M0 block scales), against the bf16 measured peak
+    times the nominal 8-bit/16-bit tensor ratio (2)."""
+    mx = args.dtype == "mxfp8"
     peaks, peak_src = load_peaks()
     peak = 2.0 * float(peaks["bf16_tflops"])
     flops = float(w.flops)
     achieved = flops / (ms_mean * 1e-3) / 1e12
     bytes_moved = w.batch * (w.M * w.K + w.K * w.N + 4 * w.M * w.N)
+    if mx:
+        bytes_moved += w.batch * (w.M + w.N) * (-(-w.K // 32))
     if rank == 0:
         line = {
-            "metric": "e4m3->fp32 GEMM TFLOP/s at 1 GB300 and % of dense FP8 tensor roofline",
+            "metric": ("MXFP8 (e4m3, E8M0 scales per 32) " if mx else "e4m3") +
+                      "->fp32 GEMM TFLOP/s at 1 GB300 and % of dense FP8 tensor roofline",
             "value": round(world * flops / (ms_max * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": args.dtype,
             "data": "synthetic",
             "config": {"workload": w.name, "batch": w.batch, "M": w.M, "N": w.N, "K": w.K,
                        "layout": "A row-major, B column-major (both K-major)", "accumulate": "fp32",
@@ -412,9 +426,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--clock-window", type=float, default=0.5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--dtype", default="bf16", choices=["bf16", "e4m3"],
-                    help="operand type; e4m3 runs the same shape through tg_gemm_fp8 (an extra line, "
-                         "not the contract's metric)")
+    ap.add_argument("--dtype", default="bf16", choices=["bf16", "e4m3", "mxfp8"],
+                    help="operand type; e4m3 (mxfp8) runs the same shape through tg_gemm_fp8 "
+                         "(tg_gemm_mxfp8): an extra line, not the contract's metric")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "tg":
         ap.error("--warmup must be at least 3")

@@ -266,56 +266,68 @@ __device__ __forceinline__ uint16_t ld_shared_u16(uint32_t addr)
 //   D = act(alpha * acc + bias[col]) + beta * R[row][col]
 // The products and sums are rounded one by one (no fused multiply-add), so
 // with no activation or relu the fused result equals, bit for bit, the same
-// formula applied in fp32 to the stored product.
+// formula applied in fp32 to the stored product.  Each step is one unrolled
+// loop over the 32 values behind a single uniform branch (the activation's
+// switch sits outside its loop): this code runs from the instruction cache
+// between the accumulator loads, and an unrolled loop with every activation
+// inlined into each of its 32 bodies would not fit there.
 __device__ __forceinline__ void apply_epilogue(const KernelParams &p, uint32_t (&v)[32], int32_t row,
                                                int32_t col0, int32_t b)
 {
-    const bool row_ok = row < p.M;
-    float bias[32], res[32];
+    float x[32];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        bias[j] = 0.0f;
-        res[j] = 0.0f;
-    }
+    for (int j = 0; j < 32; ++j) x[j] = __fmul_rn(p.alpha, __uint_as_float(v[j]));
     if (p.bias) {
         const float *bp = p.bias + static_cast<int64_t>(b) * p.bias_stride + col0;
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-            if (col0 + j < p.N) bias[j] = __ldg(bp + j);
+            if (col0 + j < p.N) x[j] = __fadd_rn(x[j], __ldg(bp + j));
     }
-    if (p.residual && row_ok) {
+    switch (p.act) {
+        case 1:
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x[j] = activation(x[j], 1);
+            break;
+        case 2:
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x[j] = activation(x[j], 2);
+            break;
+        case 3:
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x[j] = activation(x[j], 3);
+            break;
+        default:
+            break;
+    }
+    // Rows past M are never stored: their residual is not read.
+    if (p.residual && row < p.M) {
         const int64_t off = static_cast<int64_t>(b) * p.strideR + static_cast<int64_t>(row) * p.ldr + col0;
         if (p.out_bf16) {
             const uint16_t *rp = static_cast<const uint16_t *>(p.residual) + off;
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-                if (col0 + j < p.N) res[j] = __uint_as_float(static_cast<uint32_t>(rp[j]) << 16);
+                if (col0 + j < p.N)
+                    x[j] = __fadd_rn(x[j], __fmul_rn(p.beta, __uint_as_float(static_cast<uint32_t>(rp[j]) << 16)));
         } else {
             const float *rp = static_cast<const float *>(p.residual) + off;
             if ((reinterpret_cast<uintptr_t>(rp) & 15u) == 0 && col0 + 32 <= p.N) {
 #pragma unroll
                 for (int j = 0; j < 32; j += 4) {
                     const float4 t = *reinterpret_cast<const float4 *>(rp + j);
-                    res[j] = t.x;
-                    res[j + 1] = t.y;
-                    res[j + 2] = t.z;
-                    res[j + 3] = t.w;
+                    x[j] = __fadd_rn(x[j], __fmul_rn(p.beta, t.x));
+                    x[j + 1] = __fadd_rn(x[j + 1], __fmul_rn(p.beta, t.y));
+                    x[j + 2] = __fadd_rn(x[j + 2], __fmul_rn(p.beta, t.z));
+                    x[j + 3] = __fadd_rn(x[j + 3], __fmul_rn(p.beta, t.w));
                 }
             } else {
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
-                    if (col0 + j < p.N) res[j] = rp[j];
+                    if (col0 + j < p.N) x[j] = __fadd_rn(x[j], __fmul_rn(p.beta, rp[j]));
             }
         }
     }
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        float x = __fmul_rn(p.alpha, __uint_as_float(v[j]));
-        if (p.bias) x = __fadd_rn(x, bias[j]);
-        x = activation(x, p.act);
-        if (p.residual) x = __fadd_rn(x, __fmul_rn(p.beta, res[j]));
-        v[j] = __float_as_uint(x);
-    }
+    for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(x[j]);
 }
 
 // F8: 8-bit floating-point operands (tcgen05 kind::f8f6f4, formats in
