@@ -231,9 +231,12 @@ tg_status tg_gemm_fp8(const void *A, const void *B, void *D,
  * A scale stride of 0 shares one scale matrix across the batch; where A (B)
  * is shared (strideA == 0 with batch > 1) its scales must be too.  Scales
  * are read, never written, and may alias anything but D.  The library
- * re-arranges them into device scratch it owns (one 512-byte block per 128
- * rows or columns and 128 elements of K) on `stream` before the GEMM.
- * Tiles are 128 x 128 (one CTA each); opt->block_n must be 0 or 128,
+ * re-arranges them into device scratch it owns (512-byte blocks per 128
+ * rows or columns of a tile and 128 elements of K) on `stream` before the
+ * GEMM.
+ * Tiles are 128 rows x 224 columns (128 where that needs fewer column
+ * tiles), one CTA each: tensor memory holds two 224-column accumulators and
+ * the scales of every ring slot.  opt->block_n must be 0, 128 or 224,
  * opt->cta_pair 0 or 1, opt->stages 0, 2 or 4 (else TG_ERR_INVALID_ARG).
  * TG_ERR_INVALID_ARG also for a NULL scale pointer with K > 0, ld_sfa or
  * ld_sfb < ceil(K/32), or a negative scale stride. */

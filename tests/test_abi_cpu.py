@@ -277,6 +277,7 @@ def test_mxfp8_rejects_bad_arguments_before_any_cuda_call(lib):
     assert call(s_sfa=-8) == bad
     assert call(fa=2) == bad                            # unknown format
     assert call(opt=tg.make_options(block_n=256)) == bad
+    assert call(opt=tg.make_options(block_n=192)) == bad
     assert call(opt=tg.make_options(cta_pair=2)) == bad
     assert call(opt=tg.make_options(stages=6)) == bad
     assert call(opt=tg.make_options(a_col_major=1)) == bad
@@ -284,6 +285,18 @@ def test_mxfp8_rejects_bad_arguments_before_any_cuda_call(lib):
     assert call(batch=2, sA=0, sB=N * K, s_sfa=M * 8) == bad
     # scales overlapping D
     assert call(sfa=D + 64) == bad
+    # valid calls get past every host check (and then need a GPU): both tile
+    # widths plan, with and without options
+    assert call() == tg.TG_ERR_CUDA
+    for bn in (128, 224):
+        for st in (2, 4):
+            assert call(opt=tg.make_options(block_n=bn, stages=st)) == tg.TG_ERR_CUDA
+    assert call(opt=tg.make_options(split_k=2)) == tg.TG_ERR_CUDA
+    # the default width for a wide N (224 columns) plans too
+    wide = tg.tg_gemm_mxfp8(A, B, 0x10000000, M, 4096, K, K, K, 4096, 1, 0, 0, 0, 0, 0,
+                            0x20000000, 8, 0, 0x30000000, 8, 0, None, None, None)
+    assert wide == tg.TG_ERR_CUDA
+    assert call(opt=tg.make_options(stream_k=2)) == tg.TG_ERR_CUDA
     # K == 0: no scales needed, nothing to check (and M == 0: nothing to do)
     assert tg.tg_gemm_mxfp8(A, B, D, 0, N, K, K, K, N, 1, 0, 0, 0, 0, 0,
                             SF, 8, 0, SF, 8, 0, None, None, None) == tg.TG_OK

@@ -48,6 +48,32 @@ def test_exact_integer(M, N, K):
     assert np.array_equal(got, _oracle(A, Bt, sfa, sfb))
 
 
+@pytest.mark.parametrize("bn", [128, 224])
+@pytest.mark.parametrize("M,N,K", [(130, 224, 256), (129, 225, 160), (257, 447, 528), (64, 465, 1024),
+                                   (300, 700, 2080)])
+def test_exact_integer_tile_widths(bn, M, N, K):
+    """Both block-scaled tile widths; N around the 224-column tile and the
+    128-column scale blocks inside it."""
+    A = synth.make_fp8_codes((M, K), 0, seed=M + 5 * K)
+    Bt = synth.make_fp8_codes((N, K), 0, seed=N + 7 * K)
+    sfa = synth.make_e8m0_codes((M, _runs(K)), seed=3 + M, lo=126, hi=128)
+    sfb = synth.make_e8m0_codes((N, _runs(K)), seed=4 + N, lo=126, hi=128)
+    got = _run(A, Bt, sfa, sfb, options=tg.make_options(block_n=bn))
+    assert np.array_equal(got, _oracle(A, Bt, sfa, sfb))
+
+
+def test_tile_widths_bitwise_equal():
+    """Each output element sees the same MMA sequence at either width."""
+    M, N, K = 300, 520, 1024
+    A = synth.make_fp8_codes((M, K), 0, seed=61, kind="normal")
+    Bt = synth.make_fp8_codes((N, K), 0, seed=62, kind="normal")
+    sfa = synth.make_e8m0_codes((M, K // 32), seed=63)
+    sfb = synth.make_e8m0_codes((N, K // 32), seed=64)
+    outs = [_run(A, Bt, sfa, sfb, options=tg.make_options(block_n=bn, stream_k=1)) for bn in (128, 224)]
+    assert np.array_equal(outs[0], outs[1])
+    assert_close(outs[1], _oracle(A, Bt, sfa, sfb), K, "224 vs oracle")
+
+
 @pytest.mark.parametrize("fa,fb", [(1, 0), (0, 1), (1, 1)])
 def test_exact_integer_mixed_formats(fa, fb):
     M, N, K = 190, 333, 528
@@ -123,13 +149,14 @@ def test_shared_operand_and_scales():
     assert np.array_equal(got, want)
 
 
-def test_ring_depth_bitwise_invariance():
+@pytest.mark.parametrize("bn", [128, 224])
+def test_ring_depth_bitwise_invariance(bn):
     M, N, K = 300, 520, 1088
     A = synth.make_fp8_codes((M, K), 0, seed=9, kind="normal")
     Bt = synth.make_fp8_codes((N, K), 0, seed=10, kind="normal")
     sfa = synth.make_e8m0_codes((M, _runs(K)), seed=11)
     sfb = synth.make_e8m0_codes((N, _runs(K)), seed=12)
-    outs = [_run(A, Bt, sfa, sfb, options=tg.make_options(stages=s)) for s in (2, 4)]
+    outs = [_run(A, Bt, sfa, sfb, options=tg.make_options(stages=s, block_n=bn)) for s in (2, 4)]
     assert np.array_equal(outs[0], outs[1])
 
 
@@ -164,6 +191,8 @@ def test_argument_errors():
     assert call(sfa=None) == tg.TG_ERR_INVALID_ARG
     assert call(ld_sfb=1) == tg.TG_ERR_INVALID_ARG
     assert call(opt=tg.make_options(block_n=256)) == tg.TG_ERR_INVALID_ARG
+    assert call(opt=tg.make_options(block_n=224)) == tg.TG_OK
+    assert call(opt=tg.make_options(block_n=192)) == tg.TG_ERR_INVALID_ARG
     assert call(opt=tg.make_options(cta_pair=2)) == tg.TG_ERR_INVALID_ARG
     assert call(opt=tg.make_options(stages=6)) == tg.TG_ERR_INVALID_ARG
     assert call(s_sfa=-1) == tg.TG_ERR_INVALID_ARG

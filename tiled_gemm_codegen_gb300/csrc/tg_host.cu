@@ -125,12 +125,15 @@ __global__ void pack_bf16_kernel(PackJob ja, PackJob jb, int blocks_a)
 // Layout", Case study: Blackwell tensor memory, the scale-factor atom of 32
 // rows on lanes, 4 scales per 32-bit column cell, replicated over the four
 // lane quadrants).  Rows and runs past the operand read as 127 (2^0): their
-// operand elements are the TMA unit's zero fill.
+// operand elements are the TMA unit's zero fill.  A tile of `tile_rows` rows
+// (128, or 224 for B's 224-wide tiles) has `subs` = ceil(tile_rows / 128)
+// consecutive blocks per k-block; tile rows past tile_rows read as 127 too.
 struct ScaleJob {
     const uint8_t *src;
     uint8_t *dst;
     int64_t rows, runs, ld, stride;  // stride: between problems (0: shared)
-    int64_t tiles, k_blocks, chunks;  // chunks = problems * tiles * k_blocks * 32
+    int64_t tiles, k_blocks, chunks;  // chunks = problems * tiles * k_blocks * subs * 32
+    int64_t tile_rows, subs;
 };
 
 __global__ void scale_tile_kernel(ScaleJob ja, ScaleJob jb, int blocks_a)
@@ -143,19 +146,22 @@ __global__ void scale_tile_kernel(ScaleJob ja, ScaleJob jb, int blocks_a)
     for (int64_t c = bid * blockDim.x + threadIdx.x; c < j.chunks; c += nblocks * blockDim.x) {
         const int64_t l = c & 31;
         const int64_t blk = c >> 5;
-        const int64_t kb = blk % j.k_blocks;
-        const int64_t t = (blk / j.k_blocks) % j.tiles;
-        const int64_t z = blk / (j.k_blocks * j.tiles);
+        const int64_t sub = blk % j.subs;
+        const int64_t kb = (blk / j.subs) % j.k_blocks;
+        const int64_t t = (blk / (j.subs * j.k_blocks)) % j.tiles;
+        const int64_t z = blk / (j.subs * j.k_blocks * j.tiles);
         const uint8_t *src = j.src + z * j.stride;
         uint32_t w[4];
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
-            const int64_t row = t * 128 + 32 * g + l;
+            const int64_t in_tile = sub * 128 + 32 * g + l;
+            const int64_t row = t * j.tile_rows + in_tile;
+            const bool row_ok = in_tile < j.tile_rows && row < j.rows;
             uint32_t cell = 0;
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 const int64_t run = 4 * kb + r;
-                const uint32_t e = (row < j.rows && run < j.runs) ? src[row * j.ld + run] : 127u;
+                const uint32_t e = (row_ok && run < j.runs) ? src[row * j.ld + run] : 127u;
                 cell |= e << (8 * r);
             }
             w[g] = cell;
@@ -518,6 +524,7 @@ cudaError_t launch_gemm(int bn, bool pair, bool f8, bool mx, const CUtensorMap &
                         const CUtensorMap &tc, const KernelParams &p, int stages, int grid,
                         cudaStream_t s)
 {
+    if (mx && bn == 224) return pair || !f8 ? cudaErrorInvalidValue : launch_gemm_mx224(ta, tb, tc, p, stages, grid, s);
     switch (bn) {
         case 64: return launch_gemm_bn64(ta, tb, tc, p, stages, pair, f8, mx, grid, s);
         case 128: return launch_gemm_bn128(ta, tb, tc, p, stages, pair, f8, mx, grid, s);
@@ -714,10 +721,13 @@ tg_status run_gemm(const Args &a, cudaStream_t stream, const tg_options *opt,
     if (plan.mx) {
         const int64_t runs = ceil_div(a.K, 32);
         const int64_t za = in.a_bcast ? 1 : a.batch, zb = in.b_bcast ? 1 : a.batch;
+        const int64_t subs_b = ceil_div(plan.bn, 128);
         const ScaleJob ja{a.sfa, scales_a, a.M, runs, a.ld_sfa, a.batch > 1 ? a.s_sfa : 0,
-                          plan.tiles_m, plan.k_blocks, za * plan.tiles_m * static_cast<int64_t>(plan.k_blocks) * 32};
+                          plan.tiles_m, plan.k_blocks, za * plan.tiles_m * static_cast<int64_t>(plan.k_blocks) * 32,
+                          128, 1};
         const ScaleJob jb{a.sfb, scales_b, a.N, runs, a.ld_sfb, a.batch > 1 ? a.s_sfb : 0,
-                          plan.tiles_n, plan.k_blocks, zb * plan.tiles_n * static_cast<int64_t>(plan.k_blocks) * 32};
+                          plan.tiles_n, plan.k_blocks,
+                          zb * plan.tiles_n * static_cast<int64_t>(plan.k_blocks) * subs_b * 32, plan.bn, subs_b};
         const int blocks_a = grid_for(ja.chunks, sms), blocks_b = grid_for(jb.chunks, sms);
         scale_tile_kernel<<<blocks_a + blocks_b, 256, 0, stream>>>(ja, jb, blocks_a);
         if ((e = cudaGetLastError()) != cudaSuccess) return cuda_status(e);
@@ -1083,11 +1093,10 @@ tg_status run_fp8(Args a, int32_t a_format, int32_t b_format, const tg_epilogue 
         if ((reinterpret_cast<uintptr_t>(a.A) & 15u) || (reinterpret_cast<uintptr_t>(a.B) & 15u) || a.lda % 16 ||
             a.ldb % 16 || (batched_a && a.sA % 16) || (batched_b && a.sB % 16))
             return TG_ERR_UNSUPPORTED;
-        if (opt) {
-            PlanInput in = plan_input(a, 148, opt);
-            Plan pl;
-            if (!make_plan(in, pl)) return TG_ERR_INVALID_ARG;
-        }
+        // the plan exists (checked with a nominal SM count before any CUDA call)
+        PlanInput in = plan_input(a, 148, opt);
+        Plan pl;
+        if (!make_plan(in, pl)) return TG_ERR_INVALID_ARG;
     }
     return run_gemm(a, stream, opt, ep);
 }
@@ -1121,7 +1130,7 @@ TG_API tg_status tg_gemm_mxfp8(const void *A, const void *B, void *D, int64_t M,
     a.s_sfa = stride_sfa;
     a.ld_sfb = ld_sfb;
     a.s_sfb = stride_sfb;
-    if (opt && ((opt->block_n != 0 && opt->block_n != 128) || opt->cta_pair == 2 ||
+    if (opt && ((opt->block_n != 0 && opt->block_n != 128 && opt->block_n != 224) || opt->cta_pair == 2 ||
                 (opt->stages != 0 && opt->stages != 2 && opt->stages != 4)))
         return TG_ERR_INVALID_ARG;
     if (stride_sfa < 0 || stride_sfb < 0 || K < 0) return TG_ERR_INVALID_ARG;

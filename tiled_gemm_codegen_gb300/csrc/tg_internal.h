@@ -83,7 +83,10 @@ struct Geometry {
     static constexpr int STAGE = A_STAGE + B_STAGE;
     static constexpr int EPI_BYTES = 4 * EPI_BUFS * EPI_CHUNK * EPI_CHUNK * 4;  // 32 KB
     static constexpr int BAR_BYTES = 512;
-    static constexpr int SF_STAGE = 1024;  // block-scaled operands: scales of one slot
+    // Block-scaled operands: the scale blocks of one slot - A's 512 bytes,
+    // then B's 512 bytes per 128 columns of the tile.
+    static constexpr int SF_B_BLOCKS = (BN + 127) / 128;
+    static constexpr int SF_STAGE = 512 * (1 + SF_B_BLOCKS);
     static constexpr int ALIGN_SLACK = 1024;
     static constexpr int MAX_STAGES_RAW = (SMEM_LIMIT - EPI_BYTES - BAR_BYTES - ALIGN_SLACK) / STAGE;
     static constexpr int MAX_STAGES = MAX_STAGES_RAW > 8 ? 8 : MAX_STAGES_RAW;
@@ -113,5 +116,8 @@ TG_DECLARE_LAUNCH(128)
 TG_DECLARE_LAUNCH(192)
 TG_DECLARE_LAUNCH(256)
 #undef TG_DECLARE_LAUNCH
+// Block-scaled 8-bit operands on 224-wide one-CTA tiles.
+cudaError_t launch_gemm_mx224(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
+                              const KernelParams &p, int stages, int grid, cudaStream_t s);
 
 }  // namespace tg

@@ -333,25 +333,29 @@ __device__ __forceinline__ void apply_epilogue(const KernelParams &p, uint32_t (
 // F8: 8-bit floating-point operands (tcgen05 kind::f8f6f4, formats in
 // p.mma_fmt), K-major A and B only; a k-block is then 128 elements (still
 // 128 bytes a row) and each of its 4 MMAs takes K = 32.
-// MX (with F8, one-CTA 128 x 128 tiles): block-scaled operands
-// (kind::mxf8f6f4): every 32 consecutive elements of a row of A (of a
-// column of B) along K share one E8M0 power-of-two scale.  The scales of a
-// k-block come pre-arranged as one 512-byte block per 128 rows of A and one
-// per 128 columns of B (the byte of row 32g + l and K group j at
-// l * 16 + g * 4 + j); the producer bulk-copies both with the slot's
-// operands, and the MMA thread moves them to tensor memory (tcgen05.cp,
-// columns 256 + 8s ..) ahead of the slot's four MMAs, the j-th of which
-// reads byte j of each 32-bit scale cell.
+// MX (with F8, one-CTA tiles 128 rows x 128 or 224 columns): block-scaled
+// operands (kind::mxf8f6f4): every 32 consecutive elements of a row of A
+// (of a column of B) along K share one E8M0 power-of-two scale.  The scales
+// of a k-block come pre-arranged as one 512-byte block per 128 rows of A and
+// per 128 columns of B's tile (the byte of row 32g + l and K group j at
+// l * 16 + g * 4 + j); the producer bulk-copies them with the slot's
+// operands, and the MMA thread moves them to tensor memory (tcgen05.cp)
+// ahead of the slot's four MMAs, the j-th of which reads byte j of each
+// 32-bit scale cell.  Tensor memory holds the two accumulators (2 x BN
+// columns) and every slot's scales (4 columns per block), which is why a
+// block-scaled tile is at most 224 wide: 2 x 224 + 4 x 12 = 496 of the 512
+// columns (TVM "Tensor Layout", Case study: Blackwell tensor memory).
 template <int BN, int STAGES, bool PAIR, bool F8 = false, bool MX = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const KernelParams p)
 {
     using G = Geometry<BN, PAIR>;
-    static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "tile width");
+    // widths that are not a multiple of 64 only with K-major 8-bit B (one box)
+    static_assert((BN % 64 == 0 || (F8 && BN % 32 == 0)) && BN >= 64 && BN <= 256, "tile width");
     static_assert(!PAIR || G::B_COLS % 64 == 0, "two-SM tiles need 64-column halves of B");
     static_assert(G::smem_bytes(STAGES) <= SMEM_LIMIT, "shared memory budget");
-    static_assert(!MX || (F8 && !PAIR && BN == 128), "block scaling: one-CTA 128 x 128 tiles");
+    static_assert(!MX || (F8 && !PAIR && (BN == 128 || BN == 224)), "block scaling: one-CTA 128- or 224-wide tiles");
     static_assert(!MX || G::smem_bytes_mx(STAGES) <= SMEM_LIMIT, "shared memory budget (scales)");
     constexpr int TILE_M = PAIR ? 2 * BM : BM;
     constexpr int B_BOXES = G::B_COLS / 64;
@@ -359,13 +363,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     constexpr uint32_t EPI_BOX_BYTES = EPI_CHUNK * EPI_CHUNK * 4;  // 4 KB
     constexpr uint32_t EPI_WARPS_TOTAL = PAIR ? 8 : 4;  // arrivals on tempty per tile
     constexpr int KBLK = F8 ? 2 * BK : BK;              // elements of K per k-block (128 bytes)
-    // MX: the scale blocks of a slot (512 B of A's, 512 B of B's) travel with
-    // its operands; tensor memory holds both accumulators (columns 0-255)
-    // and the slots' scales (columns 256 + 8s: A's 4, then B's 4).
+    // MX: the scale blocks of a slot (A's 512 B, B's 512 B per 128 columns)
+    // travel with its operands; tensor memory holds both accumulators
+    // (columns 0 .. 2 BN - 1) and the slots' scales (SF_COLS columns a slot
+    // from 2 BN: A's 4, then B's 4 per block).
     constexpr uint32_t TX_BYTES = G::STAGE + (MX ? G::SF_STAGE : 0);
     constexpr uint32_t TMEM_ALLOC = MX ? 512u : static_cast<uint32_t>(G::TMEM_COLS);
     constexpr uint32_t SF_COL0 = 2 * BN;
-    static_assert(!MX || SF_COL0 + 8 * STAGES <= TMEM_ALLOC, "scale columns");
+    constexpr uint32_t SF_COLS = 4 * (1 + G::SF_B_BLOCKS);
+    static_assert(!MX || SF_COL0 + SF_COLS * STAGES <= TMEM_ALLOC, "scale columns");
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
@@ -509,8 +515,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if constexpr (MX) {
                         const int64_t fa = (static_cast<int64_t>(zA) * p.tiles_m + w.tm) * p.k_blocks + kb;
                         const int64_t fbk = (static_cast<int64_t>(zB) * p.tiles_n + w.tn) * p.k_blocks + kb;
+                        constexpr uint32_t SFB_BYTES = 512 * G::SF_B_BLOCKS;
                         ptx::bulk_load(sSF + s * G::SF_STAGE, p.sfa + fa * 512, 512, fb);
-                        ptx::bulk_load(sSF + s * G::SF_STAGE + 512, p.sfb + fbk * 512, 512, fb);
+                        ptx::bulk_load(sSF + s * G::SF_STAGE + 512, p.sfb + fbk * SFB_BYTES, SFB_BYTES, fb);
                     }
                 }
             }
@@ -570,15 +577,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     ptx::tc_fence_after();
                     const uint32_t a_addr = sA + s * G::A_STAGE;
                     const uint32_t b_addr = sB + s * G::B_STAGE;
-                    const uint32_t sf_tmem = tmem_base + SF_COL0 + 8u * s;
+                    const uint32_t sf_tmem = tmem_base + SF_COL0 + SF_COLS * s;
                     if constexpr (MX) {
-                        // no-swizzle descriptors of the two 512-byte scale
-                        // blocks: 8-row core matrices 128 B apart
+                        // no-swizzle descriptors of the 512-byte scale
+                        // blocks: 8-row core matrices 128 B apart; block j
+                        // of B (columns 128j ..) to columns 4 + 4j
                         const uint64_t sf_desc = (static_cast<uint64_t>(128 >> 4) << 16) |
                                                  (static_cast<uint64_t>(128 >> 4) << 32) | (1ull << 46);
                         const uint32_t sf_smem = sSF + s * G::SF_STAGE;
-                        ptx::tmem_cp_32x128b_x4(sf_tmem, sf_desc | ((sf_smem >> 4) & 0x3FFFu));
-                        ptx::tmem_cp_32x128b_x4(sf_tmem + 4, sf_desc | (((sf_smem + 512) >> 4) & 0x3FFFu));
+#pragma unroll
+                        for (int j = 0; j <= G::SF_B_BLOCKS; ++j)
+                            ptx::tmem_cp_32x128b_x4(sf_tmem + 4 * j, sf_desc | (((sf_smem + 512 * j) >> 4) & 0x3FFFu));
                     }
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
@@ -758,11 +767,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // Two register sets: the load of chunk c+1 is in flight while
                 // chunk c is staged and stored.
                 constexpr int NCH = BN / EPI_CHUNK;
-                static_assert(NCH % 2 == 0, "chunk count");
                 uint32_t va[32], vb[32];
                 ptx::tmem_load_32cols(taddr, va);
 #pragma unroll 1
-                for (int c = 0; c < NCH; c += 2) {
+                for (int c = 0; c + 1 < NCH; c += 2) {
                     ptx::tmem_load_32cols_async(taddr + (c + 1) * EPI_CHUNK, vb);
                     store_chunk(va, m_base, n_base + c * EPI_CHUNK, w.b);
                     ptx::tmem_wait_ld(vb);
@@ -770,6 +778,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     else release_tmem(buf);
                     store_chunk(vb, m_base, n_base + (c + 1) * EPI_CHUNK, w.b);
                     if (c + 2 < NCH) ptx::tmem_wait_ld(va);
+                }
+                if constexpr (NCH % 2 != 0) {
+                    // odd chunk count: the last chunk is in va, loaded above
+                    release_tmem(buf);
+                    store_chunk(va, m_base, n_base + (NCH - 1) * EPI_CHUNK, w.b);
                 }
             } else {
                 // Partial (half-)tile -> scratch.  Layout inside one part:
@@ -904,6 +917,7 @@ cudaError_t launch_fixed(const CUtensorMap &ta, const CUtensorMap &tb, const CUt
                          const KernelParams &p, int grid, cudaStream_t s)
 {
     constexpr int smem = MX ? Geometry<BN, PAIR>::smem_bytes_mx(STAGES) : Geometry<BN, PAIR>::smem_bytes(STAGES);
+    static_assert(smem <= SMEM_LIMIT, "shared memory budget");
     auto kern = gemm_kernel<BN, STAGES, PAIR, F8, MX>;
     // the shared-memory opt-in is per device; set it once per device
     static std::atomic<unsigned long long> configured{0};

@@ -2,9 +2,10 @@
 // width (selected at build time with -DTG_BN=...), so the widths compile in
 // parallel.  Each width instantiates a few ring depths, with one CTA per tile
 // and (widths 128 and 256) two-SM tiles, for bf16 operands and (a subset)
-// 8-bit floating-point ones (width 128 also block-scaled 8-bit ones, rings
-// 2 and 4); stage_supported() and mx_stage_supported() in tg_plan.h list
-// them and the host planner only picks listed configurations.
+// 8-bit floating-point ones (block-scaled 8-bit ones at widths 128 and 224,
+// rings 2 and 4, in the width-128 unit); stage_supported() and
+// mx_stage_supported() in tg_plan.h list them and the host planner only
+// picks listed configurations.
 #include "tg_kernel.cuh"
 #include "tg_plan.h"
 
@@ -47,7 +48,8 @@ cudaError_t TG_CAT(launch_gemm_bn, TG_BN)(const CUtensorMap &ta, const CUtensorM
                                           int stages, bool pair, bool f8, bool mx, int grid, cudaStream_t s)
 {
     if (mx) {
-        // block-scaled 8-bit operands: width 128, one CTA per tile
+        // block-scaled 8-bit operands, one CTA per tile: width 128 here, and
+        // width 224 (launch_gemm_mx224, instantiated in this unit too)
         if (pair || !f8) return cudaErrorInvalidValue;
 #if TG_BN == 128
         switch (stages) {
@@ -64,6 +66,18 @@ cudaError_t TG_CAT(launch_gemm_bn, TG_BN)(const CUtensorMap &ta, const CUtensorM
     if (f8) TG_SWITCH(false, true)
     TG_SWITCH(false, false)
 }
+
+#if TG_BN == 128
+cudaError_t launch_gemm_mx224(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
+                              const KernelParams &p, int stages, int grid, cudaStream_t s)
+{
+    switch (stages) {
+        case 2: return launch_fixed<224, 2, false, true, true>(ta, tb, tc, p, grid, s);
+        case 4: return launch_fixed<224, 4, false, true, true>(ta, tb, tc, p, grid, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+#endif
 
 int TG_CAT(max_pairs_bn, TG_BN)(int stages, bool f8)
 {

@@ -46,10 +46,11 @@ constexpr bool stage_supported(int bn, int s, bool pair = false, bool f8 = false
     }
 }
 
-// Block-scaled 8-bit operands: one-CTA tiles of width 128, rings 2 and 4.
+// Block-scaled 8-bit operands: one-CTA tiles of widths 128 and 224, rings 2
+// and 4.
 constexpr bool mx_stage_supported(int bn, int s, bool pair = false)
 {
-    return !pair && bn == 128 && (s == 2 || s == 4);
+    return !pair && (bn == 128 || bn == 224) && (s == 2 || s == 4);
 }
 
 template <bool PAIR>
@@ -190,8 +191,16 @@ inline bool sk_schedule(int64_t tiles, int64_t kb, int64_t workers, SkSchedule &
 // spread over `workers` = SMs (one CTA per tile) or SMs/2 (two-SM tiles).
 // The memory time is the unique A/B/C bytes plus split-K partial traffic at
 // the lower of HBM bandwidth and what the active SMs can pull.
-inline double tile_efficiency(int bn, bool pair)
+// 8-bit operands: a k-block holds twice the K at twice the MMA rate, so its
+// ideal time is the bf16 one; their measured rates (E4M3, GB300) favour
+// one-CTA 256-wide tiles unless K is long (two-SM tiles: 4096^3 equal,
+// 8192^3 11% faster, K <= 2048 up to 15% slower).
+inline double tile_efficiency(int bn, bool pair, bool f8 = false, int k_blocks = 0)
 {
+    if (f8) {
+        if (pair) return bn >= 256 ? (k_blocks >= 48 ? 0.89 : 0.78) : 0.50;
+        return bn >= 256 ? 0.80 : 0.62;
+    }
     // measured in-wave rates on GB300 (fraction of the measured bf16 peak)
     if (pair) return bn >= 256 ? 0.97 : 0.53;
     return bn >= 256 ? 0.80 : bn >= 192 ? 0.645 : bn >= 128 ? 0.54 : 0.29;
@@ -201,7 +210,7 @@ inline double plan_cost_ns(const PlanInput &in, int bn, bool pair, int splits, i
                            int64_t tiles, int sms, bool stream_k = false)
 {
     const double sm_flops = 1.95e15 / 152.0;  // per-SM dense bf16, flop/s
-    const double kb_ns = (2.0 * BM * bn * BK) / sm_flops * 1e9 / tile_efficiency(bn, pair);
+    const double kb_ns = (2.0 * BM * bn * BK) / sm_flops * 1e9 / tile_efficiency(bn, pair, in.f8, k_blocks);
     const int64_t workers = pair ? std::max(1, sms / 2) : sms;
     const int64_t units = tiles * splits;
     double t_mma = 0.0, partial = 0.0;
@@ -217,7 +226,7 @@ inline double plan_cost_ns(const PlanInput &in, int bn, bool pair, int splits, i
         t_mma = static_cast<double>(waves) * static_cast<double>(kb_unit) * kb_ns;
         partial = splits > 1 ? 2.0 * 4.0 * in.batch * in.M * in.N * splits : 0.0;
     }
-    const double ab = 2.0 * in.batch * (in.M * in.K + in.K * in.N);
+    const double ab = (in.f8 ? 1.0 : 2.0) * in.batch * (in.M * in.K + in.K * in.N);
     const double c = 4.0 * in.batch * in.M * in.N;
     const int64_t active_sms = std::min<int64_t>(units, workers) * (pair ? 2 : 1);
     const double bw = std::min(6.5e12, static_cast<double>(active_sms) * 50e9);
@@ -278,7 +287,7 @@ inline bool make_plan(const PlanInput &in, Plan &out)
     p.k_blocks = static_cast<int>(kb);
 
     if (in.block_n != 0 && in.block_n != 64 && in.block_n != 128 && in.block_n != 192 &&
-        in.block_n != 256)
+        in.block_n != 256 && !(in.mx && in.block_n == 224))
         return false;
     if (in.split_k < 0 || in.stages < 0 || in.max_ctas < 0) return false;
     if (in.epilogue < 0 || in.epilogue > 2) return false;
@@ -292,16 +301,24 @@ inline bool make_plan(const PlanInput &in, Plan &out)
         int bn;
         bool pair;
     };
-    const Cand cands[6] = {{256, true}, {128, true}, {256, false}, {192, false}, {128, false}, {64, false}};
+    // block-scaled: 224 columns (two accumulators and the scales fill tensor
+    // memory), or 128 where that needs fewer column tiles
+    const Cand cands_mx[2] = {{224, false}, {128, false}};
+    const Cand cands_all[6] = {{256, true}, {128, true}, {256, false}, {192, false}, {128, false}, {64, false}};
+    const Cand *cands = in.mx ? cands_mx : cands_all;
+    const int n_cands = in.mx ? 2 : 6;
     double best = 0.0;
     bool have = false;
-    for (const Cand &cd : cands) {
+    for (int ci = 0; ci < n_cands; ++ci) {
+        const Cand &cd = cands[ci];
         if (in.block_n != 0 && cd.bn != in.block_n) continue;
+        if (in.mx && in.block_n == 0 && (cd.bn == 224) != (ceil_div(in.N, 224) < ceil_div(in.N, 128))) continue;
         if (in.cta_pair == 1 && cd.pair) continue;
         if (in.cta_pair == 2 && !cd.pair) continue;
         if (in.cta_pair == 0 && cd.pair && !PAIR_BY_DEFAULT) continue;
-        if (in.f8 && !stage_supported(cd.bn, 2, cd.pair, true)) continue;  // no 8-bit instance
+        if (in.f8 && !in.mx && !stage_supported(cd.bn, 2, cd.pair, true)) continue;  // no 8-bit instance
         if (in.mx && !mx_stage_supported(cd.bn, 2, cd.pair)) continue;
+        if (!in.mx && cd.bn == 224) continue;
         const int tile_m = cd.pair ? 2 * BM : BM;
         const int64_t tiles_m = ceil_div(in.M, tile_m);
         const int64_t tiles_n = ceil_div(in.N, cd.bn);
@@ -319,6 +336,9 @@ inline bool make_plan(const PlanInput &in, Plan &out)
             for (int sk = 0; sk < 2; ++sk) {
                 const bool use_sk = sk == 1;
                 if (use_sk && (s > 1 || in.stream_k == 1 || tiles % workers == 0)) continue;
+                // 8-bit operands: stream-K only on request (its partial-tile
+                // traffic outweighs the balance at the measured sizes)
+                if (use_sk && in.f8 && in.stream_k != 2) continue;
                 if (!use_sk && in.stream_k == 2 && tiles % workers != 0) continue;
                 const double c = plan_cost_ns(in, cd.bn, cd.pair, s, p.k_blocks, tiles, sms, use_sk);
                 if (!have || c < best * 0.999) {
@@ -378,7 +398,7 @@ inline bool make_plan(const PlanInput &in, Plan &out)
     p.smem = smem_bytes_for(p.bn, p.stages, p.pair);
     p.tmem = tmem_cols_for(p.bn);
     if (p.mx) {
-        p.smem = Geometry<128>::smem_bytes_mx(p.stages);
+        p.smem = p.bn == 224 ? Geometry<224>::smem_bytes_mx(p.stages) : Geometry<128>::smem_bytes_mx(p.stages);
         p.tmem = 512;  // accumulators and the slots' scales
     }
 
@@ -391,7 +411,7 @@ inline bool make_plan(const PlanInput &in, Plan &out)
     p.ws_pack_b = p.pack_b ? round_up(batch_b * b_rows * pack_pitch(b_cols) * 2, 256) : 0;
     if (p.mx) {
         p.ws_scales_a = round_up(batch_a * p.tiles_m * static_cast<int64_t>(p.k_blocks) * 512, 256);
-        p.ws_scales_b = round_up(batch_b * p.tiles_n * static_cast<int64_t>(p.k_blocks) * 512, 256);
+        p.ws_scales_b = round_up(batch_b * p.tiles_n * static_cast<int64_t>(p.k_blocks) * 512 * ceil_div(p.bn, 128), 256);
     }
     set_partial_workspace(in, p);
     out = p;
