@@ -224,6 +224,14 @@ __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, const 
     }
 }
 
+// wait_bounded by every lane of a warp, with lane 0's result for all: the
+// warp leaves (or stays in) its loop as one.
+__device__ __forceinline__ int wait_bounded_warp(uint32_t bar, uint32_t parity, const Watchdog &wd)
+{
+    const int r = wait_bounded(bar, parity, wd);
+    return __shfl_sync(0xffffffffu, r, 0);
+}
+
 __device__ __forceinline__ void raise_abort(const Watchdog &wd, uint32_t code)
 {
     atomicCAS(wd.err, 0u, code);
@@ -530,8 +538,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
         }
     } else if (warp == 1) {
-        if (lane == 0 && (!PAIR || leader)) {
+        if (!PAIR || leader) {
             // ------------------------------------------------ MMA issuer
+            // The whole warp runs the issue loop, so its control flow is
+            // warp-uniform; one elected lane issues the tcgen05 instructions.
             // kind::f8f6f4 keeps the layout of the descriptor; only the A and
             // B format fields (bits 7-12) differ
             const uint32_t idesc_bf16 = instr_desc_bf16<TILE_M, BN>(p.a_mn != 0, p.b_k == 0);
@@ -557,9 +567,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (; ok && work_next(p, worker, n_workers, wi, w); ++t) {
                 const uint32_t buf = t & 1u;
                 const uint32_t tph = (t >> 1) & 1u;
-                int r = wait_bounded(tempty_bar(buf), tph ^ 1u, wd);
+                int r = wait_bounded_warp(tempty_bar(buf), tph ^ 1u, wd);
                 if (r != WAIT_OK) {
-                    if (r == WAIT_TIMEOUT) raise_abort(wd, ERR_TIMEOUT_MMA);
+                    if (r == WAIT_TIMEOUT && lane == 0) raise_abort(wd, ERR_TIMEOUT_MMA);
                     break;
                 }
                 ptx::tc_fence_after();
@@ -567,64 +577,76 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int32_t kb = w.kb0; kb < w.kb1; ++kb, ++it) {
                     const uint32_t s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1u;
-                    r = wait_bounded(full_bar(s), ph, wd);
+                    r = wait_bounded_warp(full_bar(s), ph, wd);
                     if (r != WAIT_OK) {
-                        if (r == WAIT_TIMEOUT) raise_abort(wd, ERR_TIMEOUT_MMA);
+                        if (r == WAIT_TIMEOUT && lane == 0) raise_abort(wd, ERR_TIMEOUT_MMA);
                         ok = false;
                         break;
                     }
-                    if (it == 0) stamp(2);
+                    if (it == 0 && lane == 0) stamp(2);
                     ptx::tc_fence_after();
-                    const uint32_t a_addr = sA + s * G::A_STAGE;
-                    const uint32_t b_addr = sB + s * G::B_STAGE;
-                    const uint32_t sf_tmem = tmem_base + SF_COL0 + SF_COLS * s;
-                    if constexpr (MX) {
-                        // no-swizzle descriptors of the 512-byte scale
-                        // blocks: 8-row core matrices 128 B apart; block j
-                        // of B (columns 128j ..) to columns 4 + 4j
-                        const uint64_t sf_desc = (static_cast<uint64_t>(128 >> 4) << 16) |
-                                                 (static_cast<uint64_t>(128 >> 4) << 32) | (1ull << 46);
-                        const uint32_t sf_smem = sSF + s * G::SF_STAGE;
+                    if (ptx::elect_one()) {
+                        const uint32_t a_addr = sA + s * G::A_STAGE;
+                        const uint32_t b_addr = sB + s * G::B_STAGE;
+                        const uint32_t sf_tmem = tmem_base + SF_COL0 + SF_COLS * s;
+                        if constexpr (MX) {
+                            // no-swizzle descriptors of the 512-byte scale
+                            // blocks: 8-row core matrices 128 B apart; block j
+                            // of B (columns 128j ..) to columns 4 + 4j
+                            const uint64_t sf_desc = (static_cast<uint64_t>(128 >> 4) << 16) |
+                                                     (static_cast<uint64_t>(128 >> 4) << 32) | (1ull << 46);
+                            const uint32_t sf_smem = sSF + s * G::SF_STAGE;
 #pragma unroll
-                        for (int j = 0; j <= G::SF_B_BLOCKS; ++j)
-                            ptx::tmem_cp_32x128b_x4(sf_tmem + 4 * j, sf_desc | (((sf_smem + 512 * j) >> 4) & 0x3FFFu));
-                    }
+                            for (int j = 0; j <= G::SF_B_BLOCKS; ++j)
+                                ptx::tmem_cp_32x128b_x4(sf_tmem + 4 * j, sf_desc | (((sf_smem + 512 * j) >> 4) & 0x3FFFu));
+                        }
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
-                        const uint64_t ad = a_desc0 | (((a_addr + kk * a_step) >> 4) & 0x3FFFu);
-                        const uint64_t bd = b_desc0 | (((b_addr + kk * b_step) >> 4) & 0x3FFFu);
-                        const uint32_t acc = (kb > w.kb0 || kk > 0) ? 1u : 0u;
-                        if constexpr (MX)
-                            ptx::mma_mx(d_tmem, ad, bd,
-                                        idesc_mx | (static_cast<uint32_t>(kk) << 29) | (static_cast<uint32_t>(kk) << 4),
-                                        sf_tmem, sf_tmem + 4, acc);
-                        else if constexpr (PAIR && F8)
-                            ptx::mma_f8_pair(d_tmem, ad, bd, idesc, acc);
-                        else if constexpr (PAIR)
-                            ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, acc);
-                        else if constexpr (F8)
-                            ptx::mma_f8(d_tmem, ad, bd, idesc, acc);
+                        for (int kk = 0; kk < BK / 16; ++kk) {
+                            const uint64_t ad = a_desc0 | (((a_addr + kk * a_step) >> 4) & 0x3FFFu);
+                            const uint64_t bd = b_desc0 | (((b_addr + kk * b_step) >> 4) & 0x3FFFu);
+                            const uint32_t acc = (kb > w.kb0 || kk > 0) ? 1u : 0u;
+                            if constexpr (MX)
+                                ptx::mma_mx(d_tmem, ad, bd,
+                                            idesc_mx | (static_cast<uint32_t>(kk) << 29) | (static_cast<uint32_t>(kk) << 4),
+                                            sf_tmem, sf_tmem + 4, acc);
+                            else if constexpr (PAIR && F8)
+                                ptx::mma_f8_pair(d_tmem, ad, bd, idesc, acc);
+                            else if constexpr (PAIR)
+                                ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, acc);
+                            else if constexpr (F8)
+                                ptx::mma_f8(d_tmem, ad, bd, idesc, acc);
+                            else
+                                ptx::mma_bf16(d_tmem, ad, bd, idesc, acc);
+                        }
+                        if constexpr (PAIR)
+                            ptx::mma_commit_pair_multicast(empty_bar(s), 0x3);
                         else
-                            ptx::mma_bf16(d_tmem, ad, bd, idesc, acc);
+                            ptx::mma_commit(empty_bar(s));
                     }
-                    if constexpr (PAIR)
-                        ptx::mma_commit_pair_multicast(empty_bar(s), 0x3);
-                    else
-                        ptx::mma_commit(empty_bar(s));
+                    __syncwarp();
                 }
                 if (!ok) break;
-                if constexpr (PAIR)
-                    ptx::mma_commit_pair_multicast(tfull_bar(buf), 0x3);
-                else
-                    ptx::mma_commit(tfull_bar(buf));
+                // every tcgen05 instruction of the loop comes from the elected
+                // lane (elect.sync on the converged warp: the same lane each
+                // time), so each commit covers the MMAs before it
+                if (ptx::elect_one()) {
+                    if constexpr (PAIR)
+                        ptx::mma_commit_pair_multicast(tfull_bar(buf), 0x3);
+                    else
+                        ptx::mma_commit(tfull_bar(buf));
+                }
+                __syncwarp();
             }
-            stamp(3);
-            // Every MMA issued above completes before tensor memory is freed.
-            if constexpr (PAIR)
-                ptx::mma_commit_pair_multicast(done_bar, 0x1);
-            else
-                ptx::mma_commit(done_bar);
-            wait_drain(done_bar, 0, wd);
+            if (ptx::elect_one()) {
+                stamp(3);
+                // Every MMA issued above completes before tensor memory is freed.
+                if constexpr (PAIR)
+                    ptx::mma_commit_pair_multicast(done_bar, 0x1);
+                else
+                    ptx::mma_commit(done_bar);
+                wait_drain(done_bar, 0, wd);
+            }
+            __syncwarp();
         }
     } else {
         // ------------------------------------------------ epilogue

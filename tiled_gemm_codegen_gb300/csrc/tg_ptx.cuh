@@ -68,6 +68,18 @@ __device__ __forceinline__ void prefetch_tensormap(const void *tmap)
 // Programmatic dependent launch: wait until every kernel this grid depends
 // on has completed and its memory is visible; let dependents be scheduled.
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// One lane of the (fully converged) warp is elected: true on that lane.
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t pred;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
 __device__ __forceinline__ void griddep_launch_dependents()
 {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
