@@ -464,7 +464,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
-        if (lane == 0) {
+        // The whole warp runs the loop (warp-uniform control flow); one
+        // elected lane issues the barrier arrivals and the copies.
+        {
             uint32_t it = 0;
             bool ok = true;
             // pair: both CTAs' copies complete on the leader's full barrier
@@ -480,62 +482,68 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int32_t kb = w.kb0; kb < w.kb1; ++kb, ++it) {
                     const uint32_t s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1u;
-                    const int r = wait_bounded(empty_bar(s), ph ^ 1u, wd);
+                    const int r = wait_bounded_warp(empty_bar(s), ph ^ 1u, wd);
                     if (r != WAIT_OK) {
-                        if (r == WAIT_TIMEOUT) raise_abort(wd, ERR_TIMEOUT_PRODUCER);
+                        if (r == WAIT_TIMEOUT && lane == 0) raise_abort(wd, ERR_TIMEOUT_PRODUCER);
                         ok = false;
                         break;
                     }
-                    // One copy: this CTA's own barrier; a pair: the leader's.
-                    uint32_t fb;
-                    if constexpr (PAIR) {
-                        if (leader) ptx::mbar_arrive_expect_tx(full_bar(s), 2 * G::STAGE);
-                        fb = full0 + 8u * s;
-                    } else {
-                        ptx::mbar_arrive_expect_tx(full_bar(s), TX_BYTES);
-                        fb = full_bar(s);
-                    }
-                    auto load = [&](uint32_t dst, const CUtensorMap *map, int32_t c0, int32_t c1, int32_t c2) {
-                        if constexpr (PAIR)
-                            ptx::tma_load_3d_pair(dst, map, fb, c0, c1, c2);
-                        else
-                            ptx::tma_load_3d(dst, map, fb, c0, c1, c2);
-                    };
-                    const uint32_t a_dst = sA + s * G::A_STAGE;
-                    const uint32_t b_dst = sB + s * G::B_STAGE;
-                    if (!p.a_mn) {
-                        // A row-major: one box [128 rows x 64 k], K-major atoms
-                        load(a_dst, &tmA, kb * KBLK, m_rows, zA);
-                    } else {
-                        // A column-major: two boxes [64 k x 64 rows], MN-major atoms
-                        load(a_dst, &tmA, m_rows, kb * KBLK, zA);
-                        load(a_dst + B_BOX_BYTES, &tmA, m_rows + 64, kb * KBLK, zA);
-                    }
-                    if (!p.b_k) {
-                        // B row-major: boxes [64 k x 64 columns], MN-major atoms
+                    if (ptx::elect_one()) {
+                        // One copy: this CTA's own barrier; a pair: the leader's.
+                        uint32_t fb;
+                        if constexpr (PAIR) {
+                            if (leader) ptx::mbar_arrive_expect_tx(full_bar(s), 2 * G::STAGE);
+                            fb = full0 + 8u * s;
+                        } else {
+                            ptx::mbar_arrive_expect_tx(full_bar(s), TX_BYTES);
+                            fb = full_bar(s);
+                        }
+                        auto load = [&](uint32_t dst, const CUtensorMap *map, int32_t c0, int32_t c1, int32_t c2) {
+                            if constexpr (PAIR)
+                                ptx::tma_load_3d_pair(dst, map, fb, c0, c1, c2);
+                            else
+                                ptx::tma_load_3d(dst, map, fb, c0, c1, c2);
+                        };
+                        const uint32_t a_dst = sA + s * G::A_STAGE;
+                        const uint32_t b_dst = sB + s * G::B_STAGE;
+                        if (!p.a_mn) {
+                            // A row-major: one box [128 rows x 64 k], K-major atoms
+                            load(a_dst, &tmA, kb * KBLK, m_rows, zA);
+                        } else {
+                            // A column-major: two boxes [64 k x 64 rows], MN-major atoms
+                            load(a_dst, &tmA, m_rows, kb * KBLK, zA);
+                            load(a_dst + B_BOX_BYTES, &tmA, m_rows + 64, kb * KBLK, zA);
+                        }
+                        if (!p.b_k) {
+                            // B row-major: boxes [64 k x 64 columns], MN-major atoms
 #pragma unroll
-                        for (int j = 0; j < B_BOXES; ++j)
-                            load(b_dst + j * B_BOX_BYTES, &tmB, n_cols + 64 * j, kb * KBLK, zB);
-                    } else {
-                        // B column-major: one box [B_COLS columns x 64 k], K-major atoms
-                        load(b_dst, &tmB, kb * KBLK, n_cols, zB);
+                            for (int j = 0; j < B_BOXES; ++j)
+                                load(b_dst + j * B_BOX_BYTES, &tmB, n_cols + 64 * j, kb * KBLK, zB);
+                        } else {
+                            // B column-major: one box [B_COLS columns x 64 k], K-major atoms
+                            load(b_dst, &tmB, kb * KBLK, n_cols, zB);
+                        }
+                        if constexpr (MX) {
+                            const int64_t fa = (static_cast<int64_t>(zA) * p.tiles_m + w.tm) * p.k_blocks + kb;
+                            const int64_t fbk = (static_cast<int64_t>(zB) * p.tiles_n + w.tn) * p.k_blocks + kb;
+                            constexpr uint32_t SFB_BYTES = 512 * G::SF_B_BLOCKS;
+                            ptx::bulk_load(sSF + s * G::SF_STAGE, p.sfa + fa * 512, 512, fb);
+                            ptx::bulk_load(sSF + s * G::SF_STAGE + 512, p.sfb + fbk * SFB_BYTES, SFB_BYTES, fb);
+                        }
                     }
-                    if constexpr (MX) {
-                        const int64_t fa = (static_cast<int64_t>(zA) * p.tiles_m + w.tm) * p.k_blocks + kb;
-                        const int64_t fbk = (static_cast<int64_t>(zB) * p.tiles_n + w.tn) * p.k_blocks + kb;
-                        constexpr uint32_t SFB_BYTES = 512 * G::SF_B_BLOCKS;
-                        ptx::bulk_load(sSF + s * G::SF_STAGE, p.sfa + fa * 512, 512, fb);
-                        ptx::bulk_load(sSF + s * G::SF_STAGE + 512, p.sfb + fbk * SFB_BYTES, SFB_BYTES, fb);
-                    }
+                    __syncwarp();
                 }
             }
-            *issued_slot = it;
-            if constexpr (!PAIR) {
-                // Drain: the last load issued into every slot has landed.
-                const uint32_t first = it > STAGES ? it - STAGES : 0u;
-                for (uint32_t j = first; j < it; ++j)
-                    if (!wait_drain(full_bar(j % STAGES), (j / STAGES) & 1u, wd)) break;
+            if (lane == 0) {
+                *issued_slot = it;
+                if constexpr (!PAIR) {
+                    // Drain: the last load issued into every slot has landed.
+                    const uint32_t first = it > STAGES ? it - STAGES : 0u;
+                    for (uint32_t j = first; j < it; ++j)
+                        if (!wait_drain(full_bar(j % STAGES), (j / STAGES) & 1u, wd)) break;
+                }
             }
+            __syncwarp();
         }
     } else if (warp == 1) {
         if (!PAIR || leader) {
