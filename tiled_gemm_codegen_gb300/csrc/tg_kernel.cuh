@@ -4,17 +4,20 @@
 // list of work units (output tile x K split).  Roles (the "Active subsets"
 // of one accumulator's producers and consumers, LuisaCompute "Execution
 // Nests and coordinates", Logical anchor and execution frontier):
-//   warp 0, lane 0 : TMA producer.  Loads this CTA's A rows [128 x BK]
+//   warp 0         : TMA producer.  Loads this CTA's A rows [128 x BK]
 //                    (K-major) and its B columns [BK x BN or BN/2] (N-major)
 //                    of k-block kb into ring slot kb mod STAGES with the
 //                    128-byte swizzle; boxes that run past M, N or K are
 //                    zero-filled by the TMA unit (OCANNL "Module
 //                    Ir.Schedule", Pad-to-tile and Stage: out-of-range slots
 //                    hold the additive identity 0).
-//   warp 1, lane 0 : MMA issuer (the leader CTA of a pair).  BK/16
+//   warp 1         : MMA issuer (the leader CTA of a pair).  BK/16
 //                    tcgen05.mma per slot into a tensor-memory accumulator;
 //                    the first one of a unit overwrites (the zero-initialised
 //                    accumulator of OCANNL Privatize).
+//                    Both run their loop on all 32 lanes (barrier waits by
+//                    every lane, lane 0's result for all: warp-uniform
+//                    control flow) and issue from one elect.sync lane.
 //   warps 2..5     : epilogue.  tcgen05.ld of the accumulator (warp w reads
 //                    TMEM lanes 32*(w%4) ..) into a 128B-swizzled 32 x 32
 //                    fp32 box in shared memory, then a TMA store of the box
