@@ -17,7 +17,7 @@ from oracle import fp8 as ofp8
 
 pytestmark = pytest.mark.gpu
 
-CONFIGS = [(128, 1), (256, 1), (256, 2)]  # (block_n, cta_pair) with 8-bit instances
+CONFIGS = [(128, 1), (192, 1), (256, 1), (256, 2)]  # (block_n, cta_pair) with 8-bit instances
 
 
 def _run(Ac, Btc, fa, fb, options=None, out_dtype=None, **ep):
@@ -71,7 +71,8 @@ def test_batched_split_and_stream_k():
         assert np.array_equal(got, want), opts
 
 
-@pytest.mark.parametrize("bn,pair,depths", [(128, 1, [2, 4, 6]), (256, 1, [2, 4]), (256, 2, [2, 4, 6])])
+@pytest.mark.parametrize("bn,pair,depths", [(128, 1, [2, 4, 6]), (192, 1, [2, 4]), (256, 1, [2, 4]),
+                                            (256, 2, [2, 4, 6])])
 def test_ring_depth_bitwise_invariance(bn, pair, depths):
     M, N, K = 300, 520, 1100 // 16 * 16
     A = synth.make_fp8_codes((M, K), 0, seed=9, kind="normal")

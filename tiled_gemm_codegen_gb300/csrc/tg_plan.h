@@ -23,12 +23,13 @@ constexpr bool pair_width(int bn) { return bn == 128 || bn == 256; }
 
 // Ring depths instantiated for each tile width (kept small for build time).
 // 8-bit operands (f8): two-SM tiles of width 256 and one-CTA tiles of widths
-// 128 and 256 only.
+// 128, 192 and 256 only.
 constexpr bool stage_supported(int bn, int s, bool pair = false, bool f8 = false)
 {
     if (f8) {
         if (pair) return bn == 256 && (s == 2 || s == 4 || s == 6);
-        return (bn == 128 && (s == 2 || s == 4 || s == 6)) || (bn == 256 && (s == 2 || s == 4));
+        return (bn == 128 && (s == 2 || s == 4 || s == 6)) || (bn == 192 && (s == 2 || s == 4)) ||
+               (bn == 256 && (s == 2 || s == 4));
     }
     if (pair) {
         switch (bn) {
@@ -199,7 +200,7 @@ inline double tile_efficiency(int bn, bool pair, bool f8 = false, int k_blocks =
 {
     if (f8) {
         if (pair) return bn >= 256 ? (k_blocks >= 48 ? 0.89 : 0.78) : 0.50;
-        return bn >= 256 ? 0.80 : 0.62;
+        return bn >= 256 ? 0.80 : bn >= 192 ? 0.70 : 0.62;
     }
     // measured in-wave rates on GB300 (fraction of the measured bf16 peak)
     if (pair) return bn >= 256 ? 0.97 : 0.53;
