@@ -234,9 +234,9 @@ tg_status tg_gemm_fp8(const void *A, const void *B, void *D,
  * re-arranges them into device scratch it owns (512-byte blocks per 128
  * rows or columns of a tile and 128 elements of K) on `stream` before the
  * GEMM.
- * Tiles are 128 rows x 224 columns (128 where that needs fewer column
- * tiles), one CTA each: tensor memory holds two 224-column accumulators and
- * the scales of every ring slot.  opt->block_n must be 0, 128 or 224,
+ * Tiles are 128 rows x 128, 192 or 224 columns (the planner's choice), one
+ * CTA each: tensor memory holds two accumulators of up to 224 columns and
+ * the scales of every ring slot.  opt->block_n must be 0, 128, 192 or 224,
  * opt->cta_pair 0 or 1, opt->stages 0, 2 or 4 (else TG_ERR_INVALID_ARG).
  * TG_ERR_INVALID_ARG also for a NULL scale pointer with K > 0, ld_sfa or
  * ld_sfb < ceil(K/32), or a negative scale stride. */

@@ -277,7 +277,7 @@ def test_mxfp8_rejects_bad_arguments_before_any_cuda_call(lib):
     assert call(s_sfa=-8) == bad
     assert call(fa=2) == bad                            # unknown format
     assert call(opt=tg.make_options(block_n=256)) == bad
-    assert call(opt=tg.make_options(block_n=192)) == bad
+    assert call(opt=tg.make_options(block_n=64)) == bad
     assert call(opt=tg.make_options(cta_pair=2)) == bad
     assert call(opt=tg.make_options(stages=6)) == bad
     assert call(opt=tg.make_options(a_col_major=1)) == bad
@@ -288,7 +288,7 @@ def test_mxfp8_rejects_bad_arguments_before_any_cuda_call(lib):
     # valid calls get past every host check (and then need a GPU): both tile
     # widths plan, with and without options
     assert call() == tg.TG_ERR_CUDA
-    for bn in (128, 224):
+    for bn in (128, 192, 224):
         for st in (2, 4):
             assert call(opt=tg.make_options(block_n=bn, stages=st)) == tg.TG_ERR_CUDA
     assert call(opt=tg.make_options(split_k=2)) == tg.TG_ERR_CUDA

@@ -48,12 +48,12 @@ def test_exact_integer(M, N, K):
     assert np.array_equal(got, _oracle(A, Bt, sfa, sfb))
 
 
-@pytest.mark.parametrize("bn", [128, 224])
+@pytest.mark.parametrize("bn", [128, 192, 224])
 @pytest.mark.parametrize("M,N,K", [(130, 224, 256), (129, 225, 160), (257, 447, 528), (64, 465, 1024),
                                    (300, 700, 2080)])
 def test_exact_integer_tile_widths(bn, M, N, K):
-    """Both block-scaled tile widths; N around the 224-column tile and the
-    128-column scale blocks inside it."""
+    """Every block-scaled tile width; N around the 192- and 224-column tiles
+    and the 128-column scale blocks inside them."""
     A = synth.make_fp8_codes((M, K), 0, seed=M + 5 * K)
     Bt = synth.make_fp8_codes((N, K), 0, seed=N + 7 * K)
     sfa = synth.make_e8m0_codes((M, _runs(K)), seed=3 + M, lo=126, hi=128)
@@ -69,9 +69,9 @@ def test_tile_widths_bitwise_equal():
     Bt = synth.make_fp8_codes((N, K), 0, seed=62, kind="normal")
     sfa = synth.make_e8m0_codes((M, K // 32), seed=63)
     sfb = synth.make_e8m0_codes((N, K // 32), seed=64)
-    outs = [_run(A, Bt, sfa, sfb, options=tg.make_options(block_n=bn, stream_k=1)) for bn in (128, 224)]
-    assert np.array_equal(outs[0], outs[1])
-    assert_close(outs[1], _oracle(A, Bt, sfa, sfb), K, "224 vs oracle")
+    outs = [_run(A, Bt, sfa, sfb, options=tg.make_options(block_n=bn, stream_k=1)) for bn in (128, 192, 224)]
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+    assert_close(outs[2], _oracle(A, Bt, sfa, sfb), K, "224 vs oracle")
 
 
 @pytest.mark.parametrize("fa,fb", [(1, 0), (0, 1), (1, 1)])
@@ -149,7 +149,7 @@ def test_shared_operand_and_scales():
     assert np.array_equal(got, want)
 
 
-@pytest.mark.parametrize("bn", [128, 224])
+@pytest.mark.parametrize("bn", [128, 192, 224])
 def test_ring_depth_bitwise_invariance(bn):
     M, N, K = 300, 520, 1088
     A = synth.make_fp8_codes((M, K), 0, seed=9, kind="normal")
@@ -192,7 +192,8 @@ def test_argument_errors():
     assert call(ld_sfb=1) == tg.TG_ERR_INVALID_ARG
     assert call(opt=tg.make_options(block_n=256)) == tg.TG_ERR_INVALID_ARG
     assert call(opt=tg.make_options(block_n=224)) == tg.TG_OK
-    assert call(opt=tg.make_options(block_n=192)) == tg.TG_ERR_INVALID_ARG
+    assert call(opt=tg.make_options(block_n=192)) == tg.TG_OK
+    assert call(opt=tg.make_options(block_n=64)) == tg.TG_ERR_INVALID_ARG
     assert call(opt=tg.make_options(cta_pair=2)) == tg.TG_ERR_INVALID_ARG
     assert call(opt=tg.make_options(stages=6)) == tg.TG_ERR_INVALID_ARG
     assert call(s_sfa=-1) == tg.TG_ERR_INVALID_ARG

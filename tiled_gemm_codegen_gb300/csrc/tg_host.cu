@@ -126,47 +126,65 @@ __global__ void pack_bf16_kernel(PackJob ja, PackJob jb, int blocks_a)
 // rows on lanes, 4 scales per 32-bit column cell, replicated over the four
 // lane quadrants).  Rows and runs past the operand read as 127 (2^0): their
 // operand elements are the TMA unit's zero fill.  A tile of `tile_rows` rows
-// (128, or 224 for B's 224-wide tiles) has `subs` = ceil(tile_rows / 128)
-// consecutive blocks per k-block; tile rows past tile_rows read as 127 too.
+// (128, or B's tile width) has `subs` = ceil(tile_rows / 128) consecutive
+// blocks per k-block; tile rows past tile_rows read as 127 too.
 struct ScaleJob {
     const uint8_t *src;
     uint8_t *dst;
     int64_t rows, runs, ld, stride;  // stride: between problems (0: shared)
-    int64_t tiles, k_blocks, chunks;  // chunks = problems * tiles * k_blocks * subs * 32
-    int64_t tile_rows, subs;
+    int64_t problems, tiles, k_blocks, tile_rows, subs;
 };
 
-__global__ void scale_tile_kernel(ScaleJob ja, ScaleJob jb, int blocks_a)
+// One CTA re-arranges the scales of one 128-row block (sub) of one tile for
+// SC_KB consecutive k-blocks: the 128 rows x 4 SC_KB runs are read with
+// coalesced byte loads into shared memory (rows SC_PITCH bytes apart, so the
+// 32 rows a warp reads next fall in 32 different banks), then each warp
+// writes whole 512-byte blocks, lane l's 16 bytes holding rows l, 32 + l,
+// 64 + l and 96 + l.
+constexpr int SC_KB = 16;
+constexpr int SC_RUNS = 4 * SC_KB;
+constexpr int SC_PITCH = SC_RUNS + 4;
+
+inline int64_t scale_blocks(const ScaleJob &j)
+{
+    return j.problems * j.tiles * j.subs * ((j.k_blocks + SC_KB - 1) / SC_KB);
+}
+
+__global__ void __launch_bounds__(256) scale_tile_kernel(ScaleJob ja, ScaleJob jb, int64_t blocks_a)
 {
     ptx::griddep_launch_dependents();
-    const bool is_a = static_cast<int>(blockIdx.x) < blocks_a;
+    __shared__ __align__(16) uint8_t slab[128 * SC_PITCH];
+    const bool is_a = static_cast<int64_t>(blockIdx.x) < blocks_a;
     const ScaleJob j = is_a ? ja : jb;
-    const int64_t bid = is_a ? blockIdx.x : blockIdx.x - blocks_a;
-    const int64_t nblocks = is_a ? blocks_a : gridDim.x - blocks_a;
-    for (int64_t c = bid * blockDim.x + threadIdx.x; c < j.chunks; c += nblocks * blockDim.x) {
-        const int64_t l = c & 31;
-        const int64_t blk = c >> 5;
-        const int64_t sub = blk % j.subs;
-        const int64_t kb = (blk / j.subs) % j.k_blocks;
-        const int64_t t = (blk / (j.subs * j.k_blocks)) % j.tiles;
-        const int64_t z = blk / (j.subs * j.k_blocks * j.tiles);
-        const uint8_t *src = j.src + z * j.stride;
+    int64_t bid = is_a ? blockIdx.x : blockIdx.x - blocks_a;
+    const int64_t kchunks = (j.k_blocks + SC_KB - 1) / SC_KB;
+    const int64_t kc = bid % kchunks;
+    bid /= kchunks;
+    const int64_t sub = bid % j.subs;
+    bid /= j.subs;
+    const int64_t t = bid % j.tiles;
+    const int64_t z = bid / j.tiles;
+    const uint8_t *src = j.src + z * j.stride;
+    const int64_t run0 = kc * SC_RUNS;
+    for (int i = threadIdx.x; i < 128 * SC_RUNS; i += blockDim.x) {
+        const int r = i / SC_RUNS, c = i % SC_RUNS;
+        const int64_t in_tile = sub * 128 + r;
+        const int64_t row = t * j.tile_rows + in_tile;
+        const int64_t run = run0 + c;
+        const bool ok = in_tile < j.tile_rows && row < j.rows && run < j.runs;
+        slab[r * SC_PITCH + c] = ok ? src[row * j.ld + run] : static_cast<uint8_t>(127);
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int kb = warp; kb < SC_KB; kb += blockDim.x / 32) {
+        const int64_t kbg = kc * SC_KB + kb;
+        if (kbg >= j.k_blocks) break;
         uint32_t w[4];
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-            const int64_t in_tile = sub * 128 + 32 * g + l;
-            const int64_t row = t * j.tile_rows + in_tile;
-            const bool row_ok = in_tile < j.tile_rows && row < j.rows;
-            uint32_t cell = 0;
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int64_t run = 4 * kb + r;
-                const uint32_t e = (row_ok && run < j.runs) ? src[row * j.ld + run] : 127u;
-                cell |= e << (8 * r);
-            }
-            w[g] = cell;
-        }
-        *reinterpret_cast<uint4 *>(j.dst + c * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int g = 0; g < 4; ++g)
+            w[g] = *reinterpret_cast<const uint32_t *>(slab + (32 * g + lane) * SC_PITCH + 4 * kb);
+        const int64_t blk = ((z * j.tiles + t) * j.k_blocks + kbg) * j.subs + sub;
+        *reinterpret_cast<uint4 *>(j.dst + blk * 512 + lane * 16) = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
@@ -722,14 +740,13 @@ tg_status run_gemm(const Args &a, cudaStream_t stream, const tg_options *opt,
         const int64_t runs = ceil_div(a.K, 32);
         const int64_t za = in.a_bcast ? 1 : a.batch, zb = in.b_bcast ? 1 : a.batch;
         const int64_t subs_b = ceil_div(plan.bn, 128);
-        const ScaleJob ja{a.sfa, scales_a, a.M, runs, a.ld_sfa, a.batch > 1 ? a.s_sfa : 0,
-                          plan.tiles_m, plan.k_blocks, za * plan.tiles_m * static_cast<int64_t>(plan.k_blocks) * 32,
-                          128, 1};
-        const ScaleJob jb{a.sfb, scales_b, a.N, runs, a.ld_sfb, a.batch > 1 ? a.s_sfb : 0,
-                          plan.tiles_n, plan.k_blocks,
-                          zb * plan.tiles_n * static_cast<int64_t>(plan.k_blocks) * subs_b * 32, plan.bn, subs_b};
-        const int blocks_a = grid_for(ja.chunks, sms), blocks_b = grid_for(jb.chunks, sms);
-        scale_tile_kernel<<<blocks_a + blocks_b, 256, 0, stream>>>(ja, jb, blocks_a);
+        const ScaleJob ja{a.sfa, scales_a, a.M, runs, a.ld_sfa, a.batch > 1 ? a.s_sfa : 0, za, plan.tiles_m,
+                          plan.k_blocks, 128, 1};
+        const ScaleJob jb{a.sfb, scales_b, a.N, runs, a.ld_sfb, a.batch > 1 ? a.s_sfb : 0, zb, plan.tiles_n,
+                          plan.k_blocks, plan.bn, subs_b};
+        const int64_t blocks_a = scale_blocks(ja), blocks_b = scale_blocks(jb);
+        if (blocks_a + blocks_b > INT32_MAX) return TG_ERR_UNSUPPORTED;
+        scale_tile_kernel<<<static_cast<unsigned>(blocks_a + blocks_b), 256, 0, stream>>>(ja, jb, blocks_a);
         if ((e = cudaGetLastError()) != cudaSuccess) return cuda_status(e);
     }
 
@@ -1130,7 +1147,8 @@ TG_API tg_status tg_gemm_mxfp8(const void *A, const void *B, void *D, int64_t M,
     a.s_sfa = stride_sfa;
     a.ld_sfb = ld_sfb;
     a.s_sfb = stride_sfb;
-    if (opt && ((opt->block_n != 0 && opt->block_n != 128 && opt->block_n != 224) || opt->cta_pair == 2 ||
+    if (opt && ((opt->block_n != 0 && opt->block_n != 128 && opt->block_n != 192 && opt->block_n != 224) ||
+                opt->cta_pair == 2 ||
                 (opt->stages != 0 && opt->stages != 2 && opt->stages != 4)))
         return TG_ERR_INVALID_ARG;
     if (stride_sfa < 0 || stride_sfb < 0 || K < 0) return TG_ERR_INVALID_ARG;

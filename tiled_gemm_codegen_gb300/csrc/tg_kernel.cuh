@@ -344,7 +344,7 @@ __device__ __forceinline__ void apply_epilogue(const KernelParams &p, uint32_t (
 // F8: 8-bit floating-point operands (tcgen05 kind::f8f6f4, formats in
 // p.mma_fmt), K-major A and B only; a k-block is then 128 elements (still
 // 128 bytes a row) and each of its 4 MMAs takes K = 32.
-// MX (with F8, one-CTA tiles 128 rows x 128 or 224 columns): block-scaled
+// MX (with F8, one-CTA tiles 128 rows x 128, 192 or 224 columns): block-scaled
 // operands (kind::mxf8f6f4): every 32 consecutive elements of a row of A
 // (of a column of B) along K share one E8M0 power-of-two scale.  The scales
 // of a k-block come pre-arranged as one 512-byte block per 128 rows of A and
@@ -366,7 +366,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     static_assert((BN % 64 == 0 || (F8 && BN % 32 == 0)) && BN >= 64 && BN <= 256, "tile width");
     static_assert(!PAIR || G::B_COLS % 64 == 0, "two-SM tiles need 64-column halves of B");
     static_assert(G::smem_bytes(STAGES) <= SMEM_LIMIT, "shared memory budget");
-    static_assert(!MX || (F8 && !PAIR && (BN == 128 || BN == 224)), "block scaling: one-CTA 128- or 224-wide tiles");
+    static_assert(!MX || (F8 && !PAIR && (BN == 128 || BN == 192 || BN == 224)),
+                  "block scaling: one-CTA 128-, 192- or 224-wide tiles");
     static_assert(!MX || G::smem_bytes_mx(STAGES) <= SMEM_LIMIT, "shared memory budget (scales)");
     constexpr int TILE_M = PAIR ? 2 * BM : BM;
     constexpr int B_BOXES = G::B_COLS / 64;

@@ -2,8 +2,8 @@
 // width (selected at build time with -DTG_BN=...), so the widths compile in
 // parallel.  Each width instantiates a few ring depths, with one CTA per tile
 // and (widths 128 and 256) two-SM tiles, for bf16 operands and (a subset)
-// 8-bit floating-point ones (block-scaled 8-bit ones at widths 128 and 224,
-// rings 2 and 4, in the width-128 unit); stage_supported() and
+// 8-bit floating-point ones (block-scaled 8-bit ones at widths 128, 192 and
+// 224, rings 2 and 4); stage_supported() and
 // mx_stage_supported() in tg_plan.h list them and the host planner only
 // picks listed configurations.
 #include "tg_kernel.cuh"
@@ -48,13 +48,13 @@ cudaError_t TG_CAT(launch_gemm_bn, TG_BN)(const CUtensorMap &ta, const CUtensorM
                                           int stages, bool pair, bool f8, bool mx, int grid, cudaStream_t s)
 {
     if (mx) {
-        // block-scaled 8-bit operands, one CTA per tile: width 128 here, and
-        // width 224 (launch_gemm_mx224, instantiated in this unit too)
+        // block-scaled 8-bit operands, one CTA per tile: widths 128 and 192
+        // in their units, width 224 (launch_gemm_mx224) in the width-128 unit
         if (pair || !f8) return cudaErrorInvalidValue;
-#if TG_BN == 128
+#if TG_BN == 128 || TG_BN == 192
         switch (stages) {
-            case 2: return launch_fixed<128, 2, false, true, true>(ta, tb, tc, p, grid, s);
-            case 4: return launch_fixed<128, 4, false, true, true>(ta, tb, tc, p, grid, s);
+            case 2: return launch_fixed<TG_BN, 2, false, true, true>(ta, tb, tc, p, grid, s);
+            case 4: return launch_fixed<TG_BN, 4, false, true, true>(ta, tb, tc, p, grid, s);
             default: return cudaErrorInvalidValue;
         }
 #else

@@ -47,11 +47,11 @@ constexpr bool stage_supported(int bn, int s, bool pair = false, bool f8 = false
     }
 }
 
-// Block-scaled 8-bit operands: one-CTA tiles of widths 128 and 224, rings 2
-// and 4.
+// Block-scaled 8-bit operands: one-CTA tiles of widths 128, 192 and 224,
+// rings 2 and 4.
 constexpr bool mx_stage_supported(int bn, int s, bool pair = false)
 {
-    return !pair && (bn == 128 || bn == 224) && (s == 2 || s == 4);
+    return !pair && (bn == 128 || bn == 192 || bn == 224) && (s == 2 || s == 4);
 }
 
 template <bool PAIR>
@@ -200,7 +200,7 @@ inline double tile_efficiency(int bn, bool pair, bool f8 = false, int k_blocks =
 {
     if (f8) {
         if (pair) return bn >= 256 ? (k_blocks >= 48 ? 0.89 : 0.78) : 0.50;
-        return bn >= 256 ? 0.80 : bn >= 192 ? 0.70 : 0.62;
+        return bn >= 256 ? 0.80 : bn >= 224 ? 0.75 : bn >= 192 ? 0.70 : 0.62;
     }
     // measured in-wave rates on GB300 (fraction of the measured bf16 peak)
     if (pair) return bn >= 256 ? 0.97 : 0.53;
@@ -290,6 +290,7 @@ inline bool make_plan(const PlanInput &in, Plan &out)
     if (in.block_n != 0 && in.block_n != 64 && in.block_n != 128 && in.block_n != 192 &&
         in.block_n != 256 && !(in.mx && in.block_n == 224))
         return false;
+    if (in.mx && in.block_n != 0 && !mx_stage_supported(in.block_n, 2)) return false;
     if (in.split_k < 0 || in.stages < 0 || in.max_ctas < 0) return false;
     if (in.epilogue < 0 || in.epilogue > 2) return false;
     if (in.cta_pair < 0 || in.cta_pair > 2) return false;
@@ -302,18 +303,17 @@ inline bool make_plan(const PlanInput &in, Plan &out)
         int bn;
         bool pair;
     };
-    // block-scaled: 224 columns (two accumulators and the scales fill tensor
-    // memory), or 128 where that needs fewer column tiles
-    const Cand cands_mx[2] = {{224, false}, {128, false}};
+    // block-scaled: at most 224 columns (two accumulators and the scales
+    // fill tensor memory); the cost model picks among the instantiated widths
+    const Cand cands_mx[3] = {{224, false}, {192, false}, {128, false}};
     const Cand cands_all[6] = {{256, true}, {128, true}, {256, false}, {192, false}, {128, false}, {64, false}};
     const Cand *cands = in.mx ? cands_mx : cands_all;
-    const int n_cands = in.mx ? 2 : 6;
+    const int n_cands = in.mx ? 3 : 6;
     double best = 0.0;
     bool have = false;
     for (int ci = 0; ci < n_cands; ++ci) {
         const Cand &cd = cands[ci];
         if (in.block_n != 0 && cd.bn != in.block_n) continue;
-        if (in.mx && in.block_n == 0 && (cd.bn == 224) != (ceil_div(in.N, 224) < ceil_div(in.N, 128))) continue;
         if (in.cta_pair == 1 && cd.pair) continue;
         if (in.cta_pair == 2 && !cd.pair) continue;
         if (in.cta_pair == 0 && cd.pair && !PAIR_BY_DEFAULT) continue;
@@ -399,7 +399,9 @@ inline bool make_plan(const PlanInput &in, Plan &out)
     p.smem = smem_bytes_for(p.bn, p.stages, p.pair);
     p.tmem = tmem_cols_for(p.bn);
     if (p.mx) {
-        p.smem = p.bn == 224 ? Geometry<224>::smem_bytes_mx(p.stages) : Geometry<128>::smem_bytes_mx(p.stages);
+        p.smem = p.bn == 224   ? Geometry<224>::smem_bytes_mx(p.stages)
+                 : p.bn == 192 ? Geometry<192>::smem_bytes_mx(p.stages)
+                               : Geometry<128>::smem_bytes_mx(p.stages);
         p.tmem = 512;  // accumulators and the slots' scales
     }
 
