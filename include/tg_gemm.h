@@ -97,7 +97,11 @@ typedef struct tg_options {
                          /* tiles, then an equal share of the remaining       */
                          /* tiles' k-blocks; split tiles are combined in a    */
                          /* fixed k order (cannot be combined with split_k)   */
-    int32_t reserved0;
+    int32_t operands;    /* tg_plan only: the operand family to plan for - 0  */
+                         /* bf16 (tg_gemm_ex), 1 8-bit (tg_gemm_fp8 layout:   */
+                         /* ldb is the pitch of B stored N x K), 2 block-     */
+                         /* scaled 8-bit (tg_gemm_mxfp8); the compute calls   */
+                         /* ignore it                                         */
     uint64_t trace_buffer; /* device address of grid x 8 uint64 (0 = off): per */
                          /* CTA %globaltimer stamps in ns: [0] entry, [1] set- */
                          /* up done, [2] first k-block ready, [3] last MMA    */
@@ -286,8 +290,11 @@ tg_status tg_tune(const void *A, const void *B, float *C,
                   tg_options *best, float *best_us);
 
 /* The plan tg_gemm_ex would use for these arguments, without touching the
- * pointers' memory.  sm_count > 0 plans for that many SMs and makes no CUDA
- * call at all (host-only); sm_count == 0 queries the current device. */
+ * pointers' memory (opt->operands = 1 or 2: the plan of tg_gemm_fp8 or
+ * tg_gemm_mxfp8 instead, with B stored N x K; TG_ERR_UNSUPPORTED where those
+ * calls would refuse the alignment).  sm_count > 0 plans for that many SMs
+ * and makes no CUDA call at all (host-only); sm_count == 0 queries the
+ * current device. */
 tg_status tg_plan(const void *A, const void *B, const float *C,
                   int64_t M, int64_t N, int64_t K,
                   int64_t lda, int64_t ldb, int64_t ldc,

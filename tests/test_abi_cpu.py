@@ -300,3 +300,36 @@ def test_mxfp8_rejects_bad_arguments_before_any_cuda_call(lib):
     # K == 0: no scales needed, nothing to check (and M == 0: nothing to do)
     assert tg.tg_gemm_mxfp8(A, B, D, 0, N, K, K, K, N, 1, 0, 0, 0, 0, 0,
                             SF, 8, 0, SF, 8, 0, None, None, None) == tg.TG_OK
+
+
+def test_plan_8bit_and_block_scaled_choices(lib):
+    """tg_plan with opt->operands: the 8-bit planner's measured choices (one
+    CTA 256 wide unless K is long, 192 wide on the skinny shape, no stream-K
+    by default) and the block-scaled widths (224 where tensor memory allows,
+    192 on the skinny shape), host-only."""
+    p = tg.plan(4096, 4096, 4096, sm_count=152, operands="fp8")
+    assert (p["block_n"], p["cta_pair"], p["stream_k"], p["block_k"]) == (256, 1, 1, 128)
+    assert tg.plan(8192, 8192, 8192, sm_count=152, operands="fp8")["cta_pair"] == 2
+    assert tg.plan(64, 28672, 8192, sm_count=152, operands="fp8")["block_n"] == 192
+    p = tg.plan(4096, 4096, 4096, sm_count=152, operands="mxfp8")
+    assert (p["block_n"], p["cta_pair"], p["tmem_cols"]) == (224, 1, 512)
+    # the re-arranged scales: 512 bytes per 128 rows of A / per 128 columns
+    # of a B tile (two blocks for 224) per k-block of 128
+    assert p["workspace_bytes"] == 32 * 32 * 512 + 19 * 32 * 2 * 512
+    assert tg.plan(64, 28672, 8192, sm_count=152, operands="mxfp8")["block_n"] == 192
+    assert tg.plan(4096, 4096, 4096, sm_count=152, operands="mxfp8",
+                   options=tg.make_options(block_n=128))["block_n"] == 128
+
+
+def test_plan_8bit_rejections(lib):
+    def plan(M, N, K, ops, **kw):
+        o = tg.make_options(**kw)
+        o.operands = tg.OPERAND_FAMILIES[ops] if ops in tg.OPERAND_FAMILIES else ops
+        return tg.tg_plan(0x1000, 0x100000000, 0x200000000, M, N, K, K, K, N, 1, 0, 0, 0, 152, o)[0]
+
+    assert plan(256, 256, 256, "mxfp8", block_n=256) == tg.TG_ERR_INVALID_ARG
+    assert plan(256, 256, 256, "mxfp8", cta_pair=2) == tg.TG_ERR_INVALID_ARG
+    assert plan(256, 256, 256, "fp8", a_col_major=1) == tg.TG_ERR_INVALID_ARG
+    assert plan(256, 256, 256, 3) == tg.TG_ERR_INVALID_ARG
+    assert plan(256, 256, 264, "fp8") == tg.TG_ERR_UNSUPPORTED  # rows of 264 bytes: not 16-byte multiples
+    assert plan(256, 256, 256, "fp8") == tg.TG_OK

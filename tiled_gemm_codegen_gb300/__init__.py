@@ -28,7 +28,7 @@ __all__ = [
     "tg_gemm_fp8", "gemm_fp8", "TG_FP8_E4M3", "TG_FP8_E5M2",
     "tg_gemm_mxfp8", "gemm_mxfp8", "tg_tune", "tune",
     "tg_epilogue", "gemm_fused", "ACTIVATIONS", "tg_device_error", "tg_status_string",
-    "tg_shutdown", "make_options", "gemm", "gemm_host", "plan", "device_error",
+    "tg_shutdown", "make_options", "gemm", "gemm_host", "plan", "OPERAND_FAMILIES", "device_error",
 ]
 
 
@@ -423,16 +423,26 @@ def gemm_host(A, B, C=None, *, options: tg_options | None = None, stream=None):
     return C
 
 
+OPERAND_FAMILIES = {"bf16": 0, "fp8": 1, "mxfp8": 2}
+
+
 def plan(M, N, K, batch=1, *, lda=None, ldb=None, ldc=None, strideA=None, strideB=None,
-         strideC=None, A=0x1000, B=0x100000000, C=0x200000000, sm_count=0, options=None) -> dict:
-    """The plan tg_gemm_ex would use (host-only when sm_count > 0).  The
-    default addresses are placeholders with 16-byte alignment; pass real or
-    deliberately misaligned addresses to see the pack decisions."""
+         strideC=None, A=0x1000, B=0x100000000, C=0x200000000, sm_count=0, options=None,
+         operands: str = "bf16") -> dict:
+    """The plan tg_gemm_ex would use (host-only when sm_count > 0); with
+    operands="fp8" / "mxfp8" the plan of gemm_fp8 / gemm_mxfp8 (B stored
+    N x K, so ldb defaults to K).  The default addresses are placeholders
+    with 16-byte alignment; pass real or deliberately misaligned addresses
+    to see the pack decisions."""
+    family = OPERAND_FAMILIES[operands]
+    if family:
+        options = options if options is not None else tg_options()
+        options.operands = family
     lda = K if lda is None else lda
-    ldb = N if ldb is None else ldb
+    ldb = (K if family else N) if ldb is None else ldb
     ldc = N if ldc is None else ldc
     strideA = M * lda if strideA is None else strideA
-    strideB = K * ldb if strideB is None else strideB
+    strideB = (N if family else K) * ldb if strideB is None else strideB
     strideC = M * ldc if strideC is None else strideC
     st, info = tg_plan(A, B, C, M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC,
                        sm_count, options)

@@ -41,7 +41,7 @@ class tg_options(ctypes.Structure):
         ("debug_stall", ctypes.c_int32),
         ("cta_pair", ctypes.c_int32),
         ("stream_k", ctypes.c_int32),
-        ("reserved0", ctypes.c_int32),
+        ("operands", ctypes.c_int32),
         ("trace_buffer", ctypes.c_uint64),
         ("a_col_major", ctypes.c_int32),
         ("b_col_major", ctypes.c_int32),

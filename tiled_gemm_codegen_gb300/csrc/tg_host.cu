@@ -1171,10 +1171,25 @@ TG_API tg_status tg_plan(const void *A, const void *B, const float *C, int64_t M
                          const tg_options *opt, tg_plan_info *out)
 {
     if (!out || sm_count < 0) return TG_ERR_INVALID_ARG;
-    const Args a =
-        with_layout(Args{A, B, const_cast<float *>(C), M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC}, opt);
+    const int32_t family = opt ? opt->operands : 0;
+    if (family < 0 || family > 2) return TG_ERR_INVALID_ARG;
+    Args a = with_layout(Args{A, B, const_cast<float *>(C), M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC},
+                         opt);
+    if (family != 0) {
+        // the 8-bit entry points' layout: A row-major, B stored N x K
+        if (opt->a_col_major || opt->b_col_major || opt->force_pack) return TG_ERR_INVALID_ARG;
+        a.b_cm = true;
+        a.ab_bytes = 1;
+        a.mx = family == 2;
+    }
     tg_status st = validate(a);
     if (st != TG_OK) return st;
+    if (family != 0 && K > 0) {
+        const bool batched_a = batch > 1 && strideA != 0, batched_b = batch > 1 && strideB != 0;
+        if ((reinterpret_cast<uintptr_t>(A) & 15u) || (reinterpret_cast<uintptr_t>(B) & 15u) || lda % 16 ||
+            ldb % 16 || (batched_a && strideA % 16) || (batched_b && strideB % 16))
+            return TG_ERR_UNSUPPORTED;
+    }
     int sms = sm_count;
     if (sms == 0) {
         int dev = 0;
