@@ -303,13 +303,19 @@ def test_mxfp8_rejects_bad_arguments_before_any_cuda_call(lib):
 
 
 def test_plan_8bit_and_block_scaled_choices(lib):
-    """tg_plan with opt->operands: the 8-bit planner's measured choices (one
-    CTA 256 wide unless K is long, 192 wide on the skinny shape, no stream-K
-    by default) and the block-scaled widths (224 where tensor memory allows,
-    192 on the skinny shape), host-only."""
+    """tg_plan with opt->operands: the 8-bit planner's measured choices
+    (two-SM 256-wide tiles for long K and a full wave, one CTA otherwise,
+    192 wide on the skinny shape, no stream-K by default) and the
+    block-scaled widths (224 where tensor memory allows, 192 on the skinny
+    shape), host-only."""
     p = tg.plan(4096, 4096, 4096, sm_count=152, operands="fp8")
-    assert (p["block_n"], p["cta_pair"], p["stream_k"], p["block_k"]) == (256, 1, 1, 128)
+    assert (p["block_n"], p["cta_pair"], p["stream_k"], p["block_k"]) == (256, 2, 1, 128)
     assert tg.plan(8192, 8192, 8192, sm_count=152, operands="fp8")["cta_pair"] == 2
+    assert tg.plan(4096, 4096, 1024, sm_count=152, operands="fp8")["cta_pair"] == 1   # short K
+    assert tg.plan(2048, 2048, 2048, sm_count=152, operands="fp8")["cta_pair"] == 1   # under a wave
+    # ... unless asked for
+    assert tg.plan(16, 16, 16, sm_count=152, operands="fp8",
+                   options=tg.make_options(block_n=256, cta_pair=2))["cta_pair"] == 2
     assert tg.plan(64, 28672, 8192, sm_count=152, operands="fp8")["block_n"] == 192
     p = tg.plan(4096, 4096, 4096, sm_count=152, operands="mxfp8")
     assert (p["block_n"], p["cta_pair"], p["tmem_cols"]) == (224, 1, 512)

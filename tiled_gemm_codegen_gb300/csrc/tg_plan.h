@@ -194,12 +194,14 @@ inline bool sk_schedule(int64_t tiles, int64_t kb, int64_t workers, SkSchedule &
 // the lower of HBM bandwidth and what the active SMs can pull.
 // 8-bit operands: a k-block holds twice the K at twice the MMA rate, so its
 // ideal time is the bf16 one; their measured rates (E4M3, GB300) favour
-// one-CTA 256-wide tiles unless K is long (two-SM tiles: 4096^3 equal,
-// 8192^3 11% faster, K <= 2048 up to 15% slower).
+// two-SM 256-wide tiles once K >= 2048 and the tiles fill a wave (4096^3
+// 8% faster, 8192^3 and 8192x8192x2048 4% faster), one-CTA 256-wide tiles
+// below that (K = 1024: two-SM tiles 12% slower; 2048^3, under one wave of
+// pairs: 9% slower).
 inline double tile_efficiency(int bn, bool pair, bool f8 = false, int k_blocks = 0)
 {
     if (f8) {
-        if (pair) return bn >= 256 ? (k_blocks >= 48 ? 0.89 : 0.78) : 0.50;
+        if (pair) return bn >= 256 ? (k_blocks >= 16 ? 0.89 : 0.78) : 0.50;
         return bn >= 256 ? 0.80 : bn >= 224 ? 0.75 : bn >= 192 ? 0.70 : 0.62;
     }
     // measured in-wave rates on GB300 (fraction of the measured bf16 peak)
@@ -320,6 +322,11 @@ inline bool make_plan(const PlanInput &in, Plan &out)
         if (in.f8 && !in.mx && !stage_supported(cd.bn, 2, cd.pair, true)) continue;  // no 8-bit instance
         if (in.mx && !mx_stage_supported(cd.bn, 2, cd.pair)) continue;
         if (!in.mx && cd.bn == 224) continue;
+        // the planner's own choice of 8-bit two-SM tiles needs a full wave
+        // of pairs (measured, see tile_efficiency)
+        if (in.f8 && cd.pair && in.cta_pair == 0 &&
+            in.batch * ceil_div(in.M, 2 * BM) * ceil_div(in.N, cd.bn) < std::max(1, sms / 2))
+            continue;
         const int tile_m = cd.pair ? 2 * BM : BM;
         const int64_t tiles_m = ceil_div(in.M, tile_m);
         const int64_t tiles_n = ceil_div(in.N, cd.bn);
