@@ -144,13 +144,14 @@ struct ScaleJob {
 constexpr int SC_KB = 16;
 constexpr int SC_RUNS = 4 * SC_KB;
 constexpr int SC_PITCH = SC_RUNS + 4;
+constexpr int SC_THREADS = 256;
 
 inline int64_t scale_blocks(const ScaleJob &j)
 {
     return j.problems * j.tiles * j.subs * ((j.k_blocks + SC_KB - 1) / SC_KB);
 }
 
-__global__ void __launch_bounds__(256) scale_tile_kernel(ScaleJob ja, ScaleJob jb, int64_t blocks_a)
+__global__ void __launch_bounds__(SC_THREADS) scale_tile_kernel(ScaleJob ja, ScaleJob jb, int64_t blocks_a)
 {
     ptx::griddep_launch_dependents();
     __shared__ __align__(16) uint8_t slab[128 * SC_PITCH];
@@ -166,17 +167,27 @@ __global__ void __launch_bounds__(256) scale_tile_kernel(ScaleJob ja, ScaleJob j
     const int64_t z = bid / j.tiles;
     const uint8_t *src = j.src + z * j.stride;
     const int64_t run0 = kc * SC_RUNS;
-    for (int i = threadIdx.x; i < 128 * SC_RUNS; i += blockDim.x) {
+    // all of a thread's loads in flight at once (the sources are cold)
+    constexpr int PER_THREAD = 128 * SC_RUNS / SC_THREADS;
+    uint8_t v[PER_THREAD];
+#pragma unroll
+    for (int u = 0; u < PER_THREAD; ++u) {
+        const int i = static_cast<int>(threadIdx.x) + u * SC_THREADS;
         const int r = i / SC_RUNS, c = i % SC_RUNS;
         const int64_t in_tile = sub * 128 + r;
         const int64_t row = t * j.tile_rows + in_tile;
         const int64_t run = run0 + c;
         const bool ok = in_tile < j.tile_rows && row < j.rows && run < j.runs;
-        slab[r * SC_PITCH + c] = ok ? src[row * j.ld + run] : static_cast<uint8_t>(127);
+        v[u] = ok ? src[row * j.ld + run] : static_cast<uint8_t>(127);
+    }
+#pragma unroll
+    for (int u = 0; u < PER_THREAD; ++u) {
+        const int i = static_cast<int>(threadIdx.x) + u * SC_THREADS;
+        slab[(i / SC_RUNS) * SC_PITCH + i % SC_RUNS] = v[u];
     }
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int kb = warp; kb < SC_KB; kb += blockDim.x / 32) {
+    for (int kb = warp; kb < SC_KB; kb += SC_THREADS / 32) {
         const int64_t kbg = kc * SC_KB + kb;
         if (kbg >= j.k_blocks) break;
         uint32_t w[4];
@@ -746,7 +757,7 @@ tg_status run_gemm(const Args &a, cudaStream_t stream, const tg_options *opt,
                           plan.k_blocks, plan.bn, subs_b};
         const int64_t blocks_a = scale_blocks(ja), blocks_b = scale_blocks(jb);
         if (blocks_a + blocks_b > INT32_MAX) return TG_ERR_UNSUPPORTED;
-        scale_tile_kernel<<<static_cast<unsigned>(blocks_a + blocks_b), 256, 0, stream>>>(ja, jb, blocks_a);
+        scale_tile_kernel<<<static_cast<unsigned>(blocks_a + blocks_b), SC_THREADS, 0, stream>>>(ja, jb, blocks_a);
         if ((e = cudaGetLastError()) != cudaSuccess) return cuda_status(e);
     }
 
