@@ -339,3 +339,43 @@ def test_plan_8bit_rejections(lib):
     assert plan(256, 256, 256, 3) == tg.TG_ERR_INVALID_ARG
     assert plan(256, 256, 264, "fp8") == tg.TG_ERR_UNSUPPORTED  # rows of 264 bytes: not 16-byte multiples
     assert plan(256, 256, 256, "fp8") == tg.TG_OK
+
+
+def test_c_caller_links_and_plans(lib):
+    """A plain C program (no Python, no torch) includes the header, links the
+    library and uses it host-only: plan queries for the three operand
+    families, argument rejection and status strings."""
+    from tiled_gemm_codegen_gb300 import build as _build
+
+    src = r"""
+#include <stdio.h>
+#include <string.h>
+#include "tg_gemm.h"
+int main(void) {
+  tg_plan_info info;
+  tg_options opt;
+  memset(&opt, 0, sizeof(opt));
+  const void *A = (const void *)0x1000, *B = (const void *)0x100000000ull;
+  const float *C = (const float *)0x200000000ull;
+  if (tg_plan(A, B, C, 4096, 4096, 4096, 4096, 4096, 4096, 1, 0, 0, 0, 152, &opt, &info) != TG_OK) return 1;
+  printf("%d %d %d %d\n", info.block_n, info.cta_pair, info.stages, info.k_blocks);
+  opt.operands = 2;  /* block-scaled 8-bit: B stored N x K */
+  if (tg_plan(A, B, C, 4096, 4096, 4096, 4096, 4096, 4096, 1, 0, 0, 0, 152, &opt, &info) != TG_OK) return 2;
+  printf("%d %d %d %d\n", info.block_n, info.cta_pair, info.stages, info.k_blocks);
+  /* lda < K is rejected before anything else happens */
+  tg_status st = tg_gemm(A, B, (float *)C, 64, 64, 64, 32, 64, 64, 1, 0, 0, 0, NULL);
+  printf("%d %s\n", (int)st, tg_status_string(st));
+  return 0;
+}
+"""
+    libpath = _build.library_path()
+    with tempfile.TemporaryDirectory() as d:
+        c = os.path.join(d, "caller.c")
+        exe = os.path.join(d, "caller")
+        open(c, "w").write(src)
+        subprocess.run(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), c, "-o", exe, libpath,
+                        "-Wl,-rpath," + os.path.dirname(libpath)], check=True)
+        out = subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split("\n")
+    assert out[0].split() == ["256", "2", "6", "64"]       # bf16: two-SM 256 x 256 tiles, 64-element k-blocks
+    assert out[1].split() == ["224", "1", "4", "32"]       # MXFP8: 224-wide tiles, 128-element k-blocks
+    assert out[2].split()[0] == str(tg.TG_ERR_INVALID_ARG)
