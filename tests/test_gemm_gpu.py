@@ -277,6 +277,27 @@ def test_broadcast_operand():
     assert np.array_equal(got.cpu().double().numpy(), ref)
 
 
+def test_broadcast_a_and_many_tiny_problems():
+    """A shared across the batch (stride 0); and 3000 tiny problems (one
+    tile each, far more units than workers: the persistent schedule's
+    strided walk over problems), both exact, under each tile form."""
+    batch, M, N, K = 4, 150, 260, 300
+    _, Bi = synth.make_int_inputs(batch, M, N, K, seed=33)
+    Ai, _ = synth.make_int_inputs(1, M, N, K, seed=34)
+    got = tg.gemm(Ai.to(dev()), Bi.to(dev()))
+    assert tg.device_error() == tg.TG_OK
+    ref = oracle_dense(Ai.unsqueeze(0).expand(batch, M, K).contiguous(), Bi)
+    assert np.array_equal(got.cpu().double().numpy(), ref)
+    batch, M, N, K = 3000, 9, 17, 40
+    Ai, Bi = synth.make_int_inputs(batch, M, N, K, seed=35)
+    ref = oracle_dense(Ai, Bi)
+    Ad, Bd = Ai.to(dev()), Bi.to(dev())
+    for opts in ({}, {"block_n": 64}, {"block_n": 256, "cta_pair": 2}, {"split_k": 1, "max_ctas": 7}):
+        got = tg.gemm(Ad, Bd, options=tg.make_options(**opts))
+        assert tg.device_error() == tg.TG_OK
+        assert np.array_equal(got.cpu().double().numpy(), ref), opts
+
+
 def test_k_zero_and_empty():
     C = torch.full((5, 6), 7.0, device=dev())
     A = torch.empty(5, 0, dtype=torch.bfloat16, device=dev())
