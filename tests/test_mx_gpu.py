@@ -199,3 +199,31 @@ def test_argument_errors():
     assert call(s_sfa=-1) == tg.TG_ERR_INVALID_ARG
     torch.cuda.synchronize()
     assert tg.device_error() == tg.TG_OK
+
+
+@pytest.mark.parametrize("bn", [128, 192, 224])
+def test_scale_pitches_agree(bn):
+    """The same scales at two pitches (a multiple of 4 and an odd one),
+    batched, with a K whose last run is partial: bit for bit equal, and equal
+    to the oracle."""
+    batch, M, N, K = 2, 260, 470, 1040
+    runs = K // 32 + 1  # 33 runs, the last one half full
+    A = synth.make_fp8_codes((batch, M, K), 0, seed=71)
+    Bt = synth.make_fp8_codes((batch, N, K), 0, seed=72)
+    sfa = synth.make_e8m0_codes((batch, M, runs), seed=73, lo=126, hi=128)
+    sfb = synth.make_e8m0_codes((batch, N, runs), seed=74, lo=126, hi=128)
+    want = _oracle(A, Bt, sfa, sfb)
+    outs = []
+    for pitch in (36, 35):
+        fa = torch.full((batch, M, pitch), 255, dtype=torch.uint8)
+        fa[:, :, :runs] = sfa
+        fb = torch.full((batch, N, pitch), 255, dtype=torch.uint8)
+        fb[:, :, :runs] = sfb
+        Ad = A.to(dev()).view(torch.float8_e4m3fn)
+        Bd = Bt.to(dev()).view(torch.float8_e4m3fn)
+        D = tg.gemm_mxfp8(Ad, Bd, fa.to(dev())[:, :, :runs], fb.to(dev())[:, :, :runs],
+                          options=tg.make_options(block_n=bn))
+        assert tg.device_error() == tg.TG_OK
+        outs.append(D.cpu().double().numpy())
+    assert np.array_equal(outs[0], outs[1])
+    assert np.array_equal(outs[0], want)
