@@ -34,6 +34,10 @@ KERNEL_SOURCES = ["tiled_gemm_codegen_gb300/csrc/tg_kernel.cuh", "tiled_gemm_cod
                   "tiled_gemm_codegen_gb300/csrc/tg_internal.h", "tiled_gemm_codegen_gb300/csrc/tg_epilogue.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Nominal GB300 figures (dense bf16 tensor rate, HBM3e bandwidth), reported
+# next to the fractions of the measured peaks.
+NOMINAL_PEAKS = {"bf16_tflops": 2250.0, "hbm_gbs": 8000.0}
+EXTRA_STEPS = 50  # timed steps of each non-headline workload (median reported)
 
 
 # ------------------------------------------------------------------ helpers
@@ -216,6 +220,68 @@ def run_reference(args, rank, world, dist):
 
 
 # ------------------------------------------------------------------ GPU arm
+def roofline_of(w, ms: float, peaks: dict, peak_src: str) -> dict:
+    """The binding roofline of workload `w` at `ms` per call: HBM when its
+    arithmetic intensity (algorithmic flop per algorithmic byte) is below
+    the ridge point of the measured peaks, else the bf16 tensor peak; the
+    fraction of the nominal figure is given beside the measured one."""
+    peak = float(peaks["bf16_tflops"])
+    hbm = float(peaks["hbm_gbs"])
+    flops = float(w.flops)
+    achieved = flops / (ms * 1e-3) / 1e12
+    gbs = w.bytes_moved / (ms * 1e-3) / 1e9
+    if flops / w.bytes_moved < peak * 1e12 / (hbm * 1e9):
+        return {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(gbs / hbm, 4), "traffic": measured_traffic(w.name),
+                "peak_source": f"{peak_src} hbm_gbs (copy)",
+                "algorithmic_bytes_per_launch": int(w.bytes_moved),
+                "nominal_peak": NOMINAL_PEAKS["hbm_gbs"],
+                "nominal_frac": round(gbs / NOMINAL_PEAKS["hbm_gbs"], 4),
+                "tensor_frac": round(achieved / peak, 4)}
+    return {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4), "traffic": measured_traffic(w.name),
+            "peak_source": f"{peak_src} bf16_tflops (burst; kernel timed alone)",
+            "algorithmic_flops_per_launch": int(flops),
+            "nominal_peak": NOMINAL_PEAKS["bf16_tflops"],
+            "nominal_frac": round(achieved / NOMINAL_PEAKS["bf16_tflops"], 4),
+            "hbm_frac": round(gbs / hbm, 4)}
+
+
+PLAN_KEYS = ("block_n", "stages", "split_k", "grid", "pack_a", "pack_b", "epilogue", "cta_pair", "stream_k",
+             "sk_tiles")
+
+
+def time_extra_workload(tg, torch, w, device, flush_l2, steps: int, warmup: int) -> dict:
+    """One non-headline workload at its full size: `warmup` untimed calls,
+    then `steps` calls each timed with CUDA events on the launching stream,
+    L2 flushed before every call (outside the events)."""
+    A_cpu, B_cpu = synth.workload_inputs(w)
+    A, B = A_cpu.to(device), B_cpu.to(device)
+    del A_cpu, B_cpu
+    C = torch.empty((w.batch, w.M, w.N) if w.batch > 1 else (w.M, w.N), dtype=torch.float32, device=device)
+    info = tg.plan(w.M, w.N, w.K, w.batch, A=A.data_ptr(), B=B.data_ptr(), C=C.data_ptr())
+    stream = torch.cuda.current_stream(device)
+    for _ in range(warmup):
+        flush_l2(1.0)
+        tg.gemm(A, B, C)
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush_l2(float(i))
+        starts[i].record(stream)
+        tg.gemm(A, B, C)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    st = tg.device_error()
+    if st != tg.TG_OK:
+        raise RuntimeError(f"device error while timing {w.name}: {st}")
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    del A, B, C
+    return {"per": per, "plan": {k: info[k] for k in PLAN_KEYS},
+            "launches_per_step": 1 + info["pack_a"] + info["pack_b"]}
+
+
 def run_gpu(args, rank, world, local, dist):
     import torch
 
@@ -331,24 +397,32 @@ def run_gpu(args, rank, world, local, dist):
     e2e_value = world * flops / (e2e_ms_max * 1e-3) / 1e12
 
     peaks, peak_src = load_peaks()
-    peak = float(peaks["bf16_tflops"])
-    hbm = float(peaks["hbm_gbs"])
-    achieved = flops / (ms_mean * 1e-3) / 1e12  # this rank's kernel
-    gbs = w.bytes_moved / (ms_mean * 1e-3) / 1e9
-    # the binding roofline: HBM when the workload's arithmetic intensity
-    # (algorithmic flop per algorithmic byte) is below the ridge point
-    if flops / w.bytes_moved < peak * 1e12 / (hbm * 1e9):
-        roofline = {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
-                    "frac": round(gbs / hbm, 4), "traffic": measured_traffic(w.name),
-                    "peak_source": f"{peak_src} hbm_gbs (copy)",
-                    "algorithmic_bytes_per_launch": int(w.bytes_moved),
-                    "tensor_frac": round(achieved / peak, 4)}
-    else:
-        roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                    "frac": round(achieved / peak, 4), "traffic": measured_traffic(w.name),
-                    "peak_source": f"{peak_src} bf16_tflops (burst; kernel timed alone)",
-                    "algorithmic_flops_per_launch": int(flops),
-                    "hbm_frac": round(gbs / hbm, 4)}
+    roofline = roofline_of(w, ms_mean, peaks, peak_src)  # this rank's kernel
+
+    # Every other workload at its full size, in the launch configuration of
+    # the default plan: median of EXTRA_STEPS cold-L2 calls each (rank 0's
+    # GPU; the replicas are identical).
+    extra = {}
+    extra_clk = None
+    if not args.no_extra and rank == 0:
+        sampler = ClockSampler(local)
+        sampler.start()
+        for name, wx in synth.WORKLOADS.items():
+            if name == w.name:
+                continue
+            r = time_extra_workload(tg, torch, wx, device, flush_l2, EXTRA_STEPS, args.warmup)
+            per_x = r["per"]
+            med = statistics.median(per_x)
+            extra[name] = {
+                "batch": wx.batch, "M": wx.M, "N": wx.N, "K": wx.K, "dist": wx.dist, "seed": wx.seed,
+                "steps": len(per_x), "ms_median": round(med, 4), "ms_mean": round(sum(per_x) / len(per_x), 4),
+                "ms_min": round(min(per_x), 4),
+                "value": round(wx.flops / (med * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                "roofline": roofline_of(wx, med, peaks, peak_src),
+                "plan": r["plan"], "gpu_launches_per_step": r["launches_per_step"],
+            }
+            torch.cuda.empty_cache()
+        extra_clk = sampler.stop()
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = oracle_sample(w, seconds=args.cpu_seconds)
@@ -375,8 +449,14 @@ def run_gpu(args, rank, world, local, dist):
             "clocks": dict(clk, window=f"{args.clock_window:.1f} s of the same steps (flush, GEMM) just "
                                           "before the timed region, and the timed region"),
             "ms_min": round(min(per), 4),
+            "ms_median": round(statistics.median(per), 4),
             "wall_s": round(wall, 3),
         }
+        if extra:
+            line["workloads"] = extra
+            line["workloads_note"] = (f"each: {EXTRA_STEPS} calls after {args.warmup} warm-up calls, CUDA events "
+                                      "per call, L2 flushed before every call; value and roofline from the median")
+            line["workloads_clocks"] = extra_clk
         print(json.dumps(line), flush=True)
 
 
@@ -426,6 +506,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--clock-window", type=float, default=0.5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="time only the headline workload (skip the other workloads' lines)")
     ap.add_argument("--dtype", default="bf16", choices=["bf16", "e4m3", "mxfp8"],
                     help="operand type; e4m3 (mxfp8) runs the same shape through tg_gemm_fp8 "
                          "(tg_gemm_mxfp8): an extra line, not the contract's metric")

@@ -1,11 +1,8 @@
 """Parity at the five workloads' full sizes, in the launch configuration the
-benchmark times (the default plan).
-
-The oracle computes sampled entries one by one (every tile-fringe row and
-column near the edges, plus random positions); a property that holds at any
-size - row and column sums of C against A (B 1) and (1^T A) B in fp64 -
-covers every output element.  With small-integer inputs of the same shapes
-the sampled entries must match the oracle bit for bit.
+benchmark times (the default plan): every element of C against the fp64
+oracle's full product (the oracle does 4096^3 in a few seconds on a
+many-core host), within the contract's tolerance for random inputs and bit
+for bit for small-integer inputs of the same shapes.
 """
 from __future__ import annotations
 
@@ -16,7 +13,7 @@ import torch
 import oracle
 import synth
 import tiled_gemm_codegen_gb300 as tg
-from gpu_helpers import PER_ELEM, REL_FRO, assert_close, dev
+from gpu_helpers import assert_close, dev
 
 pytestmark = pytest.mark.gpu
 
@@ -45,54 +42,32 @@ def _sampled(w, A, B, C, count=3000, seed=0):
     return got, ref
 
 
-def _checksums(w, A, B, C):
-    """Row sums and column sums of the GPU output against fp64 products of
-    A with B's row sums and of A's column sums with B, problem by problem."""
-    Cc = C if C.dim() == 3 else C.unsqueeze(0)
-    Ac = A if A.dim() == 3 else A.unsqueeze(0)
-    Bc = B if B.dim() == 3 else B.unsqueeze(0)
-    worst = 0.0
-    for b in range(w.batch):
-        c64 = Cc[b].double()
-        a64 = Ac[b].to(dev()).double()
-        b64 = Bc[b].to(dev()).double()
-        row_ref = a64 @ b64.sum(dim=1)
-        col_ref = a64.sum(dim=0) @ b64
-        scale = float(torch.max(torch.abs(c64)))
-        row_tol = w.N * PER_ELEM * np.sqrt(w.K) * scale
-        col_tol = w.M * PER_ELEM * np.sqrt(w.K) * scale
-        rerr = float(torch.max(torch.abs(c64.sum(dim=1) - row_ref)))
-        cerr = float(torch.max(torch.abs(c64.sum(dim=0) - col_ref)))
-        assert rerr <= row_tol, (b, rerr, row_tol)
-        assert cerr <= col_tol, (b, cerr, col_tol)
-        worst = max(worst, rerr / row_tol, cerr / col_tol)
-        del c64, a64, b64
-    return worst
-
-
 @pytest.mark.parametrize("name", NAMES)
 def test_workload_float_parity(name):
+    """Every element of C against the fp64 oracle's full product, under the
+    contract's bounds (relative Frobenius error over the whole output, and
+    per element against the largest |C_ref|).  The one-by-one dot-product
+    form of the oracle on sampled entries (every tile-fringe row and column
+    near the edges, plus random positions) is checked as well."""
     w = synth.WORKLOADS[name]
     A, B = synth.workload_inputs(w)
     C = _run_default(A, B)
-    assert bool(torch.isfinite(C).all())
-    if w.M * w.N * w.K * w.batch <= 10 ** 8:
-        assert_close(C.cpu().double().numpy(), oracle.gemm_dense_f64(A, B), w.K, name)
-        return
-    got, ref = _sampled(w, A, B, C)
-    # tolerance on the sampled entries: per element against the largest
-    # sampled magnitude (stricter than the whole-output max), relative
-    # Frobenius error over the sample
-    diff = got - ref
-    assert np.abs(diff).max() <= PER_ELEM * np.sqrt(w.K) * np.abs(ref).max(), name
-    assert np.linalg.norm(diff) / np.linalg.norm(ref) <= REL_FRO, name
-    _checksums(w, A, B, C)
+    got = C.cpu().double().numpy()
+    assert np.all(np.isfinite(got))
+    ref = oracle.gemm_dense_f64(A, B)
+    assert_close(got, ref, w.K, name)
+    g, r = _sampled(w, A, B, C)
+    assert_close(g, r, w.K, name + " (sampled entries)")
 
 
 @pytest.mark.parametrize("name", NAMES)
 def test_workload_exact_integer(name):
+    """Small-integer inputs of the same shapes: every partial sum is an exact
+    fp32 integer, so every element of C must equal the oracle bit for bit."""
     w = synth.WORKLOADS[name]
     A, B = synth.make_int_inputs(w.batch, w.M, w.N, w.K, seed=w.seed + 100)
     C = _run_default(A, B)
-    got, ref = _sampled(w, A, B, C, count=2000, seed=1)
-    assert np.array_equal(got, ref), name
+    got = C.cpu().double().numpy()
+    ref = oracle.gemm_dense_f64(A, B)
+    bad = np.argwhere(got != ref)
+    assert bad.size == 0, f"{name}: {len(bad)} elements differ, first at {bad[:4].tolist()}"
