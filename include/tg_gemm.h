@@ -327,22 +327,30 @@ tg_status tg_plan(const void *A, const void *B, const float *C,
  * library until the process exits.  The first call on a device looks up the
  * array's device address (cudaGetSymbolAddress) once; make that first call
  * before any stream capture.  Every call shares the one array, which keeps
- * the previous call's contents; each call clears the tile counters and the
- * error word it uses before its kernel.  Calls whose kernels overlap on the
- * GPU (different streams, or graph branches) race on the array: serialise
- * them.  A watchdog expiry in this entry point's kernel is recorded in the
- * array's own error word (cleared by the next call), not in the per-stream
- * word that tg_device_error() reads. */
+ * the previous call's contents; each call clears the tile counters it uses
+ * before its kernel.  Calls whose kernels overlap on the GPU (different
+ * streams, or graph branches) race on the array: serialise them.
+ * A watchdog expiry in this entry point's kernel is recorded in the array's
+ * own error word (one per device, shared by all calls of this entry point),
+ * which keeps the first expiry until tg_device_error() - on any stream of
+ * that device - reads and clears it; synchronise the stream the call ran on
+ * (or pass it to tg_device_error) first.  Self-test: with the environment
+ * variable TG_DEBUG_STALL_NS set to a positive number of nanoseconds, the
+ * kernel first waits on a barrier that nothing completes, with that limit,
+ * so the call leaves C unwritten and tg_device_error() returns
+ * TG_ERR_TIMEOUT. */
 tg_status tg_gemm_splitk_static(const void *A, const void *B, float *C,
                                 int64_t M, int64_t N, int64_t K,
                                 int64_t lda, int64_t ldb, int64_t ldc,
                                 int64_t batch, int64_t strideA, int64_t strideB,
                                 int64_t strideC, int32_t split_k, tg_stream_t stream);
 
-/* Synchronises `stream`, then reads and clears the device error word that
- * the kernels' watchdog writes.  TG_ERR_TIMEOUT if a wait expired since the
- * last call (the split-K tile counters are then reset too), TG_ERR_CUDA if
- * the stream reports a CUDA error, else TG_OK. */
+/* Synchronises `stream`, then reads and clears the device error words that
+ * the kernels' watchdog writes: the one of `stream`'s workspace, and the one
+ * of tg_gemm_splitk_static on the current device.  TG_ERR_TIMEOUT if a wait
+ * expired since the last call (the split-K tile counters of the stream's
+ * workspace are then reset too), TG_ERR_CUDA if the stream reports a CUDA
+ * error, else TG_OK.  Allocates nothing. */
 tg_status tg_device_error(tg_stream_t stream);
 
 /* Static English name of a status code. */

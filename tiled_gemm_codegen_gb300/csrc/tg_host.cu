@@ -471,19 +471,23 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_
                                    const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+EncodeTiledFn query_encode_fn()
+{
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+        return reinterpret_cast<EncodeTiledFn>(p);
+    return nullptr;
+}
+
+// The driver's encoder, looked up once.  A function-local static with an
+// initialiser: C++ runs the lookup exactly once and every caller, from any
+// thread, sees the finished pointer (some callers hold no library mutex).
 EncodeTiledFn encode_fn()
 {
-    static EncodeTiledFn fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q{};
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    }
+    static const EncodeTiledFn fn = query_encode_fn();
     return fn;
 }
 
@@ -1442,15 +1446,19 @@ TG_API tg_status tg_device_error(tg_stream_t stream_)
     if (e != cudaSuccess) return TG_ERR_CUDA;
     int dev = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return TG_ERR_CUDA;
+    // The static-scratch entry point's own word (one per device, shared by
+    // all its calls): read and cleared here as well.
+    bool static_timeout = false;
+    if (static_error_take(dev, stream, &static_timeout) != cudaSuccess) return TG_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_mutex);
     auto it = g_workspaces.find({dev, stream});
-    if (it == g_workspaces.end() || !it->second.err) return TG_OK;
+    if (it == g_workspaces.end() || !it->second.err) return static_timeout ? TG_ERR_TIMEOUT : TG_OK;
     Workspace &w = it->second;
     uint32_t word = 0;
     if ((e = cudaMemcpyAsync(&word, w.err, 4, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
         return TG_ERR_CUDA;
     if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return TG_ERR_CUDA;
-    if (word == ERR_NONE) return TG_OK;
+    if (word == ERR_NONE) return static_timeout ? TG_ERR_TIMEOUT : TG_OK;
     // Clear the word, and the split-K counters an aborted kernel may have
     // left part-way.
     cudaMemsetAsync(w.err, 0, 4, stream);

@@ -11,6 +11,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdlib>
 #include <mutex>
 
 #include "tg_gemm.h"
@@ -55,7 +56,55 @@ tg_status scratch_address(int dev, uint8_t **out)
     return TG_OK;
 }
 
+// The array's error word on device `dev`, or null if no call has set the
+// device up yet (then no kernel of this entry point has run there).
+uint32_t *error_word(int dev)
+{
+    if (dev < 0 || dev >= MAX_DEVICES) return nullptr;
+    std::lock_guard<std::mutex> lock(g_setup_mutex);
+    uint8_t *base = static_cast<uint8_t *>(g_scratch_addr[dev]);
+    return base ? reinterpret_cast<uint32_t *>(base + PARTIAL_BYTES + COUNTER_BYTES) : nullptr;
+}
+
+// Watchdog self-test of this entry point: with TG_DEBUG_STALL_NS set to a
+// positive number of nanoseconds, the kernel's epilogue first waits on a
+// barrier that nothing completes, with that limit, so the wait must expire
+// and tg_device_error() must report it.  Read on every call (tests set and
+// unset it within one process).
+uint64_t debug_stall_ns()
+{
+    const char *v = std::getenv("TG_DEBUG_STALL_NS");
+    if (!v || !*v) return 0;
+    char *end = nullptr;
+    const unsigned long long ns = std::strtoull(v, &end, 10);
+    return (end && *end == '\0') ? static_cast<uint64_t>(ns) : 0;
+}
+
 }  // namespace
+
+namespace tg {
+
+// Reads the array's error word on the current device after `stream` has
+// been synchronised by the caller; a nonzero word is cleared and reported
+// through *timed_out.  Reads nothing (and reports nothing) on a device where
+// the entry point has never run.  Allocates nothing: the word goes through
+// one 4-byte copy into a host variable.
+cudaError_t static_error_take(int dev, cudaStream_t stream, bool *timed_out)
+{
+    *timed_out = false;
+    uint32_t *err = error_word(dev);
+    if (!err) return cudaSuccess;
+    uint32_t word = 0;
+    cudaError_t e = cudaMemcpyAsync(&word, err, 4, cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess || word == ERR_NONE) return e;
+    *timed_out = true;
+    e = cudaMemsetAsync(err, 0, 4, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    return e;
+}
+
+}  // namespace tg
 
 TG_API tg_status tg_gemm_splitk_static(const void *A, const void *B, float *C, int64_t M,
                                        int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
@@ -96,9 +145,13 @@ TG_API tg_status tg_gemm_splitk_static(const void *A, const void *B, float *C, i
     float *partials = reinterpret_cast<float *>(scratch);
     int32_t *counters = reinterpret_cast<int32_t *>(scratch + PARTIAL_BYTES);
     uint32_t *err = reinterpret_cast<uint32_t *>(scratch + PARTIAL_BYTES + COUNTER_BYTES);
-    // What must start at zero: this call's tile counters and the error word.
+    // What must start at zero: this call's tile counters (an earlier call
+    // that timed out may have left some part-way).  The error word is not
+    // cleared here: like the per-stream word, it keeps the first expiry
+    // until tg_device_error() reads and clears it (it starts at zero: global
+    // variables without an initializer are zero-initialised when the module
+    // loads).
     if (cudaMemsetAsync(counters, 0, static_cast<size_t>(tiles) * 4, stream) != cudaSuccess) return TG_ERR_CUDA;
-    if (cudaMemsetAsync(err, 0, ERR_BYTES, stream) != cudaSuccess) return TG_ERR_CUDA;
 
     CUtensorMap ta{}, tb{}, tc{};
     const uint64_t za = in.a_bcast || batch == 1 ? 1 : static_cast<uint64_t>(batch);
@@ -136,8 +189,9 @@ TG_API tg_status tg_gemm_splitk_static(const void *A, const void *B, float *C, i
     p.maxparts = plan.splits;
     p.counters = counters;
     p.err = err;
-    p.timeout_ns = 2000000000ull;
-    p.debug_stall = 0;
+    const uint64_t stall_ns = debug_stall_ns();
+    p.timeout_ns = stall_ns ? stall_ns : 2000000000ull;
+    p.debug_stall = stall_ns ? 1 : 0;
     const cudaError_t e = shared_launch_gemm(plan.bn, ta, tb, tc, p, plan.stages, plan.grid, stream);
     return e == cudaSuccess ? TG_OK : TG_ERR_CUDA;
 }
