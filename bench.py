@@ -291,10 +291,23 @@ def run_gpu(args, rank, world, local, dist):
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     w = synth.WORKLOADS[args.workload]
-    f8 = args.dtype in ("e4m3", "mxfp8")
-    mx = args.dtype == "mxfp8"
+    f8 = args.dtype in ("e4m3", "mxfp8", "mxfp4")
+    mx = args.dtype in ("mxfp8", "mxfp4")
+    fp4 = args.dtype == "mxfp4"
     C = torch.empty((w.batch, w.M, w.N) if w.batch > 1 else (w.M, w.N), dtype=torch.float32, device=device)
-    if f8:
+    if fp4:
+        # the same shape with packed E2M1 operands (codes drawn uniformly,
+        # two a byte), A row-major and B column-major (stored N x K), E8M0
+        # scales 2^-3 .. 2^3 per 32 elements of K
+        lead = (w.batch,) if w.batch > 1 else ()
+        A = synth.pack_fp4_codes(synth.make_fp4_codes(lead + (w.M, w.K), seed=w.seed)).to(device)
+        B = synth.pack_fp4_codes(synth.make_fp4_codes(lead + (w.N, w.K), seed=w.seed + 1)).to(device)
+        runs = -(-w.K // 32)
+        SFA = synth.make_e8m0_codes(lead + (w.M, runs), seed=w.seed + 2).to(device)
+        SFB = synth.make_e8m0_codes(lead + (w.N, runs), seed=w.seed + 3).to(device)
+        launches_per_step = 2
+        info = {}
+    elif f8:
         # the same shape with E4M3 operands (N(0,1) draws rounded to E4M3),
         # A row-major and B column-major (stored N x K)
         lead = (w.batch,) if w.batch > 1 else ()
@@ -328,7 +341,9 @@ def run_gpu(args, rank, world, local, dist):
         torch.sum(flush_read, dim=0, out=sink)  # read > L2: dirty flush lines written back now
 
     def step():
-        if mx:
+        if fp4:
+            tg.gemm_mxfp4(A, B, SFA, SFB, C)
+        elif mx:
             tg.gemm_mxfp8(A, B, SFA, SFB, C)
         elif f8:
             tg.gemm_fp8(A, B, C)
@@ -461,31 +476,39 @@ def run_gpu(args, rank, world, local, dist):
 
 
 def report_f8(args, w, per, ms_mean, ms_max, world, rank, clk, wall, launches_per_step):
-    """The line of an --dtype e4m3 / mxfp8 run: the same shape with 8-bit
-    operands (mxfp8: with E8M0 block scales), against the bf16 measured peak
-    times the nominal 8-bit/16-bit tensor ratio (2)."""
-    mx = args.dtype == "mxfp8"
+    """The line of an --dtype e4m3 / mxfp8 / mxfp4 run: the same shape with
+    8-bit operands (mxfp8: with E8M0 block scales) or packed 4-bit ones
+    (mxfp4), against the bf16 measured peak times the nominal dense
+    8-bit/16-bit (2) or 4-bit/16-bit (13.5 / 2.25 = 6) tensor ratio."""
+    mx = args.dtype in ("mxfp8", "mxfp4")
+    fp4 = args.dtype == "mxfp4"
     peaks, peak_src = load_peaks()
-    peak = 2.0 * float(peaks["bf16_tflops"])
+    ratio = 6.0 if fp4 else 2.0
+    peak = ratio * float(peaks["bf16_tflops"])
     flops = float(w.flops)
     achieved = flops / (ms_mean * 1e-3) / 1e12
-    bytes_moved = w.batch * (w.M * w.K + w.K * w.N + 4 * w.M * w.N)
+    elem = 0.5 if fp4 else 1.0
+    bytes_moved = w.batch * (elem * w.M * w.K + elem * w.K * w.N + 4 * w.M * w.N)
     if mx:
         bytes_moved += w.batch * (w.M + w.N) * (-(-w.K // 32))
     if rank == 0:
         line = {
-            "metric": ("MXFP8 (e4m3, E8M0 scales per 32) " if mx else "e4m3") +
-                      "->fp32 GEMM TFLOP/s at 1 GB300 and % of dense FP8 tensor roofline",
+            "metric": ("MXFP4 (e2m1, E8M0 scales per 32) ->fp32 GEMM TFLOP/s at 1 GB300 and % of dense FP4 "
+                       "tensor roofline" if fp4 else
+                       ("MXFP8 (e4m3, E8M0 scales per 32) " if mx else "e4m3") +
+                       "->fp32 GEMM TFLOP/s at 1 GB300 and % of dense FP8 tensor roofline"),
             "value": round(world * flops / (ms_max * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": args.dtype,
             "data": "synthetic",
             "config": {"workload": w.name, "batch": w.batch, "M": w.M, "N": w.N, "K": w.K,
-                       "layout": "A row-major, B column-major (both K-major)", "accumulate": "fp32",
+                       "layout": "A row-major, B column-major (both K-major)" +
+                                 (", two E2M1 codes a byte" if fp4 else ""), "accumulate": "fp32",
                        "l2": "flushed between steps (512 MB write, then 256 MB read)"},
             "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                          "frac": round(achieved / peak, 4), "traffic": None,
-                         "peak_source": f"{peak_src} bf16_tflops x 2 (nominal fp8/bf16 dense ratio)",
+                         "peak_source": f"{peak_src} bf16_tflops x {ratio:g} (nominal "
+                                        f"{'fp4' if fp4 else 'fp8'}/bf16 dense ratio)",
                          "hbm_frac": round(bytes_moved / (ms_mean * 1e-3) / 1e9 / float(peaks["hbm_gbs"]), 4)},
             "cpu_baseline": None, "e2e": None,
             "gpu_launches": launches_per_step * args.steps,
@@ -508,9 +531,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true",
                     help="time only the headline workload (skip the other workloads' lines)")
-    ap.add_argument("--dtype", default="bf16", choices=["bf16", "e4m3", "mxfp8"],
-                    help="operand type; e4m3 (mxfp8) runs the same shape through tg_gemm_fp8 "
-                         "(tg_gemm_mxfp8): an extra line, not the contract's metric")
+    ap.add_argument("--dtype", default="bf16", choices=["bf16", "e4m3", "mxfp8", "mxfp4"],
+                    help="operand type; e4m3 (mxfp8, mxfp4) runs the same shape through tg_gemm_fp8 "
+                         "(tg_gemm_mxfp8, tg_gemm_mxfp4): an extra line, not the contract's metric")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "tg":
         ap.error("--warmup must be at least 3")

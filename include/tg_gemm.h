@@ -100,8 +100,9 @@ typedef struct tg_options {
     int32_t operands;    /* tg_plan only: the operand family to plan for - 0  */
                          /* bf16 (tg_gemm_ex), 1 8-bit (tg_gemm_fp8 layout:   */
                          /* ldb is the pitch of B stored N x K), 2 block-     */
-                         /* scaled 8-bit (tg_gemm_mxfp8); the compute calls   */
-                         /* ignore it                                         */
+                         /* scaled 8-bit (tg_gemm_mxfp8), 3 block-scaled      */
+                         /* packed 4-bit (tg_gemm_mxfp4: K and pitches in     */
+                         /* elements); the compute calls ignore it            */
     uint64_t trace_buffer; /* device address of grid x 8 uint64 (0 = off): per */
                          /* CTA %globaltimer stamps in ns: [0] entry, [1] set- */
                          /* up done, [2] first k-block ready, [3] last MMA    */
@@ -249,6 +250,37 @@ tg_status tg_gemm_mxfp8(const void *A, const void *B, void *D,
                         int64_t lda, int64_t ldb, int64_t ldd,
                         int64_t batch, int64_t strideA, int64_t strideB, int64_t strideD,
                         int32_t a_format, int32_t b_format,
+                        const uint8_t *SFA, int64_t ld_sfa, int64_t stride_sfa,
+                        const uint8_t *SFB, int64_t ld_sfb, int64_t stride_sfb,
+                        const tg_epilogue *ep, tg_stream_t stream, const tg_options *opt);
+
+/* Block-scaled 4-bit GEMM (MXFP4: the block-scaled family of TVM "Tensor
+ * Layout", Case study: Blackwell tensor memory, on 4-bit elements):
+ *     D[b][i][j] = sum_k  2^(SFA[b][i][k/32] - 127) * A[b][i][k]
+ *                       * 2^(SFB[b][j][k/32] - 127) * B[b][k][j]
+ * then the fused epilogue of tg_gemm_fused (ep may be NULL: D in fp32).
+ * Elements are E2M1 codes (OCP MX: sign bit 3, exponent bits 2-1 with bias
+ * 1, mantissa bit 0; values 0, 0.5, 1, 1.5, 2, 3, 4, 6 and their negatives),
+ * two to a byte: element k of a stored row is in byte k/2, in the low nibble
+ * when k is even and in the high nibble when k is odd.  A row-major M x K
+ * (element (i,k) in byte A[(i*lda + k)/2]); B column-major, i.e. stored
+ * N x K (element (k,j) in byte B[(j*ldb + k)/2]).  K, lda, ldb, strideA and
+ * strideB count ELEMENTS and must be even (else TG_ERR_INVALID_ARG);
+ * A and B 16-byte aligned, lda, ldb and the batch strides multiples of 32
+ * elements (16 bytes), else TG_ERR_UNSUPPORTED.  Scales SFA, SFB: E8M0
+ * bytes, one per 32 elements of K, laid out and checked as in
+ * tg_gemm_mxfp8.  D (ldd, strideD in elements of D's type) and ep as
+ * tg_gemm_fused.  The library re-arranges the scales into device scratch it
+ * owns (two 512-byte blocks per 128 rows or columns of a tile and 256
+ * elements of K) on `stream` before the GEMM (tcgen05 kind::mxf4, 64
+ * elements of K per instruction).  Tiles: 128 rows x 128, 192 or 224
+ * columns, one CTA each; opt->block_n 0, 128, 192 or 224, opt->cta_pair 0
+ * or 1, opt->stages 0, 2 or 4 (224-wide tiles: 0 or 2), else
+ * TG_ERR_INVALID_ARG. */
+tg_status tg_gemm_mxfp4(const void *A, const void *B, void *D,
+                        int64_t M, int64_t N, int64_t K,
+                        int64_t lda, int64_t ldb, int64_t ldd,
+                        int64_t batch, int64_t strideA, int64_t strideB, int64_t strideD,
                         const uint8_t *SFA, int64_t ld_sfa, int64_t stride_sfa,
                         const uint8_t *SFB, int64_t ld_sfb, int64_t stride_sfb,
                         const tg_epilogue *ep, tg_stream_t stream, const tg_options *opt);

@@ -171,3 +171,21 @@ def make_e8m0_codes(shape, seed: int, lo: int = 124, hi: int = 130) -> torch.Ten
     default range is scales 2^-3 .. 2^3."""
     gen = torch.Generator("cpu").manual_seed(seed)
     return torch.randint(lo, hi + 1, tuple(shape), generator=gen).to(torch.uint8)
+
+
+# ------------------------------------------------------------ packed 4-bit operands
+def make_fp4_codes(shape, seed: int, lo: int = 0, hi: int = 15) -> torch.Tensor:
+    """Seeded 4-bit E2M1 codes (uint8, one code per element, values lo..hi
+    drawn uniformly; the default covers all 16 codes, every one finite)."""
+    gen = torch.Generator("cpu").manual_seed(seed)
+    return torch.randint(lo, hi + 1, tuple(shape), generator=gen).to(torch.uint8)
+
+
+def pack_fp4_codes(codes: torch.Tensor) -> torch.Tensor:
+    """[.., K] codes (K even) -> [.., K/2] bytes, element 2i in the low
+    nibble of byte i and element 2i + 1 in the high nibble: the storage of
+    the library's packed 4-bit operands.  A layout step, no arithmetic."""
+    if codes.shape[-1] % 2:
+        raise ValueError("K must be even")
+    c = codes.to(torch.uint8).reshape(*codes.shape[:-1], -1, 2)
+    return (c[..., 0] | (c[..., 1] << 4)).contiguous()

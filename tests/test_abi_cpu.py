@@ -336,9 +336,33 @@ def test_plan_8bit_rejections(lib):
     assert plan(256, 256, 256, "mxfp8", block_n=256) == tg.TG_ERR_INVALID_ARG
     assert plan(256, 256, 256, "mxfp8", cta_pair=2) == tg.TG_ERR_INVALID_ARG
     assert plan(256, 256, 256, "fp8", a_col_major=1) == tg.TG_ERR_INVALID_ARG
-    assert plan(256, 256, 256, 3) == tg.TG_ERR_INVALID_ARG
+    assert plan(256, 256, 256, 4) == tg.TG_ERR_INVALID_ARG
     assert plan(256, 256, 264, "fp8") == tg.TG_ERR_UNSUPPORTED  # rows of 264 bytes: not 16-byte multiples
     assert plan(256, 256, 256, "fp8") == tg.TG_OK
+    # packed 4-bit: K and pitches count elements, two a byte
+    assert plan(256, 256, 255, "mxfp4") == tg.TG_ERR_INVALID_ARG  # half a byte
+    assert plan(256, 256, 272, "mxfp4") == tg.TG_ERR_UNSUPPORTED  # rows of 136 bytes
+    assert plan(256, 256, 256, "mxfp4", block_n=224, stages=4) == tg.TG_ERR_INVALID_ARG
+    assert plan(256, 256, 256, "mxfp4", block_n=256) == tg.TG_ERR_INVALID_ARG
+    assert plan(256, 256, 256, "mxfp4") == tg.TG_OK
+
+
+def test_plan_4bit_block_scaled(lib):
+    """The packed 4-bit family: 256 elements of K per k-block (128 bytes a
+    row), one-CTA tiles of 128, 192 or 224 columns, 224 with a two-slot
+    ring; the scale scratch holds two blocks per 128 rows and k-block."""
+    p = tg.plan(4096, 4096, 4096, sm_count=152, operands="mxfp4")
+    assert p["block_k"] == 256 and p["k_blocks"] == 16 and p["cta_pair"] == 1
+    assert p["block_n"] in (128, 192, 224)
+    if p["block_n"] == 224:
+        assert p["stages"] == 2
+    for bn, st in ((128, 4), (192, 4), (224, 2), (128, 2)):
+        q = tg.plan(1000, 1000, 1056, sm_count=152, operands="mxfp4",
+                    options=tg.make_options(block_n=bn, stages=st))
+        assert (q["block_n"], q["stages"]) == (bn, st)
+        tiles_m, tiles_n, kb = -(-1000 // 128), -(-1000 // bn), -(-1056 // 256)
+        scales = -(-tiles_m * kb * 1024 // 256) * 256 + -(-tiles_n * kb * 1024 * -(-bn // 128) // 256) * 256
+        assert q["workspace_bytes"] == scales
 
 
 def test_c_caller_links_and_plans(lib):

@@ -3,7 +3,7 @@
 The product is the C-ABI CUDA library declared in ``include/tg_gemm.h``.
 This package is its thin Python binding: the C functions under the same
 names (``tg_gemm``, ``tg_gemm_ex``, ``tg_gemm_host``, ``tg_gemm_splitk_static``, ``tg_plan``,
-``tg_gemm_fp8``, ``tg_gemm_mxfp8``, ``tg_tune``,
+``tg_gemm_fp8``, ``tg_gemm_mxfp8``, ``tg_gemm_mxfp4``, ``tg_tune``,
 ``tg_device_error``, ``tg_status_string``, ``tg_shutdown``) taking raw
 pointers and sizes, plus conveniences that read pointers, shapes and
 strides off torch tensors.  PyTorch only provides device memory and
@@ -26,7 +26,7 @@ __all__ = [
     "TG_ERR_TIMEOUT", "TgError", "tg_options", "tg_plan_info", "load", "library_path",
     "tg_gemm", "tg_gemm_ex", "tg_gemm_host", "tg_gemm_fused", "tg_gemm_splitk_static", "tg_plan",
     "tg_gemm_fp8", "gemm_fp8", "TG_FP8_E4M3", "TG_FP8_E5M2",
-    "tg_gemm_mxfp8", "gemm_mxfp8", "tg_tune", "tune",
+    "tg_gemm_mxfp8", "gemm_mxfp8", "tg_gemm_mxfp4", "gemm_mxfp4", "tg_tune", "tune",
     "tg_epilogue", "gemm_fused", "ACTIVATIONS", "tg_device_error", "tg_status_string",
     "tg_shutdown", "make_options", "gemm", "gemm_host", "plan", "OPERAND_FAMILIES", "device_error",
 ]
@@ -81,6 +81,14 @@ def tg_gemm_mxfp8(A, B, D, M, N, K, lda, ldb, ldd, batch, strideA, strideB, stri
                   opt=None) -> int:
     return load().tg_gemm_mxfp8(A, B, D, M, N, K, lda, ldb, ldd, batch, strideA, strideB, strideD,
                                 a_format, b_format, SFA, ld_sfa, stride_sfa, SFB, ld_sfb, stride_sfb,
+                                ctypes.byref(ep) if ep is not None else None, stream,
+                                ctypes.byref(opt) if opt is not None else None)
+
+
+def tg_gemm_mxfp4(A, B, D, M, N, K, lda, ldb, ldd, batch, strideA, strideB, strideD, SFA, ld_sfa,
+                  stride_sfa, SFB, ld_sfb, stride_sfb, ep=None, stream=None, opt=None) -> int:
+    return load().tg_gemm_mxfp4(A, B, D, M, N, K, lda, ldb, ldd, batch, strideA, strideB, strideD,
+                                SFA, ld_sfa, stride_sfa, SFB, ld_sfb, stride_sfb,
                                 ctypes.byref(ep) if ep is not None else None, stream,
                                 ctypes.byref(opt) if opt is not None else None)
 
@@ -274,15 +282,24 @@ def _fp8_format(t, what):
     raise TypeError(f"{what} must be float8_e4m3fn or float8_e5m2")
 
 
-def _fp8_call(A, Bt, D, scale, bias, residual, beta, activation, out_dtype):
-    """Shapes, D and the epilogue of the 8-bit entry points."""
+def _fp8_call(A, Bt, D, scale, bias, residual, beta, activation, out_dtype, fp4=False):
+    """Shapes, D and the epilogue of the 8-bit entry points (fp4: packed
+    4-bit operands, uint8 tensors of two elements a byte; K, the leading
+    dimensions and the batch strides passed on count elements)."""
     import torch
 
-    fa, fb = _fp8_format(A, "A"), _fp8_format(Bt, "Bt")
+    if fp4:
+        if A.dtype != torch.uint8 or Bt.dtype != torch.uint8:
+            raise TypeError("packed 4-bit A and Bt must be uint8 tensors (two E2M1 codes a byte)")
+        fa = fb = 0
+    else:
+        fa, fb = _fp8_format(A, "A"), _fp8_format(Bt, "Bt")
     if not (A.is_cuda and Bt.is_cuda):
         raise ValueError("A and Bt must be CUDA tensors")
     pa, M, K, lda, ba, sA = _operand_geometry(A, -2, "A")
     pb, N, K2, ldb, bb, sB = _operand_geometry(Bt, -2, "Bt")
+    if fp4:
+        K, K2, lda, ldb, sA, sB = 2 * K, 2 * K2, 2 * lda, 2 * ldb, 2 * sA, 2 * sB
     if K2 != K:
         raise ValueError(f"inner dimensions differ: {K} vs {K2}")
     batch = max(ba, bb)
@@ -361,6 +378,35 @@ def gemm_mxfp8(A, Bt, SFA, SFB, D=None, *, scale: float = 1.0, bias=None, residu
     return D
 
 
+def gemm_mxfp4(A, Bt, SFA, SFB, D=None, *, scale: float = 1.0, bias=None, residual=None,
+               beta: float = 1.0, activation: str = "none", out_dtype=None,
+               options: tg_options | None = None, stream=None):
+    """Block-scaled 4-bit (MXFP4) GEMM: A [.., M, K/2] and Bt [.., N, K/2]
+    are uint8 tensors of packed E2M1 codes (element k of a row in byte k // 2,
+    the low nibble for even k), so K = 2 * A.shape[-1]; every 32 consecutive
+    elements along K of a row of A (of Bt) are scaled by 2^(e - 127), e the
+    uint8 E8M0 code in SFA [.., M, ceil(K/32)] (SFB [.., N, ceil(K/32)]).
+    Epilogue arguments as gemm_fp8."""
+    import torch
+
+    D, ep, args = _fp8_call(A, Bt, D, scale, bias, residual, beta, activation, out_dtype, fp4=True)
+    M, N, K, batch = args[3], args[4], args[5], args[9]
+    runs = -(-K // 32)
+    geo = []
+    for sf, rows, name in ((SFA, M, "SFA"), (SFB, N, "SFB")):
+        if sf.dtype != torch.uint8 or not sf.is_cuda:
+            raise TypeError(f"{name} must be a uint8 CUDA tensor")
+        p, r, c, ld, b, sb = _operand_geometry(sf, -2, name)
+        if (r, c) != (rows, runs) or b not in (1, batch):
+            raise ValueError(f"{name} must have shape [.., {rows}, {runs}]")
+        geo.append((p, ld, sb if b > 1 else 0))
+    (pfa, ldfa, sfa_s), (pfb, ldfb, sfb_s) = geo
+    st = tg_gemm_mxfp4(*args[:13], pfa, ldfa, sfa_s, pfb, ldfb, sfb_s, ep, _stream_ptr(stream), options)
+    if st != TG_OK:
+        raise TgError(st, "tg_gemm_mxfp4")
+    return D
+
+
 def tune(A, B, C=None, *, options: tg_options | None = None, reps: int = 3, stream=None):
     """Run-time plan search on these CUDA tensors (tg_tune): returns
     (options of the fastest plan, its median time in microseconds).  C is
@@ -423,15 +469,16 @@ def gemm_host(A, B, C=None, *, options: tg_options | None = None, stream=None):
     return C
 
 
-OPERAND_FAMILIES = {"bf16": 0, "fp8": 1, "mxfp8": 2}
+OPERAND_FAMILIES = {"bf16": 0, "fp8": 1, "mxfp8": 2, "mxfp4": 3}
 
 
 def plan(M, N, K, batch=1, *, lda=None, ldb=None, ldc=None, strideA=None, strideB=None,
          strideC=None, A=0x1000, B=0x100000000, C=0x200000000, sm_count=0, options=None,
          operands: str = "bf16") -> dict:
     """The plan tg_gemm_ex would use (host-only when sm_count > 0); with
-    operands="fp8" / "mxfp8" the plan of gemm_fp8 / gemm_mxfp8 (B stored
-    N x K, so ldb defaults to K).  The default addresses are placeholders
+    operands="fp8" / "mxfp8" / "mxfp4" the plan of gemm_fp8 / gemm_mxfp8 /
+    gemm_mxfp4 (B stored N x K, so ldb defaults to K; for mxfp4 K and the
+    pitches count elements).  The default addresses are placeholders
     with 16-byte alignment; pass real or deliberately misaligned addresses
     to see the pack decisions."""
     family = OPERAND_FAMILIES[operands]

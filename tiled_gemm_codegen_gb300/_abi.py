@@ -117,6 +117,9 @@ SIGNATURES = {
                                                          _vp, _i64, _i64, _vp, _i64, _i64,
                                                          ctypes.POINTER(tg_epilogue), _vp,
                                                          ctypes.POINTER(tg_options)], ctypes.c_int),
+    "tg_gemm_mxfp4": ([_vp, _vp, _vp] + [_i64] * 10 + [_vp, _i64, _i64, _vp, _i64, _i64,
+                                                         ctypes.POINTER(tg_epilogue), _vp,
+                                                         ctypes.POINTER(tg_options)], ctypes.c_int),
     "tg_device_error": ([_vp], ctypes.c_int),
     "tg_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "tg_shutdown": ([], None),

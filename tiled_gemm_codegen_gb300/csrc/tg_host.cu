@@ -119,36 +119,42 @@ __global__ void pack_bf16_kernel(PackJob ja, PackJob jb, int blocks_a)
 
 // Block-scaled operands: re-arrange one operand's E8M0 scales (rows x
 // ceil(K/32) bytes a problem, any pitch) into the blocks the GEMM kernel
-// copies with each k-block: 512 bytes per 128 rows and 128 elements of K,
-// the byte of row 32g + l and run j of the k-block at l * 16 + g * 4 + j
-// (tensor-memory lane l of cell column g after the warpx4 copy; TVM "Tensor
-// Layout", Case study: Blackwell tensor memory, the scale-factor atom of 32
-// rows on lanes, 4 scales per 32-bit column cell, replicated over the four
-// lane quadrants).  Rows and runs past the operand read as 127 (2^0): their
-// operand elements are the TMA unit's zero fill.  A tile of `tile_rows` rows
-// (128, or B's tile width) has `subs` = ceil(tile_rows / 128) consecutive
-// blocks per k-block; tile rows past tile_rows read as 127 too.
+// copies with each k-block: 512 bytes per 128 rows and four runs of 32
+// elements of K, the byte of row 32g + l and run j of the four at
+// l * 16 + g * 4 + j (tensor-memory lane l of cell column g after the warpx4
+// copy; TVM "Tensor Layout", Case study: Blackwell tensor memory, the
+// scale-factor atom of 32 rows on lanes, 4 scales per 32-bit column cell,
+// replicated over the four lane quadrants).  A k-block of 8-bit elements has
+// four runs (halves = 1), one of packed 4-bit elements eight (halves = 2:
+// runs 0-3, then 4-7).  Rows and runs past the operand read as 127 (2^0):
+// their operand elements are the TMA unit's zero fill.  A tile of
+// `tile_rows` rows (128, or B's tile width) has `subs` = ceil(tile_rows /
+// 128) blocks per half; tile rows past tile_rows read as 127 too.  Order:
+// for problem z, tile t and k-block kb, the blocks
+// ((z * tiles + t) * k_blocks + kb) * halves * subs + h * subs + sub.
 struct ScaleJob {
     const uint8_t *src;
     uint8_t *dst;
     int64_t rows, runs, ld, stride;  // stride: between problems (0: shared)
-    int64_t problems, tiles, k_blocks, tile_rows, subs;
+    int64_t problems, tiles, k_blocks, tile_rows, subs, halves;
 };
 
 // One CTA re-arranges the scales of one 128-row block (sub) of one tile for
-// SC_KB consecutive k-blocks: the 128 rows x 4 SC_KB runs are read with
-// coalesced byte loads into shared memory (rows SC_PITCH bytes apart, so the
-// 32 rows a warp reads next fall in 32 different banks), then each warp
-// writes whole 512-byte blocks, lane l's 16 bytes holding rows l, 32 + l,
-// 64 + l and 96 + l.
-constexpr int SC_KB = 16;
-constexpr int SC_RUNS = 4 * SC_KB;
+// SC_RUNS consecutive runs (16 8-bit or 8 4-bit k-blocks): the 128 rows x
+// SC_RUNS runs are read with coalesced byte loads into shared memory (rows
+// SC_PITCH bytes apart, so the 32 rows a warp reads next fall in 32
+// different banks), then each warp writes whole 512-byte blocks, lane l's 16
+// bytes holding rows l, 32 + l, 64 + l and 96 + l.
+constexpr int SC_RUNS = 64;
 constexpr int SC_PITCH = SC_RUNS + 4;
 constexpr int SC_THREADS = 256;
 
+__host__ __device__ inline int64_t scale_kb_per_cta(const ScaleJob &j) { return SC_RUNS / (4 * j.halves); }
+
 inline int64_t scale_blocks(const ScaleJob &j)
 {
-    return j.problems * j.tiles * j.subs * ((j.k_blocks + SC_KB - 1) / SC_KB);
+    const int64_t kpc = scale_kb_per_cta(j);
+    return j.problems * j.tiles * j.subs * ((j.k_blocks + kpc - 1) / kpc);
 }
 
 __global__ void __launch_bounds__(SC_THREADS) scale_tile_kernel(ScaleJob ja, ScaleJob jb, int64_t blocks_a)
@@ -158,7 +164,8 @@ __global__ void __launch_bounds__(SC_THREADS) scale_tile_kernel(ScaleJob ja, Sca
     const bool is_a = static_cast<int64_t>(blockIdx.x) < blocks_a;
     const ScaleJob j = is_a ? ja : jb;
     int64_t bid = is_a ? blockIdx.x : blockIdx.x - blocks_a;
-    const int64_t kchunks = (j.k_blocks + SC_KB - 1) / SC_KB;
+    const int64_t kpc = scale_kb_per_cta(j);
+    const int64_t kchunks = (j.k_blocks + kpc - 1) / kpc;
     const int64_t kc = bid % kchunks;
     bid /= kchunks;
     const int64_t sub = bid % j.subs;
@@ -187,14 +194,16 @@ __global__ void __launch_bounds__(SC_THREADS) scale_tile_kernel(ScaleJob ja, Sca
     }
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int kb = warp; kb < SC_KB; kb += SC_THREADS / 32) {
-        const int64_t kbg = kc * SC_KB + kb;
+    // item = (k-block, half) of this CTA's runs, four runs each
+    for (int item = warp; item < SC_RUNS / 4; item += SC_THREADS / 32) {
+        const int64_t kbg = kc * kpc + item / j.halves;
+        const int64_t h = item % j.halves;
         if (kbg >= j.k_blocks) break;
         uint32_t w[4];
 #pragma unroll
         for (int g = 0; g < 4; ++g)
-            w[g] = *reinterpret_cast<const uint32_t *>(slab + (32 * g + lane) * SC_PITCH + 4 * kb);
-        const int64_t blk = ((z * j.tiles + t) * j.k_blocks + kbg) * j.subs + sub;
+            w[g] = *reinterpret_cast<const uint32_t *>(slab + (32 * g + lane) * SC_PITCH + 4 * item);
+        const int64_t blk = ((z * j.tiles + t) * j.k_blocks + kbg) * j.halves * j.subs + h * j.subs + sub;
         *reinterpret_cast<uint4 *>(j.dst + blk * 512 + lane * 16) = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
@@ -224,8 +233,12 @@ struct Args {
     uint32_t mma_fmt = 0; // 8-bit operands: instruction-descriptor format fields
     bool a_cm = false;    // A stored K x M (column-major)
     bool b_cm = false;    // B stored N x K (column-major)
-    // block-scaled 8-bit operands: E8M0 scales per 32 elements of K
+    // block-scaled operands: E8M0 scales per 32 elements of K
     bool mx = false;
+    // packed 4-bit elements (two a byte): K, lda, ldb and the operand batch
+    // strides above are then in BYTES (element counts / 2)
+    bool fp4 = false;
+    int64_t k_elems() const { return fp4 ? 2 * K : K; }
     const uint8_t *sfa = nullptr, *sfb = nullptr;
     int64_t ld_sfa = 0, s_sfa = 0, ld_sfb = 0, s_sfb = 0;
     // stored (rows, columns) of A and B
@@ -328,6 +341,7 @@ PlanInput plan_input(const Args &a, int sms, const tg_options *opt)
     in.b_tma_ok = aligned16(a.B) && (a.ldb * eb) % 16 == 0 && (!batched_b || (a.sB * eb) % 16 == 0);
     in.f8 = a.ab_bytes == 1;
     in.mx = a.mx;
+    in.fp4 = a.fp4;
     in.c_tma_ok = aligned16(a.C) && (a.ldc * a.c_bytes) % 16 == 0 &&
                   (a.batch == 1 || (a.sC * a.c_bytes) % 16 == 0);
     in.sm_count = sms;
@@ -354,7 +368,7 @@ void fill_info(const Plan &p, tg_plan_info *out)
     out->stream_k = p.stream_k ? 2 : 1;
     out->sk_tiles = static_cast<int32_t>(p.sk_tiles);
     out->block_n = p.bn;
-    out->block_k = p.f8 ? 2 * BK : BK;
+    out->block_k = p.fp4 ? 4 * BK : p.f8 ? 2 * BK : BK;  // elements of K a k-block
     out->stages = p.stages;
     out->tiles_m = p.tiles_m;
     out->tiles_n = p.tiles_n;
@@ -553,11 +567,12 @@ uint64_t single_problem_stride(uint64_t rows, uint64_t stride1)
     return (s + 15) / 16 * 16;
 }
 
-cudaError_t launch_gemm(int bn, bool pair, bool f8, bool mx, const CUtensorMap &ta, const CUtensorMap &tb,
+cudaError_t launch_gemm(int bn, bool pair, bool f8, int mx, const CUtensorMap &ta, const CUtensorMap &tb,
                         const CUtensorMap &tc, const KernelParams &p, int stages, int grid,
                         cudaStream_t s)
 {
-    if (mx && bn == 224) return pair || !f8 ? cudaErrorInvalidValue : launch_gemm_mx224(ta, tb, tc, p, stages, grid, s);
+    if (mx != MX_NONE && bn == 224)
+        return pair || !f8 ? cudaErrorInvalidValue : launch_gemm_mx224(ta, tb, tc, p, stages, mx, grid, s);
     switch (bn) {
         case 64: return launch_gemm_bn64(ta, tb, tc, p, stages, pair, f8, mx, grid, s);
         case 128: return launch_gemm_bn128(ta, tb, tc, p, stages, pair, f8, mx, grid, s);
@@ -752,13 +767,14 @@ tg_status run_gemm(const Args &a, cudaStream_t stream, const tg_options *opt,
     uint8_t *scales_a = arena + plan.ws_pack_a + plan.ws_pack_b + plan.ws_partials;
     uint8_t *scales_b = scales_a + plan.ws_scales_a;
     if (plan.mx) {
-        const int64_t runs = ceil_div(a.K, 32);
+        const int64_t runs = ceil_div(a.k_elems(), 32);
         const int64_t za = in.a_bcast ? 1 : a.batch, zb = in.b_bcast ? 1 : a.batch;
         const int64_t subs_b = ceil_div(plan.bn, 128);
+        const int64_t halves = plan.fp4 ? 2 : 1;
         const ScaleJob ja{a.sfa, scales_a, a.M, runs, a.ld_sfa, a.batch > 1 ? a.s_sfa : 0, za, plan.tiles_m,
-                          plan.k_blocks, 128, 1};
+                          plan.k_blocks, 128, 1, halves};
         const ScaleJob jb{a.sfb, scales_b, a.N, runs, a.ld_sfb, a.batch > 1 ? a.s_sfb : 0, zb, plan.tiles_n,
-                          plan.k_blocks, plan.bn, subs_b};
+                          plan.k_blocks, plan.bn, subs_b, halves};
         const int64_t blocks_a = scale_blocks(ja), blocks_b = scale_blocks(jb);
         if (blocks_a + blocks_b > INT32_MAX) return TG_ERR_UNSUPPORTED;
         scale_tile_kernel<<<static_cast<unsigned>(blocks_a + blocks_b), SC_THREADS, 0, stream>>>(ja, jb, blocks_a);
@@ -848,7 +864,8 @@ tg_status run_gemm(const Args &a, cudaStream_t stream, const tg_options *opt,
     p.mma_fmt = a.mma_fmt;
     p.sfa = plan.mx ? scales_a : nullptr;
     p.sfb = plan.mx ? scales_b : nullptr;
-    e = launch_gemm(plan.bn, plan.pair, plan.f8, plan.mx, ta, tb, tc, p, plan.stages, grid, stream);
+    const int mx_kind = plan.fp4 ? MX_FP4 : plan.mx ? MX_FP8 : MX_NONE;
+    e = launch_gemm(plan.bn, plan.pair, plan.f8, mx_kind, ta, tb, tc, p, plan.stages, grid, stream);
     return cuda_status(e);
 }
 
@@ -889,7 +906,7 @@ cudaError_t shared_launch_gemm(int bn, const CUtensorMap &ta, const CUtensorMap 
                                const CUtensorMap &tc, const KernelParams &p, int stages, int grid,
                                cudaStream_t s)
 {
-    return launch_gemm(bn, false, false, false, ta, tb, tc, p, stages, grid, s);
+    return launch_gemm(bn, false, false, MX_NONE, ta, tb, tc, p, stages, grid, s);
 }
 
 cudaError_t shared_zero_fill(float *C, int64_t M, int64_t N, int64_t ldc, int64_t sC, int64_t batch,
@@ -1091,8 +1108,10 @@ namespace {
 tg_status run_fp8(Args a, int32_t a_format, int32_t b_format, const tg_epilogue *ep, cudaStream_t stream,
                   const tg_options *opt)
 {
-    if (a_format != TG_FP8_E4M3 && a_format != TG_FP8_E5M2) return TG_ERR_INVALID_ARG;
-    if (b_format != TG_FP8_E4M3 && b_format != TG_FP8_E5M2) return TG_ERR_INVALID_ARG;
+    if (!a.fp4) {
+        if (a_format != TG_FP8_E4M3 && a_format != TG_FP8_E5M2) return TG_ERR_INVALID_ARG;
+        if (b_format != TG_FP8_E4M3 && b_format != TG_FP8_E5M2) return TG_ERR_INVALID_ARG;
+    }
     if (opt && (opt->a_col_major || opt->b_col_major || opt->force_pack)) return TG_ERR_INVALID_ARG;
     if (ep && ep->out_type != TG_F32 && ep->out_type != TG_BF16) return TG_ERR_INVALID_ARG;
     // A row-major M x K, B stored N x K (column-major K x N): both K-major
@@ -1100,15 +1119,16 @@ tg_status run_fp8(Args a, int32_t a_format, int32_t b_format, const tg_epilogue 
     a.ab_bytes = 1;
     a.c_bytes = ep && ep->out_type == TG_BF16 ? 2 : 4;
     // kind::f8f6f4 / kind::mxf8f6f4 operand formats: E4M3 = 0, E5M2 = 1
-    // (bits 7-9 A, 10-12 B)
-    a.mma_fmt = (static_cast<uint32_t>(a_format) << 7) | (static_cast<uint32_t>(b_format) << 10);
+    // (bits 7-9 A, 10-12 B); kind::mxf4: E2M1 = 1 in both fields
+    a.mma_fmt = a.fp4 ? ((1u << 7) | (1u << 10))
+                      : (static_cast<uint32_t>(a_format) << 7) | (static_cast<uint32_t>(b_format) << 10);
     tg_status st = validate(a);
     if (st != TG_OK) return st;
     if (a.M == 0 || a.N == 0) return TG_OK;
     if (ep && (st = check_epilogue(a, ep)) != TG_OK) return st;
     if (a.mx && a.K > 0) {
         // the scale matrices lie apart from D
-        const int64_t runs = ceil_div(a.K, 32);
+        const int64_t runs = ceil_div(a.k_elems(), 32);
         if (!span_ok(a.M, runs, a.ld_sfa, a.batch, a.s_sfa) || !span_ok(a.N, runs, a.ld_sfb, a.batch, a.s_sfb))
             return TG_ERR_INVALID_ARG;
         const uintptr_t d0 = reinterpret_cast<uintptr_t>(a.C);
@@ -1146,6 +1166,42 @@ TG_API tg_status tg_gemm_fp8(const void *A, const void *B, void *D, int64_t M, i
     return run_fp8(a, a_format, b_format, ep, reinterpret_cast<cudaStream_t>(stream), opt);
 }
 
+namespace tg {
+namespace {
+
+// The scale arguments shared by both block-scaled entry points (K counts
+// elements); returns TG_OK or the status to report.
+tg_status check_scale_args(int64_t K, int64_t batch, int64_t strideA, int64_t strideB, const uint8_t *SFA,
+                           int64_t ld_sfa, int64_t stride_sfa, const uint8_t *SFB, int64_t ld_sfb,
+                           int64_t stride_sfb, const tg_options *opt, bool fp4)
+{
+    if (opt && ((opt->block_n != 0 && opt->block_n != 128 && opt->block_n != 192 && opt->block_n != 224) ||
+                opt->cta_pair == 2 || (opt->stages != 0 && opt->stages != 2 && opt->stages != 4) ||
+                (fp4 && opt->block_n == 224 && opt->stages == 4)))
+        return TG_ERR_INVALID_ARG;
+    if (stride_sfa < 0 || stride_sfb < 0 || K < 0) return TG_ERR_INVALID_ARG;
+    if (K > 0) {
+        const int64_t runs = (K + 31) / 32;
+        if (!SFA || !SFB || ld_sfa < runs || ld_sfb < runs) return TG_ERR_INVALID_ARG;
+        const int64_t LIMIT = int64_t(1) << 40;
+        if (ld_sfa > LIMIT || ld_sfb > LIMIT || stride_sfa > LIMIT || stride_sfb > LIMIT) return TG_ERR_INVALID_ARG;
+        // shared operands have shared scales (the re-arranged scales follow
+        // the operand's problem index)
+        if (batch > 1 && ((strideA == 0 && stride_sfa != 0) || (strideB == 0 && stride_sfb != 0)))
+            return TG_ERR_INVALID_ARG;
+    }
+    return TG_OK;
+}
+
+// Packed 4-bit operands: element counts that address whole bytes.
+bool fp4_counts_ok(int64_t K, int64_t lda, int64_t ldb, int64_t strideA, int64_t strideB)
+{
+    return K % 2 == 0 && lda % 2 == 0 && ldb % 2 == 0 && strideA % 2 == 0 && strideB % 2 == 0;
+}
+
+}  // namespace
+}  // namespace tg
+
 TG_API tg_status tg_gemm_mxfp8(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K,
                                int64_t lda, int64_t ldb, int64_t ldd, int64_t batch, int64_t strideA,
                                int64_t strideB, int64_t strideD, int32_t a_format, int32_t b_format,
@@ -1162,22 +1218,36 @@ TG_API tg_status tg_gemm_mxfp8(const void *A, const void *B, void *D, int64_t M,
     a.s_sfa = stride_sfa;
     a.ld_sfb = ld_sfb;
     a.s_sfb = stride_sfb;
-    if (opt && ((opt->block_n != 0 && opt->block_n != 128 && opt->block_n != 192 && opt->block_n != 224) ||
-                opt->cta_pair == 2 ||
-                (opt->stages != 0 && opt->stages != 2 && opt->stages != 4)))
-        return TG_ERR_INVALID_ARG;
-    if (stride_sfa < 0 || stride_sfb < 0 || K < 0) return TG_ERR_INVALID_ARG;
-    if (K > 0) {
-        const int64_t runs = (K + 31) / 32;
-        if (!SFA || !SFB || ld_sfa < runs || ld_sfb < runs) return TG_ERR_INVALID_ARG;
-        const int64_t LIMIT = int64_t(1) << 40;
-        if (ld_sfa > LIMIT || ld_sfb > LIMIT || stride_sfa > LIMIT || stride_sfb > LIMIT) return TG_ERR_INVALID_ARG;
-        // shared operands have shared scales (the re-arranged scales follow
-        // the operand's problem index)
-        if (batch > 1 && ((strideA == 0 && stride_sfa != 0) || (strideB == 0 && stride_sfb != 0)))
-            return TG_ERR_INVALID_ARG;
-    }
+    const tg_status st = check_scale_args(K, batch, strideA, strideB, SFA, ld_sfa, stride_sfa, SFB, ld_sfb,
+                                          stride_sfb, opt, false);
+    if (st != TG_OK) return st;
     return run_fp8(a, a_format, b_format, ep, reinterpret_cast<cudaStream_t>(stream), opt);
+}
+
+
+TG_API tg_status tg_gemm_mxfp4(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K,
+                               int64_t lda, int64_t ldb, int64_t ldd, int64_t batch, int64_t strideA,
+                               int64_t strideB, int64_t strideD, const uint8_t *SFA, int64_t ld_sfa,
+                               int64_t stride_sfa, const uint8_t *SFB, int64_t ld_sfb, int64_t stride_sfb,
+                               const tg_epilogue *ep, tg_stream_t stream, const tg_options *opt)
+{
+    using namespace tg;
+    if (K < 0 || lda < 0 || ldb < 0 || strideA < 0 || strideB < 0) return TG_ERR_INVALID_ARG;
+    if (!fp4_counts_ok(K, lda, ldb, strideA, strideB)) return TG_ERR_INVALID_ARG;
+    tg_status st = check_scale_args(K, batch, strideA, strideB, SFA, ld_sfa, stride_sfa, SFB, ld_sfb, stride_sfb,
+                                    opt, true);
+    if (st != TG_OK) return st;
+    // from here on the operands are byte matrices: K / 2 bytes a row
+    Args a{A, B, D, M, N, K / 2, lda / 2, ldb / 2, ldd, batch, strideA / 2, strideB / 2, strideD};
+    a.mx = true;
+    a.fp4 = true;
+    a.sfa = SFA;
+    a.sfb = SFB;
+    a.ld_sfa = ld_sfa;
+    a.s_sfa = stride_sfa;
+    a.ld_sfb = ld_sfb;
+    a.s_sfb = stride_sfb;
+    return run_fp8(a, 0, 0, ep, reinterpret_cast<cudaStream_t>(stream), opt);
 }
 
 TG_API tg_status tg_plan(const void *A, const void *B, const float *C, int64_t M, int64_t N,
@@ -1187,22 +1257,34 @@ TG_API tg_status tg_plan(const void *A, const void *B, const float *C, int64_t M
 {
     if (!out || sm_count < 0) return TG_ERR_INVALID_ARG;
     const int32_t family = opt ? opt->operands : 0;
-    if (family < 0 || family > 2) return TG_ERR_INVALID_ARG;
+    if (family < 0 || family > 3) return TG_ERR_INVALID_ARG;
     Args a = with_layout(Args{A, B, const_cast<float *>(C), M, N, K, lda, ldb, ldc, batch, strideA, strideB, strideC},
                          opt);
     if (family != 0) {
-        // the 8-bit entry points' layout: A row-major, B stored N x K
+        // the 8-/4-bit entry points' layout: A row-major, B stored N x K
         if (opt->a_col_major || opt->b_col_major || opt->force_pack) return TG_ERR_INVALID_ARG;
         a.b_cm = true;
         a.ab_bytes = 1;
-        a.mx = family == 2;
+        a.mx = family >= 2;
+        if (family == 3) {
+            // packed 4-bit elements: planned on the operands' bytes
+            if (K < 0 || lda < 0 || ldb < 0 || strideA < 0 || strideB < 0) return TG_ERR_INVALID_ARG;
+            if (!fp4_counts_ok(K, lda, ldb, strideA, strideB)) return TG_ERR_INVALID_ARG;
+            a.fp4 = true;
+            a.K = K / 2;
+            a.lda = lda / 2;
+            a.ldb = ldb / 2;
+            a.sA = strideA / 2;
+            a.sB = strideB / 2;
+        }
     }
     tg_status st = validate(a);
     if (st != TG_OK) return st;
     if (family != 0 && K > 0) {
-        const bool batched_a = batch > 1 && strideA != 0, batched_b = batch > 1 && strideB != 0;
-        if ((reinterpret_cast<uintptr_t>(A) & 15u) || (reinterpret_cast<uintptr_t>(B) & 15u) || lda % 16 ||
-            ldb % 16 || (batched_a && strideA % 16) || (batched_b && strideB % 16))
+        // 16-byte rows (counted in bytes)
+        const bool batched_a = batch > 1 && a.sA != 0, batched_b = batch > 1 && a.sB != 0;
+        if ((reinterpret_cast<uintptr_t>(A) & 15u) || (reinterpret_cast<uintptr_t>(B) & 15u) || a.lda % 16 ||
+            a.ldb % 16 || (batched_a && a.sA % 16) || (batched_b && a.sB % 16))
             return TG_ERR_UNSUPPORTED;
     }
     int sms = sm_count;

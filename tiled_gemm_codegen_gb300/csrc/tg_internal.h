@@ -64,10 +64,11 @@ struct KernelParams {
     int32_t maxparts;
     int64_t sk_iters;
     unsigned long long *trace;  // grid x 8 timestamps, or null
-    uint32_t mma_fmt;           // 8-bit operands: A format << 7 | B format << 10
+    uint32_t mma_fmt;           // 8-/4-bit operands: A format << 7 | B format << 10
     // Block-scaled operands: E8M0 scales pre-arranged in 512-byte blocks,
-    // block ((z * tiles + t) * k_blocks + kb) for problem z, 128-row (A) or
-    // 128-column (B) tile t and k-block kb.
+    // for problem z, 128-row (A) or BN-column (B) tile t and k-block kb the
+    // blocks ((z * tiles + t) * k_blocks + kb) * halves * subs + h * subs + sub
+    // (h: which four runs of the k-block; sub: which 128 rows or columns).
     const uint8_t *sfa;
     const uint8_t *sfb;
 };
@@ -99,25 +100,34 @@ struct Geometry {
                    ? stages * STAGE + EPI_BYTES + BAR_BYTES + ALIGN_SLACK
                    : ONE_CTA_PER_SM;
     }
-    static constexpr int smem_bytes_mx(int stages) { return smem_bytes(stages) + stages * SF_STAGE; }
+    // halves: scale blocks per 128 rows and k-block (1: 8-bit elements, four
+    // runs of 32 a k-block; 2: packed 4-bit elements, eight runs)
+    static constexpr int smem_bytes_mx(int stages, int halves = 1)
+    {
+        return smem_bytes(stages) + stages * SF_STAGE * halves;
+    }
 };
+
+// Block-scaled element families (the `mx` argument of the launches).
+enum : int { MX_NONE = 0, MX_FP8 = 1, MX_FP4 = 2 };
 
 // Launch of the persistent GEMM kernel for one tile width (defined in the
 // per-width translation units).  pair: two-SM tiles (grid counts CTAs, a
-// multiple of 2); f8: 8-bit floating-point operands; mx: block-scaled 8-bit
-// operands (width 128, one CTA per tile).  Returns the launch's cudaError_t.
+// multiple of 2); f8: 8-bit floating-point operands (or, with mx == MX_FP4,
+// packed 4-bit ones, which the kernel moves as bytes); mx: block-scaled
+// operands (one CTA per tile).  Returns the launch's cudaError_t.
 #define TG_DECLARE_LAUNCH(BN_)                                                                   \
     cudaError_t launch_gemm_bn##BN_(const CUtensorMap &ta, const CUtensorMap &tb,                \
                                     const CUtensorMap &tc, const KernelParams &p, int stages,   \
-                                    bool pair, bool f8, bool mx, int grid, cudaStream_t s);     \
+                                    bool pair, bool f8, int mx, int grid, cudaStream_t s);      \
     int max_pairs_bn##BN_(int stages, bool f8);
 TG_DECLARE_LAUNCH(64)
 TG_DECLARE_LAUNCH(128)
 TG_DECLARE_LAUNCH(192)
 TG_DECLARE_LAUNCH(256)
 #undef TG_DECLARE_LAUNCH
-// Block-scaled 8-bit operands on 224-wide one-CTA tiles.
+// Block-scaled operands (mx: MX_FP8 or MX_FP4) on 224-wide one-CTA tiles.
 cudaError_t launch_gemm_mx224(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
-                              const KernelParams &p, int stages, int grid, cudaStream_t s);
+                              const KernelParams &p, int stages, int mx, int grid, cudaStream_t s);
 
 }  // namespace tg

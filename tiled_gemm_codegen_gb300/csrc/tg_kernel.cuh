@@ -356,7 +356,14 @@ __device__ __forceinline__ void apply_epilogue(const KernelParams &p, uint32_t (
 // columns) and every slot's scales (4 columns per block), which is why a
 // block-scaled tile is at most 224 wide: 2 x 224 + 4 x 12 = 496 of the 512
 // columns (TVM "Tensor Layout", Case study: Blackwell tensor memory).
-template <int BN, int STAGES, bool PAIR, bool F8 = false, bool MX = false>
+// FP4 (with MX and F8): packed E2M1 operands, two elements a byte
+// (tcgen05 kind::mxf4).  A k-block is still 128 bytes a row, now 256
+// elements and eight runs of 32, so each slot carries two scale blocks per
+// 128 rows or columns (runs 0-3 and 4-7) and every slot takes twice the
+// scale columns; the j-th K = 64 MMA reads block j / 2, bytes 2 (j % 2) and
+// 2 (j % 2) + 1 of each cell.  Two accumulators and the scales then fit
+// 2 x 224 + 2 x 24 columns with a two-slot ring at width 224.
+template <int BN, int STAGES, bool PAIR, bool F8 = false, bool MX = false, bool FP4 = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const KernelParams p)
@@ -368,7 +375,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     static_assert(G::smem_bytes(STAGES) <= SMEM_LIMIT, "shared memory budget");
     static_assert(!MX || (F8 && !PAIR && (BN == 128 || BN == 192 || BN == 224)),
                   "block scaling: one-CTA 128-, 192- or 224-wide tiles");
-    static_assert(!MX || G::smem_bytes_mx(STAGES) <= SMEM_LIMIT, "shared memory budget (scales)");
+    static_assert(!FP4 || MX, "4-bit operands are block-scaled");
+    constexpr int SF_HALVES = FP4 ? 2 : 1;  // scale blocks per 128 rows and k-block
+    static_assert(!MX || G::smem_bytes_mx(STAGES, SF_HALVES) <= SMEM_LIMIT, "shared memory budget (scales)");
     constexpr int TILE_M = PAIR ? 2 * BM : BM;
     constexpr int B_BOXES = G::B_COLS / 64;
     constexpr uint32_t B_BOX_BYTES = BK * 64 * 2;  // one 64-column box of B: 8 KB
@@ -379,10 +388,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // travel with its operands; tensor memory holds both accumulators
     // (columns 0 .. 2 BN - 1) and the slots' scales (SF_COLS columns a slot
     // from 2 BN: A's 4, then B's 4 per block).
-    constexpr uint32_t TX_BYTES = G::STAGE + (MX ? G::SF_STAGE : 0);
+    constexpr uint32_t SF_STAGE = G::SF_STAGE * SF_HALVES;  // scale bytes a slot
+    constexpr uint32_t TX_BYTES = G::STAGE + (MX ? SF_STAGE : 0);
     constexpr uint32_t TMEM_ALLOC = MX ? 512u : static_cast<uint32_t>(G::TMEM_COLS);
     constexpr uint32_t SF_COL0 = 2 * BN;
-    constexpr uint32_t SF_COLS = 4 * (1 + G::SF_B_BLOCKS);
+    constexpr uint32_t SF_COLS = 4 * (1 + G::SF_B_BLOCKS) * SF_HALVES;
+    constexpr uint32_t SF_B_COL = 4 * SF_HALVES;  // B's scale columns after A's
     static_assert(!MX || SF_COL0 + SF_COLS * STAGES <= TMEM_ALLOC, "scale columns");
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -394,7 +405,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t sE = sB + STAGES * G::B_STAGE;   // 4 warps x EPI_BUFS x 4 KB
     uint8_t *bar_area = smem + STAGES * G::STAGE + G::EPI_BYTES;
     const uint32_t bar0 = ptx::smem_addr(bar_area);
-    const uint32_t sSF = bar0 + G::BAR_BYTES;  // MX: STAGES x 1 KB of scales
+    const uint32_t sSF = bar0 + G::BAR_BYTES;  // MX: STAGES x SF_STAGE bytes of scales
     // barrier k lives at bar0 + 8k:
     //   [0, S) full   [S, 2S) empty   2S+{0,1} tfull   2S+{2,3} tempty
     //   2S+4 mma-done   2S+5 stall (never completed)
@@ -530,9 +541,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         if constexpr (MX) {
                             const int64_t fa = (static_cast<int64_t>(zA) * p.tiles_m + w.tm) * p.k_blocks + kb;
                             const int64_t fbk = (static_cast<int64_t>(zB) * p.tiles_n + w.tn) * p.k_blocks + kb;
-                            constexpr uint32_t SFB_BYTES = 512 * G::SF_B_BLOCKS;
-                            ptx::bulk_load(sSF + s * G::SF_STAGE, p.sfa + fa * 512, 512, fb);
-                            ptx::bulk_load(sSF + s * G::SF_STAGE + 512, p.sfb + fbk * SFB_BYTES, SFB_BYTES, fb);
+                            constexpr uint32_t SFA_BYTES = 512 * SF_HALVES;
+                            constexpr uint32_t SFB_BYTES = 512 * G::SF_B_BLOCKS * SF_HALVES;
+                            ptx::bulk_load(sSF + s * SF_STAGE, p.sfa + fa * SFA_BYTES, SFA_BYTES, fb);
+                            ptx::bulk_load(sSF + s * SF_STAGE + SFA_BYTES, p.sfb + fbk * SFB_BYTES, SFB_BYTES, fb);
                         }
                     }
                     __syncwarp();
@@ -603,13 +615,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const uint32_t sf_tmem = tmem_base + SF_COL0 + SF_COLS * s;
                         if constexpr (MX) {
                             // no-swizzle descriptors of the 512-byte scale
-                            // blocks: 8-row core matrices 128 B apart; block j
-                            // of B (columns 128j ..) to columns 4 + 4j
+                            // blocks: 8-row core matrices 128 B apart.  A's
+                            // blocks (one per half) to columns 4h, then B's
+                            // blocks [half][128 columns] to the columns after
+                            // them: the slot's blocks in their order in
+                            // shared memory, 4 columns each.
                             const uint64_t sf_desc = (static_cast<uint64_t>(128 >> 4) << 16) |
                                                      (static_cast<uint64_t>(128 >> 4) << 32) | (1ull << 46);
-                            const uint32_t sf_smem = sSF + s * G::SF_STAGE;
+                            const uint32_t sf_smem = sSF + s * SF_STAGE;
 #pragma unroll
-                            for (int j = 0; j <= G::SF_B_BLOCKS; ++j)
+                            for (int j = 0; j < (1 + G::SF_B_BLOCKS) * SF_HALVES; ++j)
                                 ptx::tmem_cp_32x128b_x4(sf_tmem + 4 * j, sf_desc | (((sf_smem + 512 * j) >> 4) & 0x3FFFu));
                         }
 #pragma unroll
@@ -617,10 +632,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             const uint64_t ad = a_desc0 | (((a_addr + kk * a_step) >> 4) & 0x3FFFu);
                             const uint64_t bd = b_desc0 | (((b_addr + kk * b_step) >> 4) & 0x3FFFu);
                             const uint32_t acc = (kb > w.kb0 || kk > 0) ? 1u : 0u;
-                            if constexpr (MX)
+                            if constexpr (FP4) {
+                                const uint32_t h = static_cast<uint32_t>(kk) >> 1;
+                                const uint32_t id = 2u * (static_cast<uint32_t>(kk) & 1u);
+                                ptx::mma_mxf4(d_tmem, ad, bd, idesc_mx | (id << 29) | (id << 4), sf_tmem + 4 * h,
+                                              sf_tmem + SF_B_COL + 4 * G::SF_B_BLOCKS * h, acc);
+                            } else if constexpr (MX)
                                 ptx::mma_mx(d_tmem, ad, bd,
                                             idesc_mx | (static_cast<uint32_t>(kk) << 29) | (static_cast<uint32_t>(kk) << 4),
-                                            sf_tmem, sf_tmem + 4, acc);
+                                            sf_tmem, sf_tmem + SF_B_COL, acc);
                             else if constexpr (PAIR && F8)
                                 ptx::mma_f8_pair(d_tmem, ad, bd, idesc, acc);
                             else if constexpr (PAIR)
@@ -946,13 +966,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (threadIdx.x == 0) stamp(7);
 }
 
-template <int BN, int STAGES, bool PAIR, bool F8 = false, bool MX = false>
+template <int BN, int STAGES, bool PAIR, bool F8 = false, bool MX = false, bool FP4 = false>
 cudaError_t launch_fixed(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
                          const KernelParams &p, int grid, cudaStream_t s)
 {
-    constexpr int smem = MX ? Geometry<BN, PAIR>::smem_bytes_mx(STAGES) : Geometry<BN, PAIR>::smem_bytes(STAGES);
+    constexpr int smem = MX ? Geometry<BN, PAIR>::smem_bytes_mx(STAGES, FP4 ? 2 : 1)
+                            : Geometry<BN, PAIR>::smem_bytes(STAGES);
     static_assert(smem <= SMEM_LIMIT, "shared memory budget");
-    auto kern = gemm_kernel<BN, STAGES, PAIR, F8, MX>;
+    auto kern = gemm_kernel<BN, STAGES, PAIR, F8, MX, FP4>;
     // the shared-memory opt-in is per device; set it once per device
     static std::atomic<unsigned long long> configured{0};
     int dev = 0;

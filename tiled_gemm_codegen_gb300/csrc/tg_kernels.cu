@@ -2,8 +2,9 @@
 // width (selected at build time with -DTG_BN=...), so the widths compile in
 // parallel.  Each width instantiates a few ring depths, with one CTA per tile
 // and (widths 128 and 256) two-SM tiles, for bf16 operands and (a subset)
-// 8-bit floating-point ones (block-scaled 8-bit ones at widths 128, 192 and
-// 224, rings 2 and 4); stage_supported() and
+// 8-bit floating-point ones (block-scaled 8-bit and packed 4-bit ones at
+// widths 128, 192 and 224, rings 2 and 4 - 224-wide 4-bit tiles ring 2
+// only); stage_supported() and
 // mx_stage_supported() in tg_plan.h list them and the host planner only
 // picks listed configurations.
 #include "tg_kernel.cuh"
@@ -45,13 +46,21 @@ namespace tg {
 
 cudaError_t TG_CAT(launch_gemm_bn, TG_BN)(const CUtensorMap &ta, const CUtensorMap &tb,
                                           const CUtensorMap &tc, const KernelParams &p,
-                                          int stages, bool pair, bool f8, bool mx, int grid, cudaStream_t s)
+                                          int stages, bool pair, bool f8, int mx, int grid, cudaStream_t s)
 {
-    if (mx) {
-        // block-scaled 8-bit operands, one CTA per tile: widths 128 and 192
-        // in their units, width 224 (launch_gemm_mx224) in the width-128 unit
+    if (mx != MX_NONE) {
+        // block-scaled operands, one CTA per tile: widths 128 and 192 in
+        // their units, width 224 (launch_gemm_mx224) in the width-128 unit
         if (pair || !f8) return cudaErrorInvalidValue;
 #if TG_BN == 128 || TG_BN == 192
+        if (mx == MX_FP4) {
+            switch (stages) {
+                case 2: return launch_fixed<TG_BN, 2, false, true, true, true>(ta, tb, tc, p, grid, s);
+                case 4: return launch_fixed<TG_BN, 4, false, true, true, true>(ta, tb, tc, p, grid, s);
+                default: return cudaErrorInvalidValue;
+            }
+        }
+        if (mx != MX_FP8) return cudaErrorInvalidValue;
         switch (stages) {
             case 2: return launch_fixed<TG_BN, 2, false, true, true>(ta, tb, tc, p, grid, s);
             case 4: return launch_fixed<TG_BN, 4, false, true, true>(ta, tb, tc, p, grid, s);
@@ -69,8 +78,12 @@ cudaError_t TG_CAT(launch_gemm_bn, TG_BN)(const CUtensorMap &ta, const CUtensorM
 
 #if TG_BN == 128
 cudaError_t launch_gemm_mx224(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
-                              const KernelParams &p, int stages, int grid, cudaStream_t s)
+                              const KernelParams &p, int stages, int mx, int grid, cudaStream_t s)
 {
+    if (mx == MX_FP4)  // two slots: the scales of a third would not fit tensor memory
+        return stages == 2 ? launch_fixed<224, 2, false, true, true, true>(ta, tb, tc, p, grid, s)
+                           : cudaErrorInvalidValue;
+    if (mx != MX_FP8) return cudaErrorInvalidValue;
     switch (stages) {
         case 2: return launch_fixed<224, 2, false, true, true>(ta, tb, tc, p, grid, s);
         case 4: return launch_fixed<224, 4, false, true, true>(ta, tb, tc, p, grid, s);

@@ -47,11 +47,13 @@ constexpr bool stage_supported(int bn, int s, bool pair = false, bool f8 = false
     }
 }
 
-// Block-scaled 8-bit operands: one-CTA tiles of widths 128, 192 and 224,
-// rings 2 and 4.
-constexpr bool mx_stage_supported(int bn, int s, bool pair = false)
+// Block-scaled operands: one-CTA tiles of widths 128, 192 and 224, rings 2
+// and 4; with packed 4-bit elements (fp4) the 224-wide tiles ring 2 only
+// (every slot's scales take twice the tensor-memory columns).
+constexpr bool mx_stage_supported(int bn, int s, bool pair = false, bool fp4 = false)
 {
-    return !pair && (bn == 128 || bn == 192 || bn == 224) && (s == 2 || s == 4);
+    if (pair || !(bn == 128 || bn == 192 || bn == 224) || !(s == 2 || s == 4)) return false;
+    return !(fp4 && bn == 224 && s != 2);
 }
 
 template <bool PAIR>
@@ -110,12 +112,14 @@ struct PlanInput {
     bool a_cm = false, b_cm = false;  // column-major (transposed) operand storage
     bool f8 = false;                  // 8-bit floating-point A and B (K-major)
     bool mx = false;                  // f8 with per-32-element E8M0 block scales
+    bool fp4 = false;                 // mx with packed 4-bit elements (K, lda, ldb in bytes)
 };
 
 struct Plan {
     bool pair = false;  // two-SM tiles (256 rows, cluster of 2)
     bool f8 = false;    // 8-bit operands: 128 elements of K per k-block
     bool mx = false;    // block-scaled 8-bit operands
+    bool fp4 = false;   // block-scaled packed 4-bit operands (a k-block: 256 elements)
     int bn = 0, stages = 0;
     int tiles_m = 0, tiles_n = 0, k_blocks = 0, splits = 1;
     int64_t units = 0;
@@ -130,7 +134,7 @@ struct Plan {
     int64_t sk_first_tile = 0, sk_tiles = 0, sk_iters = 0;
     int64_t ws_pack_a = 0, ws_pack_b = 0, ws_partials = 0, ws_counters = 0;
     // block-scaled operands: the scales re-arranged into 512-byte blocks
-    // (one per 128 rows or columns and k-block), A's then B's
+    // (one per 128 rows or columns, k-block and four runs), A's then B's
     int64_t ws_scales_a = 0, ws_scales_b = 0;
     int64_t workspace() const
     {
@@ -282,7 +286,9 @@ inline bool make_plan(const PlanInput &in, Plan &out)
     Plan p;
     p.f8 = in.f8;
     p.mx = in.mx;
+    p.fp4 = in.fp4;
     if (in.mx && !in.f8) return false;
+    if (in.fp4 && !in.mx) return false;
     const int sms = in.sm_count > 0 ? in.sm_count : 1;
     const int64_t kb = ceil_div(in.K, in.f8 ? 2 * BK : BK);  // a k-block is 128 bytes of K
     if (in.f8 && (in.a_cm || !in.b_cm || in.force_pack || !in.a_tma_ok || !in.b_tma_ok)) return false;
@@ -292,7 +298,7 @@ inline bool make_plan(const PlanInput &in, Plan &out)
     if (in.block_n != 0 && in.block_n != 64 && in.block_n != 128 && in.block_n != 192 &&
         in.block_n != 256 && !(in.mx && in.block_n == 224))
         return false;
-    if (in.mx && in.block_n != 0 && !mx_stage_supported(in.block_n, 2)) return false;
+    if (in.mx && in.block_n != 0 && !mx_stage_supported(in.block_n, 2, false, in.fp4)) return false;
     if (in.split_k < 0 || in.stages < 0 || in.max_ctas < 0) return false;
     if (in.epilogue < 0 || in.epilogue > 2) return false;
     if (in.cta_pair < 0 || in.cta_pair > 2) return false;
@@ -320,7 +326,7 @@ inline bool make_plan(const PlanInput &in, Plan &out)
         if (in.cta_pair == 2 && !cd.pair) continue;
         if (in.cta_pair == 0 && cd.pair && !PAIR_BY_DEFAULT) continue;
         if (in.f8 && !in.mx && !stage_supported(cd.bn, 2, cd.pair, true)) continue;  // no 8-bit instance
-        if (in.mx && !mx_stage_supported(cd.bn, 2, cd.pair)) continue;
+        if (in.mx && !mx_stage_supported(cd.bn, 2, cd.pair, in.fp4)) continue;
         if (!in.mx && cd.bn == 224) continue;
         // the planner's own choice of 8-bit two-SM tiles needs a full wave
         // of pairs (measured, see tile_efficiency)
@@ -366,8 +372,8 @@ inline bool make_plan(const PlanInput &in, Plan &out)
 
     // Ring depth: the deepest instantiated one unless overridden.
     if (in.mx) {
-        if (in.stages != 0 && !mx_stage_supported(p.bn, in.stages, p.pair)) return false;
-        p.stages = in.stages != 0 ? in.stages : 4;
+        if (in.stages != 0 && !mx_stage_supported(p.bn, in.stages, p.pair, in.fp4)) return false;
+        p.stages = in.stages != 0 ? in.stages : (mx_stage_supported(p.bn, 4, p.pair, in.fp4) ? 4 : 2);
     } else if (in.stages != 0) {
         if (!stage_supported(p.bn, in.stages, p.pair, in.f8)) return false;
         p.stages = in.stages;
@@ -406,9 +412,10 @@ inline bool make_plan(const PlanInput &in, Plan &out)
     p.smem = smem_bytes_for(p.bn, p.stages, p.pair);
     p.tmem = tmem_cols_for(p.bn);
     if (p.mx) {
-        p.smem = p.bn == 224   ? Geometry<224>::smem_bytes_mx(p.stages)
-                 : p.bn == 192 ? Geometry<192>::smem_bytes_mx(p.stages)
-                               : Geometry<128>::smem_bytes_mx(p.stages);
+        const int halves = p.fp4 ? 2 : 1;
+        p.smem = p.bn == 224   ? Geometry<224>::smem_bytes_mx(p.stages, halves)
+                 : p.bn == 192 ? Geometry<192>::smem_bytes_mx(p.stages, halves)
+                               : Geometry<128>::smem_bytes_mx(p.stages, halves);
         p.tmem = 512;  // accumulators and the slots' scales
     }
 
@@ -420,8 +427,9 @@ inline bool make_plan(const PlanInput &in, Plan &out)
     p.ws_pack_a = p.pack_a ? round_up(batch_a * a_rows * pack_pitch(a_cols) * 2, 256) : 0;
     p.ws_pack_b = p.pack_b ? round_up(batch_b * b_rows * pack_pitch(b_cols) * 2, 256) : 0;
     if (p.mx) {
-        p.ws_scales_a = round_up(batch_a * p.tiles_m * static_cast<int64_t>(p.k_blocks) * 512, 256);
-        p.ws_scales_b = round_up(batch_b * p.tiles_n * static_cast<int64_t>(p.k_blocks) * 512 * ceil_div(p.bn, 128), 256);
+        const int64_t halves = p.fp4 ? 2 : 1;
+        p.ws_scales_a = round_up(batch_a * p.tiles_m * static_cast<int64_t>(p.k_blocks) * 512 * halves, 256);
+        p.ws_scales_b = round_up(batch_b * p.tiles_n * static_cast<int64_t>(p.k_blocks) * 512 * halves * ceil_div(p.bn, 128), 256);
     }
     set_partial_workspace(in, p);
     out = p;

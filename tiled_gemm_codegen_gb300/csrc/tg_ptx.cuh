@@ -336,6 +336,21 @@ __device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t a_desc, uint64_
         : "memory");
 }
 
+// Block-scaled 4-bit MMA (kind::mxf4: packed E2M1 operands, two elements a
+// byte, K = 64 per instruction; one E8M0 scale per 32 elements of K, so two
+// per row per instruction, read from bytes id and id + 1 of the 32-bit scale
+// cells, id = 0 or 2 from idesc).
+__device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t sfa, uint32_t sfb, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+}
+
 // Shared memory -> tensor memory: 32 rows of 16 bytes (described by the
 // no-swizzle matrix descriptor sdesc) into 4 columns of lanes 0-31,
 // replicated into each of the four 32-lane quadrants.  Ordered with the
