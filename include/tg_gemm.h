@@ -71,7 +71,9 @@ typedef enum tg_status {
     TG_ERR_UNSUPPORTED = 2, /* valid request this build cannot run          */
     TG_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed            */
     TG_ERR_OOM = 4,         /* workspace allocation failed                  */
-    TG_ERR_TIMEOUT = 5      /* a device-side wait exceeded its limit        */
+    TG_ERR_TIMEOUT = 5,     /* a device-side wait exceeded its limit        */
+    TG_ERR_DEVICE_CHECK = 6 /* a device-side consistency check failed (only */
+                            /* in a library built with TG_DEBUG_CHECKS)     */
 } tg_status;
 
 /* Plan overrides for tests and tuning (zero-initialise, then set fields).
@@ -88,7 +90,9 @@ typedef struct tg_options {
                          /* (0 = 2 s)                                         */
     int32_t debug_stall; /* nonzero: the epilogue first waits on a barrier    */
                          /* nothing completes, so the watchdog must fire and  */
-                         /* tg_device_error() must return TG_ERR_TIMEOUT      */
+                         /* tg_device_error() must return TG_ERR_TIMEOUT;     */
+                         /* 2 in a library built with TG_DEBUG_CHECKS: a      */
+                         /* planted failed check instead (TG_ERR_DEVICE_CHECK)*/
     int32_t cta_pair;    /* 1 = one CTA per output tile; 2 = two-SM tiles:    */
                          /* a cluster of two CTAs computes 256 x block_n with */
                          /* one tcgen05 cta_group::2 MMA (block_n 128 or 256) */
@@ -381,8 +385,9 @@ tg_status tg_gemm_splitk_static(const void *A, const void *B, float *C,
  * the kernels' watchdog writes: the one of `stream`'s workspace, and the one
  * of tg_gemm_splitk_static on the current device.  TG_ERR_TIMEOUT if a wait
  * expired since the last call (the split-K tile counters of the stream's
- * workspace are then reset too), TG_ERR_CUDA if the stream reports a CUDA
- * error, else TG_OK.  Allocates nothing. */
+ * workspace are then reset too), TG_ERR_DEVICE_CHECK if a consistency check
+ * of a TG_DEBUG_CHECKS build failed, TG_ERR_CUDA if the stream reports a
+ * CUDA error, else TG_OK.  Allocates nothing. */
 tg_status tg_device_error(tg_stream_t stream);
 
 /* Static English name of a status code. */

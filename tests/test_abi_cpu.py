@@ -403,3 +403,16 @@ int main(void) {
     assert out[0].split() == ["256", "2", "6", "64"]       # bf16: two-SM 256 x 256 tiles, 64-element k-blocks
     assert out[1].split() == ["224", "1", "4", "32"]       # MXFP8: 224-wide tiles, 128-element k-blocks
     assert out[2].split()[0] == str(tg.TG_ERR_INVALID_ARG)
+
+
+def test_checks_build_loads_and_plans_host_only():
+    """The TG_DEBUG_CHECKS build exports every entry point the product build
+    does and plans without a GPU like it."""
+    chk = tg.load_checks()
+    lib = tg.load()
+    info_a, info_b = tg._abi.tg_plan_info(), tg._abi.tg_plan_info()
+    for L, info in ((lib, info_a), (chk, info_b)):
+        assert L.tg_plan(0x1000, 0x100000000, 0x200000000, 4096, 4096, 4096, 4096, 4096, 4096, 1, 0, 0, 0, 152,
+                         None, ctypes.byref(info)) == tg.TG_OK
+    assert info_a.as_dict() == info_b.as_dict()
+    assert chk.tg_status_string(tg.TG_ERR_DEVICE_CHECK) == b"device-side consistency check failed"

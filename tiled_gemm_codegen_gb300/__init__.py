@@ -15,15 +15,17 @@ import ctypes
 
 from ._abi import (TG_ACT_GELU_TANH, TG_ACT_NONE, TG_ACT_RELU, TG_ACT_SILU, TG_BF16, TG_ERR_CUDA,
                    TG_FP8_E4M3, TG_FP8_E5M2,
-                   TG_ERR_INVALID_ARG, TG_ERR_OOM, TG_ERR_TIMEOUT, TG_ERR_UNSUPPORTED, TG_F32, TG_OK,
-                   STATUS_NAMES, library_path, load, tg_epilogue, tg_options, tg_plan_info)
+                   TG_ERR_DEVICE_CHECK, TG_ERR_INVALID_ARG, TG_ERR_OOM, TG_ERR_TIMEOUT, TG_ERR_UNSUPPORTED,
+                   TG_F32, TG_OK, STATUS_NAMES, library_path, load, load_checks, tg_epilogue, tg_options,
+                   tg_plan_info)
 
 ACTIVATIONS = {"none": TG_ACT_NONE, "relu": TG_ACT_RELU, "gelu_tanh": TG_ACT_GELU_TANH,
                "silu": TG_ACT_SILU}
 
 __all__ = [
     "TG_OK", "TG_ERR_INVALID_ARG", "TG_ERR_UNSUPPORTED", "TG_ERR_CUDA", "TG_ERR_OOM",
-    "TG_ERR_TIMEOUT", "TgError", "tg_options", "tg_plan_info", "load", "library_path",
+    "TG_ERR_TIMEOUT", "TG_ERR_DEVICE_CHECK", "TgError", "tg_options", "tg_plan_info", "load", "load_checks",
+    "library_path",
     "tg_gemm", "tg_gemm_ex", "tg_gemm_host", "tg_gemm_fused", "tg_gemm_splitk_static", "tg_plan",
     "tg_gemm_fp8", "gemm_fp8", "TG_FP8_E4M3", "TG_FP8_E5M2",
     "tg_gemm_mxfp8", "gemm_mxfp8", "tg_gemm_mxfp4", "gemm_mxfp4", "tg_tune", "tune",

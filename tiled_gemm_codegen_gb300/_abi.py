@@ -18,6 +18,7 @@ TG_ERR_UNSUPPORTED = 2
 TG_ERR_CUDA = 3
 TG_ERR_OOM = 4
 TG_ERR_TIMEOUT = 5
+TG_ERR_DEVICE_CHECK = 6
 
 STATUS_NAMES = {
     TG_OK: "TG_OK",
@@ -26,6 +27,7 @@ STATUS_NAMES = {
     TG_ERR_CUDA: "TG_ERR_CUDA",
     TG_ERR_OOM: "TG_ERR_OOM",
     TG_ERR_TIMEOUT: "TG_ERR_TIMEOUT",
+    TG_ERR_DEVICE_CHECK: "TG_ERR_DEVICE_CHECK",
 }
 
 
@@ -127,10 +129,29 @@ SIGNATURES = {
 
 _LOCK = threading.Lock()
 _LIB = None
+_LIB_CHECKS = None
 
 
 def library_path() -> str:
     return _build.library_path()
+
+
+def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
+    for name, (args, res) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    return lib
+
+
+def load_checks() -> ctypes.CDLL:
+    """The TG_DEBUG_CHECKS build of the library (a separate handle with the
+    same entry points), built on first use."""
+    global _LIB_CHECKS
+    with _LOCK:
+        if _LIB_CHECKS is None:
+            _LIB_CHECKS = _declare(ctypes.CDLL(_build.build(checks=True)))
+        return _LIB_CHECKS
 
 
 def load(build_if_missing: bool = False) -> ctypes.CDLL:
@@ -146,10 +167,5 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
                     f"tiled_gemm_codegen_gb300: CUDA library not built ({path} missing); "
                     "run tiled_gemm_codegen_gb300.build.build() first")
             _build.build()
-        lib = ctypes.CDLL(path)
-        for name, (args, res) in SIGNATURES.items():
-            fn = getattr(lib, name)
-            fn.argtypes = args
-            fn.restype = res
-        _LIB = lib
-        return lib
+        _LIB = _declare(ctypes.CDLL(path))
+        return _LIB

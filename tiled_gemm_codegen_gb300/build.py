@@ -10,6 +10,13 @@ Translation units (compiled in parallel, one ``-gencode`` for sm_103a):
 The CUDA runtime is linked statically, so the library loads on a machine
 without a GPU (every CUDA call then returns an error) and exports only the
 ``tg_*`` entry points of ``include/tg_gemm.h``.
+
+``build(checks=True)`` builds the same sources with ``-DTG_DEBUG_CHECKS``
+into ``_build/libtg_gemm_checks_<machine>.so``: the kernels then verify
+their work units, ring slots, tensor-memory columns, shared-memory layout
+and split-K scratch indices on the device and report a failure through
+``tg_device_error`` (TG_ERR_DEVICE_CHECK) instead of touching memory out of
+range.  Tests run it beside the product library.
 """
 from __future__ import annotations
 
@@ -28,8 +35,9 @@ WIDTHS = (64, 128, 192, 256)
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 
-def library_path() -> str:
-    return os.path.join(BUILD, f"libtg_gemm_{platform.machine()}.so")
+def library_path(checks: bool = False) -> str:
+    name = "libtg_gemm_checks" if checks else "libtg_gemm"
+    return os.path.join(BUILD, f"{name}_{platform.machine()}.so")
 
 
 def _nvcc() -> str:
@@ -62,22 +70,25 @@ def _compile(args):
     return obj, r.stderr
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None) -> str:
-    """Compile and link the library if any source is newer than it."""
-    out = library_path()
+def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None,
+          checks: bool = False) -> str:
+    """Compile and link the library if any source is newer than it (checks:
+    the TG_DEBUG_CHECKS build, objects and library under their own names)."""
+    out = library_path(checks)
     if not force and os.path.exists(out):
         newest = max(os.path.getmtime(s) for s in _sources())
         if os.path.getmtime(out) >= newest:
             return out
     os.makedirs(BUILD, exist_ok=True)
-    machine = platform.machine()
+    machine = platform.machine() + ("_checks" if checks else "")
     jobs = [(os.path.join(CSRC, "tg_host.cu"), os.path.join(BUILD, f"tg_host_{machine}.o"), []),
             (os.path.join(CSRC, "tg_noalloc.cu"), os.path.join(BUILD, f"tg_noalloc_{machine}.o"), [])]
     for bn in WIDTHS:
         jobs.append((os.path.join(CSRC, "tg_kernels.cu"),
                      os.path.join(BUILD, f"tg_kernels_bn{bn}_{machine}.o"), [f"-DTG_BN={bn}"]))
-    if extra_flags:
-        jobs = [(s, o, d + list(extra_flags)) for (s, o, d) in jobs]
+    flags = (["-DTG_DEBUG_CHECKS"] if checks else []) + list(extra_flags or [])
+    if flags:
+        jobs = [(s, o, d + flags) for (s, o, d) in jobs]
     with cf.ThreadPoolExecutor(max_workers=len(jobs)) as ex:
         results = list(ex.map(_compile, jobs))
     if verbose:
@@ -98,4 +109,5 @@ if __name__ == "__main__":
     import sys
 
     print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
-                extra_flags=["-Xptxas", "-v"] if "--ptxas-v" in sys.argv else None))
+                extra_flags=["-Xptxas", "-v"] if "--ptxas-v" in sys.argv else None,
+                checks="--checks" in sys.argv))

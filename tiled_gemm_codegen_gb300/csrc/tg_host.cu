@@ -848,7 +848,9 @@ tg_status run_gemm(const Args &a, cudaStream_t stream, const tg_options *opt,
     p.maxparts = plan.maxparts;
     p.err = w.err;
     p.timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : DEFAULT_TIMEOUT_NS;
-    p.debug_stall = (opt && opt->debug_stall) ? 1 : 0;
+    p.debug_stall = (opt && opt->debug_stall) ? (opt->debug_stall == 2 ? 2 : 1) : 0;
+    p.partial_floats = partial_tiles ? plan.ws_partials / 4 : 0;
+    p.counter_count = partial_tiles ? plan.ws_counters / 4 : 0;
     p.trace = opt ? reinterpret_cast<unsigned long long *>(opt->trace_buffer) : nullptr;
 
     if (trace_enabled())
@@ -930,6 +932,7 @@ TG_API const char *tg_status_string(tg_status s)
         case TG_ERR_CUDA: return "CUDA error";
         case TG_ERR_OOM: return "out of device memory";
         case TG_ERR_TIMEOUT: return "device wait timed out";
+        case TG_ERR_DEVICE_CHECK: return "device-side consistency check failed";
         default: return "unknown status";
     }
 }
@@ -1530,23 +1533,26 @@ TG_API tg_status tg_device_error(tg_stream_t stream_)
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return TG_ERR_CUDA;
     // The static-scratch entry point's own word (one per device, shared by
     // all its calls): read and cleared here as well.
-    bool static_timeout = false;
-    if (static_error_take(dev, stream, &static_timeout) != cudaSuccess) return TG_ERR_CUDA;
+    uint32_t static_word = ERR_NONE;
+    if (static_error_take(dev, stream, &static_word) != cudaSuccess) return TG_ERR_CUDA;
+    const tg_status static_status = static_word == ERR_NONE          ? TG_OK
+                                    : static_word == ERR_DEBUG_CHECK ? TG_ERR_DEVICE_CHECK
+                                                                     : TG_ERR_TIMEOUT;
     std::lock_guard<std::mutex> lock(g_mutex);
     auto it = g_workspaces.find({dev, stream});
-    if (it == g_workspaces.end() || !it->second.err) return static_timeout ? TG_ERR_TIMEOUT : TG_OK;
+    if (it == g_workspaces.end() || !it->second.err) return static_status;
     Workspace &w = it->second;
     uint32_t word = 0;
     if ((e = cudaMemcpyAsync(&word, w.err, 4, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
         return TG_ERR_CUDA;
     if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return TG_ERR_CUDA;
-    if (word == ERR_NONE) return static_timeout ? TG_ERR_TIMEOUT : TG_OK;
-    // Clear the word, and the split-K counters an aborted kernel may have
-    // left part-way.
-    cudaMemsetAsync(w.err, 0, 4, stream);
+    if (word == ERR_NONE) return static_status;
+    // Clear the word (and the detail word after it), and the split-K
+    // counters an aborted kernel may have left part-way.
+    cudaMemsetAsync(w.err, 0, 8, stream);
     if (w.counters) cudaMemsetAsync(w.counters, 0, w.counters_cap, stream);
     cudaStreamSynchronize(stream);
-    return TG_ERR_TIMEOUT;
+    return word == ERR_DEBUG_CHECK ? TG_ERR_DEVICE_CHECK : TG_ERR_TIMEOUT;
 }
 
 TG_API void tg_shutdown(void)

@@ -24,6 +24,9 @@ enum : uint32_t {
     ERR_TIMEOUT_MMA = 2,
     ERR_TIMEOUT_EPILOGUE = 3,
     ERR_TIMEOUT_DRAIN = 4,
+    // Builds with TG_DEBUG_CHECKS: a device-side consistency check failed
+    // (the word after the code says which; see tg_kernel.cuh).
+    ERR_DEBUG_CHECK = 5,
 };
 
 struct KernelParams {
@@ -52,7 +55,11 @@ struct KernelParams {
     int32_t *counters;    // split-K arrival counters, one per output tile
     uint32_t *err;        // device error word
     uint64_t timeout_ns;
-    int32_t debug_stall;
+    int32_t debug_stall;  // 1: watchdog self-test; 2 (TG_DEBUG_CHECKS builds): planted failed check
+    // extents of the split-K scratch, for the consistency checks of
+    // TG_DEBUG_CHECKS builds: floats of partial tiles, int32 tile counters
+    int64_t partial_floats;
+    int64_t counter_count;
     // Stream-K schedule (stream_k == 1): every worker takes dp_waves whole
     // tiles (tile = worker + i * workers), then the k-block range
     // [w * sk_iters / workers, (w + 1) * sk_iters / workers) of the sk_tiles

@@ -243,6 +243,46 @@ __device__ __forceinline__ void raise_abort(const Watchdog &wd, uint32_t code)
     __threadfence_block();
 }
 
+#ifdef TG_DEBUG_CHECKS
+constexpr bool DEBUG_CHECKS = true;
+#else
+constexpr bool DEBUG_CHECKS = false;
+#endif
+
+// Device-side consistency checks of a library built with TG_DEBUG_CHECKS
+// (compiled out otherwise).  A failed check records ERR_DEBUG_CHECK in the
+// error word and the check's number in the word after it, and raises the
+// abort flag of this CTA (and of the peer CTA); the caller skips the access
+// the check guarded and leaves its loop, so the CTA exits through the same
+// path as a watchdog expiry.  No trap, no assertion, and the out-of-range
+// access itself never happens.
+enum : uint32_t {
+    CHK_UNIT = 1,           // work unit: k range, tile and problem indices
+    CHK_SMEM = 2,           // shared-memory layout inside the dynamic allocation
+    CHK_ACC_COLS = 3,       // MMA accumulator columns inside the tensor-memory allocation
+    CHK_SCALE_COLS = 4,     // block-scale columns of a ring slot inside the allocation
+    CHK_SLOT = 5,           // ring slot index below the ring depth
+    CHK_EPI_COLS = 6,       // epilogue tensor-memory loads inside the allocation
+    CHK_PARTIAL_WRITE = 7,  // split-K / stream-K partial tile inside the scratch
+    CHK_PARTIAL_READ = 8,   // the combine's reads inside the scratch
+    CHK_COUNTER = 9,        // tile arrival counter inside the scratch
+    CHK_PLANTED = 99,       // debug_stall == 2: a planted failure (tests of the reporting path)
+};
+
+__device__ __forceinline__ bool dbg_ok(bool cond, uint32_t which, const Watchdog &wd)
+{
+    if constexpr (!DEBUG_CHECKS) {
+        return true;
+    } else {
+        if (cond) return true;
+        if (atomicCAS(wd.err, 0u, static_cast<uint32_t>(ERR_DEBUG_CHECK)) == 0u) atomicExch(wd.err + 1, which);
+        *wd.abort_flag = 1;
+        if (wd.peer_abort) ptx::st_cluster_u32(wd.peer_abort, 1u);
+        __threadfence_block();
+        return false;
+    }
+}
+
 // All 128 epilogue threads agree on a predicate (named barrier 1).
 __device__ __forceinline__ bool epi_all(bool pred)
 {
@@ -476,6 +516,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         PAIR ? ptx::map_to_cta(ptx::smem_addr(const_cast<int32_t *>(abort_flag)), rank ^ 1u) : 0u;
     const Watchdog wd{p.timeout_ns, abort_flag, p.err, peer_abort};
     if (threadIdx.x == 0) stamp(1);
+    bool skip_all = false;  // TG_DEBUG_CHECKS: the layout check failed, touch nothing
+    if constexpr (DEBUG_CHECKS) {
+        if (threadIdx.x == 0) {
+            uint32_t dyn = 0;
+            asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
+            const uint32_t end = MX ? sSF + STAGES * SF_STAGE : bar0 + static_cast<uint32_t>(G::BAR_BYTES);
+            dbg_ok(end <= raw + dyn && 8u * (2 * STAGES + 6) + 16u <= static_cast<uint32_t>(G::BAR_BYTES) &&
+                       sE + 4u * EPI_BUFS * EPI_BOX_BYTES <= bar0,
+                   CHK_SMEM, wd);
+        }
+        __syncthreads();
+        skip_all = *abort_flag != 0;
+    }
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
@@ -489,7 +542,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             WorkIter wi;
             work_begin(p, worker, n_workers, wi);
             Unit w;
-            while (ok && work_next(p, worker, n_workers, wi, w)) {
+            while (ok && !skip_all && work_next(p, worker, n_workers, wi, w)) {
+                if (!dbg_ok(w.kb0 >= 0 && w.kb0 < w.kb1 && w.kb1 <= p.k_blocks && w.tm >= 0 && w.tm < p.tiles_m &&
+                                w.tn >= 0 && w.tn < p.tiles_n && w.b >= 0 && w.b < p.batch,
+                            CHK_UNIT, wd))
+                    break;
                 const int32_t zA = p.a_bcast ? 0 : w.b;
                 const int32_t zB = p.b_bcast ? 0 : w.b;
                 const int32_t m_rows = w.tm * TILE_M + static_cast<int32_t>(rank) * BM;
@@ -500,6 +557,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const int r = wait_bounded_warp(empty_bar(s), ph ^ 1u, wd);
                     if (r != WAIT_OK) {
                         if (r == WAIT_TIMEOUT && lane == 0) raise_abort(wd, ERR_TIMEOUT_PRODUCER);
+                        ok = false;
+                        break;
+                    }
+                    if (!dbg_ok(s < STAGES, CHK_SLOT, wd)) {
                         ok = false;
                         break;
                     }
@@ -588,9 +649,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             WorkIter wi;
             work_begin(p, worker, n_workers, wi);
             Unit w;
-            for (; ok && work_next(p, worker, n_workers, wi, w); ++t) {
+            for (; ok && !skip_all && work_next(p, worker, n_workers, wi, w); ++t) {
                 const uint32_t buf = t & 1u;
                 const uint32_t tph = (t >> 1) & 1u;
+                if (!dbg_ok(buf * BN + BN <= TMEM_ALLOC, CHK_ACC_COLS, wd)) break;
                 int r = wait_bounded_warp(tempty_bar(buf), tph ^ 1u, wd);
                 if (r != WAIT_OK) {
                     if (r == WAIT_TIMEOUT && lane == 0) raise_abort(wd, ERR_TIMEOUT_MMA);
@@ -608,6 +670,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     }
                     if (it == 0 && lane == 0) stamp(2);
+                    if (!dbg_ok(s < STAGES && (!MX || SF_COL0 + SF_COLS * (s + 1) <= TMEM_ALLOC), CHK_SCALE_COLS, wd)) {
+                        ok = false;
+                        break;
+                    }
                     ptx::tc_fence_after();
                     if (ptx::elect_one()) {
                         const uint32_t a_addr = sA + s * G::A_STAGE;
@@ -688,12 +754,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t tempty_leader0 = PAIR ? ptx::map_to_cta(tempty_bar(0), 0u) : tempty_bar(0);
         uint32_t st_cnt = 0;
         bool ok = true;
-        if (p.debug_stall) {
+        if (DEBUG_CHECKS && p.debug_stall == 2) {
+            // Self-test of the consistency checks' reporting path.
+            ok = epi_all(dbg_ok(false, CHK_PLANTED, wd));
+        } else if (p.debug_stall) {
             // Watchdog self-test: a barrier that nothing ever completes.
             const int r = wait_bounded(stall_bar, 0, wd);
             if (r == WAIT_TIMEOUT) raise_abort(wd, ERR_TIMEOUT_EPILOGUE);
             ok = epi_all(r == WAIT_OK);
         }
+        if (skip_all) ok = false;
 
         // One 32 x 32 fp32 chunk (rows m_base + 32q .., columns col0 ..) of
         // this warp's accumulator rows -> C.
@@ -813,6 +883,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (r == WAIT_TIMEOUT) raise_abort(wd, ERR_TIMEOUT_EPILOGUE);
             if (!epi_all(r == WAIT_OK)) break;
             if (t == 0 && warp == 2 && lane == 0) stamp(4);
+            if (!dbg_ok(buf * BN + BN <= TMEM_ALLOC, CHK_EPI_COLS, wd)) break;
             ptx::tc_fence_after();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
             const int32_t m_base = w.tm * TILE_M + static_cast<int32_t>(rank) * BM;
@@ -844,6 +915,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // rows of one column quad are 512 contiguous bytes and every
                 // access below is a coalesced 16-byte vector per thread.
                 const int64_t half = w.slot * (PAIR ? 2 : 1) + rank;
+                constexpr int64_t PART_FLOATS = static_cast<int64_t>(BM) * BN;
+                if (!dbg_ok(w.part >= 0 && w.part < w.nparts && w.nparts <= p.maxparts &&
+                                (half * p.maxparts + w.part + 1) * PART_FLOATS <= p.partial_floats,
+                            CHK_PARTIAL_WRITE, wd) ||
+                    !dbg_ok((half * p.maxparts + w.nparts) * PART_FLOATS <= p.partial_floats, CHK_PARTIAL_READ, wd) ||
+                    !dbg_ok(half >= 0 && half < p.counter_count, CHK_COUNTER, wd))
+                    break;
                 const bool row_ok = (m_base + row) < p.M;
                 const float4 *ws0 = reinterpret_cast<const float4 *>(
                     p.partials + half * static_cast<int64_t>(p.maxparts) * (BM * BN));

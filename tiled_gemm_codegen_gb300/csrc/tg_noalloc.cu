@@ -84,22 +84,22 @@ uint64_t debug_stall_ns()
 
 namespace tg {
 
-// Reads the array's error word on the current device after `stream` has
-// been synchronised by the caller; a nonzero word is cleared and reported
-// through *timed_out.  Reads nothing (and reports nothing) on a device where
-// the entry point has never run.  Allocates nothing: the word goes through
-// one 4-byte copy into a host variable.
-cudaError_t static_error_take(int dev, cudaStream_t stream, bool *timed_out)
+// Reads the array's error word on device `dev` after `stream` has been
+// synchronised by the caller; a nonzero word is cleared (with the detail
+// word after it) and returned in *code (ERR_NONE otherwise).  Reads nothing
+// on a device where the entry point has never run.  Allocates nothing: the
+// word goes through one 4-byte copy into a host variable.
+cudaError_t static_error_take(int dev, cudaStream_t stream, uint32_t *code)
 {
-    *timed_out = false;
+    *code = ERR_NONE;
     uint32_t *err = error_word(dev);
     if (!err) return cudaSuccess;
     uint32_t word = 0;
     cudaError_t e = cudaMemcpyAsync(&word, err, 4, cudaMemcpyDeviceToHost, stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess || word == ERR_NONE) return e;
-    *timed_out = true;
-    e = cudaMemsetAsync(err, 0, 4, stream);
+    *code = word;
+    e = cudaMemsetAsync(err, 0, 8, stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
     return e;
 }
@@ -189,6 +189,8 @@ TG_API tg_status tg_gemm_splitk_static(const void *A, const void *B, float *C, i
     p.maxparts = plan.splits;
     p.counters = counters;
     p.err = err;
+    p.partial_floats = static_cast<int64_t>(PARTIAL_BYTES / 4);
+    p.counter_count = MAX_TILES;
     const uint64_t stall_ns = debug_stall_ns();
     p.timeout_ns = stall_ns ? stall_ns : 2000000000ull;
     p.debug_stall = stall_ns ? 1 : 0;

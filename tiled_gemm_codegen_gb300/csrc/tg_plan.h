@@ -503,7 +503,7 @@ cudaError_t shared_launch_gemm(int bn, const CUtensorMap &ta, const CUtensorMap 
                                cudaStream_t s);
 cudaError_t shared_zero_fill(float *C, int64_t M, int64_t N, int64_t ldc, int64_t sC, int64_t batch,
                              int sms, cudaStream_t s);
-// Defined in tg_noalloc.cu: reads (and clears, reporting *timed_out) the
+// Defined in tg_noalloc.cu: reads (and clears, returning it in *code) the
 // static-scratch entry point's error word on device `dev`.
-cudaError_t static_error_take(int dev, cudaStream_t stream, bool *timed_out);
+cudaError_t static_error_take(int dev, cudaStream_t stream, uint32_t *code);
 }  // namespace tg
