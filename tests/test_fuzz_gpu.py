@@ -212,3 +212,73 @@ def test_random_mx_cases(i):
             mask[lo: lo + N] = True
             assert np.array_equal(host[lo: lo + N].astype(np.float64), want[b, i_]), (c, b, i_)
     assert np.all(np.isnan(host[~mask])), ("write outside D", c)
+
+
+def _case_mx4(i):
+    r = random.Random(9000 + i)
+    M, N = r.randint(1, 600), r.randint(1, 800)
+    K = 32 * r.randint(1, 40)                 # whole 16-byte rows of packed elements
+    k_used = K - 2 * r.randint(0, 7) if r.random() < 0.4 else K  # even K, the rest row padding
+    batch = r.choice([1, 1, 2])
+    opts = {}
+    bn = r.choice([0, 128, 192, 224])
+    if bn:
+        opts["block_n"] = bn
+    if r.random() < 0.25 and k_used >= 512:
+        opts["split_k"] = 2
+    elif r.random() < 0.2:
+        opts["stream_k"] = 2
+    if r.random() < 0.3 or bn == 224:
+        opts["stages"] = 2
+    runs = -(-k_used // 32)
+    return dict(M=M, N=N, K=k_used, pitch=K, batch=batch, opts=opts, ld_sfa=runs + r.choice([0, 0, 5]),
+                ld_sfb=runs + r.choice([0, 3]), shared_sfb=batch > 1 and r.random() < 0.3,
+                ldd_pad=r.choice([0, 3, 8]), seed=r.randint(0, 10 ** 6))
+
+
+@pytest.mark.parametrize("i", range(24))
+def test_random_mxfp4_cases(i):
+    """Block-scaled packed 4-bit operands: random extents (K not a multiple of
+    32, rows padded past K), scale pitches, shared scales, tile widths,
+    rings and K splits; exact against the oracle (all E2M1 codes, scales
+    2^-1..2^1), and nothing written outside D."""
+    from oracle import mx as omx
+
+    c = _case_mx4(i)
+    M, N, K, P, batch = c["M"], c["N"], c["K"], c["pitch"], c["batch"]
+    runs = -(-K // 32)
+    Ac = synth.make_fp4_codes((batch, M, K), seed=c["seed"])
+    Bc = synth.make_fp4_codes((batch, N, K), seed=c["seed"] + 1)
+    # packed rows of P elements; the padding past K holds the code of 6.0
+    pad = lambda t: torch.cat([t, torch.full(t.shape[:-1] + (P - K,), 7, dtype=torch.uint8)], dim=-1)
+    ad = synth.pack_fp4_codes(pad(Ac)).to(dev())
+    bd = synth.pack_fp4_codes(pad(Bc)).to(dev())
+    sfa = synth.make_e8m0_codes((batch, M, runs), seed=c["seed"] + 2, lo=126, hi=128)
+    nb_sf = 1 if c["shared_sfb"] else batch
+    sfb = synth.make_e8m0_codes((nb_sf, N, runs), seed=c["seed"] + 3, lo=126, hi=128)
+    fa_buf = torch.full((batch, M, c["ld_sfa"]), 255, dtype=torch.uint8)
+    fa_buf[:, :, :runs] = sfa
+    fb_buf = torch.full((nb_sf, N, c["ld_sfb"]), 255, dtype=torch.uint8)
+    fb_buf[:, :, :runs] = sfb
+    fad, fbd = fa_buf.to(dev()), fb_buf.to(dev())
+    ldd = N + c["ldd_pad"]
+    sD = M * ldd + 8
+    dbuf = torch.full(((batch - 1) * sD + M * ldd + 8,), float("nan"), dtype=torch.float32, device=dev())
+    st = tg.tg_gemm_mxfp4(ad.data_ptr(), bd.data_ptr(), dbuf.data_ptr(), M, N, K, P, P, ldd, batch,
+                          M * P if batch > 1 else 0, N * P if batch > 1 else 0, sD if batch > 1 else 0,
+                          fad.data_ptr(), c["ld_sfa"], M * c["ld_sfa"] if batch > 1 else 0,
+                          fbd.data_ptr(), c["ld_sfb"], N * c["ld_sfb"] if nb_sf > 1 else 0, None,
+                          torch.cuda.current_stream().cuda_stream, tg.make_options(**c["opts"]))
+    assert st == tg.TG_OK, (c, tg.STATUS_NAMES.get(st, st))
+    assert tg.device_error() == tg.TG_OK, c
+    host = dbuf.cpu().numpy()
+    sfb_full = sfb.expand(batch, N, runs) if nb_sf == 1 else sfb
+    want = omx.gemm_mxfp4_f64(omx.pack_fp4(Ac.numpy()), omx.pack_fp4(Bc.numpy()), K, sfa.numpy(),
+                              sfb_full.numpy())
+    mask = np.zeros(host.shape, dtype=bool)
+    for b in range(batch):
+        for i_ in range(M):
+            lo = b * sD + i_ * ldd
+            mask[lo: lo + N] = True
+            assert np.array_equal(host[lo: lo + N].astype(np.float64), want[b, i_]), (c, b, i_)
+    assert np.all(np.isnan(host[~mask])), ("write outside D", c)
