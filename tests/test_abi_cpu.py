@@ -353,9 +353,10 @@ def test_plan_4bit_block_scaled(lib):
     ring; the scale scratch holds two blocks per 128 rows and k-block."""
     p = tg.plan(4096, 4096, 4096, sm_count=152, operands="mxfp4")
     assert p["block_k"] == 256 and p["k_blocks"] == 16 and p["cta_pair"] == 1
-    assert p["block_n"] in (128, 192, 224)
-    if p["block_n"] == 224:
-        assert p["stages"] == 2
+    # the two-slot 224-wide tiles only on request (measured slower)
+    assert p["block_n"] in (128, 192) and p["stages"] == 4
+    q = tg.plan(4096, 4096, 4096, sm_count=152, operands="mxfp4", options=tg.make_options(block_n=224))
+    assert (q["block_n"], q["stages"]) == (224, 2)
     for bn, st in ((128, 4), (192, 4), (224, 2), (128, 2)):
         q = tg.plan(1000, 1000, 1056, sm_count=152, operands="mxfp4",
                     options=tg.make_options(block_n=bn, stages=st))
