@@ -417,3 +417,25 @@ def test_checks_build_loads_and_plans_host_only():
                          None, ctypes.byref(info)) == tg.TG_OK
     assert info_a.as_dict() == info_b.as_dict()
     assert chk.tg_status_string(tg.TG_ERR_DEVICE_CHECK) == b"device-side consistency check failed"
+
+
+def test_plan_rules_from_the_tuner_sweep():
+    """The planner's measured rules (default plan against the run-time
+    tuner's best on GB300): no stream-K with few k-blocks, no two-SM tiles
+    when their rows would be half padding or a tile has few k-blocks, no
+    tile twice as wide as N - and the five workloads keep their plans."""
+    def P(M, N, K, b=1):
+        return tg.plan(M, N, K, b, sm_count=152)
+    assert P(2048, 8192, 2048)["stream_k"] == 1          # 32 k-blocks
+    assert P(4096, 4096, 4096)["stream_k"] == 2          # 64 k-blocks
+    assert P(128, 4096, 4096)["cta_pair"] == 1           # M = 128
+    assert P(512, 512, 512, 32)["cta_pair"] == 1         # 8 k-blocks a tile
+    assert P(4096, 128, 4096)["block_n"] <= 128          # N = 128
+    p = P(4096, 4096, 4096)
+    assert (p["block_n"], p["cta_pair"], p["stages"]) == (256, 2, 6)
+    p = P(4097, 4095, 4100)
+    assert (p["block_n"], p["cta_pair"], p["stream_k"]) == (256, 2, 2)
+    p = P(384, 640, 1000, 64)
+    assert (p["block_n"], p["cta_pair"], p["stages"]) == (256, 1, 4)
+    p = P(64, 28672, 8192)
+    assert (p["block_n"], p["cta_pair"]) == (192, 1)

@@ -338,6 +338,14 @@ inline bool make_plan(const PlanInput &in, Plan &out)
         if (in.f8 && cd.pair && in.cta_pair == 0 &&
             in.batch * ceil_div(in.M, 2 * BM) * ceil_div(in.N, cd.bn) < std::max(1, sms / 2))
             continue;
+        // bf16 rules from the default plan against the run-time tuner's best
+        // on 20 shapes (GB300): two-SM tiles lost where the pair's 256 rows
+        // were half padding (M = 128: 32.8 vs 22.5 us) or a tile has few
+        // k-blocks (batches of 512^3 and 256^3: 24.6 vs 20.5 us); a tile at
+        // least twice as wide as N (N = 128 in 256-wide tiles: 30.8 vs 22.5
+        // us) lost to narrower ones.  Planner's own choices only.
+        if (!in.f8 && in.cta_pair == 0 && cd.pair && (in.M <= BM || p.k_blocks < 10)) continue;
+        if (!in.f8 && in.block_n == 0 && cd.bn > 64 && cd.bn >= 2 * round_up(in.N, 64)) continue;
         const int tile_m = cd.pair ? 2 * BM : BM;
         const int64_t tiles_m = ceil_div(in.M, tile_m);
         const int64_t tiles_n = ceil_div(in.N, cd.bn);
@@ -358,6 +366,10 @@ inline bool make_plan(const PlanInput &in, Plan &out)
                 // 8-bit operands: stream-K only on request (its partial-tile
                 // traffic outweighs the balance at the measured sizes)
                 if (use_sk && in.f8 && in.stream_k != 2) continue;
+                // bf16: stream-K pays for its partial tiles only with enough
+                // k-blocks per tile (measured: 64 k-blocks 90 -> 84 us with
+                // it; 32 k-blocks 55.2 -> 63.5 and 88.1 -> 96.3 us with it)
+                if (use_sk && in.stream_k != 2 && p.k_blocks < 48) continue;
                 if (!use_sk && in.stream_k == 2 && tiles % workers != 0) continue;
                 const double c = plan_cost_ns(in, cd.bn, cd.pair, s, p.k_blocks, tiles, sms, use_sk);
                 if (!have || c < best * 0.999) {
