@@ -439,3 +439,10 @@ def test_plan_rules_from_the_tuner_sweep():
     assert (p["block_n"], p["cta_pair"], p["stages"]) == (256, 1, 4)
     p = P(64, 28672, 8192)
     assert (p["block_n"], p["cta_pair"]) == (192, 1)
+    # the rules shape the planner's own choices only: a requested form is
+    # always planned (two-SM tiles for a 39-column output, stream-K with
+    # few k-blocks)
+    q = tg.plan(693, 39, 719, 2, sm_count=152, options=tg.make_options(cta_pair=2))
+    assert q["cta_pair"] == 2
+    q = tg.plan(2048, 8192, 2048, sm_count=152, options=tg.make_options(stream_k=2))
+    assert q["stream_k"] == 2

@@ -345,7 +345,8 @@ inline bool make_plan(const PlanInput &in, Plan &out)
         // least twice as wide as N (N = 128 in 256-wide tiles: 30.8 vs 22.5
         // us) lost to narrower ones.  Planner's own choices only.
         if (!in.f8 && in.cta_pair == 0 && cd.pair && (in.M <= BM || p.k_blocks < 10)) continue;
-        if (!in.f8 && in.block_n == 0 && cd.bn > 64 && cd.bn >= 2 * round_up(in.N, 64)) continue;
+        if (!in.f8 && in.block_n == 0 && in.cta_pair != 2 && cd.bn > 64 && cd.bn >= 2 * round_up(in.N, 64))
+            continue;
         const int tile_m = cd.pair ? 2 * BM : BM;
         const int64_t tiles_m = ceil_div(in.M, tile_m);
         const int64_t tiles_n = ceil_div(in.N, cd.bn);
