@@ -446,3 +446,26 @@ def test_plan_rules_from_the_tuner_sweep():
     assert q["cta_pair"] == 2
     q = tg.plan(2048, 8192, 2048, sm_count=152, options=tg.make_options(stream_k=2))
     assert q["stream_k"] == 2
+
+
+def test_plan_rules_for_every_operand_family():
+    """The narrowest width that holds N, no two-SM tile that spans all of N,
+    and (8-bit) no two-SM tile with fewer than 20 k-blocks; every operand
+    family still has a plan for every narrow N, and a requested width is
+    kept."""
+    for ops in ("bf16", "fp8", "mxfp8", "mxfp4"):
+        for N in list(range(1, 300, 7)) + [64, 128, 192, 256]:
+            p = tg.plan(4096, N, 4096, sm_count=152, operands=ops)
+            assert p["block_n"] >= 64 and p["grid"] > 0, (ops, N)
+            if N <= 128:
+                assert p["block_n"] <= 128, (ops, N, p["block_n"])
+            if N <= p["block_n"]:
+                assert p["cta_pair"] == 1, (ops, N)
+        assert tg.plan(4096, 128, 4096, sm_count=152, operands=ops,
+                       options=tg.make_options(block_n=192))["block_n"] == 192
+    for b, M, N, K in ((1, 16384, 16384, 512), (32, 512, 512, 512), (1, 2048, 8192, 2048)):
+        assert tg.plan(M, N, K, b, sm_count=152, operands="fp8")["cta_pair"] == 1
+    p = tg.plan(4096, 4096, 4096, sm_count=152, operands="fp8")
+    assert (p["block_n"], p["cta_pair"]) == (256, 2)                 # 32 k-blocks
+    assert tg.plan(4096, 160, 4096, sm_count=152)["cta_pair"] == 1
+    assert tg.plan(4096, 160, 4096, sm_count=152, options=tg.make_options(cta_pair=2))["cta_pair"] == 2

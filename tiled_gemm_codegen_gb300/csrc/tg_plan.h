@@ -317,6 +317,15 @@ inline bool make_plan(const PlanInput &in, Plan &out)
     const Cand cands_all[6] = {{256, true}, {128, true}, {256, false}, {192, false}, {128, false}, {64, false}};
     const Cand *cands = in.mx ? cands_mx : cands_all;
     const int n_cands = in.mx ? 3 : 6;
+    // The narrowest one-CTA width of this operand family that holds all of N
+    // in one tile column (0: none does).
+    int cover_bn = 0;
+    for (int ci = 0; ci < n_cands; ++ci) {
+        const Cand &cd = cands[ci];
+        if (cd.pair || cd.bn < in.N) continue;
+        if (in.mx ? !mx_stage_supported(cd.bn, 2, false, in.fp4) : !stage_supported(cd.bn, 2, false, in.f8)) continue;
+        if (cover_bn == 0 || cd.bn < cover_bn) cover_bn = cd.bn;
+    }
     double best = 0.0;
     bool have = false;
     for (int ci = 0; ci < n_cands; ++ci) {
@@ -338,15 +347,24 @@ inline bool make_plan(const PlanInput &in, Plan &out)
         if (in.f8 && cd.pair && in.cta_pair == 0 &&
             in.batch * ceil_div(in.M, 2 * BM) * ceil_div(in.N, cd.bn) < std::max(1, sms / 2))
             continue;
-        // bf16 rules from the default plan against the run-time tuner's best
-        // on 20 shapes (GB300): two-SM tiles lost where the pair's 256 rows
-        // were half padding (M = 128: 32.8 vs 22.5 us) or a tile has few
-        // k-blocks (batches of 512^3 and 256^3: 24.6 vs 20.5 us); a tile at
-        // least twice as wide as N (N = 128 in 256-wide tiles: 30.8 vs 22.5
-        // us) lost to narrower ones.  Planner's own choices only.
-        if (!in.f8 && in.cta_pair == 0 && cd.pair && (in.M <= BM || p.k_blocks < 10)) continue;
-        if (!in.f8 && in.block_n == 0 && in.cta_pair != 2 && cd.bn > 64 && cd.bn >= 2 * round_up(in.N, 64))
-            continue;
+        // Rules from the default plan against the run-time tuner's best on
+        // 20 bf16 and 12 8-bit shapes (GB300), for the planner's own choices
+        // only.  Two-SM tiles lost where the pair's 256 rows were half
+        // padding (M = 128: 32.8 vs 22.5 us) or a tile has few k-blocks
+        // (bf16 batches of 512^3 and 256^3: 24.6 vs 20.5 us; 8-bit 16384^2 x
+        // 512: 327 vs 281 us, 2048 x 8192 x 2048: 43.0 vs 39.0 us).  An
+        // 8-bit k-block takes half the MMA time of a bf16 one, so the
+        // pair's fixed cost per tile needs twice as many of them.  A tile
+        // wider than the narrowest width that holds N lost to it (bf16
+        // N = 128 in 256-wide tiles: 30.8 vs 22.5 us; 8-bit N = 128 in
+        // 192-wide ones: 24.5 vs 20.5 us; MXFP8 N = 128 in 224-wide ones:
+        // 30.7 vs 26.3 us), for every operand family.  A two-SM tile that
+        // spans all of N shares no B tile worth the pairing (bf16 N = 160 in
+        // two-SM 256-wide tiles: 32.8 vs 24.6 us; N = 128 in two-SM 128-wide
+        // ones: 26.6 vs 22.5 us).
+        if (!in.mx && in.cta_pair == 0 && cd.pair && (in.M <= BM || p.k_blocks < (in.f8 ? 20 : 10))) continue;
+        if (!in.mx && in.cta_pair == 0 && cd.pair && in.N <= cd.bn) continue;
+        if (in.block_n == 0 && in.cta_pair != 2 && cover_bn != 0 && cd.bn > cover_bn) continue;
         const int tile_m = cd.pair ? 2 * BM : BM;
         const int64_t tiles_m = ceil_div(in.M, tile_m);
         const int64_t tiles_n = ceil_div(in.N, cd.bn);
