@@ -607,3 +607,56 @@ def test_store_never_writes_row_padding(N, out):
         assert np.array_equal(got, want)
     else:
         assert np.array_equal(got, torch.from_numpy(want).to(torch.bfloat16).double().numpy())
+
+
+# Outputs of at most 64 rows take ring slots of 64 rows of A (8 slots at
+# width 128, 6 at width 192); the MMA reads the upper 64 rows from the memory
+# after the slot and their accumulator rows are never stored.
+HALF_A_SHAPES = [(1, 129, 64), (5, 700, 77), (33, 257, 300), (64, 1000, 1000), (64, 192, 4100)]
+
+
+@pytest.mark.parametrize("bn", [128, 192])
+@pytest.mark.parametrize("shape", HALF_A_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_half_height_a_exact(bn, shape):
+    M, N, K = shape
+    info = tg.plan(M, N, K, sm_count=152, options=tg.make_options(block_n=bn))
+    assert info["block_m"] == 64 and info["stages"] == (8 if bn == 128 else 6)
+    A, B = synth.make_int_inputs(1, M, N, K, seed=_seed(M, N, K, bn, 64))
+    got = run(A, B, options=tg.make_options(block_n=bn))
+    assert np.array_equal(got, oracle_dense(A, B))
+
+
+@pytest.mark.parametrize("bn", [128, 192])
+@pytest.mark.parametrize("layout", ["nn", "tn", "nt", "tt"])
+def test_half_height_a_bitwise_equals_full_slots(bn, layout):
+    """The same tile and k order with 64-row A slots and with 128-row ones
+    (an explicit shallower ring): bitwise equal, for every operand layout,
+    batched and with a K split."""
+    b, M, N, K = 3, 50, 517, 1100
+    gen = torch.Generator().manual_seed(_seed(b, M, N, K, bn))
+    A = torch.randn(b, M, K, generator=gen).to(torch.bfloat16).to(dev())
+    B = torch.randn(b, K, N, generator=gen).to(torch.bfloat16).to(dev())
+    if layout[0] == "t":
+        A = A.transpose(-1, -2).contiguous().transpose(-1, -2)
+    if layout[1] == "t":
+        B = B.transpose(-1, -2).contiguous().transpose(-1, -2)
+    for split in (1, 3):
+        half = tg.gemm(A, B, options=tg.make_options(block_n=bn, split_k=split))
+        full = tg.gemm(A, B, options=tg.make_options(block_n=bn, split_k=split, stages=4))
+        assert tg.device_error() == tg.TG_OK
+        assert torch.equal(half, full)
+    ref = oracle.gemm_dense_f64(A.cpu(), B.cpu())
+    assert_close(half.cpu().double().numpy(), ref, K)
+
+
+@pytest.mark.parametrize("bn", [128, 192])
+def test_half_height_a_fp8_bitwise_equals_full_slots(bn):
+    M, N, K = 64, 28672 // 8, 2048
+    A = synth.make_fp8_codes((M, K), 0, seed=_seed(M, K, bn), kind="normal").to(dev()).view(torch.float8_e4m3fn)
+    Bt = synth.make_fp8_codes((N, K), 0, seed=_seed(N, K, bn), kind="normal").to(dev()).view(torch.float8_e4m3fn)
+    info = tg.plan(M, N, K, sm_count=152, operands="fp8", options=tg.make_options(block_n=bn))
+    assert info["block_m"] == 64
+    half = tg.gemm_fp8(A, Bt, options=tg.make_options(block_n=bn))
+    full = tg.gemm_fp8(A, Bt, options=tg.make_options(block_n=bn, stages=4))
+    assert tg.device_error() == tg.TG_OK
+    assert torch.equal(half, full)

@@ -363,7 +363,7 @@ PlanInput plan_input(const Args &a, int sms, const tg_options *opt)
 void fill_info(const Plan &p, tg_plan_info *out)
 {
     std::memset(out, 0, sizeof(*out));
-    out->block_m = p.pair ? 2 * BM : BM;
+    out->block_m = p.pair ? 2 * BM : p.half_a ? BM / 2 : BM;
     out->cta_pair = p.pair ? 2 : 1;
     out->stream_k = p.stream_k ? 2 : 1;
     out->sk_tiles = static_cast<int32_t>(p.sk_tiles);
@@ -582,6 +582,18 @@ cudaError_t launch_gemm(int bn, bool pair, bool f8, int mx, const CUtensorMap &t
     }
 }
 
+// Half-height A slots (one CTA per tile): widths 128 (8 slots) and 192 (6).
+cudaError_t launch_gemm_half_a(int bn, bool f8, const CUtensorMap &ta, const CUtensorMap &tb,
+                               const CUtensorMap &tc, const KernelParams &p, int stages, int grid, cudaStream_t s)
+{
+    if (stages != half_a_stages(bn)) return cudaErrorInvalidValue;
+    switch (bn) {
+        case 128: return launch_gemm_bn128_half_a(ta, tb, tc, p, f8, grid, s);
+        case 192: return launch_gemm_bn192_half_a(ta, tb, tc, p, f8, grid, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 // Co-resident two-CTA clusters of a pair configuration, cached per device.
 int max_pairs(int dev, int bn, int stages, bool f8)
 {
@@ -706,7 +718,8 @@ tg_status run_gemm(const Args &a, cudaStream_t stream, const tg_options *opt,
 
     // Encode the operand maps; an operand TMA cannot describe is packed.
     CUtensorMap ta{}, tb{}, tc{};
-    // Row-major A: boxes [128 rows x 64 k]; column-major A: [64 k x 64 rows].
+    // Row-major A: boxes [128 rows x 64 k] ([64 rows x 64 k] for half-height
+    // A slots); column-major A: [64 k x 64 rows].
     // Row-major B: [64 k x 64 columns]; column-major B: [B columns x 64 k].
     const uint32_t b_cols_cta = static_cast<uint32_t>(plan.pair ? plan.bn / 2 : plan.bn);
     // Element type and the K extent of a 128-byte box row: 64 bf16 or 128
@@ -718,7 +731,7 @@ tg_status run_gemm(const Args &a, cudaStream_t stream, const tg_options *opt,
         const uint64_t z = in.a_bcast || a.batch == 1 ? 1 : static_cast<uint64_t>(a.batch);
         const uint64_t s2 = z == 1 ? single_problem_stride(a.a_rows(), lda * eb) : static_cast<uint64_t>(sA) * eb;
         if (a.a_cm) return encode_3d(&ta, dt, A, a.M, a.K, z, lda * eb, s2, 64, BK);
-        return encode_3d(&ta, dt, A, a.K, a.M, z, lda * eb, s2, kbox, BM);
+        return encode_3d(&ta, dt, A, a.K, a.M, z, lda * eb, s2, kbox, plan.half_a ? BM / 2 : BM);
     };
     auto encode_b = [&]() {
         const uint64_t z = in.b_bcast || a.batch == 1 ? 1 : static_cast<uint64_t>(a.batch);
@@ -867,7 +880,8 @@ tg_status run_gemm(const Args &a, cudaStream_t stream, const tg_options *opt,
     p.sfa = plan.mx ? scales_a : nullptr;
     p.sfb = plan.mx ? scales_b : nullptr;
     const int mx_kind = plan.fp4 ? MX_FP4 : plan.mx ? MX_FP8 : MX_NONE;
-    e = launch_gemm(plan.bn, plan.pair, plan.f8, mx_kind, ta, tb, tc, p, plan.stages, grid, stream);
+    e = plan.half_a ? launch_gemm_half_a(plan.bn, plan.f8, ta, tb, tc, p, plan.stages, grid, stream)
+                    : launch_gemm(plan.bn, plan.pair, plan.f8, mx_kind, ta, tb, tc, p, plan.stages, grid, stream);
     return cuda_status(e);
 }
 
@@ -886,8 +900,9 @@ bool shared_plan(const void *A, const void *B, const float *C, int64_t M, int64_
                  int64_t lda, int64_t ldb, int64_t ldc, int64_t batch, int64_t sA, int64_t sB,
                  int64_t sC, int sms, const tg_options *opt, Plan *out, PlanInput *in_out)
 {
-    const PlanInput in =
+    PlanInput in =
         plan_input(Args{A, B, const_cast<float *>(C), M, N, K, lda, ldb, ldc, batch, sA, sB, sC}, sms, opt);
+    in.half_a_ok = false;  // the static entry point launches full-height A slots
     if (in_out) *in_out = in;
     return make_plan(in, *out);
 }

@@ -82,11 +82,15 @@ struct KernelParams {
 
 // Shared-memory budget of one tile width.  PAIR: the tile is computed by a
 // cluster of two CTAs on two SMs (tcgen05 cta_group::2): each CTA holds its
-// own 128 rows of A and half of the BN columns of B.
-template <int BN, bool PAIR = false>
+// own 128 rows of A and half of the BN columns of B.  HALF_A (one CTA per
+// tile, outputs of at most 64 rows): a ring slot holds 64 rows of A, so more
+// slots fit; the MMA still reads 128 rows, the upper 64 from the memory
+// after the slot, and the accumulator rows they produce are never stored.
+template <int BN, bool PAIR = false, bool HALF_A = false>
 struct Geometry {
     static constexpr int B_COLS = PAIR ? BN / 2 : BN;     // B columns this CTA loads
-    static constexpr int A_STAGE = BM * BK * 2;           // 16 KB
+    static constexpr int A_ROWS = HALF_A ? BM / 2 : BM;   // A rows a slot holds
+    static constexpr int A_STAGE = A_ROWS * BK * 2;       // 16 KB (8 KB)
     static constexpr int B_STAGE = BK * B_COLS * 2;       // B_COLS * 128 B
     static constexpr int STAGE = A_STAGE + B_STAGE;
     static constexpr int EPI_BYTES = 4 * EPI_BUFS * EPI_CHUNK * EPI_CHUNK * 4;  // 32 KB
@@ -130,6 +134,12 @@ enum : int { MX_NONE = 0, MX_FP8 = 1, MX_FP4 = 2 };
     int max_pairs_bn##BN_(int stages, bool f8);
 TG_DECLARE_LAUNCH(64)
 TG_DECLARE_LAUNCH(128)
+// Half-height A slots (outputs of at most 64 rows): width 128 with 8 slots
+// and width 192 with 6; f8 as above.
+cudaError_t launch_gemm_bn128_half_a(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
+                                     const KernelParams &p, bool f8, int grid, cudaStream_t s);
+cudaError_t launch_gemm_bn192_half_a(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
+                                     const KernelParams &p, bool f8, int grid, cudaStream_t s);
 TG_DECLARE_LAUNCH(192)
 TG_DECLARE_LAUNCH(256)
 #undef TG_DECLARE_LAUNCH

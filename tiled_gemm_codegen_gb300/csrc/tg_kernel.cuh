@@ -403,12 +403,15 @@ __device__ __forceinline__ void apply_epilogue(const KernelParams &p, uint32_t (
 // scale columns; the j-th K = 64 MMA reads block j / 2, bytes 2 (j % 2) and
 // 2 (j % 2) + 1 of each cell.  Two accumulators and the scales then fit
 // 2 x 224 + 2 x 24 columns with a two-slot ring at width 224.
-template <int BN, int STAGES, bool PAIR, bool F8 = false, bool MX = false, bool FP4 = false>
+// HALF_A (outputs of at most 64 rows, one CTA per tile): ring slots of 64
+// rows of A (Geometry), loaded as one 64-row box; the MMAs are unchanged.
+template <int BN, int STAGES, bool PAIR, bool F8 = false, bool MX = false, bool FP4 = false, bool HALF_A = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const KernelParams p)
 {
-    using G = Geometry<BN, PAIR>;
+    using G = Geometry<BN, PAIR, HALF_A>;
+    static_assert(!HALF_A || (!PAIR && !MX), "half-height A slots: one CTA per tile");
     // widths that are not a multiple of 64 only with K-major 8-bit B (one box)
     static_assert((BN % 64 == 0 || (F8 && BN % 32 == 0)) && BN >= 64 && BN <= 256, "tile width");
     static_assert(!PAIR || G::B_COLS % 64 == 0, "two-SM tiles need 64-column halves of B");
@@ -587,8 +590,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             load(a_dst, &tmA, kb * KBLK, m_rows, zA);
                         } else {
                             // A column-major: two boxes [64 k x 64 rows], MN-major atoms
+                            // (HALF_A: the first only)
                             load(a_dst, &tmA, m_rows, kb * KBLK, zA);
-                            load(a_dst + B_BOX_BYTES, &tmA, m_rows + 64, kb * KBLK, zA);
+                            if constexpr (!HALF_A) load(a_dst + B_BOX_BYTES, &tmA, m_rows + 64, kb * KBLK, zA);
                         }
                         if (!p.b_k) {
                             // B row-major: boxes [64 k x 64 columns], MN-major atoms
@@ -1044,14 +1048,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (threadIdx.x == 0) stamp(7);
 }
 
-template <int BN, int STAGES, bool PAIR, bool F8 = false, bool MX = false, bool FP4 = false>
+template <int BN, int STAGES, bool PAIR, bool F8 = false, bool MX = false, bool FP4 = false, bool HALF_A = false>
 cudaError_t launch_fixed(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
                          const KernelParams &p, int grid, cudaStream_t s)
 {
     constexpr int smem = MX ? Geometry<BN, PAIR>::smem_bytes_mx(STAGES, FP4 ? 2 : 1)
-                            : Geometry<BN, PAIR>::smem_bytes(STAGES);
+                            : Geometry<BN, PAIR, HALF_A>::smem_bytes(STAGES);
     static_assert(smem <= SMEM_LIMIT, "shared memory budget");
-    auto kern = gemm_kernel<BN, STAGES, PAIR, F8, MX, FP4>;
+    auto kern = gemm_kernel<BN, STAGES, PAIR, F8, MX, FP4, HALF_A>;
     // the shared-memory opt-in is per device; set it once per device
     static std::atomic<unsigned long long> configured{0};
     int dev = 0;

@@ -92,6 +92,17 @@ cudaError_t launch_gemm_mx224(const CUtensorMap &ta, const CUtensorMap &tb, cons
 }
 #endif
 
+#if TG_BN == 128 || TG_BN == 192
+cudaError_t TG_CAT(TG_CAT(launch_gemm_bn, TG_BN), _half_a)(const CUtensorMap &ta, const CUtensorMap &tb,
+                                                          const CUtensorMap &tc, const KernelParams &p, bool f8,
+                                                          int grid, cudaStream_t s)
+{
+    constexpr int S = half_a_stages(TG_BN);
+    if (f8) return launch_fixed<TG_BN, S, false, true, false, false, true>(ta, tb, tc, p, grid, s);
+    return launch_fixed<TG_BN, S, false, false, false, false, true>(ta, tb, tc, p, grid, s);
+}
+#endif
+
 int TG_CAT(max_pairs_bn, TG_BN)(int stages, bool f8)
 {
     if (f8) {

@@ -47,6 +47,11 @@ constexpr bool stage_supported(int bn, int s, bool pair = false, bool f8 = false
     }
 }
 
+// Outputs of at most 64 rows (one CTA per tile, bf16 or unscaled 8-bit):
+// ring slots of 64 rows of A, as deep as shared memory allows - 8 slots at
+// width 128, 6 at width 192 (0: no such instance).
+constexpr int half_a_stages(int bn) { return bn == 128 ? 8 : bn == 192 ? 6 : 0; }
+
 // Block-scaled operands: one-CTA tiles of widths 128, 192 and 224, rings 2
 // and 4; with packed 4-bit elements (fp4) the 224-wide tiles ring 2 only
 // (every slot's scales take twice the tensor-memory columns).
@@ -77,6 +82,8 @@ static_assert(stage_supported(192, max_stages(192)), "deepest ring of BN=192 ins
 static_assert(stage_supported(256, max_stages(256)), "deepest ring of BN=256 instantiated");
 static_assert(stage_supported(128, max_stages(128, true), true), "deepest pair ring of BN=128");
 static_assert(stage_supported(256, max_stages(256, true), true), "deepest pair ring of BN=256");
+static_assert(Geometry<128, false, true>::smem_bytes(8) <= SMEM_LIMIT, "half-height A ring, width 128");
+static_assert(Geometry<192, false, true>::smem_bytes(6) <= SMEM_LIMIT, "half-height A ring, width 192");
 
 template <bool PAIR>
 constexpr int smem_bytes_t(int bn, int stages)
@@ -113,6 +120,7 @@ struct PlanInput {
     bool f8 = false;                  // 8-bit floating-point A and B (K-major)
     bool mx = false;                  // f8 with per-32-element E8M0 block scales
     bool fp4 = false;                 // mx with packed 4-bit elements (K, lda, ldb in bytes)
+    bool half_a_ok = true;            // M <= 64 may use slots of 64 rows of A
 };
 
 struct Plan {
@@ -120,6 +128,7 @@ struct Plan {
     bool f8 = false;    // 8-bit operands: 128 elements of K per k-block
     bool mx = false;    // block-scaled 8-bit operands
     bool fp4 = false;   // block-scaled packed 4-bit operands (a k-block: 256 elements)
+    bool half_a = false;  // ring slots of 64 rows of A (M <= 64, one CTA per tile)
     int bn = 0, stages = 0;
     int tiles_m = 0, tiles_n = 0, k_blocks = 0, splits = 1;
     int64_t units = 0;
@@ -410,6 +419,12 @@ inline bool make_plan(const PlanInput &in, Plan &out)
     if (in.mx) {
         if (in.stages != 0 && !mx_stage_supported(p.bn, in.stages, p.pair, in.fp4)) return false;
         p.stages = in.stages != 0 ? in.stages : (mx_stage_supported(p.bn, 4, p.pair, in.fp4) ? 4 : 2);
+    } else if (in.half_a_ok && in.M <= BM / 2 && !p.pair && half_a_stages(p.bn) != 0 &&
+               (in.stages == 0 || in.stages == half_a_stages(p.bn))) {
+        // at most 64 rows: half-height A slots, half again as many of them
+        // (the ring then keeps ~50% more of B in flight)
+        p.half_a = true;
+        p.stages = half_a_stages(p.bn);
     } else if (in.stages != 0) {
         if (!stage_supported(p.bn, in.stages, p.pair, in.f8)) return false;
         p.stages = in.stages;
@@ -445,7 +460,9 @@ inline bool make_plan(const PlanInput &in, Plan &out)
     p.pack_b = in.force_pack || !in.b_tma_ok;
     if (in.epilogue == 1 && !in.c_tma_ok) return false;
     p.epilogue = in.epilogue != 0 ? in.epilogue : (in.c_tma_ok ? 1 : 2);
-    p.smem = smem_bytes_for(p.bn, p.stages, p.pair);
+    p.smem = p.half_a ? (p.bn == 128 ? Geometry<128, false, true>::smem_bytes(p.stages)
+                                     : Geometry<192, false, true>::smem_bytes(p.stages))
+                      : smem_bytes_for(p.bn, p.stages, p.pair);
     p.tmem = tmem_cols_for(p.bn);
     if (p.mx) {
         const int halves = p.fp4 ? 2 : 1;
