@@ -81,6 +81,9 @@ typedef enum tg_status {
 typedef struct tg_options {
     int32_t block_n;     /* output tile width: 64, 128, 192 or 256            */
     int32_t stages;      /* shared-memory ring depth, 2 .. the tile's maximum */
+                         /* (outputs of at most 64 rows: 8 at width 128 and  */
+                         /* 6 at width 192 select rings of 64-row A slots,   */
+                         /* the planner's own choice there)                  */
     int32_t split_k;     /* K splits per output tile (1 = none)               */
     int32_t force_pack;  /* nonzero: copy A and B through the pack pass       */
     int32_t epilogue;    /* 1 = tensor-memory-accelerator stores, 2 = plain   */
@@ -120,7 +123,9 @@ typedef struct tg_options {
 
 /* What the planner chose (tg_plan output). */
 typedef struct tg_plan_info {
-    int32_t block_m, block_n, block_k, stages;
+    int32_t block_m, block_n, block_k, stages;  /* block_m: rows of A a tile     */
+                         /* loads - 128, 256 for two-SM tiles, 64 for rings  */
+                         /* of 64-row A slots (outputs of at most 64 rows)   */
     int32_t tiles_m, tiles_n, k_blocks, split_k;
     int64_t num_units;   /* batch * tiles_m * tiles_n * split_k                */
     int32_t grid;        /* persistent CTAs launched                          */
@@ -310,7 +315,8 @@ tg_status tg_gemm_host(const void *A_host, const void *B_host, float *C_host,
 
 /* Run-time plan search (a tuner): times candidate plans for these arguments
  * on the caller's buffers and stream - every instantiated tile width, one
- * CTA or two-SM tiles, the two deepest ring depths, stream-K on and off,
+ * CTA or two-SM tiles, the two deepest ring depths (for outputs of at most
+ * 64 rows also the rings of 64-row A slots), stream-K on and off,
  * and split-K factors where there are fewer tiles than SMs - each `reps`
  * times (1..100) with CUDA events, and returns the fastest (median) as
  * options in *best (the layout fields and other fields of `base` kept; base

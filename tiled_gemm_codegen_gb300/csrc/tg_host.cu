@@ -1012,7 +1012,9 @@ TG_API tg_status tg_tune(const void *A, const void *B, float *C, int64_t M, int6
             const bool pair = pr == 2;
             if (pair && !pair_width(widths[wi])) continue;
             for (int di = 0; di < 5 && st == TG_OK; ++di) {
-                if (!stage_supported(widths[wi], depths[di], pair)) continue;
+                // outputs of at most 64 rows also have rings of 64-row A slots
+                const bool half_a = !pair && a.M <= BM / 2 && depths[di] == half_a_stages(widths[wi]);
+                if (!stage_supported(widths[wi], depths[di], pair) && !half_a) continue;
                 for (int si = 0; si < 6 && st == TG_OK; ++si) {
                     for (int sk = 1; sk <= 2 && st == TG_OK; ++sk) {
                         if (sk == 2 && splits[si] > 1) continue;
