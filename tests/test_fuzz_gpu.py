@@ -55,9 +55,34 @@ def _place(t, rows, cols, ld, off, stride, batch):
     return d, torch.as_strided(d, (batch, rows, cols), (stride, ld, 1), off)
 
 
+def _case_short(i):
+    """Outputs of at most 64 rows (the planner's rings of 64-row A slots at
+    widths 128 and 192), with long N and K."""
+    r = random.Random(9000 + i)
+    M, N, K = r.randint(1, 64), r.randint(1, 3000), r.randint(1, 3000)
+    opts = {}
+    bn = r.choice([0, 128, 128, 192, 192])
+    if bn:
+        opts["block_n"] = bn
+    kb = (K + 63) // 64
+    if r.random() < 0.3 and kb > 1:
+        opts["split_k"] = r.randint(2, min(8, kb))
+    return dict(M=M, N=N, K=K, batch=r.choice([1, 1, 2, 4]), a_cm=r.random() < 0.3, b_cm=r.random() < 0.3,
+                opts=opts, a_pad=r.choice([0, 0, 1, 8]), b_pad=r.choice([0, 0, 3, 8]), c_pad=r.choice([0, 0, 5, 4]),
+                a_off=r.choice([0, 0, 1, 4]), seed=r.randint(0, 10 ** 6))
+
+
 @pytest.mark.parametrize("i", range(N_CASES))
 def test_random_exact_cases(i):
-    c = _case(i)
+    _run_exact_case(_case(i))
+
+
+@pytest.mark.parametrize("i", range(30))
+def test_random_short_outputs(i):
+    _run_exact_case(_case_short(i))
+
+
+def _run_exact_case(c):
     M, N, K, batch = c["M"], c["N"], c["K"], c["batch"]
     A, B = synth.make_int_inputs(batch, M, N, K, seed=c["seed"])
     A3 = A.reshape(batch, M, K)
