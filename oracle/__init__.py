@@ -16,9 +16,11 @@ Contents
   pattern on the host.
 
 Parity status: every function here is pinned by ``tests/test_oracle.py`` and
-``tests/test_layout.py`` (brute force, closed forms, page tables).  The
-end-to-end float values of random-input GEMMs are "parity unpinned" beyond the
-tolerance, because the pages print no numeric GEMM result.
+``tests/test_layout.py``: brute force (exact rational sums of integer and of
+random bf16 inputs, the latter within the textbook fp64 summation bound),
+closed forms, invariants and planted mistakes for the GEMM, and the pages'
+printed tables for the layout calculus.  The pages print no numeric GEMM
+result, so no GEMM pin is a page value.
 """
 from __future__ import annotations
 
