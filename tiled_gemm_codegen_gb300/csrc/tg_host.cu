@@ -400,7 +400,7 @@ struct Workspace {
     size_t host_cap = 0;
     // tg_gemm_host's copy streams and events (created on first use)
     cudaStream_t h2d = nullptr, d2h = nullptr;
-    static constexpr int HOST_EVENTS = 1 + 3 * 8;
+    static constexpr int HOST_EVENTS = 1 + 3 * HOST_MAX_PIECES;
     cudaEvent_t ev[HOST_EVENTS] = {};
 };
 

@@ -510,10 +510,13 @@ struct HostPieces {
     }
 };
 
+// Most pieces of the host-buffer pipeline (it keeps three events a piece).
+constexpr int HOST_MAX_PIECES = 8;
+
 inline HostPieces host_pieces(int64_t M, int64_t N, int64_t K, int64_t batch, bool a_bcast, bool b_bcast,
                               bool a_cm, bool b_cm, bool a_stacked, bool b_stacked)
 {
-    constexpr int MAX_PIECES = 8;
+    constexpr int MAX_PIECES = HOST_MAX_PIECES;
     constexpr int64_t PIECE_MIN = 512;
     HostPieces h;
     if (K == 0 || M == 0 || N == 0) return h;
