@@ -470,3 +470,27 @@ def test_plan_rules_for_every_operand_family():
     assert (p["block_n"], p["cta_pair"]) == (256, 2)                 # 32 k-blocks
     assert tg.plan(4096, 160, 4096, sm_count=152)["cta_pair"] == 1
     assert tg.plan(4096, 160, 4096, sm_count=152, options=tg.make_options(cta_pair=2))["cta_pair"] == 2
+
+
+def test_plan_half_height_a_rings():
+    """Outputs of at most 64 rows take 64-row A slots (8 at width 128, 6 at
+    width 192) when the ring depth is the planner's or that one; an explicit
+    other depth, two-SM tiles, widths without such an instance and outputs
+    of more than 64 rows keep the 128-row slots."""
+    def P(M, N=4096, K=4096, ops="bf16", **kw):
+        return tg.plan(M, N, K, sm_count=152, operands=ops, options=tg.make_options(**kw) if kw else None)
+    for ops in ("bf16", "fp8"):
+        for bn, s in ((128, 8), (192, 6)):
+            for M in (1, 33, 64):
+                p = P(M, ops=ops, block_n=bn)
+                assert (p["block_m"], p["stages"]) == (64, s), (ops, bn, M, p)
+                p = P(M, ops=ops, block_n=bn, stages=s)
+                assert p["block_m"] == 64
+                p = P(M, ops=ops, block_n=bn, stages=4)
+                assert (p["block_m"], p["stages"]) == (128, 4)
+            assert P(65, ops=ops, block_n=bn)["block_m"] == 128
+        assert P(64, ops=ops, block_n=256)["block_m"] == 128
+    assert P(64, block_n=64)["block_m"] == 128
+    assert P(64, block_n=128, cta_pair=2)["block_m"] == 256
+    # block-scaled operands keep their own rings
+    assert P(64, ops="mxfp8")["block_m"] == 128
