@@ -143,32 +143,41 @@ def _stream_ptr(stream):
     return stream.cuda_stream
 
 
-def _operand_geometry(t, rows_dim, what):
-    """(ptr, rows, cols, ld, batch, batch_stride) of a 2-D or 3-D tensor
-    whose last dim has unit stride."""
-    if t.dim() not in (2, 3):
+def _geometry(t, shape, st, what):
+    """_operand_geometry on the tensor's shape and strides, read once (each
+    read is a call into the framework)."""
+    nd = len(shape)
+    if nd not in (2, 3):
         raise ValueError(f"{what} must be 2-D or 3-D")
-    if t.stride(-1) != 1 and t.size(-1) > 1:
+    rows, cols = shape[-2], shape[-1]
+    if st[-1] != 1 and cols > 1:
         raise ValueError(f"{what} must have unit stride in its last dimension")
-    rows, cols = t.shape[-2], t.shape[-1]
-    ld = t.stride(-2) if rows > 1 else max(cols, 1)
-    if t.dim() == 3:
-        batch, sb = t.shape[0], (t.stride(0) if t.shape[0] > 1 else 0)
+    ld = st[-2] if rows > 1 else max(cols, 1)
+    if nd == 3:
+        batch, sb = shape[0], (st[0] if shape[0] > 1 else 0)
     else:
         batch, sb = 1, 0
     return t.data_ptr(), rows, cols, max(ld, cols), batch, sb
+
+
+def _operand_geometry(t, rows_dim, what):
+    """(ptr, rows, cols, ld, batch, batch_stride) of a 2-D or 3-D tensor
+    whose last dim has unit stride."""
+    return _geometry(t, t.shape, t.stride(), what)
 
 
 def _operand(t, what):
     """(ptr, rows, cols, ld, batch, batch_stride, col_major) of a logical
     rows x cols operand: row-major when its last dim has unit stride,
     column-major (a transposed view) when its second-last dim has."""
-    rows, cols = t.shape[-2], t.shape[-1]
-    if t.dim() in (2, 3) and cols > 1 and t.stride(-1) != 1 and (t.stride(-2) == 1 or rows == 1):
-        ld = max(t.stride(-1), rows, 1)
-        batch, sb = (t.shape[0], t.stride(0) if t.shape[0] > 1 else 0) if t.dim() == 3 else (1, 0)
+    shape, st = t.shape, t.stride()
+    nd = len(shape)
+    rows, cols = shape[-2], shape[-1]
+    if nd in (2, 3) and cols > 1 and st[-1] != 1 and (st[-2] == 1 or rows == 1):
+        ld = max(st[-1], rows, 1)
+        batch, sb = (shape[0], st[0] if shape[0] > 1 else 0) if nd == 3 else (1, 0)
         return t.data_ptr(), rows, cols, ld, batch, sb, True
-    return (*_operand_geometry(t, -2, what), False)
+    return (*_geometry(t, shape, st, what), False)
 
 
 def _with_layout(options, a_cm, b_cm):
