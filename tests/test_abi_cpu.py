@@ -192,28 +192,40 @@ def test_stream_k_schedule_covers_every_k_block_once(lib):
     def owner(x, W, L):
         return min(W - 1, ((x + 1) * W - 1) // L)
 
-    for tiles, kb, W in [(256, 64, 76), (64, 32, 7), (10, 1, 7), (5, 3, 16), (29, 65, 4)]:
+    for tiles, kb, W in [(256, 64, 76), (64, 32, 7), (10, 1, 7), (5, 3, 16), (29, 65, 4), (96, 64, 76),
+                         (176, 64, 76), (272, 65, 76), (1024, 128, 76), (80, 3, 76)]:
         if tiles % W == 0:
             continue
         dp = tiles // W
         sk_tiles = tiles - dp * W
         L = sk_tiles * kb
-        cover = {}
+        # the shared tiles cut into P >= 2 equal parts when they fit, else
+        # an even split over all workers
+        P = min(W // sk_tiles, kb)
+        SW = P * sk_tiles if P >= 2 else W
+        cover, units = {}, {}
         for w in range(W):
             for i in range(dp):
                 t = w + i * W
                 for k in range(kb):
                     cover[(t, k)] = cover.get((t, k), 0) + 1
-            pos, end = w * L // W, (w + 1) * L // W
+            pos, end = (w * L // SW, (w + 1) * L // SW) if w < SW else (0, 0)
             while pos < end:
                 ts = pos // kb
                 e = min(end, (ts + 1) * kb)
-                first, last = owner(ts * kb, W, L), owner((ts + 1) * kb - 1, W, L)
+                first, last = owner(ts * kb, SW, L), owner((ts + 1) * kb - 1, SW, L)
                 assert first <= w <= last
+                units[w] = units.get(w, 0) + 1
                 for k in range(pos - ts * kb, e - ts * kb):
                     cover[(dp * W + ts, k)] = cover.get((dp * W + ts, k), 0) + 1
                 pos = e
         assert len(cover) == tiles * kb and set(cover.values()) == {1}
+        if P >= 2:
+            assert set(units.values()) == {1}  # no range crosses a tile
+        if tiles > W:  # (with fewer tiles than SMs the grid shrinks to the tiles)
+            p = tg.plan(128 * tiles, 64, 64 * kb, sm_count=W,
+                        options=tg.make_options(block_n=64, cta_pair=1, stream_k=2))
+            assert p["sk_tiles"] == sk_tiles
 
 
 def test_plan_stream_k_overrides(lib):
@@ -306,11 +318,14 @@ def test_mxfp8_rejects_bad_arguments_before_any_cuda_call(lib):
 def test_plan_8bit_and_block_scaled_choices(lib):
     """tg_plan with opt->operands: the 8-bit planner's measured choices
     (two-SM 256-wide tiles for long K and a full wave, one CTA otherwise,
-    192 wide on the skinny shape, no stream-K by default) and the
+    192 wide on the skinny shape, stream-K only with the shared tiles cut
+    into parts and 32 k-blocks or more) and the
     block-scaled widths (224 where tensor memory allows, 192 on the skinny
     shape), host-only."""
     p = tg.plan(4096, 4096, 4096, sm_count=152, operands="fp8")
-    assert (p["block_n"], p["cta_pair"], p["stream_k"], p["block_k"]) == (256, 2, 1, 128)
+    # stream-K with the 28 shared tiles cut in two (32 k-blocks of 128)
+    assert (p["block_n"], p["cta_pair"], p["stream_k"], p["block_k"], p["sk_tiles"]) == (256, 2, 2, 128, 28)
+    assert tg.plan(4096, 4096, 2048, sm_count=152, operands="fp8")["stream_k"] == 1  # 16 k-blocks
     assert tg.plan(8192, 8192, 8192, sm_count=152, operands="fp8")["cta_pair"] == 2
     assert tg.plan(4096, 4096, 1024, sm_count=152, operands="fp8")["cta_pair"] == 1   # short K
     assert tg.plan(2048, 2048, 2048, sm_count=152, operands="fp8")["cta_pair"] == 1   # under a wave

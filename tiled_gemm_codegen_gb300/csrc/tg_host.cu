@@ -858,6 +858,7 @@ tg_status run_gemm(const Args &a, cudaStream_t stream, const tg_options *opt,
     p.dp_waves = plan.dp_waves;
     p.sk_first_tile = static_cast<int32_t>(plan.sk_first_tile);
     p.sk_iters = plan.sk_iters;
+    p.sk_workers = plan.sk_workers;
     p.maxparts = plan.maxparts;
     p.err = w.err;
     p.timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : DEFAULT_TIMEOUT_NS;

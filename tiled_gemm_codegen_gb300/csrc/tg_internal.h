@@ -70,6 +70,9 @@ struct KernelParams {
     int32_t sk_first_tile;
     int32_t maxparts;
     int64_t sk_iters;
+    // Workers that take a stream-K range: P * sk_tiles when each shared tile
+    // is cut into P >= 2 equal parts (each range inside one tile), else all.
+    int32_t sk_workers;
     unsigned long long *trace;  // grid x 8 timestamps, or null
     uint32_t mma_fmt;           // 8-/4-bit operands: A format << 7 | B format << 10
     // Block-scaled operands: E8M0 scales pre-arranged in 512-byte blocks,

@@ -122,7 +122,9 @@ __device__ __forceinline__ void decode_tile(const KernelParams &p, int64_t t, Un
 //    split reduction).
 //  - stream-K: first the worker's contiguous range of the stream-K tiles'
 //    k-blocks, cut at tile boundaries (the parts of a tile are numbered by
-//    the order of their k ranges), then its dp_waves whole tiles.  Shared
+//    the order of their k ranges), then its dp_waves whole tiles.  Only the
+//    first sk_workers workers take a range: with P * sk_tiles of them every
+//    shared tile is cut into P equal parts and no range crosses a tile.  Shared
 //    tiles come first so that their partial writes and combines run in the
 //    epilogue while the MMA works on the whole tiles.
 struct WorkIter {
@@ -134,8 +136,10 @@ __device__ __forceinline__ void work_begin(const KernelParams &p, int64_t worker
                                            WorkIter &it)
 {
     it.i = 0;
-    it.sk_pos = p.stream_k ? worker * p.sk_iters / workers : 0;
-    it.sk_end = p.stream_k ? (worker + 1) * p.sk_iters / workers : 0;
+    // workers past sk_workers have no stream-K range
+    const int64_t sw = p.sk_workers;
+    it.sk_pos = (p.stream_k && worker < sw) ? worker * p.sk_iters / sw : 0;
+    it.sk_end = (p.stream_k && worker < sw) ? (worker + 1) * p.sk_iters / sw : 0;
 }
 
 // The worker whose stream-K range holds position x (ranges may be empty).
@@ -170,8 +174,8 @@ __device__ __forceinline__ bool work_next(const KernelParams &p, int64_t worker,
         decode_tile(p, p.sk_first_tile + ts, w);
         w.kb0 = static_cast<int32_t>(it.sk_pos - ts * KB);
         w.kb1 = static_cast<int32_t>(end - ts * KB);
-        const int64_t first = sk_owner(p, ts * KB, workers);
-        const int64_t last = sk_owner(p, tile_end - 1, workers);
+        const int64_t first = sk_owner(p, ts * KB, p.sk_workers);
+        const int64_t last = sk_owner(p, tile_end - 1, p.sk_workers);
         w.nparts = static_cast<int32_t>(last - first + 1);
         w.part = static_cast<int32_t>(worker - first);
         w.slot = ts;

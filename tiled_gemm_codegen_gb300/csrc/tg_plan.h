@@ -139,7 +139,7 @@ struct Plan {
     int group_m = 8;
     // stream-K schedule (see KernelParams)
     bool stream_k = false;
-    int dp_waves = 0, maxparts = 1;
+    int dp_waves = 0, maxparts = 1, sk_workers = 0;
     int64_t sk_first_tile = 0, sk_tiles = 0, sk_iters = 0;
     int64_t ws_pack_a = 0, ws_pack_b = 0, ws_partials = 0, ws_counters = 0;
     // block-scaled operands: the scales re-arranged into 512-byte blocks
@@ -163,11 +163,17 @@ inline int64_t pack_pitch(int64_t cols) { return round_up(cols, 64); }
 
 // Stream-K schedule of `tiles` tiles of `kb` k-blocks on `workers` workers:
 // whole tiles for dp_waves full waves, then the remaining sk_tiles tiles'
-// k-blocks split into `workers` contiguous ranges.  maxparts = the largest
-// number of ranges one tile meets (its partial slots).  Returns false when
-// the last wave is already full (nothing to balance).
+// k-blocks split into sk_workers contiguous ranges.  When P = workers /
+// sk_tiles is at least 2, sk_workers = P * sk_tiles: every shared tile is cut
+// into P equal parts and no range crosses a tile (each of those workers has
+// one partial unit); otherwise all workers share the k-blocks evenly.
+// Measured on GB300 against the even split over all workers: 4096^3 81.9 ->
+// 79.9 us, 4096 x 1536 x 4096 49.2 -> 41.0, 4096 x 2816 x 4096 61.4 -> 59.4,
+// 8192^3 501.8 -> 499.7; E4M3 4096^3 65.5 -> 53.3 (55.3 without stream-K).
+// maxparts = the largest number of ranges one tile meets (its partial
+// slots).  Returns false when the last wave is already full.
 struct SkSchedule {
-    int dp_waves = 0, maxparts = 1;
+    int dp_waves = 0, maxparts = 1, sk_workers = 0;
     int64_t sk_first_tile = 0, sk_tiles = 0, sk_iters = 0;
 };
 
@@ -185,10 +191,12 @@ inline bool sk_schedule(int64_t tiles, int64_t kb, int64_t workers, SkSchedule &
     s.sk_first_tile = static_cast<int64_t>(s.dp_waves) * workers;
     s.sk_tiles = tiles - s.sk_first_tile;
     s.sk_iters = s.sk_tiles * kb;
+    const int64_t parts = std::min<int64_t>(workers / s.sk_tiles, kb);
+    s.sk_workers = static_cast<int>(parts >= 2 ? parts * s.sk_tiles : workers);
     int maxp = 1;
     for (int64_t ts = 0; ts < s.sk_tiles; ++ts) {
-        const int64_t first = sk_owner_host(ts * kb, workers, s.sk_iters);
-        const int64_t last = sk_owner_host((ts + 1) * kb - 1, workers, s.sk_iters);
+        const int64_t first = sk_owner_host(ts * kb, s.sk_workers, s.sk_iters);
+        const int64_t last = sk_owner_host((ts + 1) * kb - 1, s.sk_workers, s.sk_iters);
         maxp = std::max<int>(maxp, static_cast<int>(last - first + 1));
     }
     s.maxparts = maxp;
@@ -231,10 +239,14 @@ inline double plan_cost_ns(const PlanInput &in, int bn, bool pair, int splits, i
     const int64_t units = tiles * splits;
     double t_mma = 0.0, partial = 0.0;
     if (stream_k) {
-        // whole waves, then an even share of the remaining k-blocks
+        // whole waves, then the busiest share of the remaining k-blocks:
+        // a P-th of a tile when they are cut into P >= 2 parts a tile
+        // (sk_schedule), else an even share over all workers
         const int64_t dp = tiles / workers;
-        const int64_t sk_iters = (tiles - dp * workers) * k_blocks;
-        t_mma = (static_cast<double>(dp * k_blocks) + static_cast<double>(ceil_div(sk_iters, workers))) * kb_ns;
+        const int64_t sk_tiles = tiles - dp * workers;
+        const int64_t parts = sk_tiles > 0 ? std::min<int64_t>(workers / sk_tiles, k_blocks) : 0;
+        const int64_t share = parts >= 2 ? ceil_div(k_blocks, parts) : ceil_div(sk_tiles * k_blocks, workers);
+        t_mma = (static_cast<double>(dp * k_blocks) + static_cast<double>(share)) * kb_ns;
         partial = 2.0 * 4.0 * (pair ? 2 : 1) * BM * bn * 2.0 * static_cast<double>(tiles - dp * workers);
     } else {
         const int64_t waves = ceil_div(units, workers);
@@ -282,6 +294,7 @@ inline void replan_stream_k(const PlanInput &in, Plan &p, int grid)
         p.sk_tiles = sk.sk_tiles;
         p.sk_iters = sk.sk_iters;
         p.maxparts = sk.maxparts;
+        p.sk_workers = sk.sk_workers;
     } else {
         p.stream_k = false;
         p.maxparts = p.splits;
@@ -391,13 +404,18 @@ inline bool make_plan(const PlanInput &in, Plan &out)
             for (int sk = 0; sk < 2; ++sk) {
                 const bool use_sk = sk == 1;
                 if (use_sk && (s > 1 || in.stream_k == 1 || tiles % workers == 0)) continue;
-                // 8-bit operands: stream-K only on request (its partial-tile
-                // traffic outweighs the balance at the measured sizes)
-                if (use_sk && in.f8 && in.stream_k != 2) continue;
-                // bf16: stream-K pays for its partial tiles only with enough
-                // k-blocks per tile (measured: 64 k-blocks 90 -> 84 us with
-                // it; 32 k-blocks 55.2 -> 63.5 and 88.1 -> 96.3 us with it)
-                if (use_sk && in.stream_k != 2 && p.k_blocks < 48) continue;
+                // stream-K pays for its partial tiles only with enough
+                // k-blocks per tile.  bf16 (measured with the even split: 64
+                // k-blocks 90 -> 84 us with it; 32 k-blocks 55.2 -> 63.5 and
+                // 88.1 -> 96.3 us with it): at least 48.  8-bit operands
+                // (E4M3 4096^3, 32 k-blocks: 55.3 without, 65.5 with the even
+                // split, 53.3 with the shared tiles cut in two): at least 32,
+                // and only when the shared tiles are cut into parts
+                if (use_sk && in.stream_k != 2) {
+                    const int64_t sk_tiles = tiles % workers;
+                    const bool cut = sk_tiles > 0 && workers / sk_tiles >= 2;
+                    if (in.f8 ? (p.k_blocks < 32 || !cut) : p.k_blocks < 48) continue;
+                }
                 if (!use_sk && in.stream_k == 2 && tiles % workers != 0) continue;
                 const double c = plan_cost_ns(in, cd.bn, cd.pair, s, p.k_blocks, tiles, sms, use_sk);
                 if (!have || c < best * 0.999) {
@@ -452,6 +470,7 @@ inline bool make_plan(const PlanInput &in, Plan &out)
             p.sk_tiles = sk.sk_tiles;
             p.sk_iters = sk.sk_iters;
             p.maxparts = sk.maxparts;
+            p.sk_workers = sk.sk_workers;
         }
     }
     if (!p.stream_k) p.maxparts = p.splits;
