@@ -437,12 +437,13 @@ def test_checks_build_loads_and_plans_host_only():
 
 def test_plan_rules_from_the_tuner_sweep():
     """The planner's measured rules (default plan against the run-time
-    tuner's best on GB300): no stream-K with few k-blocks, no two-SM tiles
+    tuner's best on GB300): no stream-K with short partial units, no two-SM tiles
     when their rows would be half padding or a tile has few k-blocks, no
     tile twice as wide as N - and the five workloads keep their plans."""
     def P(M, N, K, b=1):
         return tg.plan(M, N, K, b, sm_count=152)
-    assert P(2048, 8192, 2048)["stream_k"] == 1          # 32 k-blocks
+    assert P(2048, 8192, 2048)["stream_k"] == 2          # 32 k-blocks, shared tiles in halves
+    assert P(4096, 1536, 2048)["stream_k"] == 1          # in thirds: parts of 10 k-blocks
     assert P(4096, 4096, 4096)["stream_k"] == 2          # 64 k-blocks
     assert P(128, 4096, 4096)["cta_pair"] == 1           # M = 128
     assert P(512, 512, 512, 32)["cta_pair"] == 1         # 8 k-blocks a tile

@@ -404,17 +404,19 @@ inline bool make_plan(const PlanInput &in, Plan &out)
             for (int sk = 0; sk < 2; ++sk) {
                 const bool use_sk = sk == 1;
                 if (use_sk && (s > 1 || in.stream_k == 1 || tiles % workers == 0)) continue;
-                // stream-K pays for its partial tiles only with enough
-                // k-blocks per tile.  bf16 (measured with the even split: 64
-                // k-blocks 90 -> 84 us with it; 32 k-blocks 55.2 -> 63.5 and
-                // 88.1 -> 96.3 us with it): at least 48.  8-bit operands
-                // (E4M3 4096^3, 32 k-blocks: 55.3 without, 65.5 with the even
-                // split, 53.3 with the shared tiles cut in two): at least 32,
-                // and only when the shared tiles are cut into parts
+                // stream-K pays for its partial units only when they are
+                // long enough.  Shared tiles cut into P >= 2 parts: at least
+                // 16 k-blocks a part (bf16 2048 x 8192 x 2048, 32 k-blocks in
+                // halves: 55.3 -> 51.2 us; 4096 x 1536 x 2048 in thirds:
+                // 32.8 -> 34.8; E4M3 4096^3 in halves: 55.3 -> 53.3).  An
+                // even split over all workers: bf16 with at least 48 k-blocks
+                // a tile (64: 90 -> 84 us; 32: 55.2 -> 63.5 and 88.1 -> 96.3),
+                // never for 8-bit operands (E4M3 4096^3: 55.3 -> 65.5).
                 if (use_sk && in.stream_k != 2) {
                     const int64_t sk_tiles = tiles % workers;
-                    const bool cut = sk_tiles > 0 && workers / sk_tiles >= 2;
-                    if (in.f8 ? (p.k_blocks < 32 || !cut) : p.k_blocks < 48) continue;
+                    const int64_t parts = sk_tiles > 0 ? std::min<int64_t>(workers / sk_tiles, p.k_blocks) : 0;
+                    const bool pays = parts >= 2 ? p.k_blocks / parts >= 16 : (!in.f8 && p.k_blocks >= 48);
+                    if (!pays) continue;
                 }
                 if (!use_sk && in.stream_k == 2 && tiles % workers != 0) continue;
                 const double c = plan_cost_ns(in, cd.bn, cd.pair, s, p.k_blocks, tiles, sms, use_sk);
