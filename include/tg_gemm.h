@@ -119,6 +119,16 @@ typedef struct tg_options {
                          /* A[b*strideA + k*lda + i], lda >= M)               */
     int32_t b_col_major; /* nonzero: B is stored N x K (element B_b[k][j] at   */
                          /* B[b*strideB + j*ldb + k], ldb >= K)               */
+    int32_t direct;      /* direct-load kernel for small problems: 0 = the    */
+                         /* planner decides, 1 = off, 2 = on (bf16 calls     */
+                         /* with no other override but the layouts; else     */
+                         /* TG_ERR_INVALID_ARG).  One CTA per 128 x 64 tile  */
+                         /* of C copies its operand tiles into shared memory */
+                         /* with plain loads (any pitch and alignment, so no */
+                         /* pack pass), up to 4 k-blocks at a time, and      */
+                         /* multiplies them with tcgen05.mma (OCANNL "Module */
+                         /* Ir.Schedule", Stage with a cooperative copy, and */
+                         /* Pad-to-tile)                                     */
 } tg_options;
 
 /* What the planner chose (tg_plan output). */
@@ -140,7 +150,10 @@ typedef struct tg_plan_info {
                          /* is then 256 and grid counts CTAs, 2 per cluster) */
     int32_t stream_k;    /* 1 = off, 2 = on                                  */
     int32_t sk_tiles;    /* tiles whose k-blocks are shared between workers  */
-    int32_t reserved[3];
+    int32_t direct;      /* 1 = persistent kernel, 2 = direct-load kernel    */
+                         /* (block 128 x 64, stages = k-blocks staged at     */
+                         /* once, grid = one CTA per tile)                   */
+    int32_t reserved[2];
 } tg_plan_info;
 
 /* The GEMM (see the header comment for the operation and conventions). */

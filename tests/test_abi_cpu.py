@@ -122,6 +122,16 @@ def _plan(w, **kw):
 def test_plan_of_each_workload(lib):
     for w in synth.WORKLOADS.values():
         info = _plan(w)
+        if info["direct"] == 2:
+            # small problem: the direct-load kernel, one CTA per 128 x 64 tile
+            assert w.name == "ragged_197x131x77"
+            assert (info["block_m"], info["block_n"], info["block_k"]) == (128, 64, 64)
+            assert info["grid"] == info["num_units"] == w.batch * -(-w.M // 128) * -(-w.N // 64)
+            assert info["stages"] == min(4, -(-w.K // 64)) and info["tmem_cols"] == 64
+            assert info["pack_a"] == info["pack_b"] == 0 and info["workspace_bytes"] == 0
+            assert info["epilogue"] == 2 and info["split_k"] == 1 and info["smem_bytes"] <= 232448
+            continue
+        assert info["direct"] == 1
         assert info["block_k"] == 64 and info["cta_pair"] in (1, 2)
         # outputs of at most 64 rows: ring slots of 64 rows of A
         assert info["block_m"] == (64 if w.M <= 64 and info["cta_pair"] == 1 else 128 * info["cta_pair"])
@@ -510,3 +520,46 @@ def test_plan_half_height_a_rings():
     assert P(64, block_n=128, cta_pair=2)["block_m"] == 256
     # block-scaled operands keep their own rings
     assert P(64, ops="mxfp8")["block_m"] == 128
+
+
+def test_direct_plan_fields_and_requests(lib):
+    """direct = 2 asks for the direct-load kernel: bf16 operands and no
+    override but the operand layouts; any other override with it is an
+    invalid request."""
+    d = tg.make_options(direct=2)
+    info = tg.plan(300, 200, 600, 3, sm_count=152, options=d)
+    assert info["direct"] == 2 and (info["block_m"], info["block_n"]) == (128, 64)
+    assert (info["tiles_m"], info["tiles_n"], info["k_blocks"]) == (3, 4, 10)
+    assert info["grid"] == info["num_units"] == 3 * 3 * 4 and info["stages"] == 4
+    assert info["tmem_cols"] == 64 and info["workspace_bytes"] == 0 and info["epilogue"] == 2
+    assert tg.plan(5, 5, 40, sm_count=152, options=d)["stages"] == 1
+    for extra in (dict(block_n=128), dict(stages=4), dict(split_k=2), dict(force_pack=1), dict(epilogue=1),
+                  dict(cta_pair=2), dict(stream_k=2), dict(max_ctas=8)):
+        with pytest.raises(tg.TgError):
+            tg.plan(300, 200, 600, sm_count=152, options=tg.make_options(direct=2, **extra))
+    with pytest.raises(tg.TgError):
+        tg.plan(300, 200, 600, sm_count=152, options=tg.make_options(direct=3))
+    with pytest.raises(tg.TgError):  # 8-bit operands
+        tg.plan(256, 256, 256, sm_count=152, operands="fp8", options=tg.make_options(direct=2))
+    # overrides the direct kernel shares are accepted
+    assert tg.plan(300, 200, 600, sm_count=152, options=tg.make_options(direct=2, block_n=64, split_k=1, cta_pair=1,
+                                                                      stream_k=1, epilogue=2))["direct"] == 2
+
+
+def test_direct_planner_rule(lib):
+    """The planner's own choice: at most one tile per SM, at most 2
+    k-blocks (operands TMA can address) or 5 (operands it cannot, which the
+    persistent kernel would first realign)."""
+    def direct(M, N, K, batch=1, lda=None, opts=None):
+        return tg.plan(M, N, K, batch, sm_count=152, lda=lda, options=opts)["direct"] == 2
+    assert direct(197, 131, 77)                    # odd pitches, 2 k-blocks
+    assert direct(129, 65, 257)                    # odd pitch, 5 k-blocks
+    assert not direct(100, 300, 500, lda=501)      # 8 k-blocks
+    assert direct(1000, 1000, 64)                  # 128 tiles, 1 k-block
+    assert direct(128, 128, 128)
+    assert not direct(256, 256, 256)               # 4 k-blocks, aligned
+    assert not direct(4096, 4096, 64)              # 2048 tiles
+    assert direct(64, 64, 64, 64)                  # 64 problems of one tile
+    assert not direct(128, 128, 128, opts=tg.make_options(block_n=64))  # an override: the persistent kernel
+    assert not direct(128, 128, 128, opts=tg.make_options(direct=1))
+    assert not direct(4096, 4096, 4096)

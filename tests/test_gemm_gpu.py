@@ -214,25 +214,30 @@ def test_misaligned_operands_use_pack(a_off, b_off, lda_pad, ldb_pad):
     A = ad[a_off:].view(M, lda)[:, :K]
     B = bd[b_off:].view(K, ldb)[:, :N]
     C = torch.empty(M, N, dtype=torch.float32, device=dev())
-    info = tg.plan(M, N, K, lda=lda, ldb=ldb, A=A.data_ptr(), B=B.data_ptr(), C=C.data_ptr())
+    # the persistent kernel (the planner would take the direct-load kernel
+    # for a problem this small)
+    opts = tg.make_options(direct=1)
+    info = tg.plan(M, N, K, lda=lda, ldb=ldb, A=A.data_ptr(), B=B.data_ptr(), C=C.data_ptr(), options=opts)
     assert info["pack_a"] == int(a_off % 8 != 0 or lda % 8 != 0)
     assert info["pack_b"] == int(b_off % 8 != 0 or ldb % 8 != 0)
-    tg.gemm(A, B, C)
+    tg.gemm(A, B, C, options=opts)
     assert tg.device_error() == tg.TG_OK
     assert np.array_equal(C.cpu().double().numpy(), oracle_dense(Ai, Bi))
 
 
+@pytest.mark.parametrize("direct", [1, 2], ids=["persistent", "direct"])
 @pytest.mark.parametrize("a_off,b_off,lda_pad,ldb_pad,M,N,K", [
     (1, 7, 0, 0, 131, 257, 300),     # every row start misaligned, odd ld
     (0, 0, 0, 1, 64, 95, 4100),      # A rows alternate 8- and 16-byte alignment
     (3, 5, 2, 3, 5, 9, 7),           # rows shorter than one 16-byte chunk
     (0, 2, 0, 1, 33, 1031, 1031),    # a ragged last chunk in every row
 ])
-def test_pack_reads_nothing_outside_rows(a_off, b_off, lda_pad, ldb_pad, M, N, K):
+def test_pack_reads_nothing_outside_rows(a_off, b_off, lda_pad, ldb_pad, M, N, K, direct):
     """Every element around and between the operands' rows is NaN: the
     realigning pack reads whole aligned 16-byte blocks, so a stray byte
     shifted into a packed row, or a tail not masked, would turn outputs
-    into NaN.  Integer inputs make the product exact."""
+    into NaN; the direct-load kernel reads the rows in place, element by
+    element.  Integer inputs make the product exact."""
     lda, ldb = K + lda_pad, N + ldb_pad
     Ai, Bi = synth.make_int_inputs(1, M, N, K, seed=M + N)
     nan = float("nan")
@@ -244,7 +249,7 @@ def test_pack_reads_nothing_outside_rows(a_off, b_off, lda_pad, ldb_pad, M, N, K
     A = ad[a_off:a_off + M * lda].view(M, lda)[:, :K]
     B = bd[b_off:b_off + K * ldb].view(K, ldb)[:, :N]
     C = torch.empty(M, N, dtype=torch.float32, device=dev())
-    tg.gemm(A, B, C)
+    tg.gemm(A, B, C, options=tg.make_options(direct=direct))
     assert tg.device_error() == tg.TG_OK
     assert np.array_equal(C.cpu().double().numpy(), oracle_dense(Ai, Bi))
 
@@ -582,22 +587,25 @@ def test_host_entry_empty_sum():
     assert torch.all(C == 0)
 
 
+@pytest.mark.parametrize("direct", [1, 2], ids=["persistent", "direct"])
 @pytest.mark.parametrize("N", [423, 422, 421, 420])
 @pytest.mark.parametrize("out", ["f32", "bf16"])
-def test_store_never_writes_row_padding(N, out):
-    """C rows 16-byte aligned (the tensor-memory-accelerator store path) but
-    N not ending on a 16-byte boundary: the padding between rows stays
-    untouched (a TMA store clips only at 16-byte granularity)."""
+def test_store_never_writes_row_padding(N, out, direct):
+    """C rows 16-byte aligned (the persistent kernel's tensor-memory-
+    accelerator store path; the direct-load kernel's plain stores) but N not
+    ending on a 16-byte boundary: the padding between rows stays untouched
+    (a TMA store clips only at 16-byte granularity)."""
     M, K = 70, 64
     A, B = synth.make_int_inputs(1, M, N, K, seed=N)
     ldc = (N + 8) // 8 * 8 + 8
     dt = torch.float32 if out == "f32" else torch.bfloat16
     buf = torch.full((M * ldc,), float("nan"), dtype=dt, device=dev())
     D = buf.view(M, ldc)[:, :N]
+    opts = tg.make_options(direct=direct)
     if out == "f32":
-        tg.gemm(A.to(dev()), B.to(dev()), D)
+        tg.gemm(A.to(dev()), B.to(dev()), D, options=opts)
     else:
-        tg.gemm_fused(A.to(dev()), B.to(dev()), D)
+        tg.gemm_fused(A.to(dev()), B.to(dev()), D, options=opts)
     assert tg.device_error() == tg.TG_OK
     host = buf.view(M, ldc).float().cpu().numpy()
     assert np.all(np.isnan(host[:, N:])), "write into the row padding"

@@ -47,6 +47,7 @@ class tg_options(ctypes.Structure):
         ("trace_buffer", ctypes.c_uint64),
         ("a_col_major", ctypes.c_int32),
         ("b_col_major", ctypes.c_int32),
+        ("direct", ctypes.c_int32),
     ]
 
 
@@ -71,7 +72,8 @@ class tg_plan_info(ctypes.Structure):
         ("cta_pair", ctypes.c_int32),
         ("stream_k", ctypes.c_int32),
         ("sk_tiles", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 3),
+        ("direct", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 2),
     ]
 
     def as_dict(self) -> dict:

@@ -6,7 +6,8 @@ Translation units (compiled in parallel, one ``-gencode`` for sm_103a):
 * ``csrc/tg_kernels.cu`` - the persistent GEMM kernel, once per tile width
                            (-DTG_BN=64/128/192/256);
 * ``csrc/tg_noalloc.cu`` - the split-K entry point whose scratch is a static
-                           device array (no run-time allocation).
+                           device array (no run-time allocation);
+* ``csrc/tg_direct.cu``  - the direct-load kernel for small problems.
 The CUDA runtime is linked statically, so the library loads on a machine
 without a GPU (every CUDA call then returns an error) and exports only the
 ``tg_*`` entry points of ``include/tg_gemm.h``.
@@ -82,7 +83,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
     os.makedirs(BUILD, exist_ok=True)
     machine = platform.machine() + ("_checks" if checks else "")
     jobs = [(os.path.join(CSRC, "tg_host.cu"), os.path.join(BUILD, f"tg_host_{machine}.o"), []),
-            (os.path.join(CSRC, "tg_noalloc.cu"), os.path.join(BUILD, f"tg_noalloc_{machine}.o"), [])]
+            (os.path.join(CSRC, "tg_noalloc.cu"), os.path.join(BUILD, f"tg_noalloc_{machine}.o"), []),
+            (os.path.join(CSRC, "tg_direct.cu"), os.path.join(BUILD, f"tg_direct_{machine}.o"), [])]
     for bn in WIDTHS:
         jobs.append((os.path.join(CSRC, "tg_kernels.cu"),
                      os.path.join(BUILD, f"tg_kernels_bn{bn}_{machine}.o"), [f"-DTG_BN={bn}"]))

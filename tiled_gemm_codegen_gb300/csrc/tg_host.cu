@@ -356,6 +356,7 @@ PlanInput plan_input(const Args &a, int sms, const tg_options *opt)
         in.max_ctas = opt->max_ctas;
         in.cta_pair = opt->cta_pair;
         in.stream_k = opt->stream_k;
+        in.direct = opt->direct;
     }
     return in;
 }
@@ -382,6 +383,7 @@ void fill_info(const Plan &p, tg_plan_info *out)
     out->smem_bytes = p.smem;
     out->tmem_cols = p.tmem;
     out->workspace_bytes = p.workspace();
+    out->direct = p.direct ? 2 : 1;
 }
 
 // ------------------------------------------------------------ device state
@@ -712,6 +714,36 @@ tg_status run_gemm(const Args &a, cudaStream_t stream, const tg_options *opt,
     st = ensure_err_word(w, stream);
     if (st != TG_OK) return st;
 
+    if (plan.direct) {
+        KernelParams p{};
+        p.M = static_cast<int32_t>(a.M);
+        p.N = static_cast<int32_t>(a.N);
+        p.K = static_cast<int32_t>(a.K);
+        p.batch = static_cast<int32_t>(a.batch);
+        p.tiles_m = plan.tiles_m;
+        p.tiles_n = plan.tiles_n;
+        p.splits = 1;
+        p.k_blocks = plan.k_blocks;
+        p.num_units = plan.units;
+        p.a_mn = a.a_cm ? 1 : 0;
+        p.b_k = a.b_cm ? 1 : 0;
+        p.C = a.C;
+        p.ldc = a.ldc;
+        p.strideC = a.sC;
+        if (ep) fill_epilogue(p, a, ep);
+        p.err = w.err;
+        p.timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : DEFAULT_TIMEOUT_NS;
+        p.debug_stall = (opt && opt->debug_stall) ? (opt->debug_stall == 2 ? 2 : 1) : 0;
+        p.trace = opt ? reinterpret_cast<unsigned long long *>(opt->trace_buffer) : nullptr;
+        if (trace_enabled())
+            std::fprintf(stderr, "tg_gemm M=%lld N=%lld K=%lld batch=%lld: direct tiles=%dx%d kb=%d chunk=%d grid=%d\n",
+                         (long long)a.M, (long long)a.N, (long long)a.K, (long long)a.batch, plan.tiles_m,
+                         plan.tiles_n, plan.k_blocks, plan.stages, plan.grid);
+        e = launch_direct(p, a.A, a.B, a.lda, a.ldb, in.a_bcast || a.batch == 1 ? 0 : a.sA,
+                          in.b_bcast || a.batch == 1 ? 0 : a.sB, plan.stages, plan.grid, stream);
+        return cuda_status(e);
+    }
+
     const void *A = a.A;
     const void *B = a.B;
     int64_t lda = a.lda, ldb = a.ldb, sA = a.sA, sB = a.sB;
@@ -1005,6 +1037,34 @@ TG_API tg_status tg_tune(const void *A, const void *B, float *C, int64_t M, int6
     float best_t = -1.0f;
     tg_options best_o = start;
     st = TG_OK;
+    // Median time of one candidate over `reps` calls (after a warm-up call
+    // that also sizes the workspaces); the fastest is kept.
+    auto time_candidate = [&](const tg_options &o) {
+        float ts[100];
+        st = run_gemm(a, stream, &o);
+        for (int r = 0; r < reps && st == TG_OK; ++r) {
+            cudaEventRecord(e0, stream);
+            st = run_gemm(a, stream, &o);
+            cudaEventRecord(e1, stream);
+            if ((e = cudaEventSynchronize(e1)) != cudaSuccess) st = cuda_status(e);
+            if (st == TG_OK) cudaEventElapsedTime(&ts[r], e0, e1);
+        }
+        if (st != TG_OK) return;
+        std::sort(ts, ts + reps);
+        const float t = ts[reps / 2] * 1000.0f;
+        if (best_t < 0.0f || t < best_t) {
+            best_t = t;
+            best_o = o;
+        }
+    };
+    {
+        // the direct-load kernel, where it applies
+        tg_options o = start;
+        o.direct = 2;
+        PlanInput in = plan_input(a, sms, &o);
+        Plan pl;
+        if (make_plan(in, pl)) time_candidate(o);
+    }
     const int widths[4] = {64, 128, 192, 256};
     const int depths[5] = {2, 3, 4, 6, 8};
     const int splits[6] = {1, 2, 3, 4, 6, 8};
@@ -1020,6 +1080,7 @@ TG_API tg_status tg_tune(const void *A, const void *B, float *C, int64_t M, int6
                     for (int sk = 1; sk <= 2 && st == TG_OK; ++sk) {
                         if (sk == 2 && splits[si] > 1) continue;
                         tg_options o = start;
+                        o.direct = 1;
                         o.block_n = widths[wi];
                         o.cta_pair = pr;
                         o.stages = depths[di];
@@ -1034,22 +1095,8 @@ TG_API tg_status tg_tune(const void *A, const void *B, float *C, int64_t M, int6
                         if (sk == 2 && !pl.stream_k) continue;  // same plan as stream_k = 1
                         // the deeper half of the instantiated ring depths
                         if (depths[di] < max_stages(widths[wi], pair) / 2) continue;
-                        float ts[100];
-                        st = run_gemm(a, stream, &o);  // warm-up (workspaces, maps)
-                        for (int r = 0; r < reps && st == TG_OK; ++r) {
-                            cudaEventRecord(e0, stream);
-                            st = run_gemm(a, stream, &o);
-                            cudaEventRecord(e1, stream);
-                            if ((e = cudaEventSynchronize(e1)) != cudaSuccess) st = cuda_status(e);
-                            if (st == TG_OK) cudaEventElapsedTime(&ts[r], e0, e1);
-                        }
+                        time_candidate(o);
                         if (st != TG_OK) break;
-                        std::sort(ts, ts + reps);
-                        const float t = ts[reps / 2] * 1000.0f;
-                        if (best_t < 0.0f || t < best_t) {
-                            best_t = t;
-                            best_o = o;
-                        }
                     }
                 }
             }

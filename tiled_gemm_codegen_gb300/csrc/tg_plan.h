@@ -107,6 +107,29 @@ constexpr int tmem_cols_for(int bn)
                        : Geometry<256>::TMEM_COLS;
 }
 
+// Direct-load kernel (tg_direct.cu) for small problems: one CTA of 512
+// threads per 128 x 64 output tile, the operands copied into shared memory
+// by the threads themselves (any pitch and alignment), DIRECT_KB k-blocks at
+// a time, the accumulator in 64 tensor-memory columns.
+constexpr int DIRECT_BN = 64;
+constexpr int DIRECT_KB = 4;
+constexpr int DIRECT_THREADS = 512;
+constexpr int DIRECT_TMEM_COLS = 64;
+// Staging area (or the epilogue's eight 4 KB transpose boxes, which reuse
+// it), 1 KB of alignment slack, two barriers and the tensor-memory address.
+constexpr int direct_smem_bytes(int chunk_kb)
+{
+    const int stage = chunk_kb * (BM * BK * 2 + DIRECT_BN * BK * 2);
+    const int epi = 8 * EPI_CHUNK * EPI_CHUNK * 4;
+    return (stage > epi ? stage : epi) + 1024 + 64;
+}
+// At least 33 KB of shared memory a CTA keeps the CTAs resident on one SM
+// (228 KB of shared memory, 1 KB reserved per CTA) at most 6, so their
+// tensor-memory allocations never exceed the SM's 512 columns (an
+// allocation would otherwise wait for another CTA to free its columns).
+static_assert((233472 / (direct_smem_bytes(1) + 1024)) * DIRECT_TMEM_COLS <= 512, "direct kernel: tensor memory");
+static_assert(direct_smem_bytes(DIRECT_KB) <= SMEM_LIMIT, "direct kernel: shared memory");
+
 struct PlanInput {
     int64_t M, N, K, batch;
     bool a_tma_ok, b_tma_ok, c_tma_ok;  // 16-byte alignment of base and strides
@@ -121,6 +144,7 @@ struct PlanInput {
     bool mx = false;                  // f8 with per-32-element E8M0 block scales
     bool fp4 = false;                 // mx with packed 4-bit elements (K, lda, ldb in bytes)
     bool half_a_ok = true;            // M <= 64 may use slots of 64 rows of A
+    int direct = 0;                   // direct-load kernel: 0 = choose, 1 = off, 2 = on
 };
 
 struct Plan {
@@ -129,6 +153,7 @@ struct Plan {
     bool mx = false;    // block-scaled 8-bit operands
     bool fp4 = false;   // block-scaled packed 4-bit operands (a k-block: 256 elements)
     bool half_a = false;  // ring slots of 64 rows of A (M <= 64, one CTA per tile)
+    bool direct = false;  // direct-load kernel (stages = k-blocks staged at once)
     int bn = 0, stages = 0;
     int tiles_m = 0, tiles_n = 0, k_blocks = 0, splits = 1;
     int64_t units = 0;
@@ -302,6 +327,22 @@ inline void replan_stream_k(const PlanInput &in, Plan &p, int grid)
     set_partial_workspace(in, p);
 }
 
+// The planner's own choice of the direct-load kernel: at most one tile per
+// SM and few k-blocks, where one short launch beats the persistent kernel's
+// set-up and, for operands the TMA unit cannot address, its realign pass.
+// Measured (GB300, CUDA events, L2 flushed; direct against persistent, us):
+// operands TMA can address - 1000 x 1000 x 64 10.2 / 12.3, 128^3 12.3 /
+// 14.3, but 256^3 (4 k-blocks) 14.3 / 12.3 and 512^3 20.5 / 12.3; operands
+// it cannot (odd pitches) - 197 x 131 x 77 10.2 / 16.4, 129 x 65 x 257
+// (5 k-blocks) 14.3 / 18.4, but 100 x 300 x 500 (8) 20.5 / 16.3.  The copy
+// costs ~1.2 us a k-block (two k-blocks a memory round trip).
+inline bool direct_pays(const PlanInput &in, int k_blocks, int64_t units, int sms)
+{
+    if (units > sms) return false;
+    const bool realign = !in.a_tma_ok || !in.b_tma_ok;
+    return k_blocks <= (realign ? 5 : 2);
+}
+
 // Returns false (and leaves `out` unspecified) for an invalid override.
 inline bool make_plan(const PlanInput &in, Plan &out)
 {
@@ -328,6 +369,35 @@ inline bool make_plan(const PlanInput &in, Plan &out)
     if (in.stream_k == 2 && in.split_k > 1) return false;  // one way of splitting K at a time
     if (in.split_k > 0 && in.split_k > p.k_blocks) return false;
     if (in.cta_pair == 2 && in.block_n != 0 && !pair_width(in.block_n)) return false;
+
+    // Direct-load kernel: bf16 operands and no override but the operand
+    // layouts (direct = 2 with another override is an invalid request).
+    if (in.direct < 0 || in.direct > 2) return false;
+    const int64_t d_tiles_m = ceil_div(in.M, BM), d_tiles_n = ceil_div(in.N, DIRECT_BN);
+    const int64_t d_units = in.batch * d_tiles_m * d_tiles_n;
+    const bool no_override = in.block_n == 0 && in.stages == 0 && in.split_k == 0 && !in.force_pack &&
+                             in.epilogue == 0 && in.cta_pair == 0 && in.stream_k == 0 && in.max_ctas == 0;
+    const bool direct_ok = !in.f8 && p.k_blocks >= 1 && d_units <= INT32_MAX &&
+                           (in.block_n == 0 || in.block_n == DIRECT_BN) && in.stages == 0 && in.split_k <= 1 &&
+                           !in.force_pack && in.epilogue != 1 && in.cta_pair != 2 && in.stream_k != 2 &&
+                           in.max_ctas == 0;
+    if (in.direct == 2 && !direct_ok) return false;
+    if (in.direct == 2 || (in.direct == 0 && direct_ok && no_override && direct_pays(in, p.k_blocks, d_units, sms))) {
+        p.direct = true;
+        p.bn = DIRECT_BN;
+        p.stages = std::min(p.k_blocks, DIRECT_KB);
+        p.tiles_m = static_cast<int>(d_tiles_m);
+        p.tiles_n = static_cast<int>(d_tiles_n);
+        p.splits = 1;
+        p.maxparts = 1;
+        p.units = d_units;
+        p.grid = static_cast<int>(d_units);
+        p.epilogue = 2;
+        p.smem = direct_smem_bytes(p.stages);
+        p.tmem = DIRECT_TMEM_COLS;
+        out = p;
+        return true;
+    }
 
     struct Cand {
         int bn;
