@@ -32,6 +32,9 @@ DEFAULT_WORKLOAD = "square_4096"
 METRIC = "bf16->fp32 GEMM TFLOP/s at 1 GB300 and % of dense BF16 tensor (or HBM) roofline"
 KERNEL_SOURCES = ["tiled_gemm_codegen_gb300/csrc/tg_kernel.cuh", "tiled_gemm_codegen_gb300/csrc/tg_ptx.cuh",
                   "tiled_gemm_codegen_gb300/csrc/tg_internal.h", "tiled_gemm_codegen_gb300/csrc/tg_epilogue.cuh"]
+# the direct-load kernel (small problems) is its own translation unit
+DIRECT_SOURCES = KERNEL_SOURCES + ["tiled_gemm_codegen_gb300/csrc/tg_direct.cu",
+                                   "tiled_gemm_codegen_gb300/csrc/tg_direct.h"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # Nominal GB300 figures (dense bf16 tensor rate, HBM3e bandwidth), reported
@@ -41,22 +44,24 @@ EXTRA_STEPS = 50  # timed steps of each non-headline workload (median reported)
 
 
 # ------------------------------------------------------------------ helpers
-def kernel_source_hash() -> str:
+def kernel_source_hash(direct: bool = False) -> str:
+    """Hash of the sources of the kernel a plan runs: the persistent kernel,
+    or (direct) the direct-load kernel."""
     import hashlib
 
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in (DIRECT_SOURCES if direct else KERNEL_SOURCES):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def measured_traffic(workload: str):
+def measured_traffic(workload: str, direct: bool = False):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source; else None."""
+    on the current source of the kernel the plan runs; else None."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
-    want = kernel_source_hash()
+    want = kernel_source_hash(direct)
     with open(TRAFFIC_FILE) as f:
         for line in f:
             parts = line.split()
@@ -220,7 +225,7 @@ def run_reference(args, rank, world, dist):
 
 
 # ------------------------------------------------------------------ GPU arm
-def roofline_of(w, ms: float, peaks: dict, peak_src: str) -> dict:
+def roofline_of(w, ms: float, peaks: dict, peak_src: str, direct: bool = False) -> dict:
     """The binding roofline of workload `w` at `ms` per call: HBM when its
     arithmetic intensity (algorithmic flop per algorithmic byte) is below
     the ridge point of the measured peaks, else the bf16 tensor peak; the
@@ -232,14 +237,14 @@ def roofline_of(w, ms: float, peaks: dict, peak_src: str) -> dict:
     gbs = w.bytes_moved / (ms * 1e-3) / 1e9
     if flops / w.bytes_moved < peak * 1e12 / (hbm * 1e9):
         return {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(gbs / hbm, 4), "traffic": measured_traffic(w.name),
+                "frac": round(gbs / hbm, 4), "traffic": measured_traffic(w.name, direct),
                 "peak_source": f"{peak_src} hbm_gbs (copy)",
                 "algorithmic_bytes_per_launch": int(w.bytes_moved),
                 "nominal_peak": NOMINAL_PEAKS["hbm_gbs"],
                 "nominal_frac": round(gbs / NOMINAL_PEAKS["hbm_gbs"], 4),
                 "tensor_frac": round(achieved / peak, 4)}
     return {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-            "frac": round(achieved / peak, 4), "traffic": measured_traffic(w.name),
+            "frac": round(achieved / peak, 4), "traffic": measured_traffic(w.name, direct),
             "peak_source": f"{peak_src} bf16_tflops (burst; kernel timed alone)",
             "algorithmic_flops_per_launch": int(flops),
             "nominal_peak": NOMINAL_PEAKS["bf16_tflops"],
@@ -248,7 +253,7 @@ def roofline_of(w, ms: float, peaks: dict, peak_src: str) -> dict:
 
 
 PLAN_KEYS = ("block_n", "stages", "split_k", "grid", "pack_a", "pack_b", "epilogue", "cta_pair", "stream_k",
-             "sk_tiles")
+             "sk_tiles", "direct")
 
 
 def time_extra_workload(tg, torch, w, device, flush_l2, steps: int, warmup: int) -> dict:
@@ -323,8 +328,7 @@ def run_gpu(args, rank, world, local, dist):
             SFA = synth.make_e8m0_codes(lead + (w.M, runs), seed=w.seed + 2).to(device)
             SFB = synth.make_e8m0_codes(lead + (w.N, runs), seed=w.seed + 3).to(device)
             launches_per_step = 2
-        info = {k: None for k in ("block_n", "stages", "split_k", "grid", "pack_a", "pack_b", "epilogue",
-                                  "cta_pair", "stream_k", "sk_tiles")}
+        info = {k: None for k in PLAN_KEYS}
     else:
         A_cpu, B_cpu = synth.workload_inputs(w)
         A = A_cpu.to(device)
@@ -412,7 +416,7 @@ def run_gpu(args, rank, world, local, dist):
     e2e_value = world * flops / (e2e_ms_max * 1e-3) / 1e12
 
     peaks, peak_src = load_peaks()
-    roofline = roofline_of(w, ms_mean, peaks, peak_src)  # this rank's kernel
+    roofline = roofline_of(w, ms_mean, peaks, peak_src, direct=bool(info.get("direct") == 2))  # this rank's kernel
 
     # Every other workload at its full size, in the launch configuration of
     # the default plan: median of EXTRA_STEPS cold-L2 calls each (rank 0's
@@ -433,7 +437,7 @@ def run_gpu(args, rank, world, local, dist):
                 "steps": len(per_x), "ms_median": round(med, 4), "ms_mean": round(sum(per_x) / len(per_x), 4),
                 "ms_min": round(min(per_x), 4),
                 "value": round(wx.flops / (med * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
-                "roofline": roofline_of(wx, med, peaks, peak_src),
+                "roofline": roofline_of(wx, med, peaks, peak_src, direct=r["plan"]["direct"] == 2),
                 "plan": r["plan"], "gpu_launches_per_step": r["launches_per_step"],
             }
             torch.cuda.empty_cache()
@@ -452,9 +456,7 @@ def run_gpu(args, rank, world, local, dist):
                        "accumulate": "fp32",
                        "l2": "flushed between steps (512 MB write, then 256 MB read)",
                        "parallelism": "replicas" if world > 1 else "single GPU",
-                       "plan": {k: info[k] for k in ("block_n", "stages", "split_k", "grid", "pack_a",
-                                                     "pack_b", "epilogue", "cta_pair", "stream_k",
-                                                     "sk_tiles")}},
+                       "plan": {k: info[k] for k in PLAN_KEYS}},
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s",

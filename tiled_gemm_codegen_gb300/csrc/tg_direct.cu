@@ -23,6 +23,7 @@
 // one launch whose code path is short, where the persistent kernel would
 // add the realign pass of misaligned operands and its producer / consumer
 // machinery.
+#include "tg_direct.h"
 #include "tg_kernel.cuh"
 #include "tg_plan.h"
 

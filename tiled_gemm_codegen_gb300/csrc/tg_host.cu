@@ -17,6 +17,7 @@
 #include "tg_epilogue.cuh"
 #include "tg_gemm.h"
 #include "tg_internal.h"
+#include "tg_direct.h"
 #include "tg_plan.h"
 #include "tg_ptx.cuh"
 

@@ -146,12 +146,6 @@ cudaError_t launch_gemm_bn192_half_a(const CUtensorMap &ta, const CUtensorMap &t
 TG_DECLARE_LAUNCH(192)
 TG_DECLARE_LAUNCH(256)
 #undef TG_DECLARE_LAUNCH
-// Direct-load kernel (tg_direct.cu): one CTA per 128 x 64 tile of C, grid
-// CTAs; A and B read in place (element pitches lda / ldb, batch strides sA /
-// sB, 0 for an operand shared by every problem; layouts as in p.a_mn /
-// p.b_k); chunk_kb k-blocks staged at once (1 .. DIRECT_KB).
-cudaError_t launch_direct(const KernelParams &p, const void *A, const void *B, int64_t lda, int64_t ldb,
-                          int64_t sA, int64_t sB, int chunk_kb, int64_t grid, cudaStream_t s);
 // Block-scaled operands (mx: MX_FP8 or MX_FP4) on 224-wide one-CTA tiles.
 cudaError_t launch_gemm_mx224(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tc,
                               const KernelParams &p, int stages, int mx, int grid, cudaStream_t s);
