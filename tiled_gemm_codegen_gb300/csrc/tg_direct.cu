@@ -68,13 +68,11 @@ __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint32_t v)
 }
 
 // One operand as the copy sees it: element (row r, k) at
-// base[r * s_row + k * s_k] for rows [0, rows) and k [0, K); `kc`: stored
-// K-contiguous (K-major image), else M/N-contiguous (M/N-major image).
+// base[r * s_row + k * s_k] for rows [0, rows) and k [0, K).
 struct DirectOperand {
     const uint16_t *base;
     int64_t s_row, s_k;
     int32_t rows;
-    bool kc;
 };
 
 // This thread's share of one operand's k-block image of ROWS rows x 64 k
@@ -86,33 +84,40 @@ struct DirectOperand {
 // consecutive rows; the image is atoms of 64 rows x 64 k, one 128-byte k
 // row of 64 elements each, unit u of k row kk at u ^ (kk mod 8), atoms 8 KB
 // apart.  kbase: the image's first k.
-template <int ROWS>
+template <int ROWS, bool KC>
 __device__ __forceinline__ void load_image(const DirectOperand &o, int32_t kbase, int32_t K, int32_t tid,
                                            uint32_t (&v)[ROWS * BK / DIRECT_THREADS])
 {
     constexpr int PER = ROWS * BK / DIRECT_THREADS;
-    if (o.kc) {
+    // Element j is inside the operand exactly when j < nj (a prefix), so each
+    // load's predicate is one compare with a constant.
+    const uint16_t *src;
+    int64_t step;
+    int32_t nj;
+    if constexpr (KC) {
         const int32_t r0 = tid >> 6, k = kbase + (tid & 63);
-        const uint16_t *src = o.base + static_cast<int64_t>(r0) * o.s_row + k;
-        const int64_t step = 8 * o.s_row;
-#pragma unroll
-        for (int j = 0; j < PER; ++j) v[j] = ld_u16_pred(src + j * step, r0 + 8 * j < o.rows && k < K);
+        src = o.base + static_cast<int64_t>(r0) * o.s_row + k;
+        step = 8 * o.s_row;
+        nj = k < K ? min(PER, max(0, (o.rows - r0 + 7) >> 3)) : 0;
     } else {
         constexpr int KSTEP = DIRECT_THREADS / ROWS;
         const int32_t r = tid & (ROWS - 1), k0 = kbase + tid / ROWS;
-        const uint16_t *src = o.base + r + static_cast<int64_t>(k0) * o.s_k;
-        const int64_t step = KSTEP * o.s_k;
+        src = o.base + r + static_cast<int64_t>(k0) * o.s_k;
+        step = KSTEP * o.s_k;
+        nj = (r < o.rows && k0 < K) ? min(PER, (K - k0 + KSTEP - 1) / KSTEP) : 0;
+    }
 #pragma unroll
-        for (int j = 0; j < PER; ++j) v[j] = ld_u16_pred(src + j * step, r < o.rows && k0 + KSTEP * j < K);
+    for (int j = 0; j < PER; ++j) {
+        v[j] = ld_u16_pred(src, j < nj);
+        src += step;
     }
 }
 
-template <int ROWS>
-__device__ __forceinline__ void store_image(uint32_t img, bool kc, int32_t tid,
-                                            const uint32_t (&v)[ROWS * BK / DIRECT_THREADS])
+template <int ROWS, bool KC>
+__device__ __forceinline__ void store_image(uint32_t img, int32_t tid, const uint32_t (&v)[ROWS * BK / DIRECT_THREADS])
 {
     constexpr int PER = ROWS * BK / DIRECT_THREADS;
-    if (kc) {
+    if constexpr (KC) {
         const uint32_t r0 = static_cast<uint32_t>(tid) >> 6, k = static_cast<uint32_t>(tid) & 63u;
         const uint32_t base = img + r0 * 128u + (((k >> 3) ^ (r0 & 7u)) << 4) + (k & 7u) * 2u;
 #pragma unroll
@@ -136,6 +141,11 @@ struct DirectArgs {
     int32_t chunk_kb;          // k-blocks staged at once (1 .. DIRECT_KB)
 };
 
+// A_KC / B_KC: A stored row-major / B stored column-major (K-contiguous);
+// FUSED: the fused epilogue.  One instance per combination keeps each
+// kernel's code to its own path (a call this small runs largely from a cold
+// instruction cache).
+template <bool A_KC, bool B_KC, bool FUSED>
 __global__ void __launch_bounds__(DIRECT_THREADS, 1) direct_gemm_kernel(const KernelParams p, const DirectArgs d)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -183,11 +193,11 @@ __global__ void __launch_bounds__(DIRECT_THREADS, 1) direct_gemm_kernel(const Ke
     // A (M x K) staged by its rows m0 + r, B (K x N) by its columns n0 + r.
     const uint16_t *Ab = static_cast<const uint16_t *>(d.A) + static_cast<int64_t>(b) * d.sA;
     const uint16_t *Bb = static_cast<const uint16_t *>(d.B) + static_cast<int64_t>(b) * d.sB;
-    const bool a_kc = p.a_mn == 0, b_kc = p.b_k != 0;
+    constexpr bool a_kc = A_KC, b_kc = B_KC;
     const DirectOperand opA{Ab + (a_kc ? static_cast<int64_t>(m0) * d.lda : static_cast<int64_t>(m0)),
-                            a_kc ? d.lda : 1, a_kc ? 1 : d.lda, p.M - m0, a_kc};
+                            a_kc ? d.lda : 1, a_kc ? 1 : d.lda, p.M - m0};
     const DirectOperand opB{Bb + (b_kc ? static_cast<int64_t>(n0) * d.ldb : static_cast<int64_t>(n0)),
-                            b_kc ? d.ldb : 1, b_kc ? 1 : d.ldb, p.N - n0, b_kc};
+                            b_kc ? d.ldb : 1, b_kc ? 1 : d.ldb, p.N - n0};
 
     // The persistent kernel's descriptors for the same images: a K-major
     // operand steps 32 B per 16 k, an M/N-major one 16 k rows (2 KB) with
@@ -209,17 +219,17 @@ __global__ void __launch_bounds__(DIRECT_THREADS, 1) direct_gemm_kernel(const Ke
             const int32_t kbase = (kb0 + kb) * BK;
             uint32_t va0[BM * BK / DIRECT_THREADS], vb0[DIRECT_BN * BK / DIRECT_THREADS];
             uint32_t va1[BM * BK / DIRECT_THREADS], vb1[DIRECT_BN * BK / DIRECT_THREADS];
-            load_image<BM>(opA, kbase, p.K, tid, va0);
-            load_image<DIRECT_BN>(opB, kbase, p.K, tid, vb0);
+            load_image<BM, A_KC>(opA, kbase, p.K, tid, va0);
+            load_image<DIRECT_BN, B_KC>(opB, kbase, p.K, tid, vb0);
             if (two) {
-                load_image<BM>(opA, kbase + BK, p.K, tid, va1);
-                load_image<DIRECT_BN>(opB, kbase + BK, p.K, tid, vb1);
+                load_image<BM, A_KC>(opA, kbase + BK, p.K, tid, va1);
+                load_image<DIRECT_BN, B_KC>(opB, kbase + BK, p.K, tid, vb1);
             }
-            store_image<BM>(sA + static_cast<uint32_t>(kb) * D_A_KB, a_kc, tid, va0);
-            store_image<DIRECT_BN>(sB + static_cast<uint32_t>(kb) * D_B_KB, b_kc, tid, vb0);
+            store_image<BM, A_KC>(sA + static_cast<uint32_t>(kb) * D_A_KB, tid, va0);
+            store_image<DIRECT_BN, B_KC>(sB + static_cast<uint32_t>(kb) * D_B_KB, tid, vb0);
             if (two) {
-                store_image<BM>(sA + static_cast<uint32_t>(kb + 1) * D_A_KB, a_kc, tid, va1);
-                store_image<DIRECT_BN>(sB + static_cast<uint32_t>(kb + 1) * D_B_KB, b_kc, tid, vb1);
+                store_image<BM, A_KC>(sA + static_cast<uint32_t>(kb + 1) * D_A_KB, tid, va1);
+                store_image<DIRECT_BN, B_KC>(sB + static_cast<uint32_t>(kb + 1) * D_B_KB, tid, vb1);
             }
         }
         ptx::fence_proxy_async_smem();  // the generic-proxy writes, before the MMAs read them
@@ -269,7 +279,7 @@ __global__ void __launch_bounds__(DIRECT_THREADS, 1) direct_gemm_kernel(const Ke
         ptx::tmem_load_32cols(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(cb * 32), v);
         const int32_t row0 = m0 + q * 32, col0 = n0 + cb * 32;
         if (row0 < p.M && col0 < p.N) {
-            if (p.fused) apply_epilogue(p, v, row0 + lane, col0, b);
+            if constexpr (FUSED) apply_epilogue(p, v, row0 + lane, col0, b);
             // Transpose through this warp's 4 KB box (the staging area is
             // free: every MMA that read it has completed): row `lane` of the
             // block goes in as eight 16-byte units (unit j at j ^ (lane mod 8)),
@@ -290,7 +300,7 @@ __global__ void __launch_bounds__(DIRECT_THREADS, 1) direct_gemm_kernel(const Ke
 #pragma unroll
                 for (int r = 0; r < 8; ++r) vals[r] = ld_shared_f32((src ^ (((r0 + r) & 7) << 4)) + (r0 + r) * 128);
                 if (col < p.N) {
-                    if (p.out_bf16) {
+                    if (FUSED && p.out_bf16) {  // bf16 output only through the fused epilogue
                         uint16_t *dst = static_cast<uint16_t *>(p.C) + off;
 #pragma unroll
                         for (int r = 0; r < 8; ++r)
@@ -326,16 +336,24 @@ cudaError_t launch_direct(const KernelParams &p, const void *A, const void *B, i
 {
     if (chunk_kb < 1 || chunk_kb > DIRECT_KB || grid < 1 || grid > INT32_MAX) return cudaErrorInvalidValue;
     const int smem = direct_smem_bytes(chunk_kb);
-    static std::atomic<unsigned long long> configured{0};
+    using Kern = void (*)(const KernelParams, const DirectArgs);
+    static const Kern kernels[8] = {
+        direct_gemm_kernel<false, false, false>, direct_gemm_kernel<false, false, true>,
+        direct_gemm_kernel<false, true, false>,  direct_gemm_kernel<false, true, true>,
+        direct_gemm_kernel<true, false, false>,  direct_gemm_kernel<true, false, true>,
+        direct_gemm_kernel<true, true, false>,   direct_gemm_kernel<true, true, true>};
+    const int which = (p.a_mn == 0 ? 4 : 0) + (p.b_k != 0 ? 2 : 0) + (p.fused ? 1 : 0);
+    const Kern kern = kernels[which];
+    // the shared-memory opt-in is per kernel and device; set it once
+    static std::atomic<unsigned long long> configured[8] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
-    if (!bit || !(configured.load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(direct_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 direct_smem_bytes(DIRECT_KB));
+    if (!bit || !(configured[which].load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, direct_smem_bytes(DIRECT_KB));
         if (e != cudaSuccess) return e;
-        configured.fetch_or(bit, std::memory_order_acq_rel);
+        configured[which].fetch_or(bit, std::memory_order_acq_rel);
     }
     const DirectArgs d{A, B, lda, ldb, sA, sB, chunk_kb};
     // Programmatic dependent launch, as for the persistent kernel: set-up
@@ -350,7 +368,7 @@ cudaError_t launch_direct(const KernelParams &p, const void *A, const void *B, i
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, direct_gemm_kernel, p, d);
+    return cudaLaunchKernelEx(&cfg, kern, p, d);
 }
 
 }  // namespace tg
