@@ -1464,10 +1464,25 @@ TG_API tg_status tg_gemm_host(const void *A_host, const void *B_host, float *C_h
     const int64_t ldc_d = round_up(N, 4), sC_d = M * ldc_d;
     const HostPieces hp = host_pieces(M, N, K, batch, a_bcast, b_bcast, a.a_cm, a.b_cm,
                                       strideA == a_rows * lda, strideB == b_rows * ldb);
-    // the operand copied whole is realigned once if its rows are not 16-byte aligned
+    // the operand copied whole is realigned once if its rows are not 16-byte
+    // aligned - unless the whole problem goes to the direct-load kernel,
+    // which reads any pitch in place (the device copies start on 256 bytes)
+    bool direct = false;
+    if (K > 0 && hp.pieces == 1) {
+        Args dev_args = a;
+        dev_args.A = reinterpret_cast<const void *>(uintptr_t{256});
+        dev_args.B = reinterpret_cast<const void *>(uintptr_t{512});
+        dev_args.C = reinterpret_cast<float *>(uintptr_t{768});
+        dev_args.ldc = ldc_d;
+        dev_args.sC = sC_d;
+        Plan pl;
+        direct = make_plan(plan_input(dev_args, sms, opt), pl) && pl.direct;
+    }
     const bool a_whole = hp.dim == 0 || hp.dim == 3, b_whole = hp.dim == 0 || hp.dim == 2;
-    const bool a_fix = K > 0 && a_whole && (lda % 8 != 0 || (batch > 1 && !a_bcast && strideA % 8 != 0));
-    const bool b_fix = K > 0 && b_whole && (ldb % 8 != 0 || (batch > 1 && !b_bcast && strideB % 8 != 0));
+    const bool a_fix =
+        !direct && K > 0 && a_whole && (lda % 8 != 0 || (batch > 1 && !a_bcast && strideA % 8 != 0));
+    const bool b_fix =
+        !direct && K > 0 && b_whole && (ldb % 8 != 0 || (batch > 1 && !b_bcast && strideB % 8 != 0));
     const int64_t lda_f = pack_pitch(a_cols), ldb_f = pack_pitch(b_cols);
     const int64_t sA_f = a_bcast ? 0 : a_rows * lda_f, sB_f = b_bcast ? 0 : b_rows * ldb_f;
     size_t off = 0;
