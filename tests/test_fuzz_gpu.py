@@ -72,6 +72,16 @@ def _case_short(i):
                 a_off=r.choice([0, 0, 1, 4]), seed=r.randint(0, 10 ** 6))
 
 
+def _case_direct(i):
+    """The direct-load kernel (direct = 2): operands staged by the threads
+    at any pitch, offset and layout, several staged chunks of K."""
+    r = random.Random(7000 + i)
+    M, N, K = r.randint(1, 400), r.randint(1, 400), r.randint(1, 1200)
+    return dict(M=M, N=N, K=K, batch=r.choice([1, 1, 2, 3]), a_cm=r.random() < 0.4, b_cm=r.random() < 0.4,
+                opts=dict(direct=2), a_pad=r.choice([0, 1, 8, 13]), b_pad=r.choice([0, 3, 8]),
+                c_pad=r.choice([0, 5, 4]), a_off=r.choice([0, 1, 4]), seed=r.randint(0, 10 ** 6))
+
+
 @pytest.mark.parametrize("i", range(N_CASES))
 def test_random_exact_cases(i):
     _run_exact_case(_case(i))
@@ -80,6 +90,11 @@ def test_random_exact_cases(i):
 @pytest.mark.parametrize("i", range(30))
 def test_random_short_outputs(i):
     _run_exact_case(_case_short(i))
+
+
+@pytest.mark.parametrize("i", range(40))
+def test_random_direct_kernel(i):
+    _run_exact_case(_case_direct(i))
 
 
 def _run_exact_case(c):
