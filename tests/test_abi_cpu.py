@@ -547,18 +547,23 @@ def test_direct_plan_fields_and_requests(lib):
 
 
 def test_direct_planner_rule(lib):
-    """The planner's own choice: at most one tile per SM, at most 2
-    k-blocks (operands TMA can address) or 5 (operands it cannot, which the
-    persistent kernel would first realign)."""
-    def direct(M, N, K, batch=1, lda=None, opts=None):
-        return tg.plan(M, N, K, batch, sm_count=152, lda=lda, options=opts)["direct"] == 2
+    """The planner's own choice: at most one tile per SM, and at most 8
+    k-blocks when both operands can be staged in 16-byte units (aligned,
+    contiguous extent a multiple of 8), 5 when one needs the persistent
+    kernel's realign pass (staged element by element), else 2."""
+    def direct(M, N, K, batch=1, lda=None, ldb=None, opts=None):
+        return tg.plan(M, N, K, batch, sm_count=152, lda=lda, ldb=ldb, options=opts)["direct"] == 2
     assert direct(197, 131, 77)                    # odd pitches, 2 k-blocks
     assert direct(129, 65, 257)                    # odd pitch, 5 k-blocks
     assert not direct(100, 300, 500, lda=501)      # 8 k-blocks
     assert direct(1000, 1000, 64)                  # 128 tiles, 1 k-block
     assert direct(128, 128, 128)
-    assert not direct(256, 256, 256)               # 4 k-blocks, aligned
+    assert direct(256, 256, 256) and direct(512, 512, 512)      # 16-byte units, 4 and 8 k-blocks
+    assert not direct(128, 128, 1024)              # 16 k-blocks
+    assert not direct(256, 256, 260, lda=264)      # aligned but K not a multiple of 8: 5 k-blocks > 2
+    assert direct(256, 250, 128, ldb=256)          # aligned, N not a multiple of 8: 2 k-blocks
     assert not direct(4096, 4096, 64)              # 2048 tiles
+    assert not direct(2048, 2048, 128)             # 512 tiles
     assert direct(64, 64, 64, 64)                  # 64 problems of one tile
     assert not direct(128, 128, 128, opts=tg.make_options(block_n=64))  # an override: the persistent kernel
     assert not direct(128, 128, 128, opts=tg.make_options(direct=1))

@@ -145,3 +145,33 @@ def test_direct_trace_stamps_in_order():
     assert torch.all(t[:, 0] > 0)
     for k in range(7):
         assert torch.all(t[:, k + 1] >= t[:, k]), k
+
+
+@pytest.mark.parametrize("layout", LAYOUTS, ids=["nn", "nt", "tn", "tt"])
+@pytest.mark.parametrize("shape", [(8, 8, 8), (128, 64, 64), (200, 136, 256), (256, 256, 512), (64, 520, 1000)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_direct_vector_staging(shape, layout):
+    """Operands with 16-byte aligned pitches and extents that are multiples
+    of 8 are staged in 16-byte units; the same operands with a pitch one
+    element longer go element by element.  Both equal the oracle exactly."""
+    M, N, K = shape
+    A, B = synth.make_int_inputs(1, M, N, K, seed=M + 2 * N + 3 * K)
+    want = oracle_dense(A, B)
+    for pad in (0, 1):
+        Ad = _layout(A.to(dev()), layout[0])
+        Bd = _layout(B.to(dev()), layout[1])
+        if pad:
+            # the same matrices in buffers with one extra element a row (or column)
+            def padded(t):
+                buf = torch.zeros(t.shape[0] + (1 if t.stride(0) == 1 else 0),
+                                  t.shape[1] + (1 if t.stride(1) == 1 else 0), dtype=t.dtype, device=t.device)
+                if t.stride(1) == 1:
+                    buf[:, :t.shape[1]] = t
+                    return buf[:, :t.shape[1]]
+                buf = torch.zeros(t.shape[1], t.shape[0] + 1, dtype=t.dtype, device=t.device)
+                buf[:, :t.shape[0]] = t.t()
+                return buf[:, :t.shape[0]].t()
+            Ad, Bd = padded(Ad), padded(Bd)
+        C = torch.full((M, N), float("nan"), device=dev())
+        _gemm(Ad, Bd, C, **DIRECT)
+        assert np.array_equal(C.cpu().double().numpy(), want), pad

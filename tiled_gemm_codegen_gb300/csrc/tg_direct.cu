@@ -67,6 +67,21 @@ __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint32_t v)
     asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(static_cast<uint16_t>(v)) : "memory");
 }
 
+// 16-byte load (8 elements) issued only when `pred` holds (zeros otherwise).
+__device__ __forceinline__ uint4 ld_v4_pred(const uint16_t *src, bool pred)
+{
+    uint4 v;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "mov.b32 %0, 0;\n\tmov.b32 %1, 0;\n\tmov.b32 %2, 0;\n\tmov.b32 %3, 0;\n\t"
+        "@p ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];\n\t}"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(src), "r"(static_cast<uint32_t>(pred))
+        : "memory");
+    return v;
+}
+
 // One operand as the copy sees it: element (row r, k) at
 // base[r * s_row + k * s_k] for rows [0, rows) and k [0, K).
 struct DirectOperand {
@@ -135,10 +150,56 @@ __device__ __forceinline__ void store_image(uint32_t img, int32_t tid, const uin
     }
 }
 
+// The same images in 16-byte units (8 elements along the stored-contiguous
+// dimension), for an operand whose base, pitch and batch stride are 16-byte
+// aligned and whose contiguous extent (K for a K-major image, M or N for an
+// M/N-major one) is a multiple of 8, so that every unit lies wholly inside
+// or wholly outside it.  ROWS * 8 units an image, UNITS = ROWS / 64 a thread:
+// unit t + 512 j.  K-major: unit (row r, k group c) at r * 128 + ((c ^ (r mod
+// 8)) << 4).  M/N-major: unit (k row kk, row group g) at (g / 8) * 8192 +
+// kk * 128 + (((g mod 8) ^ (kk mod 8)) << 4).
+template <int ROWS, bool KC>
+__device__ __forceinline__ void load_image_v4(const DirectOperand &o, int32_t kbase, int32_t K, int32_t tid,
+                                              uint4 (&u)[ROWS / 64])
+{
+#pragma unroll
+    for (int j = 0; j < ROWS / 64; ++j) {
+        const int32_t id = tid + DIRECT_THREADS * j;
+        if constexpr (KC) {
+            const int32_t r = id >> 3, k = kbase + 8 * (id & 7);
+            u[j] = ld_v4_pred(o.base + static_cast<int64_t>(r) * o.s_row + k, r < o.rows && k < K);
+        } else {
+            constexpr int RG = ROWS / 8;
+            const int32_t k = kbase + id / RG, g = id % RG;
+            u[j] = ld_v4_pred(o.base + 8 * g + static_cast<int64_t>(k) * o.s_k, 8 * g < o.rows && k < K);
+        }
+    }
+}
+
+template <int ROWS, bool KC>
+__device__ __forceinline__ void store_image_v4(uint32_t img, int32_t tid, const uint4 (&u)[ROWS / 64])
+{
+#pragma unroll
+    for (int j = 0; j < ROWS / 64; ++j) {
+        const uint32_t id = static_cast<uint32_t>(tid + DIRECT_THREADS * j);
+        uint32_t off;
+        if constexpr (KC) {
+            const uint32_t r = id >> 3, c = id & 7u;
+            off = r * 128u + ((c ^ (r & 7u)) << 4);
+        } else {
+            constexpr uint32_t RG = ROWS / 8;
+            const uint32_t kk = id / RG, g = id % RG;
+            off = (g >> 3) * 8192u + kk * 128u + (((g & 7u) ^ (kk & 7u)) << 4);
+        }
+        ptx::st_shared_v4(img + off, u[j].x, u[j].y, u[j].z, u[j].w);
+    }
+}
+
 struct DirectArgs {
     const void *A, *B;
     int64_t lda, ldb, sA, sB;  // element pitches and batch strides (0: shared operand)
     int32_t chunk_kb;          // k-blocks staged at once (1 .. DIRECT_KB)
+    int32_t vec;               // both operands staged in 16-byte units (see load_image_v4)
 };
 
 // A_KC / B_KC: A stored row-major / B stored column-major (K-contiguous);
@@ -212,9 +273,28 @@ __global__ void __launch_bounds__(DIRECT_THREADS, 1) direct_gemm_kernel(const Ke
     for (int32_t ch = 0; ch < n_chunks; ++ch) {
         const int32_t kb0 = ch * chunk_kb;
         const int32_t nkb = min(chunk_kb, p.k_blocks - kb0);
-        // Two k-blocks a round: all 48 loads of this thread, then its stores.
+        if (d.vec) {
+            // The whole chunk in one round: at most 3 x DIRECT_KB 16-byte
+            // loads a thread, then the stores.
+            uint4 ua[DIRECT_KB][BM / 64], ub[DIRECT_KB][DIRECT_BN / 64];
+#pragma unroll
+            for (int32_t kb = 0; kb < DIRECT_KB; ++kb) {
+                if (kb < nkb) {  // uniform
+                    load_image_v4<BM, A_KC>(opA, (kb0 + kb) * BK, p.K, tid, ua[kb]);
+                    load_image_v4<DIRECT_BN, B_KC>(opB, (kb0 + kb) * BK, p.K, tid, ub[kb]);
+                }
+            }
+#pragma unroll
+            for (int32_t kb = 0; kb < DIRECT_KB; ++kb) {
+                if (kb < nkb) {
+                    store_image_v4<BM, A_KC>(sA + static_cast<uint32_t>(kb) * D_A_KB, tid, ua[kb]);
+                    store_image_v4<DIRECT_BN, B_KC>(sB + static_cast<uint32_t>(kb) * D_B_KB, tid, ub[kb]);
+                }
+            }
+        }
+        // Otherwise two k-blocks a round: all 48 loads of this thread, then its stores.
 #pragma unroll 1
-        for (int32_t kb = 0; kb < nkb; kb += 2) {
+        for (int32_t kb = 0; kb < (d.vec ? 0 : nkb); kb += 2) {
             const bool two = kb + 1 < nkb;  // uniform
             const int32_t kbase = (kb0 + kb) * BK;
             uint32_t va0[BM * BK / DIRECT_THREADS], vb0[DIRECT_BN * BK / DIRECT_THREADS];
@@ -332,7 +412,7 @@ __global__ void __launch_bounds__(DIRECT_THREADS, 1) direct_gemm_kernel(const Ke
 }  // namespace
 
 cudaError_t launch_direct(const KernelParams &p, const void *A, const void *B, int64_t lda, int64_t ldb,
-                          int64_t sA, int64_t sB, int chunk_kb, int64_t grid, cudaStream_t s)
+                          int64_t sA, int64_t sB, int chunk_kb, bool vec, int64_t grid, cudaStream_t s)
 {
     if (chunk_kb < 1 || chunk_kb > DIRECT_KB || grid < 1 || grid > INT32_MAX) return cudaErrorInvalidValue;
     const int smem = direct_smem_bytes(chunk_kb);
@@ -355,7 +435,7 @@ cudaError_t launch_direct(const KernelParams &p, const void *A, const void *B, i
         if (e != cudaSuccess) return e;
         configured[which].fetch_or(bit, std::memory_order_acq_rel);
     }
-    const DirectArgs d{A, B, lda, ldb, sA, sB, chunk_kb};
+    const DirectArgs d{A, B, lda, ldb, sA, sB, chunk_kb, vec ? 1 : 0};
     // Programmatic dependent launch, as for the persistent kernel: set-up
     // (barriers, tensor memory) may overlap the previous kernel's tail.
     cudaLaunchConfig_t cfg{};

@@ -740,8 +740,11 @@ tg_status run_gemm(const Args &a, cudaStream_t stream, const tg_options *opt,
             std::fprintf(stderr, "tg_gemm M=%lld N=%lld K=%lld batch=%lld: direct tiles=%dx%d kb=%d chunk=%d grid=%d\n",
                          (long long)a.M, (long long)a.N, (long long)a.K, (long long)a.batch, plan.tiles_m,
                          plan.tiles_n, plan.k_blocks, plan.stages, plan.grid);
-        e = launch_direct(p, a.A, a.B, a.lda, a.ldb, in.a_bcast || a.batch == 1 ? 0 : a.sA,
-                          in.b_bcast || a.batch == 1 ? 0 : a.sB, plan.stages, plan.grid, stream);
+        const int64_t dsA = in.a_bcast || a.batch == 1 ? 0 : a.sA, dsB = in.b_bcast || a.batch == 1 ? 0 : a.sB;
+        // contiguous extents: K of a row-major A or column-major B, else M or N
+        const bool vec = direct_vec_ok(a.A, a.lda, dsA, a.a_cm ? a.M : a.K) &&
+                         direct_vec_ok(a.B, a.ldb, dsB, a.b_cm ? a.K : a.N);
+        e = launch_direct(p, a.A, a.B, a.lda, a.ldb, dsA, dsB, plan.stages, vec, plan.grid, stream);
         return cuda_status(e);
     }
 

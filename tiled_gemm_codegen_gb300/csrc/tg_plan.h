@@ -330,15 +330,26 @@ inline void replan_stream_k(const PlanInput &in, Plan &p, int grid)
 // The planner's own choice of the direct-load kernel: at most one tile per
 // SM and few k-blocks, where one short launch beats the persistent kernel's
 // set-up and, for operands the TMA unit cannot address, its realign pass.
-// Measured (GB300, CUDA events, L2 flushed; direct against persistent, us):
-// operands TMA can address - 1000 x 1000 x 64 10.2 / 12.3, 128^3 12.3 /
-// 14.3, but 256^3 (4 k-blocks) 14.3 / 12.3 and 512^3 20.5 / 12.3; operands
-// it cannot (odd pitches) - 197 x 131 x 77 10.2 / 16.4, 129 x 65 x 257
-// (5 k-blocks) 14.3 / 18.4, but 100 x 300 x 500 (8) 20.5 / 16.3.  The copy
-// costs ~1.2 us a k-block (two k-blocks a memory round trip).
+// How many k-blocks pay depends on how the kernel stages the operands:
+// 16-byte units when both are 16-byte aligned with a contiguous extent that
+// is a multiple of 8 elements, else single elements (~1.2 us a k-block).
+// Measured (GB300, CUDA events, L2 flushed; direct / persistent, us):
+// 16-byte units - 128^3 8.2 / 12.3, 256^3 10.1 / 12.3, 512^3 12.3 / 14.3,
+// 1024 x 1024 x 256 10.2 / 12.3, 64 x 4096 x 512 12.3 / 12.3, 128 x 128 x
+// 1024 (16 k-blocks) 16.4 / 16.4, 256 x 256 x 2048 24.6 / 16.4, 2048^2 x 128
+// (512 tiles) 20.5 / 16.4; single elements with operands the TMA unit
+// cannot address (odd pitches) - 197 x 131 x 77 10.2 / 16.4, 129 x 65 x 257
+// (5 k-blocks) 12.3 / 16.4, 100 x 300 x 500 (8) 20.5 / 16.3; single
+// elements with operands it can - 256^3 (4 k-blocks) 14.3 / 12.3.
+inline bool direct_vec(const PlanInput &in)
+{
+    return in.a_tma_ok && in.b_tma_ok && (in.a_cm ? in.M : in.K) % 8 == 0 && (in.b_cm ? in.K : in.N) % 8 == 0;
+}
+
 inline bool direct_pays(const PlanInput &in, int k_blocks, int64_t units, int sms)
 {
     if (units > sms) return false;
+    if (direct_vec(in)) return k_blocks <= 8;
     const bool realign = !in.a_tma_ok || !in.b_tma_ok;
     return k_blocks <= (realign ? 5 : 2);
 }
