@@ -44,14 +44,21 @@
  *     K == 0: C is filled with zeros (the empty sum).
  *   - Any alignment is accepted.  Operands whose base address or row/batch
  *     stride is not a multiple of 16 bytes are first copied by the library
- *     into an aligned scratch copy (the "pack" pass); an fp32 C whose rows
- *     are not 16-byte aligned is written with plain masked stores instead of
- *     tensor-memory-accelerator stores.
+ *     into an aligned scratch copy (the "pack" pass) - except in a small
+ *     problem's direct-load kernel, which reads them in place; an fp32 C
+ *     whose rows are not 16-byte aligned is written with plain masked stores
+ *     instead of tensor-memory-accelerator stores.
  *   - Rounding: fp32 accumulation in an order fixed by the plan (tile shape
  *     and split-K factor).  Results are bitwise reproducible run to run for
  *     a fixed plan; different plans may differ in the last bits.
  *   - Thread safety: calls on different streams may run concurrently; each
  *     stream has its own scratch workspace.
+ *   - CUDA graphs: the first call on a stream may allocate that stream's
+ *     workspace and set kernel attributes; a later call of the same or a
+ *     smaller plan on the stream enqueues only kernel launches, so it can be
+ *     captured into a CUDA graph and replayed (each replay reads the
+ *     operands' current contents).  tg_gemm_host and tg_tune synchronise
+ *     and cannot be captured.
  */
 #ifndef TG_GEMM_H
 #define TG_GEMM_H
