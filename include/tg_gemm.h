@@ -127,15 +127,16 @@ typedef struct tg_options {
     int32_t b_col_major; /* nonzero: B is stored N x K (element B_b[k][j] at   */
                          /* B[b*strideB + j*ldb + k], ldb >= K)               */
     int32_t direct;      /* direct-load kernel for small problems: 0 = the    */
-                         /* planner decides, 1 = off, 2 = on (bf16 calls     */
-                         /* with no other override but the layouts; else     */
-                         /* TG_ERR_INVALID_ARG).  One CTA per 128 x 64 tile  */
-                         /* of C copies its operand tiles into shared memory */
-                         /* with plain loads (any pitch and alignment, so no */
-                         /* pack pass), up to 4 k-blocks at a time, and      */
-                         /* multiplies them with tcgen05.mma (OCANNL "Module */
-                         /* Ir.Schedule", Stage with a cooperative copy, and */
-                         /* Pad-to-tile)                                     */
+                         /* planner decides, 1 = off, 2 = on (bf16 calls;    */
+                         /* other overrides only at the kernel's own values  */
+                         /* - block_n 64, split_k 1, cta_pair 1, stream_k 1, */
+                         /* epilogue 2 - else TG_ERR_INVALID_ARG).  One CTA  */
+                         /* per 128 x 64 tile of C copies its operand tiles  */
+                         /* into shared memory with plain loads (any pitch   */
+                         /* and alignment, so no pack pass), up to 4         */
+                         /* k-blocks at a time, and multiplies them with     */
+                         /* tcgen05.mma (OCANNL "Module Ir.Schedule", Stage  */
+                         /* with a cooperative copy, and Pad-to-tile)        */
 } tg_options;
 
 /* What the planner chose (tg_plan output). */

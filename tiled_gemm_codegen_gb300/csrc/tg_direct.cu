@@ -4,17 +4,20 @@
 // OCANNL "Module Ir.Schedule", Stage with a cooperative copy: every thread
 // of the block takes part in moving the operand tiles into shared memory;
 // and Pad-to-tile: the staged fringe (rows past M or N, k past K) is stored
-// as zeros.  The copy reads single elements with plain loads, so an operand
-// of any pitch and alignment is read where it lies - no realign pass and no
-// second launch.  It writes the 128-byte-swizzled images the persistent
-// kernel's TMA loads write: K-major for an operand stored K-contiguous
-// (row-major A, column-major B), M/N-major for one stored M/N-contiguous,
-// so that neighbouring threads read neighbouring elements and write
-// neighbouring bytes, and both kernels issue the same MMAs on the same
-// values.  Up to DIRECT_KB k-blocks are staged at once, two a round: every
-// thread first issues all 48 of its loads of the two k-blocks and only then
-// stores them, so one memory round trip stages two k-blocks; the chunk's
-// MMAs go out as one batch and the next chunk's copy waits for their commit.
+// as zeros.  The copy uses plain loads - 16-byte units when both operands
+// are 16-byte aligned with a contiguous extent that is a multiple of 8,
+// else single elements - so an operand of any pitch and alignment is read
+// where it lies: no realign pass and no second launch.  It writes the
+// 128-byte-swizzled images the persistent kernel's TMA loads write: K-major
+// for an operand stored K-contiguous (row-major A, column-major B), M/N-major
+// for one stored M/N-contiguous, so that neighbouring threads read
+// neighbouring elements and write neighbouring bytes, and both kernels issue
+// the same MMAs on the same values.  Up to DIRECT_KB k-blocks are staged at
+// once.  Every thread first issues all of its loads of a round and only then
+// stores them, so one memory round trip stages a whole chunk in 16-byte units
+// (at most 12 loads a thread) or two k-blocks element by element (48 loads
+// a thread); the chunk's MMAs go out as one batch and the next chunk's copy
+// waits for their commit.
 // Eight warps then read the 128 x 64 accumulator from tensor memory, one
 // 32 x 32 block each, and store it through a shared-memory transpose, so
 // that every store instruction writes 32 consecutive columns of one row.
