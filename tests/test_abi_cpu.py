@@ -568,3 +568,65 @@ def test_direct_planner_rule(lib):
     assert not direct(128, 128, 128, opts=tg.make_options(block_n=64))  # an override: the persistent kernel
     assert not direct(128, 128, 128, opts=tg.make_options(direct=1))
     assert not direct(4096, 4096, 4096)
+
+
+def test_plan_invariants_on_random_calls(lib):
+    """Random extents, batches, pointer alignments, layouts and overrides
+    (some invalid): the planner either refuses with TG_ERR_INVALID_ARG /
+    TG_ERR_UNSUPPORTED or returns a plan whose fields are consistent - tile
+    counts cover the problem, the grid and the resources fit one GB300, and
+    the direct-load kernel's plans have its fixed geometry."""
+    import random
+
+    r = random.Random(2024)
+    SMEM_MAX, SMS = 232448, 152
+    for case in range(1500):
+        M = int(2 ** r.uniform(0, 14))
+        N = int(2 ** r.uniform(0, 14))
+        K = int(2 ** r.uniform(0, 14))
+        batch = r.choice([1, 1, 1, 2, 7, 64])
+        a_cm, b_cm = r.random() < 0.25, r.random() < 0.25
+        a_rows, a_cols = (K, M) if a_cm else (M, K)
+        b_rows, b_cols = (N, K) if b_cm else (K, N)
+        lda = a_cols + r.choice([0, 0, 1, 8])
+        ldb = b_cols + r.choice([0, 0, 3, 8])
+        opts = dict(a_col_major=int(a_cm), b_col_major=int(b_cm))
+        pick = r.random()
+        if pick < 0.15:
+            opts["direct"] = r.choice([1, 2])
+        elif pick < 0.3:
+            opts["block_n"] = r.choice([64, 128, 192, 256])
+        elif pick < 0.4:
+            opts["split_k"] = r.choice([1, 2, 3])
+        elif pick < 0.5:
+            opts["stream_k"] = r.choice([1, 2])
+        elif pick < 0.55:
+            opts["cta_pair"] = r.choice([1, 2])
+        A = 0x1000 + 2 * r.choice([0, 0, 1, 4])
+        try:
+            info = tg.plan(M, N, K, batch, lda=lda, ldb=ldb, strideA=a_rows * lda, strideB=b_rows * ldb,
+                           A=A, sm_count=SMS, options=tg.make_options(**opts))
+        except tg.TgError as e:
+            assert e.status in (tg.TG_ERR_INVALID_ARG, tg.TG_ERR_UNSUPPORTED), (case, e.status)
+            continue
+        kb = -(-K // 64)
+        where = (case, M, N, K, batch, opts, info)
+        assert info["k_blocks"] == kb and info["smem_bytes"] <= SMEM_MAX, where
+        assert info["tiles_m"] == -(-M // (128 * info["cta_pair"])) or info["block_m"] == 64, where
+        assert info["tiles_n"] == -(-N // info["block_n"]), where
+        if info["direct"] == 2:
+            assert opts.get("direct", 0) != 1, where
+            assert (info["block_m"], info["block_n"], info["cta_pair"], info["split_k"]) == (128, 64, 1, 1), where
+            assert info["grid"] == info["num_units"] == batch * info["tiles_m"] * info["tiles_n"], where
+            assert info["stages"] == min(4, kb) and info["tmem_cols"] == 64, where
+            assert info["pack_a"] == info["pack_b"] == 0 and info["workspace_bytes"] == 0, where
+            if opts.get("direct", 0) == 0:
+                assert info["num_units"] <= SMS and kb <= 8, where
+        else:
+            assert info["direct"] == 1 and opts.get("direct", 0) != 2, where
+            assert info["num_units"] == batch * info["tiles_m"] * info["tiles_n"] * info["split_k"], where
+            assert 1 <= info["grid"] <= SMS and info["grid"] <= info["num_units"] * info["cta_pair"], where
+            assert info["cta_pair"] == 1 or info["grid"] % 2 == 0, where
+            assert 1 <= info["split_k"] <= kb and 2 <= info["stages"] <= 8, where
+            assert info["tmem_cols"] in (128, 256, 512) and info["tmem_cols"] >= 2 * info["block_n"], where
+            assert info["stream_k"] == 1 or info["split_k"] == 1, where
