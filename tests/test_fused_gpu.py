@@ -27,6 +27,7 @@ PLANS = [
     dict(block_n=256, cta_pair=2, stream_k=2, max_ctas=10),
     dict(block_n=128, cta_pair=1, split_k=3),
     dict(block_n=192, cta_pair=1, epilogue=2),
+    dict(direct=2),  # the direct-load kernel: batched, per-problem bias
 ]
 
 
